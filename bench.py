@@ -1,0 +1,416 @@
+#!/usr/bin/env python
+"""Benchmark of paged GQA decode attention on GB300.
+
+Metric: paged decode attention microseconds per call and achieved HBM GB/s
+(K + V + q + out bytes over the call's time) as a fraction of the measured
+HBM peak, on one GPU.  One "step" is one ``pda_decode`` call over the whole
+batch (split kernel + merge kernel).  Default workload: the 8B-style batch
+(B=32, Hq=32, Hkv=8, D=128, block 16, 4096 tokens each; 537 MB moved per call).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload 8b|1b|wide|ragged|tiny]
+
+Prints ONE JSON line (rank 0).  ``--impl reference`` times the CPU oracle
+(the fp64 definition) on this host's cores instead of the GPU path.
+
+Timing: CUDA events on the launching stream around exactly K back-to-back
+calls after W warm-up calls; inputs are larger than L2 and rotate between
+copies at distinct addresses.  A second pass records events between the two
+kernels of each call (which disables the merge kernel's early launch) to time
+the split kernel alone for the roofline.  ``e2e`` repeats the calls with the
+inputs copied from pinned host memory and the output copied back every step.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "paged decode attn μs/call and KV GB/s as % of GB300 HBM peak (1 GPU)"
+FALLBACK_HBM_GBS = 6800.0
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "split_kernel_traffic.json")
+
+
+def parse_args():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="8b")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash() -> str:
+    import glob
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "paged_gqa_decode_05_gb300", "csrc")
+    for p in sorted(glob.glob(os.path.join(csrc, "*"))):
+        if p.endswith((".cu", ".cuh", ".h")):
+            with open(p, "rb") as f:
+                h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload_key: str):
+    """Per-launch DRAM bytes of the split kernel from the committed ncu summary,
+    or None when the kernel source changed since it was captured."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            d = json.load(f)
+    except (OSError, ValueError):
+        return None
+    if d.get("kernel_source_hash") != kernel_source_hash():
+        return None
+    entry = d.get("workloads", {}).get(workload_key)
+    return None if entry is None else float(entry["dram_bytes_per_launch"])
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.device_index = device_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200", "-i", str(self.device_index)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def stop(self):
+        if self.proc is None:
+            return
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=5)
+
+    def summary(self, t0: float, t1: float):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ts, line in self.lines:
+            if not (t0 <= ts <= t1):
+                continue
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def cpu_oracle_timing(w, budget_s: float = 10.0):
+    """Times the oracle as it stands on all host cores over a bounded sample of
+    the workload's (b, h) outputs (all of them when that fits the budget)."""
+    import numpy as np
+    import oracle
+    orc = oracle.load()
+    threads = oracle.host_threads()
+    total_pairs = w.B * w.Hq
+    args = (w.q, w.k_pool, w.v_pool, w.block_table, w.seq_lens)
+    kw = dict(Hq=w.Hq, Hkv=w.Hkv, D=w.D, block_size=w.block_size, n_threads=threads)
+    rng = np.random.default_rng(0)
+    # probe with a small sample to size the bounded one
+    probe = rng.choice(total_pairs, size=min(total_pairs, max(threads, 16)), replace=False)
+    probe_pairs = np.stack([probe // w.Hq, probe % w.Hq], axis=1).astype(np.int32)
+    t = time.perf_counter()
+    orc.decode(*args, **kw, pairs=probe_pairs)
+    per_pair = (time.perf_counter() - t) / len(probe)
+    n = int(min(total_pairs, max(len(probe), budget_s / max(per_pair, 1e-9))))
+    if n >= total_pairs:
+        pairs, desc = None, f"all {total_pairs} (b, q-head) outputs of the workload"
+    else:
+        pick = np.sort(rng.choice(total_pairs, size=n, replace=False))
+        pairs = np.stack([pick // w.Hq, pick % w.Hq], axis=1).astype(np.int32)
+        desc = f"{n} of {total_pairs} (b, q-head) outputs drawn uniformly (seed 0)"
+    reps, elapsed = 0, 0.0
+    while reps < 1 or (elapsed < budget_s and reps < 3):
+        t = time.perf_counter()
+        orc.decode(*args, **kw, pairs=pairs)
+        elapsed += time.perf_counter() - t
+        reps += 1
+    frac = (n if pairs is not None else total_pairs) / total_pairs
+    sec_per_call = elapsed / reps / frac  # scaled to the whole workload
+    gbs = w.algorithmic_bytes() / sec_per_call / 1e9
+    return {"value": gbs, "unit": "GB/s", "cores": threads, "kind": "oracle",
+            "sample": f"{desc}; fp64 C oracle, {reps} repetition(s), scaled to the full call",
+            "sec_per_call": sec_per_call}
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    from paged_gqa_decode_05_gb300 import workloads
+    w = workloads.WORKLOADS[args.workload]()
+    cb = cpu_oracle_timing(w, budget_s=10.0)
+    line = {"impl": "reference", "metric": METRIC, "value": cb["value"], "unit": "GB/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": cb["sec_per_call"] * 1e3, "us_per_call": cb["sec_per_call"] * 1e6,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded N(0,1) bf16 inputs)",
+            "config": {**w.describe(), "workload": w.name, "runs_on": "host CPU cores"},
+            "cpu_baseline": {k: cb[k] for k in ("value", "unit", "cores", "kind", "sample")},
+            "e2e": {"value": cb["value"], "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args):
+    import numpy as np
+    import torch
+
+    import paged_gqa_decode_05_gb300 as pda
+    from paged_gqa_decode_05_gb300 import workloads
+
+    rank, world, local_rank = dist_env()
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    w = workloads.WORKLOADS[args.workload]()
+    bytes_per_call = w.algorithmic_bytes()
+    props = torch.cuda.get_device_properties(dev)
+    l2 = int(getattr(props, "L2_cache_size", 129 * 2 ** 20))
+    input_bytes = (w.q.nbytes + w.k_pool.nbytes + w.v_pool.nbytes + w.block_table.nbytes
+                   + w.seq_lens.nbytes)
+    n_sets = max(2, math.ceil(3 * l2 / max(input_bytes, 1)))
+
+    def to_dev(a):
+        if a.dtype == np.uint16:
+            return torch.from_numpy(a.view(np.int16)).to(dev).view(torch.bfloat16)
+        return torch.from_numpy(a).to(dev)
+
+    host = {"q": w.q, "k_pool": w.k_pool, "v_pool": w.v_pool, "block_table": w.block_table,
+            "seq_lens": w.seq_lens}
+    sets = [{k: to_dev(v) for k, v in host.items()} for _ in range(n_sets)]
+    outs = [torch.empty((w.B, w.Hq, w.D), device=dev, dtype=torch.bfloat16) for _ in range(n_sets)]
+    ctx = pda.Context(max_seqs=w.B, num_q_heads=w.Hq, num_kv_heads=w.Hkv, head_dim=w.D,
+                      block_size=w.block_size)
+    stream = torch.cuda.current_stream()
+
+    def step(i):
+        s = sets[i % n_sets]
+        ctx.decode(s["q"], s["k_pool"], s["v_pool"], s["block_table"], s["seq_lens"],
+                   out=outs[i % n_sets])
+
+    for i in range(max(3, args.warmup)):
+        step(i)
+    torch.cuda.synchronize()
+    if ctx.read_device_errors() != 0:
+        raise RuntimeError("device error flags set during warm-up")
+
+    # --- main timed region: exactly K calls, back to back
+    sampler = ClockSampler(local_rank)
+    sampler.start()
+    t_pad0 = time.time()
+    pad_end = time.time() + 0.6  # keep the GPU busy while the sampler starts
+    i = 0
+    while time.time() < pad_end:
+        step(i); i += 1
+        if i % 64 == 0:
+            torch.cuda.synchronize()
+    barrier()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for k in range(args.steps):
+        step(k)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    ms_total = e0.elapsed_time(e1)
+    pad_end = time.time() + 0.6
+    while time.time() < pad_end:
+        step(i); i += 1
+        if i % 64 == 0:
+            torch.cuda.synchronize()
+    torch.cuda.synchronize()
+    t_pad1 = time.time()
+    sampler.stop()
+    clocks = sampler.summary(t_pad0, t_pad1)
+    clocks["window"] = "timed calls plus 0.6 s of the same calls on either side"
+
+    ms_step = ms_total / args.steps
+    if world > 1:
+        import torch.distributed as dist
+        tt = torch.tensor([ms_step], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms_step = float(tt.item())
+
+    # --- kernel timing pass: events between the split and merge kernels
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+            torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    for k in range(args.steps):
+        # torch only computes elapsed times of events it recorded itself; the
+        # library re-records the same events later, and the last record wins
+        for e in evs[k]:
+            e.record(stream)
+        ctx.set_timing_events(*evs[k])
+        step(k)
+    ctx.set_timing_events(None, None, None)
+    torch.cuda.synchronize()
+    split_ms = [a.elapsed_time(b) for a, b, _ in evs]
+    merge_ms = [b.elapsed_time(c) for _, b, c in evs]
+    split_avg = statistics.mean(split_ms)
+    merge_avg = statistics.mean(merge_ms)
+    if ctx.read_device_errors() != 0:
+        raise RuntimeError("device error flags set during timing")
+
+    # --- end to end: pinned host inputs copied in, output copied back, each step
+    e2e = None
+    if not args.no_e2e:
+        pinned = {k: torch.from_numpy(v.view(np.int16) if v.dtype == np.uint16 else v).pin_memory()
+                  for k, v in host.items()}
+        out_host = torch.empty((w.B, w.Hq, w.D), dtype=torch.bfloat16).pin_memory()
+        dst = sets[0]
+        h2d = sum(t.numel() * t.element_size() for t in pinned.values())
+        d2h = out_host.numel() * out_host.element_size()
+        k_e2e = max(3, min(args.steps, 50))
+
+        def e2e_step():
+            for k, t in pinned.items():
+                d = dst[k].view(torch.int16) if dst[k].dtype == torch.bfloat16 else dst[k]
+                d.copy_(t, non_blocking=True)
+            ctx.decode(dst["q"], dst["k_pool"], dst["v_pool"], dst["block_table"], dst["seq_lens"],
+                       out=outs[0])
+            out_host.copy_(outs[0], non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize()
+        barrier()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(k_e2e):
+            e2e_step()
+        b.record(stream)
+        torch.cuda.synchronize()
+        barrier()
+        e2e_ms = a.elapsed_time(b) / k_e2e
+        if world > 1:
+            import torch.distributed as dist
+            tt = torch.tensor([e2e_ms], device=dev)
+            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+            e2e_ms = float(tt.item())
+        e2e = {"value": world * bytes_per_call / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
+               "us_per_call": e2e_ms * 1e3, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "steps": k_e2e}
+
+    peak, peak_kind = peaks()
+    value = world * bytes_per_call / (ms_step * 1e-3) / 1e9
+    achieved = bytes_per_call / (split_avg * 1e-3) / 1e9
+    info = ctx.launch_info()
+    line = {
+        "metric": METRIC,
+        "value": value,
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms_step,
+        "us_per_call": ms_step * 1e3,
+        "pct_of_hbm_peak": 100.0 * value / (world * peak),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic: seeded N(0,1) q/K/V rounded to bf16, shuffled block table",
+        "config": {**w.describe(), "workload": w.name,
+                   "l2": f"inputs larger than L2 ({input_bytes / 1e6:.0f} MB per set, "
+                         f"{n_sets} sets rotated, L2 {l2 / 2 ** 20:.0f} MiB)",
+                   "parallelism": "replicas" if world > 1 else "single GPU",
+                   "split_ctas": info["split_ctas"], "ctas_per_sm": info["ctas_per_sm"],
+                   "stages": info["stages"], "algorithmic_bytes_per_call": bytes_per_call},
+        "roofline": {"bound": "hbm", "kernel": "split_kernel", "achieved": achieved, "peak": peak,
+                     "peak_kind": f"{peak_kind} hbm_gbs (STREAM-style copy)", "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": recorded_traffic(args.workload),
+                     "split_us": split_avg * 1e3, "merge_us": merge_avg * 1e3},
+        "gpu_launches": 2 * args.steps,
+        "clocks": clocks,
+    }
+    if e2e is not None:
+        line["e2e"] = e2e
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cb = cpu_oracle_timing(w)
+        line["cpu_baseline"] = {k: cb[k] for k in ("value", "unit", "cores", "kind", "sample")}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    ctx.close()
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

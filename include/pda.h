@@ -1,0 +1,290 @@
+/*
+ * pda.h -- paged grouped-query decode attention on GB300 (sm_103a): C ABI.
+ *
+ * One query token per sequence attends over a bf16 KV cache scattered across
+ * a pool of fixed-size blocks and addressed through a per-sequence block
+ * table.  The KV walk is split into tiles; each tile keeps an fp32
+ * online-softmax state (m, l, o); a separate merge/finalize step combines the
+ * states and writes o / l as bf16.
+ *
+ * Sources (page title, then section or item):
+ *   [TA]  tiled_attention.rs (spark_storage) -- the (m, l, o) lifecycle
+ *         begin_step / step_tile / finalize, TiledAttentionDims, its
+ *         validate() checks, the state sizes and paged_strides /
+ *         scratch_pool_strides.
+ *   [CK]  AstrAI "CUDA Kernels" -- Overview (split-KV paged decode),
+ *         Python Wrappers (scale 1/sqrt(head_dim); wrappers fail loudly when
+ *         the compiled library is missing).
+ *
+ * Conventions for every call below:
+ *   - Pointers named q, k_pool, v_pool, out, tile_*, block_table, seq_lens
+ *     are DEVICE pointers owned by the caller; the library never frees them.
+ *     bf16 tensors are passed as raw 16-bit patterns (pda_bf16).
+ *   - q, k_pool, v_pool and out must be 16-byte aligned; int32 arrays
+ *     4-byte aligned.
+ *   - stream is a cudaStream_t (NULL = the legacy default stream).  Every
+ *     call that takes a stream only enqueues work and returns; argument
+ *     errors are returned at once, kernel launch errors when they are
+ *     detected at enqueue time.  Device-side data errors (a block id outside
+ *     [0, num_blocks), a length beyond the table width) never fault: they
+ *     set a flag read by pda_read_device_errors().
+ *   - All state belongs to the pda_ctx.  Calls on one context must be
+ *     ordered (one stream, or explicit events); use one context per
+ *     concurrent stream.
+ *   - Errors: every call returns a pda_status; pda_last_error() gives the
+ *     message of the last failed call on the calling thread.
+ */
+#ifndef PDA_H
+#define PDA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define PDA_ABI_VERSION 1
+
+typedef struct pda_ctx pda_ctx;
+typedef void* pda_stream;      /* cudaStream_t */
+typedef uint16_t pda_bf16;     /* bf16 bit pattern */
+typedef int32_t pda_status;
+
+enum {
+    PDA_OK = 0,
+    PDA_ERR_INVALID_ARG = 1,   /* null/misaligned pointer, bad size or stride   */
+    PDA_ERR_UNSUPPORTED = 2,   /* valid per [TA] but not built (see pda_create) */
+    PDA_ERR_CUDA = 3,          /* a CUDA runtime/driver call failed             */
+    PDA_ERR_NO_DEVICE = 4,     /* no usable sm_103 device is current            */
+    PDA_ERR_DEVICE_DATA = 5    /* pda_read_device_errors() found a flag set      */
+};
+
+/* Device-side flags (bit mask) reported by pda_read_device_errors(). */
+#define PDA_DEVERR_BAD_BLOCK_ID 0x1u  /* a listed block id was outside [0, num_blocks); that
+                                         block's rows read as zeros                       */
+#define PDA_DEVERR_BAD_LENGTH   0x2u  /* seq_len < 0, a length beyond table width * block
+                                         size, or a tile count outside [0, tile_capacity];
+                                         the length was clamped                           */
+#define PDA_DEVERR_TIMEOUT      0x4u  /* a bounded wait inside a kernel gave up (the kernel
+                                         returned early; its output is not valid)         */
+
+/*
+ * Static sizes a context is built for -- [TA] TiledAttentionDims.
+ *   max_seqs       most sequences one call may carry (>= 1).
+ *   num_q_heads    Hq; must be a multiple of num_kv_heads ([TA] validate).
+ *   num_kv_heads   Hkv.  The group size G = Hq / Hkv ([TA] gqa_ratio) must be
+ *                  1..8 in this build.  q head h reads KV head h / G.
+ *   head_dim       D; [TA] validate caps it at 256; this build has kernels for
+ *                  64, 128 and 256.
+ *   block_size     tokens per KV block: 8, 16, 32 or 64 in this build.
+ *   tile_capacity  most block ids per sequence in one pda_step_tile call.
+ */
+typedef struct pda_dims {
+    int32_t max_seqs;
+    int32_t num_q_heads;
+    int32_t num_kv_heads;
+    int32_t head_dim;
+    int32_t block_size;
+    int32_t tile_capacity;
+} pda_dims;
+
+/* Library ABI version (PDA_ABI_VERSION). Host only. */
+int32_t pda_abi_version(void);
+
+/* Static text for a status code. Host only. */
+const char* pda_status_string(pda_status status);
+
+/* Message of the last failed call on this thread ("" if none). Host only. */
+const char* pda_last_error(void);
+
+/*
+ * Checks dims without touching the GPU -- [TA] TiledAttentionDims::validate
+ * (Hq % Hkv == 0, head_dim <= 256) plus this build's supported set.
+ * Returns PDA_ERR_INVALID_ARG for dims [TA] rejects, PDA_ERR_UNSUPPORTED for
+ * dims [TA] accepts that have no kernel here.
+ */
+pda_status pda_check_dims(const pda_dims* dims);
+
+/*
+ * Element-stride triples (block, token, kv-head), in bf16 elements, of the two
+ * pool layouts -- [TA] paged_strides and scratch_pool_strides:
+ *   paged: [num_blocks, block_size, Hkv, D]        -> (bs*Hkv*D, Hkv*D, D)
+ *   slot : [slot, K|V, Hkv, block_size, D]         -> (2*Hkv*bs*D, D, bs*D)
+ * In the slot layout the V pool pointer is the K pool pointer + Hkv*bs*D.
+ * Host only; out receives 3 values.
+ */
+pda_status pda_paged_strides(const pda_dims* dims, int64_t out[3]);
+pda_status pda_slot_strides(const pda_dims* dims, int64_t out[3]);
+
+/*
+ * Creates a context on the CURRENT CUDA device -- [TA] TiledAttention::new.
+ * Allocates the fp32 running state m, l [max_seqs*Hq] and o [max_seqs*Hq*D]
+ * ([TA] m_bytes / l_bytes / o_bytes) and the split workspace; they are reused
+ * by every later call and freed by pda_destroy.  Fails with
+ * PDA_ERR_NO_DEVICE when the current device is not compute capability 10.3.
+ */
+pda_status pda_create(const pda_dims* dims, pda_ctx** out_ctx);
+
+/* Frees the context and its device buffers (synchronises the device first). */
+void pda_destroy(pda_ctx* ctx);
+
+/*
+ * One-shot decode:
+ *   out[b, h, :] = softmax(scale * q[b, h, :] . K_t) V_t  over t < seq_lens[b],
+ * where K_t / V_t is row (block_table[b, t / bs], t % bs, h / G) of k_pool /
+ * v_pool ([CK] Overview: paged split-KV decode; the result equals the
+ * finalize of [TA]'s state after all blocks).
+ *   q            [batch, Hq, D] bf16, dense.
+ *   k_pool,
+ *   v_pool       [num_blocks, block_size, Hkv, D] bf16, dense ([TA] paged layout).
+ *   block_table  [batch, max_blocks] int32; only the first
+ *                ceil(seq_lens[b] / bs) entries of row b are read.
+ *   seq_lens     [batch] int32 token counts (device); 0 gives a zero row.
+ *   scale        softmax scale; NaN selects the default 1/sqrt(D) ([CK]).
+ *   out          [batch, Hq, D] bf16, written completely.
+ *   batch        0 .. max_seqs (0 returns PDA_OK without launching).
+ * The work is split over the flattened (sequence, kv head, block) space so
+ * every SM gets an equal share, whatever the lengths; no host copy of
+ * seq_lens is needed and the call can be captured in a CUDA graph.
+ */
+pda_status pda_decode(pda_ctx* ctx, const pda_bf16* q, const pda_bf16* k_pool,
+                      const pda_bf16* v_pool, int64_t num_blocks,
+                      const int32_t* block_table, int32_t max_blocks,
+                      const int32_t* seq_lens, int32_t batch, float scale,
+                      pda_bf16* out, pda_stream stream);
+
+/*
+ * pda_decode with an explicit pool stride triple (block, token, kv-head) in
+ * bf16 elements, e.g. pda_slot_strides() -- [TA] step_tile's stride triple.
+ * Each stride must be a positive multiple of 8; rows stay D-contiguous.
+ */
+pda_status pda_decode_strided(pda_ctx* ctx, const pda_bf16* q, const pda_bf16* k_pool,
+                              const pda_bf16* v_pool, int64_t num_blocks,
+                              int64_t blk_stride, int64_t tok_stride, int64_t kvh_stride,
+                              const int32_t* block_table, int32_t max_blocks,
+                              const int32_t* seq_lens, int32_t batch, float scale,
+                              pda_bf16* out, pda_stream stream);
+
+/*
+ * Tiled lifecycle, step 1 -- [TA] begin_step: resets the running state of
+ * sequences 0..num_seqs-1 to (m, l, o) = (-inf, 0, 0).  num_seqs > max_seqs
+ * is PDA_ERR_INVALID_ARG.
+ */
+pda_status pda_begin_step(pda_ctx* ctx, int32_t num_seqs, pda_stream stream);
+
+/*
+ * Tiled lifecycle, step 2 -- [TA] step_tile: folds one tile of blocks per
+ * sequence into the running state.
+ *   tile_blocks        [num_seqs, tile_capacity] int32 block ids; sequence s
+ *                      lists tile_block_counts[s] ids (0 leaves its state as it
+ *                      is).
+ *   tile_last_valid    [num_seqs] int32 in 1..block_size: valid token slots of
+ *                      the LAST listed block of each sequence (the other
+ *                      listed blocks are full), or NULL when every listed
+ *                      block is full.  [TA] passes one scalar for all
+ *                      sequences; a per-sequence array also serves ragged
+ *                      batches in one call.
+ *   blk/tok/kvh_stride pool stride triple in bf16 elements ([TA] paged_strides
+ *                      or scratch_pool_strides); positive multiples of 8.
+ *   scale              NaN selects 1/sqrt(D).  [TA] passes no scale.
+ * Tiles of one step may be given in any order of blocks; the state after all
+ * tiles equals the one-shot result up to fp32 rounding.
+ */
+pda_status pda_step_tile(pda_ctx* ctx, const pda_bf16* q, const pda_bf16* k_pool,
+                         const pda_bf16* v_pool, int64_t num_blocks,
+                         const int32_t* tile_blocks, const int32_t* tile_block_counts,
+                         const int32_t* tile_last_valid, int32_t num_seqs,
+                         int64_t blk_stride, int64_t tok_stride, int64_t kvh_stride,
+                         float scale, pda_stream stream);
+
+/*
+ * Tiled lifecycle, step 3 -- [TA] finalize: out[s, h, :] = bf16(o / l) for
+ * s < num_seqs (round to nearest even); l == 0 (nothing folded) gives zeros.
+ * out is [num_seqs, Hq, D].  pda_finalize_f32 writes the same quotient in fp32
+ * without rounding (for comparing tiled and one-shot runs).
+ */
+pda_status pda_finalize(pda_ctx* ctx, pda_bf16* out, int32_t num_seqs, pda_stream stream);
+pda_status pda_finalize_f32(pda_ctx* ctx, float* out, int32_t num_seqs, pda_stream stream);
+
+/*
+ * One-shot decode writing the fp32 quotient o / l instead of bf16 (same
+ * arguments as pda_decode_strided; out is [batch, Hq, D] float).  Used to
+ * compare the one-shot and tiled paths before output rounding.
+ */
+pda_status pda_decode_f32(pda_ctx* ctx, const pda_bf16* q, const pda_bf16* k_pool,
+                          const pda_bf16* v_pool, int64_t num_blocks,
+                          int64_t blk_stride, int64_t tok_stride, int64_t kvh_stride,
+                          const int32_t* block_table, int32_t max_blocks,
+                          const int32_t* seq_lens, int32_t batch, float scale,
+                          float* out, pda_stream stream);
+
+/*
+ * Gather check: runs the decode kernel's own loader (block-table lookup, TMA
+ * copies into shared memory, per-stage masking) and writes every valid K and
+ * V row it staged to k_rows / v_rows, laid out [batch, Hkv, max_blocks*bs, D]
+ * bf16 (token t of sequence b, kv head g at ((b*Hkv + g)*max_blocks*bs + t)*D).
+ * Rows past seq_lens[b] are left untouched.  Same pool arguments as
+ * pda_decode_strided.
+ */
+pda_status pda_debug_gather(pda_ctx* ctx, const pda_bf16* k_pool, const pda_bf16* v_pool,
+                            int64_t num_blocks, int64_t blk_stride, int64_t tok_stride,
+                            int64_t kvh_stride, const int32_t* block_table,
+                            int32_t max_blocks, const int32_t* seq_lens, int32_t batch,
+                            pda_bf16* k_rows, pda_bf16* v_rows, pda_stream stream);
+
+/*
+ * Reads (and with clear != 0 resets) the device error flags of this context
+ * (PDA_DEVERR_* bits).  Synchronises `stream`.  Returns PDA_ERR_DEVICE_DATA
+ * when any flag was set, PDA_OK otherwise.
+ */
+pda_status pda_read_device_errors(pda_ctx* ctx, uint32_t* flags, int32_t clear,
+                                  pda_stream stream);
+
+/*
+ * Timing hook: when the three events (cudaEvent_t) are non-NULL, every later
+ * one-shot decode records ev_begin before its split kernel, ev_split after it
+ * and ev_end after the merge kernel, on the call's stream; NULLs turn it off.
+ * Recording an event between the kernels stops the merge kernel's early
+ * (programmatic) launch, so timed calls measure each kernel on its own.
+ */
+pda_status pda_set_timing_events(pda_ctx* ctx, void* ev_begin, void* ev_split, void* ev_end);
+
+/*
+ * Describes the launch the context would make (host only, after pda_create):
+ * split-kernel CTAs (a multiple of the SM count), CTAs per SM, pipeline
+ * stages, dynamic shared memory bytes per CTA and partial-state slots.
+ */
+typedef struct pda_launch_info {
+    int32_t split_ctas;
+    int32_t ctas_per_sm;
+    int32_t num_sms;
+    int32_t stages;
+    int32_t smem_bytes;
+    int32_t stage_tokens;
+    int64_t partial_slots;
+} pda_launch_info;
+pda_status pda_get_launch_info(const pda_ctx* ctx, pda_launch_info* info);
+
+/*
+ * The split plan on its own (host only; no GPU needed).  The decode kernel
+ * walks the flattened index space of W = Hkv * sum_b nb_b blocks, ordered
+ * (sequence, kv head, block), with nb_b = ceil(max(len_b, 0) / block_size)
+ * (or the tile count when blocks_given != 0).  CTA c takes blocks
+ * [floor(c*W/P), floor((c+1)*W/P)).  For unit u = b*Hkv + g this reports the
+ * first and last CTA touching it (-1, -1 when it has no blocks); a CTA's
+ * partial state for unit u goes to slot u + c.
+ *   lens        [batch] host int32 (tokens, or block counts).
+ *   first_cta,
+ *   last_cta    [batch*Hkv] outputs.
+ *   total_blocks receives W.
+ */
+pda_status pda_plan_units(const int32_t* lens, int32_t batch, int32_t blocks_given,
+                          int32_t block_size, int32_t num_kv_heads, int32_t split_ctas,
+                          int32_t* first_cta, int32_t* last_cta, int64_t* total_blocks);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PDA_H */

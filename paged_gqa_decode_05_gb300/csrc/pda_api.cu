@@ -1,0 +1,564 @@
+// pda_api.cu -- the C ABI of include/pda.h: argument checks, context and
+// workspace ownership, TMA descriptor encoding and kernel launches.
+//
+// Lifecycle and checks follow tiled_attention.rs (spark_storage):
+// TiledAttentionDims::validate (head divisibility, head_dim <= 256),
+// TiledAttention::new (state buffers sized for the maximum dims, reused),
+// begin_step (num_seqs <= max_seqs, reset to (-inf, 0, 0)), step_tile,
+// finalize.  Errors are returned as status codes, never thrown.
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include "pda.h"
+#include "pda_params.h"
+
+#define PDA_EXPORT extern "C" __attribute__((visibility("default")))
+
+namespace {
+
+thread_local std::string g_last_error;
+
+pda_status fail(pda_status st, const char* fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    g_last_error = buf;
+    return st;
+}
+
+pda_status cuda_fail(cudaError_t e, const char* what) {
+    return fail(PDA_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+}  // namespace
+
+struct pda_ctx {
+    pda_dims dims;
+    int32_t G = 0;
+    int device = 0;
+    int num_sms = 0;
+    int stages = 0;
+    int ctas_per_sm = 0;
+    int split_ctas = 0;
+    int smem_max = 0;
+    int64_t slots = 0;
+    float* part_o = nullptr;
+    float* part_ml = nullptr;
+    int32_t* pfx = nullptr;
+    uint32_t* err = nullptr;
+    float* m_state = nullptr;
+    float* l_state = nullptr;
+    float* o_state = nullptr;
+    cudaEvent_t ev_begin = nullptr, ev_split = nullptr, ev_end = nullptr;
+};
+
+namespace {
+
+struct PoolArgs {
+    const pda_bf16* k;
+    const pda_bf16* v;
+    int64_t num_blocks;
+    int64_t blk, tok, kvh;
+};
+
+pda_status encode_pool(const pda_ctx* ctx, const void* base, const PoolArgs& a, CUtensorMap* tm,
+                       int32_t* tok_dim) {
+    auto enc = tensor_map_encoder();
+    if (!enc) return fail(PDA_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+    const pda_dims& d = ctx->dims;
+    cuuint64_t dims[4];
+    cuuint64_t strides[3];
+    cuuint32_t box[4];
+    const cuuint32_t estr[4] = {1, 1, 1, 1};
+    if (a.tok >= a.kvh) {  // [.., slot, kvh, D]: kv head is the faster axis
+        dims[0] = (cuuint64_t)d.head_dim; dims[1] = (cuuint64_t)d.num_kv_heads;
+        dims[2] = (cuuint64_t)d.block_size; dims[3] = (cuuint64_t)a.num_blocks;
+        strides[0] = (cuuint64_t)a.kvh * 2; strides[1] = (cuuint64_t)a.tok * 2;
+        box[0] = 64; box[1] = 1; box[2] = (cuuint32_t)d.block_size; box[3] = 1;
+        *tok_dim = 2;
+    } else {               // [.., kvh, slot, D]: token is the faster axis
+        dims[0] = (cuuint64_t)d.head_dim; dims[1] = (cuuint64_t)d.block_size;
+        dims[2] = (cuuint64_t)d.num_kv_heads; dims[3] = (cuuint64_t)a.num_blocks;
+        strides[0] = (cuuint64_t)a.tok * 2; strides[1] = (cuuint64_t)a.kvh * 2;
+        box[0] = 64; box[1] = (cuuint32_t)d.block_size; box[2] = 1; box[3] = 1;
+        *tok_dim = 1;
+    }
+    strides[2] = (cuuint64_t)a.blk * 2;
+    CUresult r = enc(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides,
+                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+        return fail(PDA_ERR_INVALID_ARG, "cuTensorMapEncodeTiled rejected the pool layout (CUresult %d)",
+                    (int)r);
+    return PDA_OK;
+}
+
+pda_status check_pool(const pda_ctx* ctx, const PoolArgs& a) {
+    if (!a.k || !a.v) return fail(PDA_ERR_INVALID_ARG, "k_pool / v_pool must not be NULL");
+    if (!aligned(a.k, 16) || !aligned(a.v, 16))
+        return fail(PDA_ERR_INVALID_ARG, "k_pool / v_pool must be 16-byte aligned");
+    if (a.num_blocks < 1 || a.num_blocks > INT32_MAX)
+        return fail(PDA_ERR_INVALID_ARG, "num_blocks %lld outside [1, 2^31)", (long long)a.num_blocks);
+    const int64_t s[3] = {a.blk, a.tok, a.kvh};
+    for (int i = 0; i < 3; ++i)
+        if (s[i] <= 0 || s[i] % 8 != 0 || s[i] >= (int64_t(1) << 38))
+            return fail(PDA_ERR_INVALID_ARG,
+                        "pool strides must be positive multiples of 8 elements (got %lld, %lld, %lld)",
+                        (long long)a.blk, (long long)a.tok, (long long)a.kvh);
+    (void)ctx;
+    return PDA_OK;
+}
+
+pda_status check_scale(float scale, int D, float* scale_log2) {
+    if (std::isnan(scale)) scale = 1.0f / std::sqrt((float)D);
+    if (std::isinf(scale)) return fail(PDA_ERR_INVALID_ARG, "scale must be finite (NaN = default)");
+    *scale_log2 = scale * kLog2e;
+    return PDA_OK;
+}
+
+struct RunArgs {
+    int mode;
+    const pda_bf16* q;
+    PoolArgs pool;
+    const int32_t* table;
+    int32_t table_stride;
+    const int32_t* lens;
+    int32_t lens_are_blocks;
+    const int32_t* last_valid;
+    int32_t batch;
+    float scale;
+    pda_bf16* out;
+    float* out_f32;
+    pda_bf16* dbg_k;
+    pda_bf16* dbg_v;
+    cudaStream_t stream;
+};
+
+pda_status run(pda_ctx* ctx, const RunArgs& r) {
+    if (!ctx) return fail(PDA_ERR_INVALID_ARG, "ctx is NULL");
+    const pda_dims& d = ctx->dims;
+    if (r.batch < 0 || r.batch > d.max_seqs)
+        return fail(PDA_ERR_INVALID_ARG, "batch %d outside [0, max_seqs=%d]", r.batch, d.max_seqs);
+    if (r.batch == 0) return PDA_OK;
+    pda_status st = check_pool(ctx, r.pool);
+    if (st != PDA_OK) return st;
+    if (r.mode != pda::kGather) {
+        if (!r.q || !aligned(r.q, 16)) return fail(PDA_ERR_INVALID_ARG, "q must be non-NULL and 16-byte aligned");
+    }
+    if (r.mode == pda::kOneShot) {
+        if (r.out_f32 ? !aligned(r.out_f32, 16) : (!r.out || !aligned(r.out, 16)))
+            return fail(PDA_ERR_INVALID_ARG, "out must be non-NULL and 16-byte aligned");
+    }
+    if (r.mode == pda::kGather && (!r.dbg_k || !r.dbg_v || !aligned(r.dbg_k, 16) || !aligned(r.dbg_v, 16)))
+        return fail(PDA_ERR_INVALID_ARG, "k_rows / v_rows must be non-NULL and 16-byte aligned");
+    if (!r.table || !r.lens || !aligned(r.table, 4) || !aligned(r.lens, 4) ||
+        (r.last_valid && !aligned(r.last_valid, 4)))
+        return fail(PDA_ERR_INVALID_ARG, "table / length arrays must be non-NULL and 4-byte aligned");
+    if (r.table_stride < 1)
+        return fail(PDA_ERR_INVALID_ARG, "block table width must be >= 1 (got %d)", r.table_stride);
+    float scale_log2 = 0.f;
+    st = check_scale(r.scale, d.head_dim, &scale_log2);
+    if (st != PDA_OK) return st;
+
+    pda::SplitParams p;
+    std::memset(&p, 0, sizeof p);
+    int32_t tok_dim_k = 0, tok_dim_v = 0;
+    st = encode_pool(ctx, r.pool.k, r.pool, &p.tm_k, &tok_dim_k);
+    if (st != PDA_OK) return st;
+    st = encode_pool(ctx, r.pool.v, r.pool, &p.tm_v, &tok_dim_v);
+    if (st != PDA_OK) return st;
+
+    const int32_t Hq = d.num_q_heads, Hkv = d.num_kv_heads, D = d.head_dim;
+    const bool timing = ctx->ev_begin && ctx->ev_split && ctx->ev_end && r.mode == pda::kOneShot;
+    const int64_t dbg_row_tokens = (int64_t)r.table_stride * d.block_size;
+    for (int32_t c0 = 0; c0 < r.batch; c0 += pda::kMaxLaunchBatch) {
+        const int32_t cb = std::min(pda::kMaxLaunchBatch, r.batch - c0);
+        p.q = r.q ? r.q + (int64_t)c0 * Hq * D : nullptr;
+        p.table = r.table + (int64_t)c0 * r.table_stride;
+        p.lens = r.lens + c0;
+        p.last_valid = r.last_valid ? r.last_valid + c0 : nullptr;
+        p.out = r.out ? r.out + (int64_t)c0 * Hq * D : nullptr;
+        p.out_f32 = r.out_f32 ? r.out_f32 + (int64_t)c0 * Hq * D : nullptr;
+        p.part_o = ctx->part_o;
+        p.part_ml = ctx->part_ml;
+        p.pfx = ctx->pfx;
+        p.err = ctx->err;
+        p.dbg_k = r.dbg_k ? r.dbg_k + (int64_t)c0 * Hkv * dbg_row_tokens * D : nullptr;
+        p.dbg_v = r.dbg_v ? r.dbg_v + (int64_t)c0 * Hkv * dbg_row_tokens * D : nullptr;
+        p.num_blocks = r.pool.num_blocks;
+        p.table_stride = r.table_stride;
+        p.lens_are_blocks = r.lens_are_blocks;
+        p.B = cb;
+        p.Hq = Hq;
+        p.Hkv = Hkv;
+        p.G = ctx->G;
+        p.bs = d.block_size;
+        p.tok_dim = tok_dim_k;
+        p.dbg_row_tokens = (int32_t)dbg_row_tokens;
+        p.scale_log2 = scale_log2;
+        const size_t smem = pda::smem_layout(D, ctx->stages, ctx->G, cb).total;
+
+        cudaError_t e;
+        if (timing && c0 == 0 && (e = cudaEventRecord(ctx->ev_begin, r.stream)) != cudaSuccess)
+            return cuda_fail(e, "cudaEventRecord");
+        e = pda::launch_split(D, r.mode, p, ctx->split_ctas, smem, r.stream);
+        if (e != cudaSuccess) return cuda_fail(e, "split kernel launch");
+        if (r.mode == pda::kGather) continue;
+        if (timing && (e = cudaEventRecord(ctx->ev_split, r.stream)) != cudaSuccess)
+            return cuda_fail(e, "cudaEventRecord");
+        pda::MergeParams mp;
+        std::memset(&mp, 0, sizeof mp);
+        mp.part_o = ctx->part_o;
+        mp.part_ml = ctx->part_ml;
+        mp.pfx = ctx->pfx;
+        mp.out = p.out;
+        mp.out_f32 = p.out_f32;
+        mp.m_state = ctx->m_state + (int64_t)c0 * Hq;
+        mp.l_state = ctx->l_state + (int64_t)c0 * Hq;
+        mp.o_state = ctx->o_state + (int64_t)c0 * Hq * D;
+        mp.B = cb;
+        mp.Hq = Hq;
+        mp.Hkv = Hkv;
+        mp.G = ctx->G;
+        mp.D = D;
+        mp.split_ctas = ctx->split_ctas;
+        e = pda::launch_merge(r.mode, mp, !timing, r.stream);
+        if (e != cudaSuccess) return cuda_fail(e, "merge kernel launch");
+        if (timing && (e = cudaEventRecord(ctx->ev_end, r.stream)) != cudaSuccess)
+            return cuda_fail(e, "cudaEventRecord");
+    }
+    return PDA_OK;
+}
+
+}  // namespace
+
+PDA_EXPORT int32_t pda_abi_version(void) { return PDA_ABI_VERSION; }
+
+PDA_EXPORT const char* pda_status_string(pda_status s) {
+    switch (s) {
+        case PDA_OK: return "ok";
+        case PDA_ERR_INVALID_ARG: return "invalid argument";
+        case PDA_ERR_UNSUPPORTED: return "unsupported configuration";
+        case PDA_ERR_CUDA: return "CUDA error";
+        case PDA_ERR_NO_DEVICE: return "no usable sm_103 device";
+        case PDA_ERR_DEVICE_DATA: return "device-side data error flagged";
+        default: return "unknown status";
+    }
+}
+
+PDA_EXPORT const char* pda_last_error(void) { return g_last_error.c_str(); }
+
+PDA_EXPORT pda_status pda_check_dims(const pda_dims* d) {
+    if (!d) return fail(PDA_ERR_INVALID_ARG, "dims is NULL");
+    if (d->max_seqs < 1 || d->num_q_heads < 1 || d->num_kv_heads < 1 || d->head_dim < 1 ||
+        d->block_size < 1 || d->tile_capacity < 1)
+        return fail(PDA_ERR_INVALID_ARG, "every dim must be >= 1");
+    // The check of TiledAttentionDims::validate (its message words the
+    // divisibility the other way round; the check is what counts).
+    if (d->num_q_heads % d->num_kv_heads != 0)
+        return fail(PDA_ERR_INVALID_ARG, "num_kv_heads (%d) must divide num_q_heads (%d)",
+                    d->num_kv_heads, d->num_q_heads);
+    if (d->head_dim > 256)
+        return fail(PDA_ERR_INVALID_ARG, "head_dim %d exceeds the maximum of 256", d->head_dim);
+    if (d->head_dim != 64 && d->head_dim != 128 && d->head_dim != 256)
+        return fail(PDA_ERR_UNSUPPORTED, "head_dim %d: kernels exist for 64, 128 and 256", d->head_dim);
+    const int bs = d->block_size;
+    if (bs != 8 && bs != 16 && bs != 32 && bs != 64)
+        return fail(PDA_ERR_UNSUPPORTED, "block_size %d: kernels exist for 8, 16, 32 and 64", bs);
+    const int G = d->num_q_heads / d->num_kv_heads;
+    if (G > pda::kMaxGroup)
+        return fail(PDA_ERR_UNSUPPORTED, "group size %d: at most %d q heads per kv head", G, pda::kMaxGroup);
+    return PDA_OK;
+}
+
+PDA_EXPORT pda_status pda_paged_strides(const pda_dims* d, int64_t out[3]) {
+    if (!d || !out) return fail(PDA_ERR_INVALID_ARG, "NULL argument");
+    out[0] = (int64_t)d->block_size * d->num_kv_heads * d->head_dim;
+    out[1] = (int64_t)d->num_kv_heads * d->head_dim;
+    out[2] = d->head_dim;
+    return PDA_OK;
+}
+
+PDA_EXPORT pda_status pda_slot_strides(const pda_dims* d, int64_t out[3]) {
+    if (!d || !out) return fail(PDA_ERR_INVALID_ARG, "NULL argument");
+    const int64_t stripe = (int64_t)d->num_kv_heads * d->block_size * d->head_dim;
+    out[0] = 2 * stripe;
+    out[1] = d->head_dim;
+    out[2] = (int64_t)d->block_size * d->head_dim;
+    return PDA_OK;
+}
+
+PDA_EXPORT void pda_destroy(pda_ctx* ctx) {
+    if (!ctx) return;
+    int prev = -1;
+    cudaGetDevice(&prev);
+    if (prev != ctx->device) cudaSetDevice(ctx->device);
+    cudaDeviceSynchronize();
+    cudaFree(ctx->part_o);
+    cudaFree(ctx->part_ml);
+    cudaFree(ctx->pfx);
+    cudaFree(ctx->err);
+    cudaFree(ctx->m_state);
+    cudaFree(ctx->l_state);
+    cudaFree(ctx->o_state);
+    if (prev >= 0 && prev != ctx->device) cudaSetDevice(prev);
+    delete ctx;
+}
+
+PDA_EXPORT pda_status pda_create(const pda_dims* dims, pda_ctx** out_ctx) {
+    if (!out_ctx) return fail(PDA_ERR_INVALID_ARG, "out_ctx is NULL");
+    *out_ctx = nullptr;
+    pda_status st = pda_check_dims(dims);
+    if (st != PDA_OK) return st;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return fail(PDA_ERR_NO_DEVICE, "no CUDA device: %s", cudaGetErrorString(e));
+    cudaDeviceProp prop;
+    if ((e = cudaGetDeviceProperties(&prop, dev)) != cudaSuccess) return cuda_fail(e, "cudaGetDeviceProperties");
+    if (prop.major != 10 || prop.minor != 3)
+        return fail(PDA_ERR_NO_DEVICE, "device %d is sm_%d%d; this library is built for sm_103a", dev,
+                    prop.major, prop.minor);
+    if (!tensor_map_encoder()) return fail(PDA_ERR_CUDA, "cuTensorMapEncodeTiled is not available");
+
+    pda_ctx* ctx = new pda_ctx();
+    ctx->dims = *dims;
+    ctx->G = dims->num_q_heads / dims->num_kv_heads;
+    ctx->device = dev;
+    ctx->num_sms = prop.multiProcessorCount;
+    const int D = dims->head_dim;
+    ctx->stages = pda::split_stages(D);
+    const int chunk_b = std::min(dims->max_seqs, pda::kMaxLaunchBatch);
+    ctx->smem_max = (int)pda::smem_layout(D, ctx->stages, ctx->G, chunk_b).total;
+    if (ctx->smem_max > (int)prop.sharedMemPerBlockOptin) {
+        delete ctx;
+        return fail(PDA_ERR_UNSUPPORTED, "needs %d bytes of shared memory per CTA (device allows %d)",
+                    ctx->smem_max, (int)prop.sharedMemPerBlockOptin);
+    }
+    for (int mode = 0; mode < 3; ++mode) {
+        e = cudaFuncSetAttribute(pda::split_kernel_fn(D, mode), cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 ctx->smem_max);
+        if (e != cudaSuccess) { delete ctx; return cuda_fail(e, "cudaFuncSetAttribute"); }
+    }
+    int per_sm = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, pda::split_kernel_fn(D, pda::kOneShot),
+                                                      pda::kThreads, ctx->smem_max);
+    if (e != cudaSuccess) { delete ctx; return cuda_fail(e, "occupancy query"); }
+    if (per_sm < 1) { delete ctx; return fail(PDA_ERR_UNSUPPORTED, "split kernel does not fit on an SM"); }
+    ctx->ctas_per_sm = per_sm;
+    ctx->split_ctas = per_sm * ctx->num_sms;
+    ctx->slots = (int64_t)chunk_b * dims->num_kv_heads + ctx->split_ctas;
+
+    const int64_t nq = (int64_t)dims->max_seqs * dims->num_q_heads;
+    struct { void** ptr; size_t bytes; } allocs[] = {
+        {(void**)&ctx->part_o, (size_t)ctx->slots * ctx->G * D * sizeof(float)},
+        {(void**)&ctx->part_ml, (size_t)ctx->slots * ctx->G * 2 * sizeof(float)},
+        {(void**)&ctx->pfx, (size_t)(pda::kMaxLaunchBatch + 1) * sizeof(int32_t)},
+        {(void**)&ctx->err, sizeof(uint32_t)},
+        {(void**)&ctx->m_state, (size_t)nq * sizeof(float)},
+        {(void**)&ctx->l_state, (size_t)nq * sizeof(float)},
+        {(void**)&ctx->o_state, (size_t)nq * D * sizeof(float)},
+    };
+    for (auto& a : allocs) {
+        e = cudaMalloc(a.ptr, a.bytes);
+        if (e != cudaSuccess) { pda_destroy(ctx); return cuda_fail(e, "cudaMalloc"); }
+    }
+    if ((e = cudaMemset(ctx->err, 0, sizeof(uint32_t))) != cudaSuccess) {
+        pda_destroy(ctx);
+        return cuda_fail(e, "cudaMemset");
+    }
+    // An empty running state until the first begin_step.
+    e = pda::launch_reset_state(ctx->m_state, ctx->l_state, ctx->o_state, nq, D, nullptr);
+    if (e == cudaSuccess) e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) { pda_destroy(ctx); return cuda_fail(e, "state reset"); }
+    *out_ctx = ctx;
+    return PDA_OK;
+}
+
+PDA_EXPORT pda_status pda_decode_strided(pda_ctx* ctx, const pda_bf16* q, const pda_bf16* k_pool,
+                                         const pda_bf16* v_pool, int64_t num_blocks,
+                                         int64_t blk_stride, int64_t tok_stride, int64_t kvh_stride,
+                                         const int32_t* block_table, int32_t max_blocks,
+                                         const int32_t* seq_lens, int32_t batch, float scale,
+                                         pda_bf16* out, pda_stream stream) {
+    RunArgs r = {pda::kOneShot, q, {k_pool, v_pool, num_blocks, blk_stride, tok_stride, kvh_stride},
+                 block_table, max_blocks, seq_lens, 0, nullptr, batch, scale, out, nullptr,
+                 nullptr, nullptr, (cudaStream_t)stream};
+    return run(ctx, r);
+}
+
+PDA_EXPORT pda_status pda_decode(pda_ctx* ctx, const pda_bf16* q, const pda_bf16* k_pool,
+                                 const pda_bf16* v_pool, int64_t num_blocks,
+                                 const int32_t* block_table, int32_t max_blocks,
+                                 const int32_t* seq_lens, int32_t batch, float scale, pda_bf16* out,
+                                 pda_stream stream) {
+    if (!ctx) return fail(PDA_ERR_INVALID_ARG, "ctx is NULL");
+    int64_t s[3];
+    pda_paged_strides(&ctx->dims, s);
+    return pda_decode_strided(ctx, q, k_pool, v_pool, num_blocks, s[0], s[1], s[2], block_table,
+                              max_blocks, seq_lens, batch, scale, out, stream);
+}
+
+PDA_EXPORT pda_status pda_decode_f32(pda_ctx* ctx, const pda_bf16* q, const pda_bf16* k_pool,
+                                     const pda_bf16* v_pool, int64_t num_blocks, int64_t blk_stride,
+                                     int64_t tok_stride, int64_t kvh_stride,
+                                     const int32_t* block_table, int32_t max_blocks,
+                                     const int32_t* seq_lens, int32_t batch, float scale, float* out,
+                                     pda_stream stream) {
+    if (!out && batch > 0) return fail(PDA_ERR_INVALID_ARG, "out is NULL");
+    RunArgs r = {pda::kOneShot, q, {k_pool, v_pool, num_blocks, blk_stride, tok_stride, kvh_stride},
+                 block_table, max_blocks, seq_lens, 0, nullptr, batch, scale, nullptr, out,
+                 nullptr, nullptr, (cudaStream_t)stream};
+    return run(ctx, r);
+}
+
+PDA_EXPORT pda_status pda_begin_step(pda_ctx* ctx, int32_t num_seqs, pda_stream stream) {
+    if (!ctx) return fail(PDA_ERR_INVALID_ARG, "ctx is NULL");
+    if (num_seqs < 0 || num_seqs > ctx->dims.max_seqs)
+        return fail(PDA_ERR_INVALID_ARG, "begin_step num_seqs %d > max_seqs %d", num_seqs,
+                    ctx->dims.max_seqs);
+    cudaError_t e = pda::launch_reset_state(ctx->m_state, ctx->l_state, ctx->o_state,
+                                            (int64_t)num_seqs * ctx->dims.num_q_heads,
+                                            ctx->dims.head_dim, (cudaStream_t)stream);
+    return e == cudaSuccess ? PDA_OK : cuda_fail(e, "state reset launch");
+}
+
+PDA_EXPORT pda_status pda_step_tile(pda_ctx* ctx, const pda_bf16* q, const pda_bf16* k_pool,
+                                    const pda_bf16* v_pool, int64_t num_blocks,
+                                    const int32_t* tile_blocks, const int32_t* tile_block_counts,
+                                    const int32_t* tile_last_valid, int32_t num_seqs,
+                                    int64_t blk_stride, int64_t tok_stride, int64_t kvh_stride,
+                                    float scale, pda_stream stream) {
+    if (!ctx) return fail(PDA_ERR_INVALID_ARG, "ctx is NULL");
+    RunArgs r = {pda::kTiled, q, {k_pool, v_pool, num_blocks, blk_stride, tok_stride, kvh_stride},
+                 tile_blocks, ctx->dims.tile_capacity, tile_block_counts, 1, tile_last_valid,
+                 num_seqs, scale, nullptr, nullptr, nullptr, nullptr, (cudaStream_t)stream};
+    return run(ctx, r);
+}
+
+static pda_status finalize_impl(pda_ctx* ctx, pda_bf16* out, float* out_f32, int32_t num_seqs,
+                                pda_stream stream) {
+    if (!ctx) return fail(PDA_ERR_INVALID_ARG, "ctx is NULL");
+    if (num_seqs < 0 || num_seqs > ctx->dims.max_seqs)
+        return fail(PDA_ERR_INVALID_ARG, "finalize num_seqs %d outside [0, max_seqs=%d]", num_seqs,
+                    ctx->dims.max_seqs);
+    if (num_seqs == 0) return PDA_OK;
+    if (out_f32 ? !aligned(out_f32, 4) : (!out || !aligned(out, 2)))
+        return fail(PDA_ERR_INVALID_ARG, "out must be non-NULL and aligned");
+    cudaError_t e = pda::launch_finalize(ctx->l_state, ctx->o_state, out, out_f32,
+                                         (int64_t)num_seqs * ctx->dims.num_q_heads,
+                                         ctx->dims.head_dim, (cudaStream_t)stream);
+    return e == cudaSuccess ? PDA_OK : cuda_fail(e, "finalize launch");
+}
+
+PDA_EXPORT pda_status pda_finalize(pda_ctx* ctx, pda_bf16* out, int32_t num_seqs, pda_stream stream) {
+    if (!out && num_seqs > 0) return fail(PDA_ERR_INVALID_ARG, "out is NULL");
+    return finalize_impl(ctx, out, nullptr, num_seqs, stream);
+}
+
+PDA_EXPORT pda_status pda_finalize_f32(pda_ctx* ctx, float* out, int32_t num_seqs, pda_stream stream) {
+    if (!out && num_seqs > 0) return fail(PDA_ERR_INVALID_ARG, "out is NULL");
+    return finalize_impl(ctx, nullptr, out, num_seqs, stream);
+}
+
+PDA_EXPORT pda_status pda_debug_gather(pda_ctx* ctx, const pda_bf16* k_pool, const pda_bf16* v_pool,
+                                       int64_t num_blocks, int64_t blk_stride, int64_t tok_stride,
+                                       int64_t kvh_stride, const int32_t* block_table,
+                                       int32_t max_blocks, const int32_t* seq_lens, int32_t batch,
+                                       pda_bf16* k_rows, pda_bf16* v_rows, pda_stream stream) {
+    RunArgs r = {pda::kGather, nullptr, {k_pool, v_pool, num_blocks, blk_stride, tok_stride, kvh_stride},
+                 block_table, max_blocks, seq_lens, 0, nullptr, batch, NAN, nullptr, nullptr,
+                 k_rows, v_rows, (cudaStream_t)stream};
+    return run(ctx, r);
+}
+
+PDA_EXPORT pda_status pda_read_device_errors(pda_ctx* ctx, uint32_t* flags, int32_t clear,
+                                             pda_stream stream) {
+    if (!ctx || !flags) return fail(PDA_ERR_INVALID_ARG, "NULL argument");
+    cudaStream_t s = (cudaStream_t)stream;
+    uint32_t v = 0;
+    cudaError_t e = cudaMemcpyAsync(&v, ctx->err, sizeof v, cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e == cudaSuccess && clear) {
+        e = cudaMemsetAsync(ctx->err, 0, sizeof(uint32_t), s);
+        if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    }
+    if (e != cudaSuccess) return cuda_fail(e, "reading device error flags");
+    *flags = v;
+    if (v) return fail(PDA_ERR_DEVICE_DATA, "device error flags 0x%x", v);
+    return PDA_OK;
+}
+
+PDA_EXPORT pda_status pda_set_timing_events(pda_ctx* ctx, void* ev_begin, void* ev_split, void* ev_end) {
+    if (!ctx) return fail(PDA_ERR_INVALID_ARG, "ctx is NULL");
+    ctx->ev_begin = (cudaEvent_t)ev_begin;
+    ctx->ev_split = (cudaEvent_t)ev_split;
+    ctx->ev_end = (cudaEvent_t)ev_end;
+    return PDA_OK;
+}
+
+PDA_EXPORT pda_status pda_get_launch_info(const pda_ctx* ctx, pda_launch_info* info) {
+    if (!ctx || !info) return fail(PDA_ERR_INVALID_ARG, "NULL argument");
+    info->split_ctas = ctx->split_ctas;
+    info->ctas_per_sm = ctx->ctas_per_sm;
+    info->num_sms = ctx->num_sms;
+    info->stages = ctx->stages;
+    info->smem_bytes = ctx->smem_max;
+    info->stage_tokens = pda::kStageTokens;
+    info->partial_slots = ctx->slots;
+    return PDA_OK;
+}
+
+PDA_EXPORT pda_status pda_plan_units(const int32_t* lens, int32_t batch, int32_t blocks_given,
+                                     int32_t block_size, int32_t num_kv_heads, int32_t split_ctas,
+                                     int32_t* first_cta, int32_t* last_cta, int64_t* total_blocks) {
+    if (batch < 0 || block_size < 1 || num_kv_heads < 1 || split_ctas < 1 ||
+        (batch > 0 && (!lens || !first_cta || !last_cta)) || !total_blocks)
+        return fail(PDA_ERR_INVALID_ARG, "bad plan arguments");
+    int64_t sum = 0;
+    for (int32_t b = 0; b < batch; ++b)
+        sum += blocks_given ? std::max(lens[b], 0) : pda::blocks_for_tokens(lens[b], block_size);
+    const int64_t W = sum * num_kv_heads, P = split_ctas;
+    *total_blocks = W;
+    int64_t pfx = 0;
+    for (int32_t b = 0; b < batch; ++b) {
+        const int32_t nb = blocks_given ? std::max(lens[b], 0) : pda::blocks_for_tokens(lens[b], block_size);
+        for (int32_t g = 0; g < num_kv_heads; ++g) {
+            const int64_t u = (int64_t)b * num_kv_heads + g;
+            if (nb == 0) {
+                first_cta[u] = last_cta[u] = -1;
+                continue;
+            }
+            const int64_t su = pfx * num_kv_heads + (int64_t)g * nb;
+            first_cta[u] = (int32_t)pda::cta_of_block(su, W, P);
+            last_cta[u] = (int32_t)pda::cta_of_block(su + nb - 1, W, P);
+        }
+        pfx += nb;
+    }
+    return PDA_OK;
+}

@@ -1,0 +1,616 @@
+// pda_kernels.cuh -- split-KV paged GQA decode kernels for sm_103a.
+//
+// Split kernel (one persistent CTA per resident slot; grid = SMs x CTAs/SM):
+//   * warp 4, lane 0 is the producer: it walks the CTA's share of the
+//     flattened (sequence, kv head, block) space (pda_plan.h), looks every
+//     block up in the block table and copies whole K/V block rows of one kv
+//     head into a ring of shared-memory stages with 4-D TMA tensor copies
+//     (128-byte swizzle), plus the group's q rows with one bulk copy at the
+//     start of each segment.  Stage completion is tracked by mbarriers.
+//   * warps 0..3 consume a stage of 64 rows, 16 rows each.  The GQA group
+//     (G <= 8 q heads of one kv head) shares every K/V load: S^T = K q^T is a
+//     16x8 tile per warp (mma.sync m16n8k16, tokens as M, heads as N), the
+//     online-softmax update runs on the accumulator fragments (warp-shuffle
+//     max over tokens), P is transposed in registers (movmatrix) and
+//     O^T += V^T P^T accumulates over D in 16-row slabs.
+//   * at the end of a segment the four warp states are merged in shared
+//     memory; a segment that covers its whole unit writes bf16 o / l
+//     directly, others write an fp32 partial (m, l, o) state.
+// Merge kernel: combines the partial states of every unit split across CTAs
+// and writes o / l (one-shot), or folds them into the running state (tiled).
+//
+// Method sources: tiled_attention.rs (spark_storage) for the (m, l, o) state,
+// its reset values and o / l finalize; AstrAI "CUDA Kernels" (Overview:
+// split-KV paged decode with MMA) for splitting the KV walk.  Scores are kept
+// in base-2 units (scale * log2 e folded in), an exact rewrite of exp().
+#pragma once
+
+#include "pda_params.h"
+#include "pda_ptx.cuh"
+
+namespace pda {
+
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // each mbarrier wait gives up after 2 s
+#define kNegInf (-__int_as_float(0x7f800000))
+
+#define PDA_DEVERR_BAD_BLOCK_ID_ 0x1u
+#define PDA_DEVERR_BAD_LENGTH_ 0x2u
+#define PDA_DEVERR_TIMEOUT_ 0x4u
+
+template <int D>
+struct Cfg {
+    static constexpr int kHalves = D / 64;               // 64-column swizzled slabs per row
+    static constexpr int kTileBytes = kHalves * kHalfBytes;
+    static constexpr int kStageBytes = 2 * kTileBytes + 16 * D;
+    static constexpr int kStages = D == 64 ? 6 : (D == 128 ? 4 : 2);
+    static constexpr int kKSteps = D / 16;
+};
+
+// Blocks of sequence b, validated and clamped (flags bad lengths).
+__device__ __forceinline__ int32_t seq_blocks(const SplitParams& p, int b) {
+    int32_t len = p.lens[b];
+    if (p.lens_are_blocks) {
+        if (len < 0 || len > p.table_stride) {
+            atomicOr(p.err, PDA_DEVERR_BAD_LENGTH_);
+            len = len < 0 ? 0 : p.table_stride;
+        }
+        return len;
+    }
+    if (len < 0) {
+        atomicOr(p.err, PDA_DEVERR_BAD_LENGTH_);
+        len = 0;
+    }
+    int32_t nb = blocks_for_tokens(len, p.bs);
+    if (nb > p.table_stride) {
+        atomicOr(p.err, PDA_DEVERR_BAD_LENGTH_);
+        nb = p.table_stride;
+    }
+    return nb;
+}
+
+// Valid slots of sequence b's last block (1..bs).
+__device__ __forceinline__ int32_t last_block_slots(const SplitParams& p, int b, int32_t nb) {
+    if (p.lens_are_blocks) {
+        if (p.last_valid == nullptr) return p.bs;
+        int32_t v = p.last_valid[b];
+        if (v < 1 || v > p.bs) {
+            atomicOr(p.err, PDA_DEVERR_BAD_LENGTH_);
+            v = v < 1 ? 1 : p.bs;
+        }
+        return v;
+    }
+    int32_t v = p.lens[b] - (nb - 1) * p.bs;
+    return v > p.bs ? p.bs : v;
+}
+
+// Exclusive prefix of blocks per sequence into shared pfx[0..B].
+__device__ __forceinline__ void build_prefix(const SplitParams& p, int32_t* pfx, int32_t* scan) {
+    const int tid = threadIdx.x;
+    const int per = (p.B + kThreads - 1) / kThreads;
+    const int lo = min(p.B, tid * per), hi = min(p.B, lo + per);
+    int32_t sum = 0;
+    for (int b = lo; b < hi; ++b) sum += seq_blocks(p, b);
+    scan[tid] = sum;
+    __syncthreads();
+    if (tid == 0) {
+        int32_t run = 0;
+        for (int i = 0; i < kThreads; ++i) {
+            const int32_t v = scan[i];
+            scan[i] = run;
+            run += v;
+        }
+        pfx[p.B] = run;
+    }
+    __syncthreads();
+    int32_t run = scan[tid];
+    for (int b = lo; b < hi; ++b) {
+        pfx[b] = run;
+        run += seq_blocks(p, b);
+    }
+    __syncthreads();
+}
+
+// ------------------------------------------------------------------ producer
+
+template <int D, int MODE>
+__device__ __forceinline__ void run_producer(const SplitParams& p, uint32_t base_s, const SmemLayout& L,
+                                             const int32_t* pfx, StageMeta* meta,
+                                             volatile int* abort_flag, int64_t begin, int64_t end) {
+    using C = Cfg<D>;
+    constexpr int S = C::kStages;
+    const uint32_t full0 = base_s + L.bars, empty0 = full0 + 8 * S;
+    const uint64_t pol = policy_evict_first();
+    const int bs = p.bs, Hkv = p.Hkv;
+    const int NB = kStageTokens / bs;
+    prefetch_tensormap(&p.tm_k);
+    prefetch_tensormap(&p.tm_v);
+
+    int stage = 0;
+    uint32_t phase = 0;
+    uint32_t issued = 0, issued_parity = 0;  // per-stage bits, for the drain after an abort
+    bool ok = true;
+
+    int64_t pos = begin;
+    int b = 0, kvh = 0;
+    int32_t j = 0, nb = 0;
+    if (pos < end) {
+        int lo = 0, hi = p.B - 1;  // largest b with pfx[b]*Hkv <= pos
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if ((int64_t)pfx[mid] * Hkv <= pos) lo = mid; else hi = mid - 1;
+        }
+        b = lo;
+        nb = pfx[b + 1] - pfx[b];
+        const int64_t rem = pos - (int64_t)pfx[b] * Hkv;
+        kvh = (int)(rem / nb);
+        j = (int32_t)(rem % nb);
+    }
+    bool seg_begin = true;
+    bool whole = false;
+    while (pos < end) {
+        if (*abort_flag) { ok = false; break; }
+        const int32_t n = (int32_t)min((int64_t)min(NB, nb - j), end - pos);
+        const bool unit_end = (j + n == nb);
+        const bool seg_end = unit_end || (pos + n == end);
+        if (seg_begin) whole = (j == 0) && ((int64_t)pfx[b] * Hkv + (int64_t)(kvh + 1) * nb <= end);
+
+        if (!mbar_wait_bounded(empty0 + 8 * stage, phase ^ 1u, kWaitLimitNs)) { ok = false; break; }
+
+        const int32_t lastv = unit_end ? last_block_slots(p, b, nb) : bs;
+        StageMeta m;
+        m.b = b;
+        m.kvh = kvh;
+        m.n_valid = (n - 1) * bs + lastv;
+        m.flags = (seg_begin ? kSegBegin : 0) | (seg_end ? kSegEnd : 0) | (whole ? kWholeUnit : 0);
+        m.slot = b * Hkv + kvh + (int)blockIdx.x;
+        m.j0 = j;
+        m.pad0 = m.pad1 = 0;
+        meta[stage] = m;
+
+        const bool load_q = seg_begin && MODE != kGather;
+        const uint32_t bytes = (uint32_t)n * 2u * (uint32_t)bs * D * 2u +
+                               (load_q ? (uint32_t)(p.G * D * 2) : 0u);
+        const uint32_t full = full0 + 8 * stage;
+        mbar_arrive_expect_tx(full, bytes);
+        const uint32_t sK = base_s + (uint32_t)stage * C::kStageBytes;
+        const uint32_t sV = sK + C::kTileBytes;
+        const int32_t* row = p.table + (int64_t)b * p.table_stride;
+        for (int i = 0; i < n; ++i) {
+            int32_t blk = row[j + i];
+            if (blk < 0 || (int64_t)blk >= p.num_blocks) {
+                atomicOr(p.err, PDA_DEVERR_BAD_BLOCK_ID_);
+                blk = 0;  // stays in bounds; the flag marks the result invalid
+            }
+            const int32_t c1 = p.tok_dim == 2 ? kvh : 0;
+            const int32_t c2 = p.tok_dim == 2 ? 0 : kvh;
+#pragma unroll
+            for (int h = 0; h < C::kHalves; ++h) {
+                const uint32_t off = (uint32_t)h * kHalfBytes + (uint32_t)(i * bs) * 128u;
+                tma_load_4d(sK + off, &p.tm_k, h * 64, c1, c2, blk, full, pol);
+                tma_load_4d(sV + off, &p.tm_v, h * 64, c1, c2, blk, full, pol);
+            }
+        }
+        if (load_q) {
+            const uint16_t* src = p.q + ((int64_t)b * p.Hq + (int64_t)kvh * p.G) * D;
+            bulk_load(sV + C::kTileBytes, src, (uint32_t)(p.G * D * 2), full);
+        }
+        issued |= 1u << stage;
+        issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+
+        pos += n;
+        j += n;
+        seg_begin = seg_end;
+        if (unit_end) {
+            j = 0;
+            if (++kvh == Hkv) {
+                kvh = 0;
+                do { ++b; } while (b < p.B && pfx[b + 1] == pfx[b]);
+            }
+            nb = b < p.B ? pfx[b + 1] - pfx[b] : 0;
+        }
+        if (++stage == S) { stage = 0; phase ^= 1u; }
+    }
+    if (ok) {
+        if (mbar_wait_bounded(empty0 + 8 * stage, phase ^ 1u, kWaitLimitNs)) {
+            meta[stage].flags = kDone;
+            mbar_arrive(full0 + 8 * stage);
+        } else {
+            ok = false;
+        }
+    }
+    if (!ok) {
+        atomicOr(p.err, PDA_DEVERR_TIMEOUT_);
+        *abort_flag = 1;
+        // Wait (bounded) for every copy this thread issued to land before the
+        // CTA may exit.  A phase that already completed passes at once.
+        for (int s = 0; s < S; ++s)
+            if (issued & (1u << s))
+                mbar_wait_bounded(full0 + 8 * s, (issued_parity >> s) & 1u, kWaitLimitNs);
+    }
+}
+
+// ------------------------------------------------------------------ consumers
+
+// Zeroes V rows [from, r0+16) of the warp's tile (masked rows may hold any
+// bits, and 0 * NaN would poison the P.V product).
+template <int D>
+__device__ __forceinline__ void zero_rows(uint32_t sV, int from, int to, int lane) {
+    using C = Cfg<D>;
+    const int units = (to - from) * C::kHalves * 8;
+    for (int u = lane; u < units; u += 32) {
+        const int r = from + u / (C::kHalves * 8);
+        const int rem = u % (C::kHalves * 8);
+        const uint32_t a = sV + (uint32_t)(rem >> 3) * kHalfBytes + (uint32_t)r * 128u + ((rem & 7) << 4);
+        asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(a), "r"(0) : "memory");
+    }
+}
+
+template <int D>
+__device__ __forceinline__ void gather_rows(const SplitParams& p, uint32_t base_s, const uint8_t* base,
+                                            uint32_t sK, uint32_t sV, const StageMeta& m, int r0,
+                                            int lane) {
+    using C = Cfg<D>;
+    const int rows = min(16, m.n_valid - r0);
+    if (rows <= 0) return;
+    const int units = rows * C::kHalves * 8;
+    const int64_t row0 = ((int64_t)m.b * p.Hkv + m.kvh) * p.dbg_row_tokens + (int64_t)m.j0 * p.bs + r0;
+    for (int u = lane; u < units; u += 32) {
+        const int r = u / (C::kHalves * 8);
+        const int rem = u % (C::kHalves * 8);
+        const int h = rem >> 3, c = rem & 7;
+        const int rr = r0 + r;
+        const uint32_t off = (uint32_t)h * kHalfBytes + (uint32_t)rr * 128u + (uint32_t)((c ^ (rr & 7)) << 4);
+        const uint4 kv = *reinterpret_cast<const uint4*>(base + (sK - base_s) + off);
+        const uint4 vv = *reinterpret_cast<const uint4*>(base + (sV - base_s) + off);
+        const int64_t dst = (row0 + r) * D + h * 64 + c * 8;
+        *reinterpret_cast<uint4*>(p.dbg_k + dst) = kv;
+        *reinterpret_cast<uint4*>(p.dbg_v + dst) = vv;
+    }
+}
+
+// Barrier among the 128 consumer threads (an mbarrier, so the wait is
+// bounded: a warp that gave up cannot leave the others waiting forever).
+__device__ __forceinline__ bool consumer_sync(uint32_t cbar, uint32_t& cphase, uint32_t* err,
+                                              volatile int* abort_flag) {
+    mbar_arrive(cbar);
+    const bool ok = mbar_wait_bounded(cbar, cphase, kWaitLimitNs);
+    cphase ^= 1u;
+    if (!ok) {
+        atomicOr(err, PDA_DEVERR_TIMEOUT_);
+        *abort_flag = 1;
+    }
+    return ok;
+}
+
+template <int D, int MODE>
+__device__ __forceinline__ void run_consumer(const SplitParams& p, uint32_t base_s, uint8_t* base,
+                                             const SmemLayout& L, const StageMeta* meta,
+                                             volatile int* abort_flag, int warp, int lane) {
+    using C = Cfg<D>;
+    constexpr int S = C::kStages;
+    constexpr int KS = C::kKSteps;
+    const uint32_t full0 = base_s + L.bars, empty0 = full0 + 8 * S;
+    const int g = lane >> 2, t = lane & 3;
+    const int r0 = warp * 16;
+    const int G = p.G;
+    const float sl2 = p.scale_log2;
+    // ldmatrix row addresses: QK reads K as the A operand (rows = tokens),
+    // PV reads V transposed as the A operand (rows of V = tokens = k index).
+    const int qk_row = r0 + (lane & 7) + (((lane >> 3) & 1) << 3);
+    const int qk_cpar = lane >> 4;
+    const int pv_row = r0 + (lane & 7) + ((lane >> 4) << 3);
+    const int pv_cpar = (lane >> 3) & 1;
+    const int sw = lane & 7;  // == row & 7 for both
+
+    float o[KS][4];
+    uint32_t qf[KS][2];
+    float m0 = kNegInf, m1 = kNegInf, l0 = 0.f, l1 = 0.f;
+#pragma unroll
+    for (int i = 0; i < KS; ++i) {
+        o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+        qf[i][0] = qf[i][1] = 0u;
+    }
+
+    const uint32_t cbar = base_s + L.cbar;
+    uint32_t cphase = 0;
+    int stage = 0;
+    uint32_t phase = 0;
+    while (true) {
+        if (*abort_flag) break;
+        if (!mbar_wait_bounded(full0 + 8 * stage, phase, kWaitLimitNs)) {
+            atomicOr(p.err, PDA_DEVERR_TIMEOUT_);
+            *abort_flag = 1;
+            break;
+        }
+        const StageMeta m = meta[stage];
+        if (m.flags & kDone) break;
+        const uint32_t sK = base_s + (uint32_t)stage * C::kStageBytes;
+        const uint32_t sV = sK + C::kTileBytes;
+
+        if constexpr (MODE == kGather) {
+            gather_rows<D>(p, base_s, base, sK, sV, m, r0, lane);
+        } else {
+            if (m.flags & kSegBegin) {
+                m0 = m1 = kNegInf;
+                l0 = l1 = 0.f;
+                const uint8_t* sq = base + (sV - base_s) + C::kTileBytes;
+#pragma unroll
+                for (int kk = 0; kk < KS; ++kk) {
+                    o[kk][0] = o[kk][1] = o[kk][2] = o[kk][3] = 0.f;
+                    if (g < G) {
+                        const uint8_t* r = sq + (size_t)(g * D + 16 * kk + 2 * t) * 2;
+                        qf[kk][0] = *reinterpret_cast<const uint32_t*>(r);
+                        qf[kk][1] = *reinterpret_cast<const uint32_t*>(r + 16);
+                    } else {
+                        qf[kk][0] = qf[kk][1] = 0u;
+                    }
+                }
+            }
+            if (r0 < m.n_valid) {
+                const bool partial = r0 + 16 > m.n_valid;
+                if (partial) {
+                    zero_rows<D>(sV, m.n_valid, r0 + 16, lane);
+                    __syncwarp();
+                }
+                // S^T (16 tokens x 8 heads) = K q^T, two independent chains
+                float c[4] = {0.f, 0.f, 0.f, 0.f}, e[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int kk = 0; kk < KS; kk += 2) {
+                    uint32_t a[4], a2[4];
+                    const uint32_t rowK = sK + (uint32_t)qk_row * 128u;
+                    const int c0 = (((kk & 3) << 1) + qk_cpar) ^ sw;
+                    const int c1 = ((((kk + 1) & 3) << 1) + qk_cpar) ^ sw;
+                    ldsm_x4(rowK + (uint32_t)(kk >> 2) * kHalfBytes + (c0 << 4), a);
+                    ldsm_x4(rowK + (uint32_t)((kk + 1) >> 2) * kHalfBytes + (c1 << 4), a2);
+                    mma_16816(c, a, qf[kk][0], qf[kk][1]);
+                    mma_16816(e, a2, qf[kk + 1][0], qf[kk + 1][1]);
+                }
+                float s0 = (c[0] + e[0]) * sl2, s1 = (c[1] + e[1]) * sl2;
+                float s2 = (c[2] + e[2]) * sl2, s3 = (c[3] + e[3]) * sl2;
+                if (r0 + g >= m.n_valid) { s0 = kNegInf; s1 = kNegInf; }
+                if (r0 + g + 8 >= m.n_valid) { s2 = kNegInf; s3 = kNegInf; }
+                // column max over the 16 tokens (lanes sharing t)
+                float x0 = fmaxf(s0, s2), x1 = fmaxf(s1, s3);
+#pragma unroll
+                for (int off = 4; off < 32; off <<= 1) {
+                    x0 = fmaxf(x0, __shfl_xor_sync(0xffffffffu, x0, off));
+                    x1 = fmaxf(x1, __shfl_xor_sync(0xffffffffu, x1, off));
+                }
+                const float n0 = fmaxf(m0, x0), n1 = fmaxf(m1, x1);
+                const float u0 = n0 == kNegInf ? 0.f : n0;
+                const float u1 = n1 == kNegInf ? 0.f : n1;
+                const float a0 = m0 == n0 ? 1.f : ex2(m0 - u0);
+                const float a1 = m1 == n1 ? 1.f : ex2(m1 - u1);
+                // P enters the tensor core as bf16 hi + lo parts (p = hi + lo to
+                // about 2^-17 relative), so P.V keeps fp32-level accuracy whatever
+                // running maximum the weights were taken against.
+                const float p0 = ex2(s0 - u0), p1 = ex2(s1 - u1);
+                const float p2 = ex2(s2 - u0), p3 = ex2(s3 - u1);
+                const uint32_t px = pack_bf16x2(p0, p1), py = pack_bf16x2(p2, p3);
+                const uint32_t qx = pack_bf16x2(p0 - bf16_lo(px), p1 - bf16_hi(px));
+                const uint32_t qy = pack_bf16x2(p2 - bf16_lo(py), p3 - bf16_hi(py));
+                // l sums exactly the weights that multiply V
+                l0 = l0 * a0 + ((bf16_lo(px) + bf16_lo(qx)) + (bf16_lo(py) + bf16_lo(qy)));
+                l1 = l1 * a1 + ((bf16_hi(px) + bf16_hi(qx)) + (bf16_hi(py) + bf16_hi(qy)));
+                m0 = n0;
+                m1 = n1;
+                if (!__all_sync(0xffffffffu, a0 == 1.f && a1 == 1.f)) {
+#pragma unroll
+                    for (int i = 0; i < KS; ++i) {
+                        o[i][0] *= a0; o[i][1] *= a1; o[i][2] *= a0; o[i][3] *= a1;
+                    }
+                }
+                const uint32_t pb0 = movmatrix_trans(px), pb1 = movmatrix_trans(py);
+                const uint32_t pc0 = movmatrix_trans(qx), pc1 = movmatrix_trans(qy);
+                // O^T (D x 8 heads) += V^T P^T, 16 rows of D per mma
+#pragma unroll
+                for (int mt = 0; mt < KS; ++mt) {
+                    uint32_t a[4];
+                    const int cc = ((((mt & 3) << 1) + pv_cpar) ^ sw);
+                    ldsm_x4_trans(sV + (uint32_t)(mt >> 2) * kHalfBytes + (uint32_t)pv_row * 128u + (cc << 4), a);
+                    mma_16816(o[mt], a, pb0, pb1);
+                    mma_16816(o[mt], a, pc0, pc1);
+                }
+                if (partial) fence_proxy_async_smem();  // generic writes before the next TMA
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(empty0 + 8 * stage);
+
+        if (MODE != kGather && (m.flags & kSegEnd)) {
+            // ---- merge the four warp states of this segment
+            float* st_m = reinterpret_cast<float*>(base + L.st_m);
+            float* st_l = reinterpret_cast<float*>(base + L.st_l);
+            float* st_o = reinterpret_cast<float*>(base + L.st_o);
+#pragma unroll
+            for (int off = 4; off < 32; off <<= 1) {
+                l0 += __shfl_xor_sync(0xffffffffu, l0, off);
+                l1 += __shfl_xor_sync(0xffffffffu, l1, off);
+            }
+            const int h0 = 2 * t, h1 = 2 * t + 1;
+            if (g == 0) {
+                if (h0 < G) { st_m[warp * kMaxGroup + h0] = m0; st_l[warp * kMaxGroup + h0] = l0; }
+                if (h1 < G) { st_m[warp * kMaxGroup + h1] = m1; st_l[warp * kMaxGroup + h1] = l1; }
+            }
+#pragma unroll
+            for (int mt = 0; mt < KS; ++mt) {
+                const int d = 16 * mt + g;
+                if (h0 < G) {
+                    float* r = st_o + (size_t)(warp * G + h0) * (D + 4);
+                    r[d] = o[mt][0];
+                    r[d + 8] = o[mt][2];
+                }
+                if (h1 < G) {
+                    float* r = st_o + (size_t)(warp * G + h1) * (D + 4);
+                    r[d] = o[mt][1];
+                    r[d + 8] = o[mt][3];
+                }
+            }
+            if (!consumer_sync(cbar, cphase, p.err, abort_flag)) break;
+            const int ct = warp * 32 + lane;
+            const bool direct = MODE == kOneShot && (m.flags & kWholeUnit);
+            const int64_t out_base = ((int64_t)m.b * p.Hq + (int64_t)m.kvh * G) * D;
+            for (int idx = ct; idx < G * D; idx += kConsumerWarps * 32) {
+                const int h = idx / D, d = idx - h * D;
+                float M = kNegInf;
+#pragma unroll
+                for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, st_m[w * kMaxGroup + h]);
+                float Ls = 0.f, Os = 0.f;
+                if (M != kNegInf) {
+#pragma unroll
+                    for (int w = 0; w < kConsumerWarps; ++w) {
+                        const float f = ex2(st_m[w * kMaxGroup + h] - M);
+                        Ls += st_l[w * kMaxGroup + h] * f;
+                        Os += st_o[(size_t)(w * G + h) * (D + 4) + d] * f;
+                    }
+                }
+                if (direct) {
+                    const float r = Ls > 0.f ? Os / Ls : 0.f;
+                    if (p.out_f32) p.out_f32[out_base + idx] = r;
+                    else p.out[out_base + idx] = __bfloat16_as_ushort(__float2bfloat16_rn(r));
+                } else {
+                    p.part_o[(int64_t)m.slot * G * D + idx] = Os;
+                    if (d == 0) {
+                        p.part_ml[((int64_t)m.slot * G + h) * 2] = M;
+                        p.part_ml[((int64_t)m.slot * G + h) * 2 + 1] = Ls;
+                    }
+                }
+            }
+            if (!consumer_sync(cbar, cphase, p.err, abort_flag)) break;
+        }
+        if (++stage == S) { stage = 0; phase ^= 1u; }
+    }
+}
+
+// ------------------------------------------------------------------ kernels
+
+template <int D, int MODE>
+__global__ void __launch_bounds__(kThreads, 1) split_kernel(const __grid_constant__ SplitParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ int abort_flag;
+    const uint32_t raw_s = smem_u32(smem_raw);
+    const uint32_t base_s = (raw_s + 1023u) & ~1023u;
+    uint8_t* base = smem_raw + (base_s - raw_s);
+    const SmemLayout L = smem_layout(D, Cfg<D>::kStages, p.G, p.B);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    int32_t* pfx = reinterpret_cast<int32_t*>(base + L.pfx);
+    int32_t* scan = reinterpret_cast<int32_t*>(base + L.scan);
+    StageMeta* meta = reinterpret_cast<StageMeta*>(base + L.meta);
+
+    if (MODE != kGather) pdl_launch_dependents();
+    if (tid == 0) {
+        for (int s = 0; s < Cfg<D>::kStages; ++s) {
+            mbar_init(base_s + L.bars + 8 * s, 1);
+            mbar_init(base_s + L.bars + 8 * (Cfg<D>::kStages + s), kConsumerWarps);
+        }
+        mbar_init(base_s + L.cbar, kConsumerWarps * 32);
+        fence_mbar_init();
+        abort_flag = 0;
+    }
+    build_prefix(p, pfx, scan);  // ends with __syncthreads (also publishes the barriers)
+    if (blockIdx.x == 0 && MODE != kGather)
+        for (int i = tid; i <= p.B; i += kThreads) p.pfx[i] = pfx[i];
+    const int64_t W = (int64_t)pfx[p.B] * p.Hkv;
+    const int64_t P = gridDim.x;
+    const int64_t begin = cta_begin(blockIdx.x, W, P), end = cta_begin(blockIdx.x + 1, W, P);
+
+    if (warp == kConsumerWarps) {
+        if (lane == 0)
+            run_producer<D, MODE>(p, base_s, L, pfx, meta, &abort_flag, begin, end);
+        return;
+    }
+    run_consumer<D, MODE>(p, base_s, base, L, meta, &abort_flag, warp, lane);
+}
+
+// Merge of split partial states; one CTA per (sequence, kv head) unit.
+template <int MODE>
+__global__ void __launch_bounds__(kMergeThreads) merge_kernel(const MergeParams p) {
+    pdl_wait_primary();
+    __shared__ float old_m[kMaxGroup], old_l[kMaxGroup];
+    const int u = blockIdx.x;
+    const int b = u / p.Hkv, kvh = u - b * p.Hkv;
+    const int G = p.G, D = p.D;
+    const int32_t lo = p.pfx[b], nb = p.pfx[b + 1] - lo;
+    const int64_t q0 = (int64_t)b * p.Hq + (int64_t)kvh * G;  // first q head of the unit
+    if (nb == 0) {
+        if (MODE == kOneShot)
+            for (int idx = threadIdx.x; idx < G * D; idx += blockDim.x) {
+                if (p.out_f32) p.out_f32[q0 * D + idx] = 0.f;
+                else p.out[q0 * D + idx] = 0;
+            }
+        return;
+    }
+    const int64_t W = (int64_t)p.pfx[p.B] * p.Hkv, P = p.split_ctas;
+    const int64_t su = (int64_t)lo * p.Hkv + (int64_t)kvh * nb, eu = su + nb;
+    const int64_t cf = cta_of_block(su, W, P), cl = cta_of_block(eu - 1, W, P);
+    if (MODE == kOneShot && cf == cl) return;  // written by the split kernel
+    if (MODE == kTiled) {
+        if (threadIdx.x < G) {
+            old_m[threadIdx.x] = p.m_state[q0 + threadIdx.x];
+            old_l[threadIdx.x] = p.l_state[q0 + threadIdx.x];
+        }
+        __syncthreads();
+    }
+    for (int idx = threadIdx.x; idx < G * D; idx += blockDim.x) {
+        const int h = idx / D, d = idx - h * D;
+        float M = kNegInf, Ls = 0.f, Os = 0.f;
+        if (MODE == kTiled) {
+            M = old_m[h];
+            Ls = old_l[h];
+            Os = p.o_state[q0 * D + idx];
+        }
+        for (int64_t c = cf; c <= cl; ++c) {
+            const int64_t cb = cta_begin(c, W, P), ce = cta_begin(c + 1, W, P);
+            if ((cb > su ? cb : su) >= (ce < eu ? ce : eu)) continue;  // CTA has no share
+            const int64_t slot = u + c;
+            const float mi = p.part_ml[(slot * G + h) * 2];
+            const float li = p.part_ml[(slot * G + h) * 2 + 1];
+            const float oi = p.part_o[slot * G * D + idx];
+            const float Mn = fmaxf(M, mi);
+            if (Mn == kNegInf) continue;
+            const float fa = ex2(M - Mn), fb = ex2(mi - Mn);
+            Ls = Ls * fa + li * fb;
+            Os = Os * fa + oi * fb;
+            M = Mn;
+        }
+        if (MODE == kOneShot) {
+            const float r = Ls > 0.f ? Os / Ls : 0.f;
+            if (p.out_f32) p.out_f32[q0 * D + idx] = r;
+            else p.out[q0 * D + idx] = __bfloat16_as_ushort(__float2bfloat16_rn(r));
+        } else {
+            p.o_state[q0 * D + idx] = Os;
+            if (d == 0) {
+                p.m_state[q0 + h] = M;
+                p.l_state[q0 + h] = Ls;
+            }
+        }
+    }
+}
+
+#ifdef PDA_DEFINE_AUX_KERNELS
+// (m, l, o) = (-inf, 0, 0) for n_q query slots.
+__global__ void reset_state_kernel(float* m, float* l, float* o, int64_t n_q, int32_t D) {
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n_q * D; i += stride) {
+        o[i] = 0.f;
+        if (i < n_q) {
+            m[i] = kNegInf;
+            l[i] = 0.f;
+        }
+    }
+}
+
+// out = o / l (bf16 round-to-nearest-even, or fp32); l == 0 gives 0.
+__global__ void finalize_kernel(const float* l, const float* o, uint16_t* out, float* out_f32,
+                                int64_t n_q, int32_t D) {
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n_q * D; i += stride) {
+        const float li = l[i / D];
+        const float r = li > 0.f ? o[i] / li : 0.f;
+        if (out_f32) out_f32[i] = r;
+        else out[i] = __bfloat16_as_ushort(__float2bfloat16_rn(r));
+    }
+}
+#endif  // PDA_DEFINE_AUX_KERNELS
+
+}  // namespace pda

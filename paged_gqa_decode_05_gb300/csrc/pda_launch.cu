@@ -1,0 +1,79 @@
+// Merge, state-reset and finalize kernels, and the head_dim dispatch of the
+// split kernel.
+#define PDA_DEFINE_AUX_KERNELS
+#include "pda_kernels.cuh"
+
+namespace pda {
+
+#define PDA_DECLARE_D(D)                                                                     \
+    const void* split_kernel_fn_d##D(int mode);                                             \
+    int split_stages_d##D();                                                                 \
+    cudaError_t launch_split_d##D(int mode, const SplitParams& p, int grid, size_t smem,     \
+                                  cudaStream_t stream);
+PDA_DECLARE_D(64)
+PDA_DECLARE_D(128)
+PDA_DECLARE_D(256)
+
+int split_stages(int D) {
+    switch (D) {
+        case 64: return split_stages_d64();
+        case 128: return split_stages_d128();
+        case 256: return split_stages_d256();
+        default: return 0;
+    }
+}
+
+const void* split_kernel_fn(int D, int mode) {
+    switch (D) {
+        case 64: return split_kernel_fn_d64(mode);
+        case 128: return split_kernel_fn_d128(mode);
+        case 256: return split_kernel_fn_d256(mode);
+        default: return nullptr;
+    }
+}
+
+cudaError_t launch_split(int D, int mode, const SplitParams& p, int grid, size_t smem,
+                         cudaStream_t stream) {
+    switch (D) {
+        case 64: return launch_split_d64(mode, p, grid, smem, stream);
+        case 128: return launch_split_d128(mode, p, grid, smem, stream);
+        case 256: return launch_split_d256(mode, p, grid, smem, stream);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+cudaError_t launch_merge(int mode, const MergeParams& p, bool pdl, cudaStream_t stream) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(p.B * p.Hkv), 1, 1);
+    cfg.blockDim = dim3(kMergeThreads, 1, 1);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    if (mode == kOneShot) return cudaLaunchKernelEx(&cfg, merge_kernel<kOneShot>, p);
+    if (mode == kTiled) return cudaLaunchKernelEx(&cfg, merge_kernel<kTiled>, p);
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_reset_state(float* m, float* l, float* o, int64_t n_q, int32_t D,
+                               cudaStream_t stream) {
+    if (n_q <= 0) return cudaSuccess;
+    const int64_t n = n_q * D;
+    const int grid = (int)((n + 255) / 256 < 4096 ? (n + 255) / 256 : 4096);
+    reset_state_kernel<<<grid, 256, 0, stream>>>(m, l, o, n_q, D);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_finalize(const float* l, const float* o, uint16_t* out, float* out_f32,
+                            int64_t n_q, int32_t D, cudaStream_t stream) {
+    if (n_q <= 0) return cudaSuccess;
+    const int64_t n = n_q * D;
+    const int grid = (int)((n + 255) / 256 < 4096 ? (n + 255) / 256 : 4096);
+    finalize_kernel<<<grid, 256, 0, stream>>>(l, o, out, out_f32, n_q, D);
+    return cudaGetLastError();
+}
+
+}  // namespace pda

@@ -1,0 +1,107 @@
+// pda_params.h -- kernel parameter blocks, shared-memory layout and the
+// launch entry points the host API calls (one translation unit per head_dim
+// defines them).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "pda_plan.h"
+
+namespace pda {
+
+constexpr int kConsumerWarps = 4;                        // compute warps per CTA
+constexpr int kThreads = (kConsumerWarps + 1) * 32;      // + one TMA producer warp
+constexpr int kStageTokens = 64;                         // KV rows per pipeline stage
+constexpr int kHalfBytes = kStageTokens * 128;           // one 64-column swizzled slab
+constexpr int kMaxLaunchBatch = 1024;                    // sequences per kernel launch
+constexpr int kMaxGroup = 8;                             // q heads per kv head (n8 MMA)
+constexpr int kMergeThreads = 128;
+
+enum Mode : int { kOneShot = 0, kTiled = 1, kGather = 2 };
+
+// Per-stage record the producer writes before arming the stage's barrier.
+struct StageMeta {
+    int32_t b;        // sequence
+    int32_t kvh;      // kv head
+    int32_t n_valid;  // valid rows (a prefix of the stage's 64 rows)
+    int32_t flags;    // kSegBegin | kSegEnd | kWholeUnit | kDone
+    int32_t slot;     // partial-state slot of the segment (u + c)
+    int32_t j0;       // index of the stage's first block within the sequence
+    int32_t pad0, pad1;
+};
+enum MetaFlags : int32_t { kSegBegin = 1, kSegEnd = 2, kWholeUnit = 4, kDone = 8 };
+
+struct SplitParams {
+    CUtensorMap tm_k;            // K pool, 4-D: {D, Hkv|bs, bs|Hkv, num_blocks}, box {64,1|bs,bs|1,1}
+    CUtensorMap tm_v;            // V pool, same shape
+    const uint16_t* q;           // [B, Hq, D] bf16
+    const int32_t* table;        // [B, table_stride] block ids
+    const int32_t* lens;         // [B] tokens (one-shot) or block counts (tiled)
+    const int32_t* last_valid;   // [B] valid slots of the last listed block (tiled) or null
+    uint16_t* out;               // [B, Hq, D] bf16 (one-shot)
+    float* out_f32;              // [B, Hq, D] fp32 instead of out when non-null
+    float* part_o;               // [slots, G, D]
+    float* part_ml;              // [slots, G, 2] (m in base-2 units, l)
+    int32_t* pfx;                // [B+1] block prefix, written by CTA 0 for the merge
+    uint32_t* err;               // device error flags
+    uint16_t* dbg_k;             // gather check outputs
+    uint16_t* dbg_v;
+    int64_t num_blocks;
+    int32_t table_stride;
+    int32_t lens_are_blocks;
+    int32_t B, Hq, Hkv, G, bs;
+    int32_t tok_dim;             // 2: coords (x, kvh, slot, blk); 1: (x, slot, kvh, blk)
+    int32_t dbg_row_tokens;      // tokens per (b, kvh) row of the gather output
+    float scale_log2;            // softmax scale * log2(e)
+};
+
+struct MergeParams {
+    const float* part_o;
+    const float* part_ml;
+    const int32_t* pfx;
+    uint16_t* out;
+    float* out_f32;
+    float* m_state;              // tiled: running state [B*Hq], [B*Hq], [B*Hq*D]
+    float* l_state;
+    float* o_state;
+    int32_t B, Hq, Hkv, G, D;
+    int32_t split_ctas;
+};
+
+struct SmemLayout {
+    uint32_t bars, cbar, meta, scan, st_m, st_l, st_o, pfx, total;
+};
+
+PDA_HD uint32_t stage_bytes(int D) { return 2u * (uint32_t)(D / 64) * kHalfBytes + 16u * D; }
+
+// Dynamic shared memory of the split kernel (the +1024 pays for aligning the
+// base to the 128-byte-swizzle atom).
+PDA_HD SmemLayout smem_layout(int D, int stages, int G, int B) {
+    SmemLayout L;
+    uint32_t off = (uint32_t)stages * stage_bytes(D);
+    L.bars = off;  off += 2u * stages * 8u;
+    L.cbar = off;  off += 8u;
+    L.meta = off;  off += (uint32_t)stages * (uint32_t)sizeof(StageMeta);
+    L.scan = off;  off += kThreads * 4u;
+    L.st_m = off;  off += kConsumerWarps * kMaxGroup * 4u;
+    L.st_l = off;  off += kConsumerWarps * kMaxGroup * 4u;
+    L.st_o = off;  off += (uint32_t)(kConsumerWarps * G * (D + 4)) * 4u;
+    L.pfx = off;   off += (uint32_t)(B + 1) * 4u;
+    L.total = off + 1024u;
+    return L;
+}
+
+// Entry points defined per head_dim (pda_kernels_d*.cu).
+int split_stages(int D);
+const void* split_kernel_fn(int D, int mode);
+cudaError_t launch_split(int D, int mode, const SplitParams& p, int grid, size_t smem,
+                         cudaStream_t stream);
+cudaError_t launch_merge(int mode, const MergeParams& p, bool pdl, cudaStream_t stream);
+cudaError_t launch_reset_state(float* m, float* l, float* o, int64_t n_q, int32_t D,
+                               cudaStream_t stream);
+cudaError_t launch_finalize(const float* l, const float* o, uint16_t* out, float* out_f32,
+                            int64_t n_q, int32_t D, cudaStream_t stream);
+
+}  // namespace pda
