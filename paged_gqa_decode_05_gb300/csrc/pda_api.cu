@@ -87,30 +87,22 @@ struct PoolArgs {
     int64_t blk, tok, kvh;
 };
 
-pda_status encode_pool(const pda_ctx* ctx, const void* base, const PoolArgs& a, CUtensorMap* tm,
-                       int32_t* tok_dim) {
+// One 5-D tiled view per pool, {64 columns, block_size slots, D/64 column
+// slabs, Hkv heads, num_blocks}, whose box {64, bs, D/64, 1, 1} is one kv
+// head's rows of one block: a single TMA copy per block and pool, landing in
+// shared memory as [slab][slot][128 bytes] with the 128-byte swizzle.  The
+// stride triple (block, token, kv head) places any row layout in this view.
+pda_status encode_pool(const pda_ctx* ctx, const void* base, const PoolArgs& a, CUtensorMap* tm) {
     auto enc = tensor_map_encoder();
     if (!enc) return fail(PDA_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
     const pda_dims& d = ctx->dims;
-    cuuint64_t dims[4];
-    cuuint64_t strides[3];
-    cuuint32_t box[4];
-    const cuuint32_t estr[4] = {1, 1, 1, 1};
-    if (a.tok >= a.kvh) {  // [.., slot, kvh, D]: kv head is the faster axis
-        dims[0] = (cuuint64_t)d.head_dim; dims[1] = (cuuint64_t)d.num_kv_heads;
-        dims[2] = (cuuint64_t)d.block_size; dims[3] = (cuuint64_t)a.num_blocks;
-        strides[0] = (cuuint64_t)a.kvh * 2; strides[1] = (cuuint64_t)a.tok * 2;
-        box[0] = 64; box[1] = 1; box[2] = (cuuint32_t)d.block_size; box[3] = 1;
-        *tok_dim = 2;
-    } else {               // [.., kvh, slot, D]: token is the faster axis
-        dims[0] = (cuuint64_t)d.head_dim; dims[1] = (cuuint64_t)d.block_size;
-        dims[2] = (cuuint64_t)d.num_kv_heads; dims[3] = (cuuint64_t)a.num_blocks;
-        strides[0] = (cuuint64_t)a.tok * 2; strides[1] = (cuuint64_t)a.kvh * 2;
-        box[0] = 64; box[1] = (cuuint32_t)d.block_size; box[2] = 1; box[3] = 1;
-        *tok_dim = 1;
-    }
-    strides[2] = (cuuint64_t)a.blk * 2;
-    CUresult r = enc(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides,
+    const cuuint64_t dims[5] = {64, (cuuint64_t)d.block_size, (cuuint64_t)(d.head_dim / 64),
+                                (cuuint64_t)d.num_kv_heads, (cuuint64_t)a.num_blocks};
+    const cuuint64_t strides[4] = {(cuuint64_t)a.tok * 2, 128, (cuuint64_t)a.kvh * 2,
+                                   (cuuint64_t)a.blk * 2};
+    const cuuint32_t box[5] = {64, (cuuint32_t)d.block_size, (cuuint32_t)(d.head_dim / 64), 1, 1};
+    const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+    CUresult r = enc(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(base), dims, strides,
                      box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS)
@@ -188,10 +180,9 @@ pda_status run(pda_ctx* ctx, const RunArgs& r) {
 
     pda::SplitParams p;
     std::memset(&p, 0, sizeof p);
-    int32_t tok_dim_k = 0, tok_dim_v = 0;
-    st = encode_pool(ctx, r.pool.k, r.pool, &p.tm_k, &tok_dim_k);
+    st = encode_pool(ctx, r.pool.k, r.pool, &p.tm_k);
     if (st != PDA_OK) return st;
-    st = encode_pool(ctx, r.pool.v, r.pool, &p.tm_v, &tok_dim_v);
+    st = encode_pool(ctx, r.pool.v, r.pool, &p.tm_v);
     if (st != PDA_OK) return st;
 
     const int32_t Hq = d.num_q_heads, Hkv = d.num_kv_heads, D = d.head_dim;
@@ -219,7 +210,6 @@ pda_status run(pda_ctx* ctx, const RunArgs& r) {
         p.Hkv = Hkv;
         p.G = ctx->G;
         p.bs = d.block_size;
-        p.tok_dim = tok_dim_k;
         p.dbg_row_tokens = (int32_t)dbg_row_tokens;
         p.scale_log2 = scale_log2;
         const size_t smem = pda::smem_layout(D, ctx->stages, ctx->G, cb).total;
@@ -363,6 +353,10 @@ PDA_EXPORT pda_status pda_create(const pda_dims* dims, pda_ctx** out_ctx) {
     for (int mode = 0; mode < 3; ++mode) {
         e = cudaFuncSetAttribute(pda::split_kernel_fn(D, mode), cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  ctx->smem_max);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(pda::split_kernel_fn(D, mode),
+                                     cudaFuncAttributePreferredSharedMemoryCarveout,
+                                     cudaSharedmemCarveoutMaxShared);
         if (e != cudaSuccess) { delete ctx; return cuda_fail(e, "cudaFuncSetAttribute"); }
     }
     int per_sm = 0;

@@ -4,9 +4,9 @@
 //   * warp 4, lane 0 is the producer: it walks the CTA's share of the
 //     flattened (sequence, kv head, block) space (pda_plan.h), looks every
 //     block up in the block table and copies whole K/V block rows of one kv
-//     head into a ring of shared-memory stages with 4-D TMA tensor copies
-//     (128-byte swizzle), plus the group's q rows with one bulk copy at the
-//     start of each segment.  Stage completion is tracked by mbarriers.
+//     head into a ring of shared-memory stages with one 5-D TMA tensor copy
+//     per block and pool (128-byte swizzle), plus the group's q rows with one
+//     bulk copy at the start of each segment.  Stage completion is tracked by mbarriers.
 //   * warps 0..3 consume a stage of 64 rows, 16 rows each.  The GQA group
 //     (G <= 8 q heads of one kv head) shares every K/V load: S^T = K q^T is a
 //     16x8 tile per warp (mma.sync m16n8k16, tokens as M, heads as N), the
@@ -37,12 +37,23 @@ constexpr uint64_t kWaitLimitNs = 2000000000ull;  // each mbarrier wait gives up
 #define PDA_DEVERR_BAD_LENGTH_ 0x2u
 #define PDA_DEVERR_TIMEOUT_ 0x4u
 
+// Pipeline depth per head size (tuning constants).
+#ifndef PDA_STAGES_D64
+#define PDA_STAGES_D64 6
+#endif
+#ifndef PDA_STAGES_D128
+#define PDA_STAGES_D128 4
+#endif
+#ifndef PDA_STAGES_D256
+#define PDA_STAGES_D256 2
+#endif
+
 template <int D>
 struct Cfg {
     static constexpr int kHalves = D / 64;               // 64-column swizzled slabs per row
     static constexpr int kTileBytes = kHalves * kHalfBytes;
     static constexpr int kStageBytes = 2 * kTileBytes + 16 * D;
-    static constexpr int kStages = D == 64 ? 6 : (D == 128 ? 4 : 2);
+    static constexpr int kStages = D == 64 ? PDA_STAGES_D64 : (D == 128 ? PDA_STAGES_D128 : PDA_STAGES_D256);
     static constexpr int kKSteps = D / 16;
 };
 
@@ -115,15 +126,23 @@ __device__ __forceinline__ void build_prefix(const SplitParams& p, int32_t* pfx,
 template <int D, int MODE>
 __device__ __forceinline__ void run_producer(const SplitParams& p, uint32_t base_s, const SmemLayout& L,
                                              const int32_t* pfx, StageMeta* meta,
-                                             volatile int* abort_flag, int64_t begin, int64_t end) {
+                                             volatile int* abort_flag, int64_t begin, int64_t end,
+                                             int lane) {
+    // The whole warp walks the plan in lockstep: every lane keeps two block
+    // ids of a 64-entry window of the current sequence's table row (loaded
+    // one window ahead, so table reads never stall the copies), lane 0 issues
+    // the barrier operations and the TMA copies.
     using C = Cfg<D>;
     constexpr int S = C::kStages;
     const uint32_t full0 = base_s + L.bars, empty0 = full0 + 8 * S;
+    const bool leader = lane == 0;
     const uint64_t pol = policy_evict_first();
     const int bs = p.bs, Hkv = p.Hkv;
     const int NB = kStageTokens / bs;
-    prefetch_tensormap(&p.tm_k);
-    prefetch_tensormap(&p.tm_v);
+    if (leader) {
+        prefetch_tensormap(&p.tm_k);
+        prefetch_tensormap(&p.tm_v);
+    }
 
     int stage = 0;
     uint32_t phase = 0;
@@ -133,6 +152,8 @@ __device__ __forceinline__ void run_producer(const SplitParams& p, uint32_t base
     int64_t pos = begin;
     int b = 0, kvh = 0;
     int32_t j = 0, nb = 0;
+    int32_t win = 0, id0 = 0, id1 = 0;
+    const int32_t* row = p.table;
     if (pos < end) {
         int lo = 0, hi = p.B - 1;  // largest b with pfx[b]*Hkv <= pos
         while (lo < hi) {
@@ -144,55 +165,67 @@ __device__ __forceinline__ void run_producer(const SplitParams& p, uint32_t base
         const int64_t rem = pos - (int64_t)pfx[b] * Hkv;
         kvh = (int)(rem / nb);
         j = (int32_t)(rem % nb);
+        row = p.table + (int64_t)b * p.table_stride;
+        win = j;
+        id0 = win + lane < nb ? row[win + lane] : 0;
+        id1 = win + 32 + lane < nb ? row[win + 32 + lane] : 0;
     }
     bool seg_begin = true;
     bool whole = false;
     while (pos < end) {
-        if (*abort_flag) { ok = false; break; }
+        const int stop = __shfl_sync(0xffffffffu, leader ? *abort_flag : 0, 0);
+        if (stop) { ok = false; break; }
         const int32_t n = (int32_t)min((int64_t)min(NB, nb - j), end - pos);
         const bool unit_end = (j + n == nb);
         const bool seg_end = unit_end || (pos + n == end);
         if (seg_begin) whole = (j == 0) && ((int64_t)pfx[b] * Hkv + (int64_t)(kvh + 1) * nb <= end);
 
-        if (!mbar_wait_bounded(empty0 + 8 * stage, phase ^ 1u, kWaitLimitNs)) { ok = false; break; }
-
         const int32_t lastv = unit_end ? last_block_slots(p, b, nb) : bs;
-        StageMeta m;
-        m.b = b;
-        m.kvh = kvh;
-        m.n_valid = (n - 1) * bs + lastv;
-        m.flags = (seg_begin ? kSegBegin : 0) | (seg_end ? kSegEnd : 0) | (whole ? kWholeUnit : 0);
-        m.slot = b * Hkv + kvh + (int)blockIdx.x;
-        m.j0 = j;
-        m.pad0 = m.pad1 = 0;
-        meta[stage] = m;
 
-        const bool load_q = seg_begin && MODE != kGather;
-        const uint32_t bytes = (uint32_t)n * 2u * (uint32_t)bs * D * 2u +
-                               (load_q ? (uint32_t)(p.G * D * 2) : 0u);
+        bool got = true;
+        if (leader) got = mbar_wait_bounded(empty0 + 8 * stage, phase ^ 1u, kWaitLimitNs);
+        got = __shfl_sync(0xffffffffu, got ? 1 : 0, 0) != 0;
+        if (!got) { ok = false; break; }
+
         const uint32_t full = full0 + 8 * stage;
-        mbar_arrive_expect_tx(full, bytes);
         const uint32_t sK = base_s + (uint32_t)stage * C::kStageBytes;
         const uint32_t sV = sK + C::kTileBytes;
-        const int32_t* row = p.table + (int64_t)b * p.table_stride;
-        for (int i = 0; i < n; ++i) {
-            int32_t blk = row[j + i];
-            if (blk < 0 || (int64_t)blk >= p.num_blocks) {
-                atomicOr(p.err, PDA_DEVERR_BAD_BLOCK_ID_);
-                blk = 0;  // stays in bounds; the flag marks the result invalid
-            }
-            const int32_t c1 = p.tok_dim == 2 ? kvh : 0;
-            const int32_t c2 = p.tok_dim == 2 ? 0 : kvh;
-#pragma unroll
-            for (int h = 0; h < C::kHalves; ++h) {
-                const uint32_t off = (uint32_t)h * kHalfBytes + (uint32_t)(i * bs) * 128u;
-                tma_load_4d(sK + off, &p.tm_k, h * 64, c1, c2, blk, full, pol);
-                tma_load_4d(sV + off, &p.tm_v, h * 64, c1, c2, blk, full, pol);
+        if (leader) {
+            StageMeta m;
+            m.b = b;
+            m.kvh = kvh;
+            m.n_valid = (n - 1) * bs + lastv;
+            m.flags = (seg_begin ? kSegBegin : 0) | (seg_end ? kSegEnd : 0) | (whole ? kWholeUnit : 0);
+            m.slot = b * Hkv + kvh + (int)blockIdx.x;
+            m.j0 = j;
+            m.pad0 = m.pad1 = 0;
+            meta[stage] = m;
+            const bool load_q = seg_begin && MODE != kGather;
+            const uint32_t bytes = (uint32_t)n * 2u * (uint32_t)bs * D * 2u +
+                                   (load_q ? (uint32_t)(p.G * D * 2) : 0u);
+            mbar_arrive_expect_tx(full, bytes);
+            if (load_q) {
+                const uint16_t* src = p.q + ((int64_t)b * p.Hq + (int64_t)kvh * p.G) * D;
+                bulk_load(sV + C::kTileBytes, src, (uint32_t)(p.G * D * 2), full);
             }
         }
-        if (load_q) {
-            const uint16_t* src = p.q + ((int64_t)b * p.Hq + (int64_t)kvh * p.G) * D;
-            bulk_load(sV + C::kTileBytes, src, (uint32_t)(p.G * D * 2), full);
+        __syncwarp();
+        // lane i copies block i of the stage (its id comes from the window;
+        // j + i - win < 40 by the window rule below)
+        {
+            const int idx = j + lane - win;
+            const int32_t a = __shfl_sync(0xffffffffu, id0, idx & 31);
+            const int32_t c = __shfl_sync(0xffffffffu, id1, idx & 31);
+            if (lane < n) {
+                int32_t id = idx < 32 ? a : c;
+                if (id < 0 || (int64_t)id >= p.num_blocks) {
+                    atomicOr(p.err, PDA_DEVERR_BAD_BLOCK_ID_);
+                    id = 0;  // stays in bounds; the flag marks the result invalid
+                }
+                const uint32_t off = (uint32_t)(lane * bs) * (uint32_t)(D * 2);
+                tma_load_5d(sK + off, &p.tm_k, 0, 0, 0, kvh, id, full, pol);
+                tma_load_5d(sV + off, &p.tm_v, 0, 0, 0, kvh, id, full, pol);
+            }
         }
         issued |= 1u << stage;
         issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
@@ -207,9 +240,21 @@ __device__ __forceinline__ void run_producer(const SplitParams& p, uint32_t base
                 do { ++b; } while (b < p.B && pfx[b + 1] == pfx[b]);
             }
             nb = b < p.B ? pfx[b + 1] - pfx[b] : 0;
+            if (pos < end) {
+                row = p.table + (int64_t)b * p.table_stride;
+                win = 0;
+                id0 = lane < nb ? row[lane] : 0;
+                id1 = 32 + lane < nb ? row[32 + lane] : 0;
+            }
+        } else if (j - win >= 32) {
+            // first half consumed: slide the window and fetch the next 32 ids
+            win += 32;
+            id0 = id1;
+            id1 = win + 32 + lane < nb ? row[win + 32 + lane] : 0;
         }
         if (++stage == S) { stage = 0; phase ^= 1u; }
     }
+    if (!leader) return;
     if (ok) {
         if (mbar_wait_bounded(empty0 + 8 * stage, phase ^ 1u, kWaitLimitNs)) {
             meta[stage].flags = kDone;
@@ -221,7 +266,7 @@ __device__ __forceinline__ void run_producer(const SplitParams& p, uint32_t base
     if (!ok) {
         atomicOr(p.err, PDA_DEVERR_TIMEOUT_);
         *abort_flag = 1;
-        // Wait (bounded) for every copy this thread issued to land before the
+        // Wait (bounded) for every copy this warp issued to land before the
         // CTA may exit.  A phase that already completed passes at once.
         for (int s = 0; s < S; ++s)
             if (issued & (1u << s))
@@ -231,16 +276,28 @@ __device__ __forceinline__ void run_producer(const SplitParams& p, uint32_t base
 
 // ------------------------------------------------------------------ consumers
 
+// Stage tiles hold the stage's blocks back to back; block i is one TMA box
+// laid out [D/64 slabs][bs rows][128 bytes], 128-byte swizzled, so row t of
+// the stage, slab h, 16-byte chunk c sits at
+//   row_off(t) + h * bs * 128 + ((c ^ (t & 7)) << 4)
+// with row_off(t) = (t / bs) * bs * D * 2 + (t % bs) * 128.
+template <int D>
+__device__ __forceinline__ uint32_t row_off(int t, int lbs) {
+    const int bs = 1 << lbs;
+    return (uint32_t)(t >> lbs) * (uint32_t)(bs * D * 2) + (uint32_t)(t & (bs - 1)) * 128u;
+}
+
 // Zeroes V rows [from, r0+16) of the warp's tile (masked rows may hold any
 // bits, and 0 * NaN would poison the P.V product).
 template <int D>
-__device__ __forceinline__ void zero_rows(uint32_t sV, int from, int to, int lane) {
+__device__ __forceinline__ void zero_rows(uint32_t sV, int from, int to, int lbs, int lane) {
     using C = Cfg<D>;
+    const uint32_t hs = (uint32_t)(128 << lbs);
     const int units = (to - from) * C::kHalves * 8;
     for (int u = lane; u < units; u += 32) {
         const int r = from + u / (C::kHalves * 8);
         const int rem = u % (C::kHalves * 8);
-        const uint32_t a = sV + (uint32_t)(rem >> 3) * kHalfBytes + (uint32_t)r * 128u + ((rem & 7) << 4);
+        const uint32_t a = sV + row_off<D>(r, lbs) + (uint32_t)(rem >> 3) * hs + ((rem & 7) << 4);
         asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(a), "r"(0) : "memory");
     }
 }
@@ -248,8 +305,9 @@ __device__ __forceinline__ void zero_rows(uint32_t sV, int from, int to, int lan
 template <int D>
 __device__ __forceinline__ void gather_rows(const SplitParams& p, uint32_t base_s, const uint8_t* base,
                                             uint32_t sK, uint32_t sV, const StageMeta& m, int r0,
-                                            int lane) {
+                                            int lbs, int lane) {
     using C = Cfg<D>;
+    const uint32_t hs = (uint32_t)(128 << lbs);
     const int rows = min(16, m.n_valid - r0);
     if (rows <= 0) return;
     const int units = rows * C::kHalves * 8;
@@ -259,7 +317,7 @@ __device__ __forceinline__ void gather_rows(const SplitParams& p, uint32_t base_
         const int rem = u % (C::kHalves * 8);
         const int h = rem >> 3, c = rem & 7;
         const int rr = r0 + r;
-        const uint32_t off = (uint32_t)h * kHalfBytes + (uint32_t)rr * 128u + (uint32_t)((c ^ (rr & 7)) << 4);
+        const uint32_t off = row_off<D>(rr, lbs) + (uint32_t)h * hs + (uint32_t)((c ^ (rr & 7)) << 4);
         const uint4 kv = *reinterpret_cast<const uint4*>(base + (sK - base_s) + off);
         const uint4 vv = *reinterpret_cast<const uint4*>(base + (sV - base_s) + off);
         const int64_t dst = (row0 + r) * D + h * 64 + c * 8;
@@ -301,6 +359,10 @@ __device__ __forceinline__ void run_consumer(const SplitParams& p, uint32_t base
     const int pv_row = r0 + (lane & 7) + ((lane >> 4) << 3);
     const int pv_cpar = (lane >> 3) & 1;
     const int sw = lane & 7;  // == row & 7 for both
+    const int lbs = 31 - __clz(p.bs);
+    const uint32_t hs = (uint32_t)(128 << lbs);  // bytes between 64-column slabs of a block
+    const uint32_t qk_off = row_off<D>(qk_row, lbs);
+    const uint32_t pv_off = row_off<D>(pv_row, lbs);
 
     float o[KS][4];
     uint32_t qf[KS][2];
@@ -328,7 +390,7 @@ __device__ __forceinline__ void run_consumer(const SplitParams& p, uint32_t base
         const uint32_t sV = sK + C::kTileBytes;
 
         if constexpr (MODE == kGather) {
-            gather_rows<D>(p, base_s, base, sK, sV, m, r0, lane);
+            gather_rows<D>(p, base_s, base, sK, sV, m, r0, lbs, lane);
         } else {
             if (m.flags & kSegBegin) {
                 m0 = m1 = kNegInf;
@@ -349,7 +411,7 @@ __device__ __forceinline__ void run_consumer(const SplitParams& p, uint32_t base
             if (r0 < m.n_valid) {
                 const bool partial = r0 + 16 > m.n_valid;
                 if (partial) {
-                    zero_rows<D>(sV, m.n_valid, r0 + 16, lane);
+                    zero_rows<D>(sV, m.n_valid, r0 + 16, lbs, lane);
                     __syncwarp();
                 }
                 // S^T (16 tokens x 8 heads) = K q^T, two independent chains
@@ -357,11 +419,11 @@ __device__ __forceinline__ void run_consumer(const SplitParams& p, uint32_t base
 #pragma unroll
                 for (int kk = 0; kk < KS; kk += 2) {
                     uint32_t a[4], a2[4];
-                    const uint32_t rowK = sK + (uint32_t)qk_row * 128u;
+                    const uint32_t rowK = sK + qk_off;
                     const int c0 = (((kk & 3) << 1) + qk_cpar) ^ sw;
                     const int c1 = ((((kk + 1) & 3) << 1) + qk_cpar) ^ sw;
-                    ldsm_x4(rowK + (uint32_t)(kk >> 2) * kHalfBytes + (c0 << 4), a);
-                    ldsm_x4(rowK + (uint32_t)((kk + 1) >> 2) * kHalfBytes + (c1 << 4), a2);
+                    ldsm_x4(rowK + (uint32_t)(kk >> 2) * hs + (c0 << 4), a);
+                    ldsm_x4(rowK + (uint32_t)((kk + 1) >> 2) * hs + (c1 << 4), a2);
                     mma_16816(c, a, qf[kk][0], qf[kk][1]);
                     mma_16816(e, a2, qf[kk + 1][0], qf[kk + 1][1]);
                 }
@@ -407,7 +469,7 @@ __device__ __forceinline__ void run_consumer(const SplitParams& p, uint32_t base
                 for (int mt = 0; mt < KS; ++mt) {
                     uint32_t a[4];
                     const int cc = ((((mt & 3) << 1) + pv_cpar) ^ sw);
-                    ldsm_x4_trans(sV + (uint32_t)(mt >> 2) * kHalfBytes + (uint32_t)pv_row * 128u + (cc << 4), a);
+                    ldsm_x4_trans(sV + pv_off + (uint32_t)(mt >> 2) * hs + (cc << 4), a);
                     mma_16816(o[mt], a, pb0, pb1);
                     mma_16816(o[mt], a, pc0, pc1);
                 }
@@ -484,8 +546,16 @@ __device__ __forceinline__ void run_consumer(const SplitParams& p, uint32_t base
 
 // ------------------------------------------------------------------ kernels
 
+// PDA_MAXNREG caps registers so that two CTAs fit one SM's register file
+// (each 16K-register quarter must hold 3 of the 10 warps: <= 168 per thread).
+#ifdef PDA_MAXNREG
+#define PDA_SPLIT_BOUNDS __maxnreg__(PDA_MAXNREG)
+#else
+#define PDA_SPLIT_BOUNDS __launch_bounds__(kThreads, 1)
+#endif
+
 template <int D, int MODE>
-__global__ void __launch_bounds__(kThreads, 1) split_kernel(const __grid_constant__ SplitParams p) {
+__global__ void PDA_SPLIT_BOUNDS split_kernel(const __grid_constant__ SplitParams p) {
     extern __shared__ uint8_t smem_raw[];
     __shared__ int abort_flag;
     const uint32_t raw_s = smem_u32(smem_raw);
@@ -515,74 +585,101 @@ __global__ void __launch_bounds__(kThreads, 1) split_kernel(const __grid_constan
     const int64_t begin = cta_begin(blockIdx.x, W, P), end = cta_begin(blockIdx.x + 1, W, P);
 
     if (warp == kConsumerWarps) {
-        if (lane == 0)
-            run_producer<D, MODE>(p, base_s, L, pfx, meta, &abort_flag, begin, end);
+        run_producer<D, MODE>(p, base_s, L, pfx, meta, &abort_flag, begin, end, lane);
         return;
     }
     run_consumer<D, MODE>(p, base_s, base, L, meta, &abort_flag, warp, lane);
 }
 
-// Merge of split partial states; one CTA per (sequence, kv head) unit.
+// Merge of split partial states: one CTA per (sequence, kv head) unit, one
+// thread per 4 consecutive outputs of the unit's G x D block.  The slots of
+// up to 8 CTAs are loaded together, so the merge costs one memory round trip
+// per 8 partial states.
+__device__ __forceinline__ void merge_in(float& M, float& Ls, float4& Os, float mi, float li,
+                                         const float4& oi) {
+    const float Mn = fmaxf(M, mi);
+    if (Mn == kNegInf) return;  // both states empty
+    const float fa = ex2(M - Mn), fb = ex2(mi - Mn);
+    Ls = Ls * fa + li * fb;
+    Os.x = Os.x * fa + oi.x * fb;
+    Os.y = Os.y * fa + oi.y * fb;
+    Os.z = Os.z * fa + oi.z * fb;
+    Os.w = Os.w * fa + oi.w * fb;
+    M = Mn;
+}
+
 template <int MODE>
-__global__ void __launch_bounds__(kMergeThreads) merge_kernel(const MergeParams p) {
+__global__ void __launch_bounds__(kMaxGroup * 256 / 4) merge_kernel(const MergeParams p) {
     pdl_wait_primary();
-    __shared__ float old_m[kMaxGroup], old_l[kMaxGroup];
     const int u = blockIdx.x;
     const int b = u / p.Hkv, kvh = u - b * p.Hkv;
     const int G = p.G, D = p.D;
+    const int n4 = G * D / 4;
+    const int i4 = threadIdx.x;
     const int32_t lo = p.pfx[b], nb = p.pfx[b + 1] - lo;
     const int64_t q0 = (int64_t)b * p.Hq + (int64_t)kvh * G;  // first q head of the unit
+    const bool active = i4 < n4;  // the block is rounded up to whole warps
+    const int h = active ? (4 * i4) / D : 0;
     if (nb == 0) {
-        if (MODE == kOneShot)
-            for (int idx = threadIdx.x; idx < G * D; idx += blockDim.x) {
-                if (p.out_f32) p.out_f32[q0 * D + idx] = 0.f;
-                else p.out[q0 * D + idx] = 0;
-            }
+        if (MODE == kOneShot && active) {
+            if (p.out_f32) reinterpret_cast<float4*>(p.out_f32 + q0 * D)[i4] = make_float4(0.f, 0.f, 0.f, 0.f);
+            else reinterpret_cast<uint2*>(p.out + q0 * D)[i4] = make_uint2(0u, 0u);
+        }
         return;
     }
     const int64_t W = (int64_t)p.pfx[p.B] * p.Hkv, P = p.split_ctas;
     const int64_t su = (int64_t)lo * p.Hkv + (int64_t)kvh * nb, eu = su + nb;
     const int64_t cf = cta_of_block(su, W, P), cl = cta_of_block(eu - 1, W, P);
     if (MODE == kOneShot && cf == cl) return;  // written by the split kernel
-    if (MODE == kTiled) {
-        if (threadIdx.x < G) {
-            old_m[threadIdx.x] = p.m_state[q0 + threadIdx.x];
-            old_l[threadIdx.x] = p.l_state[q0 + threadIdx.x];
-        }
-        __syncthreads();
+    float M = kNegInf, Ls = 0.f;
+    float4 Os = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (MODE == kTiled && active) {
+        M = p.m_state[q0 + h];
+        Ls = p.l_state[q0 + h];
+        Os = reinterpret_cast<const float4*>(p.o_state + q0 * D)[i4];
     }
-    for (int idx = threadIdx.x; idx < G * D; idx += blockDim.x) {
-        const int h = idx / D, d = idx - h * D;
-        float M = kNegInf, Ls = 0.f, Os = 0.f;
-        if (MODE == kTiled) {
-            M = old_m[h];
-            Ls = old_l[h];
-            Os = p.o_state[q0 * D + idx];
-        }
-        for (int64_t c = cf; c <= cl; ++c) {
+    constexpr int kBatch = 8;
+    for (int64_t c0 = cf; active && c0 <= cl; c0 += kBatch) {
+        float mi[kBatch], li[kBatch];
+        float4 oi[kBatch];
+#pragma unroll
+        for (int k = 0; k < kBatch; ++k) {
+            const int64_t c = c0 + k;
+            mi[k] = kNegInf;
+            li[k] = 0.f;
+            oi[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (c > cl) continue;
             const int64_t cb = cta_begin(c, W, P), ce = cta_begin(c + 1, W, P);
-            if ((cb > su ? cb : su) >= (ce < eu ? ce : eu)) continue;  // CTA has no share
+            if ((cb > su ? cb : su) >= (ce < eu ? ce : eu)) continue;  // no share of this unit
             const int64_t slot = u + c;
-            const float mi = p.part_ml[(slot * G + h) * 2];
-            const float li = p.part_ml[(slot * G + h) * 2 + 1];
-            const float oi = p.part_o[slot * G * D + idx];
-            const float Mn = fmaxf(M, mi);
-            if (Mn == kNegInf) continue;
-            const float fa = ex2(M - Mn), fb = ex2(mi - Mn);
-            Ls = Ls * fa + li * fb;
-            Os = Os * fa + oi * fb;
-            M = Mn;
+            mi[k] = p.part_ml[(slot * G + h) * 2];
+            li[k] = p.part_ml[(slot * G + h) * 2 + 1];
+            oi[k] = reinterpret_cast<const float4*>(p.part_o + slot * G * D)[i4];
         }
-        if (MODE == kOneShot) {
-            const float r = Ls > 0.f ? Os / Ls : 0.f;
-            if (p.out_f32) p.out_f32[q0 * D + idx] = r;
-            else p.out[q0 * D + idx] = __bfloat16_as_ushort(__float2bfloat16_rn(r));
+#pragma unroll
+        for (int k = 0; k < kBatch; ++k) merge_in(M, Ls, Os, mi[k], li[k], oi[k]);
+    }
+    if (MODE == kOneShot) {
+        if (!active) return;
+        const float4 v = Ls > 0.f ? make_float4(Os.x / Ls, Os.y / Ls, Os.z / Ls, Os.w / Ls)
+                                  : make_float4(0.f, 0.f, 0.f, 0.f);
+        if (p.out_f32) {
+            reinterpret_cast<float4*>(p.out_f32 + q0 * D)[i4] = v;
         } else {
-            p.o_state[q0 * D + idx] = Os;
-            if (d == 0) {
-                p.m_state[q0 + h] = M;
-                p.l_state[q0 + h] = Ls;
-            }
+            uint2 w;
+            w.x = pack_bf16x2(v.x, v.y);
+            w.y = pack_bf16x2(v.z, v.w);
+            reinterpret_cast<uint2*>(p.out + q0 * D)[i4] = w;
+        }
+    } else {
+        // every thread of head h computed the same (M, Ls); the first one
+        // stores them after all threads of the head have read the old values
+        __syncthreads();
+        if (!active) return;
+        reinterpret_cast<float4*>(p.o_state + q0 * D)[i4] = Os;
+        if ((4 * i4) % D == 0) {
+            p.m_state[q0 + h] = M;
+            p.l_state[q0 + h] = Ls;
         }
     }
 }

@@ -14,10 +14,9 @@ namespace pda {
 constexpr int kConsumerWarps = 4;                        // compute warps per CTA
 constexpr int kThreads = (kConsumerWarps + 1) * 32;      // + one TMA producer warp
 constexpr int kStageTokens = 64;                         // KV rows per pipeline stage
-constexpr int kHalfBytes = kStageTokens * 128;           // one 64-column swizzled slab
+constexpr int kHalfBytes = kStageTokens * 128;           // 64 rows of one 64-column slab
 constexpr int kMaxLaunchBatch = 1024;                    // sequences per kernel launch
 constexpr int kMaxGroup = 8;                             // q heads per kv head (n8 MMA)
-constexpr int kMergeThreads = 128;
 
 enum Mode : int { kOneShot = 0, kTiled = 1, kGather = 2 };
 
@@ -34,7 +33,7 @@ struct StageMeta {
 enum MetaFlags : int32_t { kSegBegin = 1, kSegEnd = 2, kWholeUnit = 4, kDone = 8 };
 
 struct SplitParams {
-    CUtensorMap tm_k;            // K pool, 4-D: {D, Hkv|bs, bs|Hkv, num_blocks}, box {64,1|bs,bs|1,1}
+    CUtensorMap tm_k;            // K pool, 5-D {64, bs, D/64, Hkv, num_blocks}, box {64, bs, D/64, 1, 1}
     CUtensorMap tm_v;            // V pool, same shape
     const uint16_t* q;           // [B, Hq, D] bf16
     const int32_t* table;        // [B, table_stride] block ids
@@ -52,7 +51,6 @@ struct SplitParams {
     int32_t table_stride;
     int32_t lens_are_blocks;
     int32_t B, Hq, Hkv, G, bs;
-    int32_t tok_dim;             // 2: coords (x, kvh, slot, blk); 1: (x, slot, kvh, blk)
     int32_t dbg_row_tokens;      // tokens per (b, kvh) row of the gather output
     float scale_log2;            // softmax scale * log2(e)
 };

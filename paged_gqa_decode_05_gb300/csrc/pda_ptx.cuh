@@ -71,14 +71,14 @@ __device__ __forceinline__ void prefetch_tensormap(const void* tm) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(tm) : "memory");
 }
 
-// 4-D tiled tensor load into this CTA's shared memory, completion on `bar`.
-__device__ __forceinline__ void tma_load_4d(uint32_t dst, const void* tm, int32_t c0, int32_t c1,
-                                            int32_t c2, int32_t c3, uint32_t bar,
+// 5-D tiled tensor load into this CTA's shared memory, completion on `bar`.
+__device__ __forceinline__ void tma_load_5d(uint32_t dst, const void* tm, int32_t c0, int32_t c1,
+                                            int32_t c2, int32_t c3, int32_t c4, uint32_t bar,
                                             uint64_t policy) {
     asm volatile(
-        "cp.async.bulk.tensor.4d.shared::cta.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
-        " [%0], [%1, {%2, %3, %4, %5}], [%6], %7;" ::"r"(dst),
-        "l"(tm), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(bar), "l"(policy)
+        "cp.async.bulk.tensor.5d.shared::cta.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3, %4, %5, %6}], [%7], %8;" ::"r"(dst),
+        "l"(tm), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4), "r"(bar), "l"(policy)
         : "memory");
 }
 
