@@ -39,10 +39,10 @@ constexpr uint64_t kWaitLimitNs = 2000000000ull;  // each mbarrier wait gives up
 
 // Pipeline depth per head size (tuning constants).
 #ifndef PDA_STAGES_D64
-#define PDA_STAGES_D64 6
+#define PDA_STAGES_D64 4
 #endif
 #ifndef PDA_STAGES_D128
-#define PDA_STAGES_D128 4
+#define PDA_STAGES_D128 2
 #endif
 #ifndef PDA_STAGES_D256
 #define PDA_STAGES_D256 2
@@ -55,6 +55,7 @@ struct Cfg {
     static constexpr int kStageBytes = 2 * kTileBytes + 16 * D;
     static constexpr int kStages = D == 64 ? PDA_STAGES_D64 : (D == 128 ? PDA_STAGES_D128 : PDA_STAGES_D256);
     static constexpr int kKSteps = D / 16;
+    static constexpr int kMaxRegs = D == 256 ? 255 : 168;
 };
 
 // Blocks of sequence b, validated and clamped (flags bad lengths).
@@ -546,16 +547,13 @@ __device__ __forceinline__ void run_consumer(const SplitParams& p, uint32_t base
 
 // ------------------------------------------------------------------ kernels
 
-// PDA_MAXNREG caps registers so that two CTAs fit one SM's register file
-// (each 16K-register quarter must hold 3 of the 10 warps: <= 168 per thread).
-#ifdef PDA_MAXNREG
-#define PDA_SPLIT_BOUNDS __maxnreg__(PDA_MAXNREG)
-#else
-#define PDA_SPLIT_BOUNDS __launch_bounds__(kThreads, 1)
-#endif
-
+// Register cap: for D <= 128 two CTAs share an SM (two 2-stage rings keep as
+// many bytes in flight as one 4-stage ring, and a second set of consumer warps
+// hides the MMA/shuffle latency), which needs each 16K-register quarter of the
+// SM to hold 3 of the 10 warps: at most 168 registers per thread.  D = 256
+// runs one CTA per SM.
 template <int D, int MODE>
-__global__ void PDA_SPLIT_BOUNDS split_kernel(const __grid_constant__ SplitParams p) {
+__global__ void __maxnreg__(Cfg<D>::kMaxRegs) split_kernel(const __grid_constant__ SplitParams p) {
     extern __shared__ uint8_t smem_raw[];
     __shared__ int abort_flag;
     const uint32_t raw_s = smem_u32(smem_raw);
