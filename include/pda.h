@@ -283,6 +283,44 @@ pda_status pda_plan_units(const int32_t* lens, int32_t batch, int32_t blocks_giv
                           int32_t block_size, int32_t num_kv_heads, int32_t split_ctas,
                           int32_t* first_cta, int32_t* last_cta, int64_t* total_blocks);
 
+/*
+ * One-shot decode that allocates nothing -- no counterpart on the pages; it
+ * exists for callers that cannot allocate device memory.
+ *
+ * Some callers cannot call cudaMalloc (or anything that allocates) at the
+ * point where they decode: code running inside a CUDA-graph capture they do
+ * not control, allocators that forbid outside allocations, or embedders with
+ * a fixed memory budget set up before any model runs.  pda_create allocates
+ * the context's state and workspace, so those callers use this entry point
+ * instead.  It needs no context: its scratch (the split kernel's partial
+ * states and block prefix) lives in one statically sized device array
+ * (PDA_NOALLOC_SCRATCH_BYTES) that every GPU loading this library holds
+ * until the process exits.
+ *
+ * Arguments and layout are those of pda_decode (default pool layout
+ * [num_blocks, block_size, Hkv, D]); the sizes that pda_create would take
+ * come as arguments.  device_flags is an optional device word that receives
+ * PDA_DEVERR_* bits (the caller zeroes it); with NULL the flags go to the
+ * scratch, where they are cleared at the start of every call and not
+ * reported.
+ *
+ * Rules: a call whose scratch need exceeds PDA_NOALLOC_SCRATCH_BYTES returns
+ * PDA_ERR_INVALID_ARG with the size in pda_last_error(); batch is limited
+ * to 1024 sequences.  The first call on each device finds the scratch's
+ * device address and sets kernel attributes there: make that first call
+ * before any stream capture.  All calls share the one scratch array and keep
+ * the last call's contents: two calls that can overlap on the GPU (different
+ * streams without ordering, or several threads) race and corrupt each
+ * other's results, so order them on one stream.
+ */
+#define PDA_NOALLOC_SCRATCH_BYTES (4u << 20)
+pda_status pda_decode_noalloc(const pda_bf16* q, const pda_bf16* k_pool, const pda_bf16* v_pool,
+                              int64_t num_blocks, const int32_t* block_table, int32_t max_blocks,
+                              const int32_t* seq_lens, int32_t batch, int32_t num_q_heads,
+                              int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                              float scale, pda_bf16* out, uint32_t* device_flags,
+                              pda_stream stream);
+
 #ifdef __cplusplus
 }
 #endif

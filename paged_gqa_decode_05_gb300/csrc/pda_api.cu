@@ -556,3 +556,155 @@ PDA_EXPORT pda_status pda_plan_units(const int32_t* lens, int32_t batch, int32_t
     }
     return PDA_OK;
 }
+
+// ---------------------------------------------------------------------------
+// pda_decode_noalloc: the one-shot decode for callers that cannot allocate.
+// Its scratch is this file-scope device array; host code reaches it only
+// through the address cudaGetSymbolAddress returns for the current device.
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[PDA_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+
+struct NoallocDevice {
+    bool ready = false;
+    unsigned char* scratch = nullptr;  // device address of g_noalloc_scratch
+    int num_sms = 0;
+};
+
+std::mutex g_noalloc_mutex;
+NoallocDevice g_noalloc_devices[64];
+
+size_t round256(size_t x) { return (x + 255) / 256 * 256; }
+
+}  // namespace
+
+PDA_EXPORT pda_status pda_decode_noalloc(const pda_bf16* q, const pda_bf16* k_pool,
+                                         const pda_bf16* v_pool, int64_t num_blocks,
+                                         const int32_t* block_table, int32_t max_blocks,
+                                         const int32_t* seq_lens, int32_t batch,
+                                         int32_t num_q_heads, int32_t num_kv_heads,
+                                         int32_t head_dim, int32_t block_size, float scale,
+                                         pda_bf16* out, uint32_t* device_flags,
+                                         pda_stream stream) {
+    if (batch < 0 || batch > pda::kMaxLaunchBatch)
+        return fail(PDA_ERR_INVALID_ARG, "batch %d outside [0, %d]", batch, pda::kMaxLaunchBatch);
+    const pda_dims dims = {batch > 0 ? batch : 1, num_q_heads, num_kv_heads, head_dim, block_size, 1};
+    pda_status st = pda_check_dims(&dims);
+    if (st != PDA_OK) return st;
+    if (batch == 0) return PDA_OK;
+    if (device_flags && !aligned(device_flags, 4))
+        return fail(PDA_ERR_INVALID_ARG, "device_flags must be 4-byte aligned");
+
+    // Scratch need: flags word, block prefix, partial states (m, l) and o.
+    const int G = num_q_heads / num_kv_heads, D = head_dim;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return fail(PDA_ERR_NO_DEVICE, "no CUDA device: %s", cudaGetErrorString(e));
+    if (dev < 0 || dev >= 64) return fail(PDA_ERR_UNSUPPORTED, "device index %d beyond 63", dev);
+
+    unsigned char* scratch = nullptr;
+    int num_sms = 0;
+    {
+        std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+        NoallocDevice& nd = g_noalloc_devices[dev];
+        if (!nd.ready) {  // once per device, with that device current
+            int major = 0, minor = 0;
+            if ((e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess ||
+                (e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess ||
+                (e = cudaDeviceGetAttribute(&nd.num_sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+                return cuda_fail(e, "device attributes");
+            if (major != 10 || minor != 3)
+                return fail(PDA_ERR_NO_DEVICE, "device %d is sm_%d%d; this library is built for sm_103a",
+                            dev, major, minor);
+            void* ptr = nullptr;
+            e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
+            if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(scratch)");
+            nd.scratch = static_cast<unsigned char*>(ptr);
+            nd.ready = true;
+        }
+        scratch = nd.scratch;
+        num_sms = nd.num_sms;
+    }
+
+    const int stages = pda::split_stages(D);
+    const size_t smem = pda::smem_layout(D, stages, G, batch).total;
+    const void* split_fn = pda::split_kernel_fn(D, pda::kOneShot);
+    // The attribute is per function and device and other contexts may have
+    // set a smaller value, so it is set on every call (no allocation).
+    if ((e = cudaFuncSetAttribute(split_fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) != cudaSuccess ||
+        (e = cudaFuncSetAttribute(split_fn, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                  cudaSharedmemCarveoutMaxShared)) != cudaSuccess)
+        return cuda_fail(e, "cudaFuncSetAttribute");
+    int per_sm = 0;
+    if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, split_fn, pda::kThreads, smem)) != cudaSuccess)
+        return cuda_fail(e, "occupancy query");
+    if (per_sm < 1) return fail(PDA_ERR_UNSUPPORTED, "split kernel does not fit on an SM");
+    const int split_ctas = per_sm * num_sms;
+
+    const int64_t slots = (int64_t)batch * num_kv_heads + split_ctas;
+    const size_t off_pfx = 256;
+    const size_t off_ml = off_pfx + round256((size_t)(batch + 1) * sizeof(int32_t));
+    const size_t off_o = off_ml + round256((size_t)slots * G * 2 * sizeof(float));
+    const size_t need = off_o + (size_t)slots * G * D * sizeof(float);
+    if (need > PDA_NOALLOC_SCRATCH_BYTES)
+        return fail(PDA_ERR_INVALID_ARG,
+                    "this call needs %zu bytes of scratch; the static scratch holds %u "
+                    "(reduce batch or use pda_create / pda_decode)",
+                    need, (unsigned)PDA_NOALLOC_SCRATCH_BYTES);
+
+    if (!q || !aligned(q, 16) || !out || !aligned(out, 16))
+        return fail(PDA_ERR_INVALID_ARG, "q and out must be non-NULL and 16-byte aligned");
+    if (!block_table || !seq_lens || !aligned(block_table, 4) || !aligned(seq_lens, 4))
+        return fail(PDA_ERR_INVALID_ARG, "block_table / seq_lens must be non-NULL and 4-byte aligned");
+    if (max_blocks < 1) return fail(PDA_ERR_INVALID_ARG, "max_blocks must be >= 1");
+    PoolArgs pool = {k_pool, v_pool, num_blocks, (int64_t)block_size * num_kv_heads * head_dim,
+                     (int64_t)num_kv_heads * head_dim, (int64_t)head_dim};
+    pda_ctx shape;  // only the dims are read by the helpers below
+    shape.dims = dims;
+    if ((st = check_pool(&shape, pool)) != PDA_OK) return st;
+    float scale_log2 = 0.f;
+    if ((st = check_scale(scale, D, &scale_log2)) != PDA_OK) return st;
+
+    pda::SplitParams p;
+    std::memset(&p, 0, sizeof p);
+    if ((st = encode_pool(&shape, k_pool, pool, &p.tm_k)) != PDA_OK) return st;
+    if ((st = encode_pool(&shape, v_pool, pool, &p.tm_v)) != PDA_OK) return st;
+    cudaStream_t s = (cudaStream_t)stream;
+    uint32_t* err = device_flags ? device_flags : reinterpret_cast<uint32_t*>(scratch);
+    if (!device_flags && (e = cudaMemsetAsync(err, 0, sizeof(uint32_t), s)) != cudaSuccess)
+        return cuda_fail(e, "clearing the scratch flags");
+    p.q = q;
+    p.table = block_table;
+    p.lens = seq_lens;
+    p.out = out;
+    p.part_o = reinterpret_cast<float*>(scratch + off_o);
+    p.part_ml = reinterpret_cast<float*>(scratch + off_ml);
+    p.pfx = reinterpret_cast<int32_t*>(scratch + off_pfx);
+    p.err = err;
+    p.num_blocks = num_blocks;
+    p.table_stride = max_blocks;
+    p.B = batch;
+    p.Hq = num_q_heads;
+    p.Hkv = num_kv_heads;
+    p.G = G;
+    p.bs = block_size;
+    p.scale_log2 = scale_log2;
+    if ((e = pda::launch_split(D, pda::kOneShot, p, split_ctas, smem, s)) != cudaSuccess)
+        return cuda_fail(e, "split kernel launch");
+    pda::MergeParams mp;
+    std::memset(&mp, 0, sizeof mp);
+    mp.part_o = p.part_o;
+    mp.part_ml = p.part_ml;
+    mp.pfx = p.pfx;
+    mp.out = out;
+    mp.B = batch;
+    mp.Hq = num_q_heads;
+    mp.Hkv = num_kv_heads;
+    mp.G = G;
+    mp.D = D;
+    mp.split_ctas = split_ctas;
+    if ((e = pda::launch_merge(pda::kOneShot, mp, true, s)) != cudaSuccess)
+        return cuda_fail(e, "merge kernel launch");
+    return PDA_OK;
+}
