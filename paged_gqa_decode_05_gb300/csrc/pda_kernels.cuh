@@ -39,13 +39,13 @@ constexpr uint64_t kWaitLimitNs = 2000000000ull;  // each mbarrier wait gives up
 
 // Pipeline depth per head size (tuning constants).
 #ifndef PDA_STAGES_D64
-#define PDA_STAGES_D64 4
+#define PDA_STAGES_D64 6
 #endif
 #ifndef PDA_STAGES_D128
-#define PDA_STAGES_D128 2
+#define PDA_STAGES_D128 3
 #endif
 #ifndef PDA_STAGES_D256
-#define PDA_STAGES_D256 2
+#define PDA_STAGES_D256 3
 #endif
 
 template <int D>
@@ -415,21 +415,21 @@ __device__ __forceinline__ void run_consumer(const SplitParams& p, uint32_t base
                     zero_rows<D>(sV, m.n_valid, r0 + 16, lbs, lane);
                     __syncwarp();
                 }
-                // S^T (16 tokens x 8 heads) = K q^T, two independent chains
-                float c[4] = {0.f, 0.f, 0.f, 0.f}, e[4] = {0.f, 0.f, 0.f, 0.f};
+                // S^T (16 tokens x 8 heads) = K q^T in four independent chains
+                float acc[4][4];
 #pragma unroll
-                for (int kk = 0; kk < KS; kk += 2) {
-                    uint32_t a[4], a2[4];
-                    const uint32_t rowK = sK + qk_off;
-                    const int c0 = (((kk & 3) << 1) + qk_cpar) ^ sw;
-                    const int c1 = ((((kk + 1) & 3) << 1) + qk_cpar) ^ sw;
-                    ldsm_x4(rowK + (uint32_t)(kk >> 2) * hs + (c0 << 4), a);
-                    ldsm_x4(rowK + (uint32_t)((kk + 1) >> 2) * hs + (c1 << 4), a2);
-                    mma_16816(c, a, qf[kk][0], qf[kk][1]);
-                    mma_16816(e, a2, qf[kk + 1][0], qf[kk + 1][1]);
+                for (int ch = 0; ch < 4; ++ch) acc[ch][0] = acc[ch][1] = acc[ch][2] = acc[ch][3] = 0.f;
+#pragma unroll
+                for (int kk = 0; kk < KS; ++kk) {
+                    uint32_t a[4];
+                    const int cc = (((kk & 3) << 1) + qk_cpar) ^ sw;
+                    ldsm_x4(sK + qk_off + (uint32_t)(kk >> 2) * hs + (cc << 4), a);
+                    mma_16816(acc[kk & 3], a, qf[kk][0], qf[kk][1]);
                 }
-                float s0 = (c[0] + e[0]) * sl2, s1 = (c[1] + e[1]) * sl2;
-                float s2 = (c[2] + e[2]) * sl2, s3 = (c[3] + e[3]) * sl2;
+                float s0 = ((acc[0][0] + acc[1][0]) + (acc[2][0] + acc[3][0])) * sl2;
+                float s1 = ((acc[0][1] + acc[1][1]) + (acc[2][1] + acc[3][1])) * sl2;
+                float s2 = ((acc[0][2] + acc[1][2]) + (acc[2][2] + acc[3][2])) * sl2;
+                float s3 = ((acc[0][3] + acc[1][3]) + (acc[2][3] + acc[3][3])) * sl2;
                 if (r0 + g >= m.n_valid) { s0 = kNegInf; s1 = kNegInf; }
                 if (r0 + g + 8 >= m.n_valid) { s2 = kNegInf; s3 = kNegInf; }
                 // column max over the 16 tokens (lanes sharing t)
@@ -477,19 +477,19 @@ __device__ __forceinline__ void run_consumer(const SplitParams& p, uint32_t base
                 if (partial) fence_proxy_async_smem();  // generic writes before the next TMA
             }
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(empty0 + 8 * stage);
-
         if (MODE != kGather && (m.flags & kSegEnd)) {
-            // ---- merge the four warp states of this segment
+            // ---- merge the four warp states of this segment.  The o tiles are
+            // staged in this stage's own K/V memory (the stage is released only
+            // after the merge), which keeps shared memory for deeper rings.
             float* st_m = reinterpret_cast<float*>(base + L.st_m);
             float* st_l = reinterpret_cast<float*>(base + L.st_l);
-            float* st_o = reinterpret_cast<float*>(base + L.st_o);
+            float* st_o = reinterpret_cast<float*>(base + (sK - base_s));
 #pragma unroll
             for (int off = 4; off < 32; off <<= 1) {
                 l0 += __shfl_xor_sync(0xffffffffu, l0, off);
                 l1 += __shfl_xor_sync(0xffffffffu, l1, off);
             }
+            if (!consumer_sync(cbar, cphase, p.err, abort_flag)) break;  // all reads of the stage done
             const int h0 = 2 * t, h1 = 2 * t + 1;
             if (g == 0) {
                 if (h0 < G) { st_m[warp * kMaxGroup + h0] = m0; st_l[warp * kMaxGroup + h0] = l0; }
@@ -540,7 +540,10 @@ __device__ __forceinline__ void run_consumer(const SplitParams& p, uint32_t base
                 }
             }
             if (!consumer_sync(cbar, cphase, p.err, abort_flag)) break;
+            fence_proxy_async_smem();  // staging writes before the next TMA into this stage
         }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(empty0 + 8 * stage);
         if (++stage == S) { stage = 0; phase ^= 1u; }
     }
 }

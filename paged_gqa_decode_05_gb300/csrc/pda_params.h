@@ -69,13 +69,14 @@ struct MergeParams {
 };
 
 struct SmemLayout {
-    uint32_t bars, cbar, meta, scan, st_m, st_l, st_o, pfx, total;
+    uint32_t bars, cbar, meta, scan, st_m, st_l, pfx, total;
 };
 
 PDA_HD uint32_t stage_bytes(int D) { return 2u * (uint32_t)(D / 64) * kHalfBytes + 16u * D; }
 
 // Dynamic shared memory of the split kernel (the +1024 pays for aligning the
-// base to the 128-byte-swizzle atom).
+// base to the 128-byte-swizzle atom).  The segment epilogue stages its o tiles
+// (4 warps x G x (D+4) floats <= 2 * 64 * D * 2 bytes) in the finished stage.
 PDA_HD SmemLayout smem_layout(int D, int stages, int G, int B) {
     SmemLayout L;
     uint32_t off = (uint32_t)stages * stage_bytes(D);
@@ -85,7 +86,6 @@ PDA_HD SmemLayout smem_layout(int D, int stages, int G, int B) {
     L.scan = off;  off += kThreads * 4u;
     L.st_m = off;  off += kConsumerWarps * kMaxGroup * 4u;
     L.st_l = off;  off += kConsumerWarps * kMaxGroup * 4u;
-    L.st_o = off;  off += (uint32_t)(kConsumerWarps * G * (D + 4)) * 4u;
     L.pfx = off;   off += (uint32_t)(B + 1) * 4u;
     L.total = off + 1024u;
     return L;
