@@ -140,10 +140,6 @@ __device__ __forceinline__ void run_producer(const SplitParams& p, uint32_t base
     const uint64_t pol = policy_evict_first();
     const int bs = p.bs, Hkv = p.Hkv;
     const int NB = kStageTokens / bs;
-    if (leader) {
-        prefetch_tensormap(&p.tm_k);
-        prefetch_tensormap(&p.tm_v);
-    }
 
     int stage = 0;
     uint32_t phase = 0;
@@ -568,6 +564,9 @@ __global__ void __maxnreg__(Cfg<D>::kMaxRegs) split_kernel(const __grid_constant
     int32_t* scan = reinterpret_cast<int32_t*>(base + L.scan);
     StageMeta* meta = reinterpret_cast<StageMeta*>(base + L.meta);
 
+    // Programmatic dependent launch: let the merge kernel be scheduled now,
+    // set up barriers and descriptors while the previous kernel in the stream
+    // finishes, and read no global memory before it has completed.
     if (MODE != kGather) pdl_launch_dependents();
     if (tid == 0) {
         for (int s = 0; s < Cfg<D>::kStages; ++s) {
@@ -578,6 +577,11 @@ __global__ void __maxnreg__(Cfg<D>::kMaxRegs) split_kernel(const __grid_constant
         fence_mbar_init();
         abort_flag = 0;
     }
+    if (tid == kConsumerWarps * 32) {
+        prefetch_tensormap(&p.tm_k);
+        prefetch_tensormap(&p.tm_v);
+    }
+    pdl_wait_primary();
     build_prefix(p, pfx, scan);  // ends with __syncthreads (also publishes the barriers)
     if (blockIdx.x == 0 && MODE != kGather)
         for (int i = tid; i <= p.B; i += kThreads) p.pfx[i] = pfx[i];
@@ -611,6 +615,7 @@ __device__ __forceinline__ void merge_in(float& M, float& Ls, float4& Os, float 
 
 template <int MODE>
 __global__ void __launch_bounds__(kMaxGroup * 256 / 4) merge_kernel(const MergeParams p) {
+    pdl_launch_dependents();  // the next call's split kernel may start its set-up
     pdl_wait_primary();
     const int u = blockIdx.x;
     const int b = u / p.Hkv, kvh = u - b * p.Hkv;

@@ -15,14 +15,26 @@ const void* split_kernel_fn_d64(int mode) {
 
 int split_stages_d64() { return Cfg<64>::kStages; }
 
+// Launched with programmatic stream serialization: the kernel's prologue may
+// overlap the previous kernel; it waits (griddepcontrol.wait) before reading
+// global memory.
 cudaError_t launch_split_d64(int mode, const SplitParams& p, int grid, size_t smem, cudaStream_t stream) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid, 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
     switch (mode) {
-        case kOneShot: split_kernel<64, kOneShot><<<grid, kThreads, smem, stream>>>(p); break;
-        case kTiled: split_kernel<64, kTiled><<<grid, kThreads, smem, stream>>>(p); break;
-        case kGather: split_kernel<64, kGather><<<grid, kThreads, smem, stream>>>(p); break;
+        case kOneShot: return cudaLaunchKernelEx(&cfg, split_kernel<64, kOneShot>, p);
+        case kTiled: return cudaLaunchKernelEx(&cfg, split_kernel<64, kTiled>, p);
+        case kGather: return cudaLaunchKernelEx(&cfg, split_kernel<64, kGather>, p);
         default: return cudaErrorInvalidValue;
     }
-    return cudaGetLastError();
 }
 
 }  // namespace pda
