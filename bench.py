@@ -48,6 +48,9 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="8b")
+    ap.add_argument("--layout", choices=["paged", "contiguous"], default="paged",
+                    help="contiguous: the same cache copied to [B, S, Hkv, D] and decoded "
+                         "with pda_decode_contiguous")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--quick", action="store_true",
@@ -218,7 +221,7 @@ def run_reference(args):
             "ms_per_step": cb["sec_per_call"] * 1e3, "us_per_call": cb["sec_per_call"] * 1e6,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic (seeded N(0,1) bf16 inputs)",
-            "config": {**w.describe(), "workload": w.name, "runs_on": "host CPU cores"},
+            "config": {**w.describe(), "workload": w.name, "kv_layout": args.layout, "runs_on": "host CPU cores"},
             "cpu_baseline": {k: cb[k] for k in ("value", "unit", "cores", "kind", "sample")},
             "e2e": {"value": cb["value"], "unit": "GB/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
@@ -257,8 +260,13 @@ def run_ours(args):
             return torch.from_numpy(a.view(np.int16)).to(dev).view(torch.bfloat16)
         return torch.from_numpy(a).to(dev)
 
-    host = {"q": w.q, "k_pool": w.k_pool, "v_pool": w.v_pool, "block_table": w.block_table,
-            "seq_lens": w.seq_lens}
+    if args.layout == "contiguous":
+        k_c, v_c = workloads.contiguous_kv(w)
+        host = {"q": w.q, "k_pool": k_c, "v_pool": v_c, "block_table": w.block_table,
+                "seq_lens": w.seq_lens}
+    else:
+        host = {"q": w.q, "k_pool": w.k_pool, "v_pool": w.v_pool, "block_table": w.block_table,
+                "seq_lens": w.seq_lens}
     sets = [{k: to_dev(v) for k, v in host.items()} for _ in range(n_sets)]
     outs = [torch.empty((w.B, w.Hq, w.D), device=dev, dtype=torch.bfloat16) for _ in range(n_sets)]
     ctx = pda.Context(max_seqs=w.B, num_q_heads=w.Hq, num_kv_heads=w.Hkv, head_dim=w.D,
@@ -272,8 +280,12 @@ def run_ours(args):
         i = counter[0]
         counter[0] += 1
         s = sets[i % n_sets]
-        ctx.decode(s["q"], s["k_pool"], s["v_pool"], s["block_table"], s["seq_lens"],
-                   out=outs[i % n_sets])
+        if args.layout == "contiguous":
+            ctx.decode_contiguous(s["q"], s["k_pool"], s["v_pool"], s["seq_lens"],
+                                  out=outs[i % n_sets])
+        else:
+            ctx.decode(s["q"], s["k_pool"], s["v_pool"], s["block_table"], s["seq_lens"],
+                       out=outs[i % n_sets])
 
     for i in range(max(3, args.warmup)):
         step(i)
@@ -351,8 +363,12 @@ def run_ours(args):
             for k, t in pinned.items():
                 d = dst[k].view(torch.int16) if dst[k].dtype == torch.bfloat16 else dst[k]
                 d.copy_(t, non_blocking=True)
-            ctx.decode(dst["q"], dst["k_pool"], dst["v_pool"], dst["block_table"], dst["seq_lens"],
-                       out=outs[0])
+            if args.layout == "contiguous":
+                ctx.decode_contiguous(dst["q"], dst["k_pool"], dst["v_pool"], dst["seq_lens"],
+                                      out=outs[0])
+            else:
+                ctx.decode(dst["q"], dst["k_pool"], dst["v_pool"], dst["block_table"],
+                           dst["seq_lens"], out=outs[0])
             out_host.copy_(outs[0], non_blocking=True)
 
         for _ in range(2):
@@ -390,7 +406,7 @@ def run_ours(args):
         "vs_baseline": None,
         "dtype": "bf16",
         "data": "synthetic: seeded N(0,1) q/K/V rounded to bf16, shuffled block table",
-        "config": {**w.describe(), "workload": w.name,
+        "config": {**w.describe(), "workload": w.name, "kv_layout": args.layout,
                    "l2": f"inputs larger than L2 ({input_bytes / 1e6:.0f} MB per set, "
                          f"{n_sets} sets rotated, L2 {l2 / 2 ** 20:.0f} MiB)",
                    "parallelism": "replicas" if world > 1 else "single GPU",

@@ -167,6 +167,21 @@ pda_status pda_decode_strided(pda_ctx* ctx, const pda_bf16* q, const pda_bf16* k
                               pda_bf16* out, pda_stream stream);
 
 /*
+ * Decode over a contiguous (unpaged) cache -- [CK] Overview (attn_decode:
+ * GQA decode over a contiguous KV cache) and Python Wrappers (layout
+ * [batch, seq_len, n_heads, head_dim]).  It is the paged kernel with the
+ * identity block table: token t of sequence b is row (b, t) of
+ *   k, v         [batch, max_seq_len, Hkv, D] bf16, dense;
+ * max_seq_len must be a multiple of the context's block_size; seq_lens[b]
+ * (device) <= max_seq_len tokens are read.  q, out and scale as pda_decode;
+ * batch <= min(max_seqs, 1024).
+ */
+pda_status pda_decode_contiguous(pda_ctx* ctx, const pda_bf16* q, const pda_bf16* k,
+                                 const pda_bf16* v, int32_t max_seq_len,
+                                 const int32_t* seq_lens, int32_t batch, float scale,
+                                 pda_bf16* out, pda_stream stream);
+
+/*
  * Tiled lifecycle, step 1 -- [TA] begin_step: resets the running state of
  * sequences 0..num_seqs-1 to (m, l, o) = (-inf, 0, 0).  num_seqs > max_seqs
  * is PDA_ERR_INVALID_ARG.

@@ -88,6 +88,7 @@ def lib() -> ctypes.CDLL:
         "pda_decode": (I32, [P, P, P, P, I64, P, I32, P, I32, F, P, P]),
         "pda_decode_strided": (I32, [P, P, P, P, I64, I64, I64, I64, P, I32, P, I32, F, P, P]),
         "pda_decode_f32": (I32, [P, P, P, P, I64, I64, I64, I64, P, I32, P, I32, F, P, P]),
+        "pda_decode_contiguous": (I32, [P, P, P, P, I32, P, I32, F, P, P]),
         "pda_begin_step": (I32, [P, I32, P]),
         "pda_step_tile": (I32, [P, P, P, P, I64, P, P, P, I32, I64, I64, I64, F, P]),
         "pda_finalize": (I32, [P, P, I32, P]),
@@ -288,6 +289,26 @@ class Context:
                                         ts_, hs_, _ptr(block_table), int(block_table.shape[1]),
                                         _ptr(seq_lens), B, self._scale(scale), _ptr(out),
                                         _stream(stream)))
+        return out
+
+    def decode_contiguous(self, q, k, v, seq_lens, scale: Optional[float] = None, out=None,
+                          stream=None):
+        """Decode over a contiguous cache k, v [B, S, Hkv, D] (S a multiple of block_size)."""
+        torch = _torch()
+        d = self.dims
+        B = int(seq_lens.shape[0])
+        self._bf16(q, "q", (B, d.num_q_heads, d.head_dim))
+        self._i32(seq_lens, "seq_lens", 1)
+        if k.dim() != 4 or k.shape[0] != B or k.shape[2:] != (d.num_kv_heads, d.head_dim):
+            raise ValueError("k must be [B, S, Hkv, D]")
+        self._bf16(k, "k")
+        self._bf16(v, "v", tuple(k.shape))
+        if out is None:
+            out = torch.empty((B, d.num_q_heads, d.head_dim), device=q.device, dtype=torch.bfloat16)
+        self._bf16(out, "out", (B, d.num_q_heads, d.head_dim))
+        _check(lib().pda_decode_contiguous(self._ctx, _ptr(q), _ptr(k), _ptr(v), int(k.shape[1]),
+                                           _ptr(seq_lens), B, self._scale(scale), _ptr(out),
+                                           _stream(stream)))
         return out
 
     # -- tiled lifecycle

@@ -150,6 +150,7 @@ struct RunArgs {
     pda_bf16* dbg_k;
     pda_bf16* dbg_v;
     cudaStream_t stream;
+    bool contiguous = false;  // no table: block b*table_stride + j (contiguous cache)
 };
 
 pda_status run(pda_ctx* ctx, const RunArgs& r) {
@@ -169,7 +170,7 @@ pda_status run(pda_ctx* ctx, const RunArgs& r) {
     }
     if (r.mode == pda::kGather && (!r.dbg_k || !r.dbg_v || !aligned(r.dbg_k, 16) || !aligned(r.dbg_v, 16)))
         return fail(PDA_ERR_INVALID_ARG, "k_rows / v_rows must be non-NULL and 16-byte aligned");
-    if (!r.table || !r.lens || !aligned(r.table, 4) || !aligned(r.lens, 4) ||
+    if ((!r.table && !r.contiguous) || !r.lens || !aligned(r.table, 4) || !aligned(r.lens, 4) ||
         (r.last_valid && !aligned(r.last_valid, 4)))
         return fail(PDA_ERR_INVALID_ARG, "table / length arrays must be non-NULL and 4-byte aligned");
     if (r.table_stride < 1)
@@ -191,7 +192,7 @@ pda_status run(pda_ctx* ctx, const RunArgs& r) {
     for (int32_t c0 = 0; c0 < r.batch; c0 += pda::kMaxLaunchBatch) {
         const int32_t cb = std::min(pda::kMaxLaunchBatch, r.batch - c0);
         p.q = r.q ? r.q + (int64_t)c0 * Hq * D : nullptr;
-        p.table = r.table + (int64_t)c0 * r.table_stride;
+        p.table = r.contiguous ? nullptr : r.table + (int64_t)c0 * r.table_stride;
         p.lens = r.lens + c0;
         p.last_valid = r.last_valid ? r.last_valid + c0 : nullptr;
         p.out = r.out ? r.out + (int64_t)c0 * Hq * D : nullptr;
@@ -555,6 +556,28 @@ PDA_EXPORT pda_status pda_plan_units(const int32_t* lens, int32_t batch, int32_t
         pfx += nb;
     }
     return PDA_OK;
+}
+
+PDA_EXPORT pda_status pda_decode_contiguous(pda_ctx* ctx, const pda_bf16* q, const pda_bf16* k,
+                                            const pda_bf16* v, int32_t max_seq_len,
+                                            const int32_t* seq_lens, int32_t batch, float scale,
+                                            pda_bf16* out, pda_stream stream) {
+    if (!ctx) return fail(PDA_ERR_INVALID_ARG, "ctx is NULL");
+    const pda_dims& d = ctx->dims;
+    if (max_seq_len < 1 || max_seq_len % d.block_size != 0)
+        return fail(PDA_ERR_INVALID_ARG, "max_seq_len %d must be a positive multiple of block_size %d",
+                    max_seq_len, d.block_size);
+    const int32_t per_seq = max_seq_len / d.block_size;
+    // [batch, S, Hkv, D] read as blocks of block_size tokens: block b*(S/bs)+j.
+    RunArgs r = {pda::kOneShot, q,
+                 {k, v, (int64_t)batch * per_seq, (int64_t)d.block_size * d.num_kv_heads * d.head_dim,
+                  (int64_t)d.num_kv_heads * d.head_dim, (int64_t)d.head_dim},
+                 nullptr, per_seq, seq_lens, 0, nullptr, batch, scale, out, nullptr, nullptr, nullptr,
+                 (cudaStream_t)stream, true};
+    if (batch > pda::kMaxLaunchBatch)
+        return fail(PDA_ERR_INVALID_ARG, "contiguous decode carries at most %d sequences per call",
+                    pda::kMaxLaunchBatch);
+    return run(ctx, r);
 }
 
 // ---------------------------------------------------------------------------

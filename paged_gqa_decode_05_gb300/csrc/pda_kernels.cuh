@@ -58,6 +58,13 @@ struct Cfg {
     static constexpr int kMaxRegs = D == 256 ? 255 : 168;
 };
 
+// Entry idx of sequence b's block list: the table row, or, for a contiguous
+// cache [B, S, Hkv, D] (no table), block b * (S / bs) + idx.
+__device__ __forceinline__ int32_t table_entry(const SplitParams& p, int b, int idx) {
+    if (p.table == nullptr) return b * p.table_stride + idx;
+    return p.table[(int64_t)b * p.table_stride + idx];
+}
+
 // Blocks of sequence b, validated and clamped (flags bad lengths).
 __device__ __forceinline__ int32_t seq_blocks(const SplitParams& p, int b) {
     int32_t len = p.lens[b];
@@ -150,7 +157,6 @@ __device__ __forceinline__ void run_producer(const SplitParams& p, uint32_t base
     int b = 0, kvh = 0;
     int32_t j = 0, nb = 0;
     int32_t win = 0, id0 = 0, id1 = 0;
-    const int32_t* row = p.table;
     if (pos < end) {
         int lo = 0, hi = p.B - 1;  // largest b with pfx[b]*Hkv <= pos
         while (lo < hi) {
@@ -162,10 +168,9 @@ __device__ __forceinline__ void run_producer(const SplitParams& p, uint32_t base
         const int64_t rem = pos - (int64_t)pfx[b] * Hkv;
         kvh = (int)(rem / nb);
         j = (int32_t)(rem % nb);
-        row = p.table + (int64_t)b * p.table_stride;
         win = j;
-        id0 = win + lane < nb ? row[win + lane] : 0;
-        id1 = win + 32 + lane < nb ? row[win + 32 + lane] : 0;
+        id0 = win + lane < nb ? table_entry(p, b, win + lane) : 0;
+        id1 = win + 32 + lane < nb ? table_entry(p, b, win + 32 + lane) : 0;
     }
     bool seg_begin = true;
     bool whole = false;
@@ -238,16 +243,15 @@ __device__ __forceinline__ void run_producer(const SplitParams& p, uint32_t base
             }
             nb = b < p.B ? pfx[b + 1] - pfx[b] : 0;
             if (pos < end) {
-                row = p.table + (int64_t)b * p.table_stride;
                 win = 0;
-                id0 = lane < nb ? row[lane] : 0;
-                id1 = 32 + lane < nb ? row[32 + lane] : 0;
+                id0 = lane < nb ? table_entry(p, b, lane) : 0;
+                id1 = 32 + lane < nb ? table_entry(p, b, 32 + lane) : 0;
             }
         } else if (j - win >= 32) {
             // first half consumed: slide the window and fetch the next 32 ids
             win += 32;
             id0 = id1;
-            id1 = win + 32 + lane < nb ? row[win + 32 + lane] : 0;
+            id1 = win + 32 + lane < nb ? table_entry(p, b, win + 32 + lane) : 0;
         }
         if (++stage == S) { stage = 0; phase ^= 1u; }
     }

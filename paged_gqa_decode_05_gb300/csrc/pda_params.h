@@ -36,7 +36,7 @@ struct SplitParams {
     CUtensorMap tm_k;            // K pool, 5-D {64, bs, D/64, Hkv, num_blocks}, box {64, bs, D/64, 1, 1}
     CUtensorMap tm_v;            // V pool, same shape
     const uint16_t* q;           // [B, Hq, D] bf16
-    const int32_t* table;        // [B, table_stride] block ids
+    const int32_t* table;        // [B, table_stride] block ids; null = contiguous cache
     const int32_t* lens;         // [B] tokens (one-shot) or block counts (tiled)
     const int32_t* last_valid;   // [B] valid slots of the last listed block (tiled) or null
     uint16_t* out;               // [B, Hq, D] bf16 (one-shot)

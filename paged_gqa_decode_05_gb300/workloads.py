@@ -215,6 +215,25 @@ def ragged(seed: int = 1004) -> Workload:
                          Hkv=8, D=128, block_size=32, seq_lens=lens, seed=seed, max_blocks=1024)
 
 
+def contiguous_kv(w: Workload, max_seq_len: Optional[int] = None):
+    """The workload's cache copied to the contiguous layout [B, S, Hkv, D]
+    (S = max_seq_len, default the longest sequence rounded up to a block),
+    rows past a sequence's length filled with N(0,1) bf16 draws.  Returns
+    (k, v) as uint16 arrays; a pure copy of the inputs."""
+    bs = w.block_size
+    S = max_seq_len or int(-(-int(w.seq_lens.max()) // bs) * bs) if w.B else bs
+    rng = np.random.Generator(np.random.PCG64(np.random.SeedSequence([w.seed, 11])))
+    k = _normal_bits(rng, (w.B, S, w.Hkv, w.D))
+    v = _normal_bits(rng, (w.B, S, w.Hkv, w.D))
+    for b in range(w.B):
+        n = int(w.seq_lens[b])
+        t = np.arange(n)
+        blk = w.block_table[b, t // bs]
+        k[b, :n] = w.k_pool[blk, t % bs]
+        v[b, :n] = w.v_pool[blk, t % bs]
+    return k, v
+
+
 WORKLOADS: Dict[str, Callable[[], Workload]] = {
     "tiny": tiny,
     "1b": one_b,
