@@ -48,6 +48,8 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="8b")
+    ap.add_argument("--block-size", type=int, default=0,
+                    help="redraw the workload with this block size (e.g. 1 for token pages)")
     ap.add_argument("--layout", choices=["paged", "contiguous"], default="paged",
                     help="contiguous: the same cache copied to [B, S, Hkv, D] and decoded "
                          "with pda_decode_contiguous")
@@ -248,6 +250,8 @@ def run_ours(args):
             dist.barrier()
 
     w = workloads.WORKLOADS[args.workload]()
+    if args.block_size:
+        w = workloads.with_block_size(w, args.block_size)
     bytes_per_call = w.algorithmic_bytes()
     props = torch.cuda.get_device_properties(dev)
     l2 = int(getattr(props, "L2_cache_size", 129 * 2 ** 20))

@@ -77,7 +77,10 @@ enum {
  *                  1..8 in this build.  q head h reads KV head h / G.
  *   head_dim       D; [TA] validate caps it at 256; this build has kernels for
  *                  64, 128 and 256.
- *   block_size     tokens per KV block: 8, 16, 32 or 64 in this build.
+ *   block_size     tokens per KV block: 1, 2, 4, 8, 16, 32 or 64 in this build
+ *                  (from 8 up, one TMA copy per block and pool; below 8 the
+ *                  rows are gathered with 16-byte copies).  block_size 1 is
+ *                  the token-granular page of [CK] Attention Backend.
  *   tile_capacity  most block ids per sequence in one pda_step_tile call.
  */
 typedef struct pda_dims {

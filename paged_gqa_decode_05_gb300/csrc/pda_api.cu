@@ -111,6 +111,26 @@ pda_status encode_pool(const pda_ctx* ctx, const void* base, const PoolArgs& a, 
     return PDA_OK;
 }
 
+// For block sizes below 8: a 2-D view {D, rows} of a pool whose three strides
+// are multiples of D, box {64, 1}, for TMA gather4 (four rows per copy).
+// Returns false (no error) when the layout does not fit that view.
+bool encode_rows(const pda_ctx* ctx, const void* base, const PoolArgs& a, CUtensorMap* tm) {
+    auto enc = tensor_map_encoder();
+    const pda_dims& d = ctx->dims;
+    const int64_t D = d.head_dim;
+    if (!enc || a.blk % D || a.tok % D || a.kvh % D) return false;
+    const int64_t rows = (a.num_blocks - 1) * (a.blk / D) + (int64_t)(d.block_size - 1) * (a.tok / D) +
+                         (int64_t)(d.num_kv_heads - 1) * (a.kvh / D) + 1;
+    if (rows >= INT32_MAX) return false;
+    const cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)D * 2};
+    const cuuint32_t box[2] = {64, 1};
+    const cuuint32_t estr[2] = {1, 1};
+    return enc(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 pda_status check_pool(const pda_ctx* ctx, const PoolArgs& a) {
     if (!a.k || !a.v) return fail(PDA_ERR_INVALID_ARG, "k_pool / v_pool must not be NULL");
     if (!aligned(a.k, 16) || !aligned(a.v, 16))
@@ -181,10 +201,16 @@ pda_status run(pda_ctx* ctx, const RunArgs& r) {
 
     pda::SplitParams p;
     std::memset(&p, 0, sizeof p);
-    st = encode_pool(ctx, r.pool.k, r.pool, &p.tm_k);
-    if (st != PDA_OK) return st;
-    st = encode_pool(ctx, r.pool.v, r.pool, &p.tm_v);
-    if (st != PDA_OK) return st;
+    int32_t row_mode = 0;
+    if (d.block_size >= 8) {
+        st = encode_pool(ctx, r.pool.k, r.pool, &p.tm_k);
+        if (st != PDA_OK) return st;
+        st = encode_pool(ctx, r.pool.v, r.pool, &p.tm_v);
+        if (st != PDA_OK) return st;
+    } else {
+        row_mode = encode_rows(ctx, r.pool.k, r.pool, &p.tm_k) &&
+                   encode_rows(ctx, r.pool.v, r.pool, &p.tm_v) ? 1 : 2;
+    }
 
     const int32_t Hq = d.num_q_heads, Hkv = d.num_kv_heads, D = d.head_dim;
     const bool timing = ctx->ev_begin && ctx->ev_split && ctx->ev_end && r.mode == pda::kOneShot;
@@ -204,6 +230,15 @@ pda_status run(pda_ctx* ctx, const RunArgs& r) {
         p.dbg_k = r.dbg_k ? r.dbg_k + (int64_t)c0 * Hkv * dbg_row_tokens * D : nullptr;
         p.dbg_v = r.dbg_v ? r.dbg_v + (int64_t)c0 * Hkv * dbg_row_tokens * D : nullptr;
         p.num_blocks = r.pool.num_blocks;
+        p.k_base = r.pool.k;
+        p.v_base = r.pool.v;
+        p.blk_s = r.pool.blk;
+        p.tok_s = r.pool.tok;
+        p.kvh_s = r.pool.kvh;
+        p.row_gather = row_mode;
+        p.row_blk = r.pool.blk / d.head_dim;
+        p.row_tok = r.pool.tok / d.head_dim;
+        p.row_kvh = r.pool.kvh / d.head_dim;
         p.table_stride = r.table_stride;
         p.lens_are_blocks = r.lens_are_blocks;
         p.B = cb;
@@ -280,8 +315,9 @@ PDA_EXPORT pda_status pda_check_dims(const pda_dims* d) {
     if (d->head_dim != 64 && d->head_dim != 128 && d->head_dim != 256)
         return fail(PDA_ERR_UNSUPPORTED, "head_dim %d: kernels exist for 64, 128 and 256", d->head_dim);
     const int bs = d->block_size;
-    if (bs != 8 && bs != 16 && bs != 32 && bs != 64)
-        return fail(PDA_ERR_UNSUPPORTED, "block_size %d: kernels exist for 8, 16, 32 and 64", bs);
+    if (bs != 1 && bs != 2 && bs != 4 && bs != 8 && bs != 16 && bs != 32 && bs != 64)
+        return fail(PDA_ERR_UNSUPPORTED, "block_size %d: kernels exist for 1, 2, 4, 8, 16, 32 and 64",
+                    bs);
     const int G = d->num_q_heads / d->num_kv_heads;
     if (G > pda::kMaxGroup)
         return fail(PDA_ERR_UNSUPPORTED, "group size %d: at most %d q heads per kv head", G, pda::kMaxGroup);

@@ -177,6 +177,11 @@ __device__ __forceinline__ void run_producer(const SplitParams& p, uint32_t base
     while (pos < end) {
         const int stop = __shfl_sync(0xffffffffu, leader ? *abort_flag : 0, 0);
         if (stop) { ok = false; break; }
+        if (p.row_gather && win != j) {  // up to 64 blocks per stage: reload the window
+            win = j;
+            id0 = win + lane < nb ? table_entry(p, b, win + lane) : 0;
+            id1 = win + 32 + lane < nb ? table_entry(p, b, win + 32 + lane) : 0;
+        }
         const int32_t n = (int32_t)min((int64_t)min(NB, nb - j), end - pos);
         const bool unit_end = (j + n == nb);
         const bool seg_end = unit_end || (pos + n == end);
@@ -203,8 +208,12 @@ __device__ __forceinline__ void run_producer(const SplitParams& p, uint32_t base
             m.pad0 = m.pad1 = 0;
             meta[stage] = m;
             const bool load_q = seg_begin && MODE != kGather;
-            const uint32_t bytes = (uint32_t)n * 2u * (uint32_t)bs * D * 2u +
-                                   (load_q ? (uint32_t)(p.G * D * 2) : 0u);
+            const int rows = (n - 1) * bs + lastv;
+            const uint32_t kv_bytes =
+                p.row_gather == 0 ? (uint32_t)n * 2u * (uint32_t)bs * D * 2u
+                : p.row_gather == 1 ? (uint32_t)((rows + 3) >> 2) * 2u * 4u * D * 2u
+                                    : 0u;  // cp.async completions arrive instead
+            const uint32_t bytes = kv_bytes + (load_q ? (uint32_t)(p.G * D * 2) : 0u);
             mbar_arrive_expect_tx(full, bytes);
             if (load_q) {
                 const uint16_t* src = p.q + ((int64_t)b * p.Hq + (int64_t)kvh * p.G) * D;
@@ -212,6 +221,68 @@ __device__ __forceinline__ void run_producer(const SplitParams& p, uint32_t base
             }
         }
         __syncwarp();
+        if (p.row_gather == 1) {
+            // Rows of small blocks, 4 per TMA gather4 copy of one 64-column slab:
+            // group g covers stage rows 4g..4g+3 (the tail repeats the last row,
+            // which the consumers mask), written as one 64-row block.
+            constexpr int H = C::kHalves;
+            const int lbs = 31 - __clz(bs);
+            const int rows = (n - 1) * bs + lastv;
+            const int groups = (rows + 3) >> 2;
+            for (int o0 = 0; o0 < 16 * H; o0 += 32) {
+                const int o = o0 + lane;
+                const int g = o / H, h = o - g * H;
+                int32_t r[4];
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const int t = min(4 * g + k, rows - 1);
+                    const int i = t >> lbs;  // block of the stage (< 64)
+                    const int32_t a = __shfl_sync(0xffffffffu, id0, i & 31);
+                    const int32_t cc = __shfl_sync(0xffffffffu, id1, i & 31);
+                    int32_t id = i < 32 ? a : cc;
+                    if (o < groups * H && (id < 0 || (int64_t)id >= p.num_blocks)) {
+                        atomicOr(p.err, PDA_DEVERR_BAD_BLOCK_ID_);
+                        id = 0;
+                    }
+                    r[k] = (int32_t)((int64_t)id * p.row_blk + (int64_t)(t & (bs - 1)) * p.row_tok +
+                                     (int64_t)kvh * p.row_kvh);
+                }
+                if (o < groups * H) {
+                    const uint32_t dst = (uint32_t)h * kHalfBytes + (uint32_t)(4 * g) * 128u;
+                    tma_gather4(sK + dst, &p.tm_k, h * 64, r[0], r[1], r[2], r[3], full, pol);
+                    tma_gather4(sV + dst, &p.tm_v, h * 64, r[0], r[1], r[2], r[3], full, pol);
+                }
+            }
+        } else if (p.row_gather == 2) {
+            // Rows of small blocks: 16-byte cp.async chunks, CH per row, written
+            // in the layout of one 64-row block ([slab][row][128 B], swizzled).
+            constexpr int CH = D / 8;
+            constexpr int RPI = 32 / CH;  // rows per pass of the warp
+            const int c = lane % CH, sub = lane / CH;
+            const int lbs = 31 - __clz(bs);
+            const int rows = (n - 1) * bs + lastv;
+            const uint16_t* kb = p.k_base + (int64_t)kvh * p.kvh_s + c * 8;
+            const uint16_t* vb = p.v_base + (int64_t)kvh * p.kvh_s + c * 8;
+            for (int t0 = 0; t0 < rows; t0 += RPI) {
+                const int t = t0 + sub;
+                const int i = t >> lbs;  // block of the stage (< 64)
+                const int32_t a = __shfl_sync(0xffffffffu, id0, i & 31);
+                const int32_t cc = __shfl_sync(0xffffffffu, id1, i & 31);
+                if (t < rows) {
+                    int32_t id = i < 32 ? a : cc;
+                    if (id < 0 || (int64_t)id >= p.num_blocks) {
+                        atomicOr(p.err, PDA_DEVERR_BAD_BLOCK_ID_);
+                        id = 0;
+                    }
+                    const int64_t off = (int64_t)id * p.blk_s + (int64_t)(t & (bs - 1)) * p.tok_s;
+                    const uint32_t dst = (uint32_t)(c >> 3) * kHalfBytes + (uint32_t)t * 128u +
+                                         (uint32_t)(((c & 7) ^ (t & 7)) << 4);
+                    cp_async_16(sK + dst, kb + off);
+                    cp_async_16(sV + dst, vb + off);
+                }
+            }
+            cp_async_mbar_arrive_noinc(full);
+        } else
         // lane i copies block i of the stage (its id comes from the window;
         // j + i - win < 40 by the window rule below)
         {
@@ -259,7 +330,8 @@ __device__ __forceinline__ void run_producer(const SplitParams& p, uint32_t base
     if (ok) {
         if (mbar_wait_bounded(empty0 + 8 * stage, phase ^ 1u, kWaitLimitNs)) {
             meta[stage].flags = kDone;
-            mbar_arrive(full0 + 8 * stage);
+            // every arrival the stage's barrier expects (33 for cp.async rows)
+            mbar_arrive_count(full0 + 8 * stage, p.row_gather == 2 ? 33u : 1u);
         } else {
             ok = false;
         }
@@ -360,7 +432,7 @@ __device__ __forceinline__ void run_consumer(const SplitParams& p, uint32_t base
     const int pv_row = r0 + (lane & 7) + ((lane >> 4) << 3);
     const int pv_cpar = (lane >> 3) & 1;
     const int sw = lane & 7;  // == row & 7 for both
-    const int lbs = 31 - __clz(p.bs);
+    const int lbs = p.row_gather ? 6 : 31 - __clz(p.bs);  // smem block = 64 rows when gathered
     const uint32_t hs = (uint32_t)(128 << lbs);  // bytes between 64-column slabs of a block
     const uint32_t qk_off = row_off<D>(qk_row, lbs);
     const uint32_t pv_off = row_off<D>(pv_row, lbs);
@@ -574,7 +646,9 @@ __global__ void __maxnreg__(Cfg<D>::kMaxRegs) split_kernel(const __grid_constant
     if (MODE != kGather) pdl_launch_dependents();
     if (tid == 0) {
         for (int s = 0; s < Cfg<D>::kStages; ++s) {
-            mbar_init(base_s + L.bars + 8 * s, 1);
+            // full: the producer's arrive (+ one cp.async arrival per lane when
+            // rows are copied with cp.async); empty: one arrival per consumer warp
+            mbar_init(base_s + L.bars + 8 * s, p.row_gather == 2 ? 33 : 1);
             mbar_init(base_s + L.bars + 8 * (Cfg<D>::kStages + s), kConsumerWarps);
         }
         mbar_init(base_s + L.cbar, kConsumerWarps * 32);

@@ -33,7 +33,8 @@ struct StageMeta {
 enum MetaFlags : int32_t { kSegBegin = 1, kSegEnd = 2, kWholeUnit = 4, kDone = 8 };
 
 struct SplitParams {
-    CUtensorMap tm_k;            // K pool, 5-D {64, bs, D/64, Hkv, num_blocks}, box {64, bs, D/64, 1, 1}
+    CUtensorMap tm_k;            // K pool, 5-D {64, bs, D/64, Hkv, num_blocks}, box {64, bs, D/64, 1, 1};
+                                 // for gather4 2-D {D, rows}, box {64, 1}
     CUtensorMap tm_v;            // V pool, same shape
     const uint16_t* q;           // [B, Hq, D] bf16
     const int32_t* table;        // [B, table_stride] block ids; null = contiguous cache
@@ -47,8 +48,14 @@ struct SplitParams {
     uint32_t* err;               // device error flags
     uint16_t* dbg_k;             // gather check outputs
     uint16_t* dbg_v;
+    const uint16_t* k_base;      // pool base pointers and element strides, for the
+    const uint16_t* v_base;      // row-gather loader (block sizes below 8)
+    int64_t blk_s, tok_s, kvh_s;
     int64_t num_blocks;
     int32_t table_stride;
+    int32_t row_gather;          // 0: one 5-D TMA box per block; 1: TMA gather4 of rows
+                                 // (block sizes below 8); 2: 16-byte cp.async rows
+    int64_t row_blk, row_tok, row_kvh;  // strides in rows of D elements (gather4)
     int32_t lens_are_blocks;
     int32_t B, Hq, Hkv, G, bs;
     int32_t dbg_row_tokens;      // tokens per (b, kvh) row of the gather output

@@ -36,6 +36,10 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
+__device__ __forceinline__ void mbar_arrive_count(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
@@ -82,6 +86,18 @@ __device__ __forceinline__ void tma_load_5d(uint32_t dst, const void* tm, int32_
         : "memory");
 }
 
+// Four rows (r0..r3) of a 2-D tiled tensor, one box {64 columns, 1 row} each,
+// starting at column c0: 4 x 128 bytes land consecutively (swizzled).
+__device__ __forceinline__ void tma_gather4(uint32_t dst, const void* tm, int32_t c0, int32_t r0,
+                                            int32_t r1, int32_t r2, int32_t r3, uint32_t bar,
+                                            uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cta.global.tile::gather4.mbarrier::complete_tx::bytes"
+        ".L2::cache_hint [%0], [%1, {%2, %3, %4, %5, %6}], [%7], %8;" ::"r"(dst),
+        "l"(tm), "r"(c0), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(bar), "l"(policy)
+        : "memory");
+}
+
 // Contiguous bulk copy global -> shared (16-byte aligned, size % 16 == 0).
 __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
                                           uint32_t bar) {
@@ -90,6 +106,17 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
             dst),
         "l"(src), "r"(bytes), "r"(bar)
         : "memory");
+}
+
+// 16-byte asynchronous copy global -> shared through L2 only.
+__device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+
+// Arrives on `bar` once all earlier cp.async copies of this thread have
+// landed (the arrival is part of the barrier's expected count).
+__device__ __forceinline__ void cp_async_mbar_arrive_noinc(uint32_t bar) {
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
 }
 
 __device__ __forceinline__ uint64_t policy_evict_first() {

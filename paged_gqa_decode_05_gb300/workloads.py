@@ -215,6 +215,13 @@ def ragged(seed: int = 1004) -> Workload:
                          Hkv=8, D=128, block_size=32, seq_lens=lens, seed=seed, max_blocks=1024)
 
 
+def with_block_size(w: Workload, block_size: int) -> Workload:
+    """The same batch shape and lengths drawn afresh with another block size
+    (the pool holds exactly the needed blocks, shuffled)."""
+    return make_workload(f"{w.name} (block {block_size})", B=w.B, Hq=w.Hq, Hkv=w.Hkv, D=w.D,
+                         block_size=block_size, seq_lens=w.seq_lens, seed=w.seed)
+
+
 def contiguous_kv(w: Workload, max_seq_len: Optional[int] = None):
     """The workload's cache copied to the contiguous layout [B, S, Hkv, D]
     (S = max_seq_len, default the longest sequence rounded up to a block),

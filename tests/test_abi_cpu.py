@@ -44,7 +44,9 @@ def test_version_and_status_strings(lib):
     (dict(num_q_heads=32, num_kv_heads=7, head_dim=128, block_size=16), pda.ERR_INVALID_ARG),
     (dict(num_q_heads=32, num_kv_heads=8, head_dim=512, block_size=16), pda.ERR_INVALID_ARG),
     (dict(num_q_heads=32, num_kv_heads=8, head_dim=96, block_size=16), pda.ERR_UNSUPPORTED),
-    (dict(num_q_heads=32, num_kv_heads=8, head_dim=128, block_size=1), pda.ERR_UNSUPPORTED),
+    (dict(num_q_heads=32, num_kv_heads=8, head_dim=128, block_size=1), 0),
+    (dict(num_q_heads=32, num_kv_heads=8, head_dim=128, block_size=3), pda.ERR_UNSUPPORTED),
+    (dict(num_q_heads=32, num_kv_heads=8, head_dim=128, block_size=128), pda.ERR_UNSUPPORTED),
     (dict(num_q_heads=32, num_kv_heads=2, head_dim=128, block_size=16), pda.ERR_UNSUPPORTED),
     (dict(num_q_heads=0, num_kv_heads=8, head_dim=128, block_size=16), pda.ERR_INVALID_ARG),
 ])

@@ -24,11 +24,12 @@ def _w(seed=1, D=128, bs=16, G=4, Hkv=2, lens=(300, 1, 0, 129, 64), pool=None, w
                          seq_lens=list(lens), seed=seed, pool_blocks=pool, max_blocks=width)
 
 
-@pytest.mark.parametrize("D,bs", [(64, 16), (128, 32), (256, 8), (128, 64)])
+@pytest.mark.parametrize("D,bs", [(64, 16), (128, 32), (256, 8), (128, 64), (128, 1), (64, 2),
+                                  (256, 4)])
 def test_gather_bit_exact(D, bs):
     """The loader's staged rows equal the oracle's gather, byte for byte."""
     import torch
-    w = _w(seed=D + bs, D=D, bs=bs, lens=(5, 200, 0, 3 * bs, 1000), pool=200)
+    w = _w(seed=D + bs, D=D, bs=bs, lens=(5, 200, 0, 3 * bs, 1000), pool=200 if bs >= 8 else None)
     ctx = context_for(w)
     t = upload(w)
     k_rows, v_rows = ctx.debug_gather(t["k_pool"], t["v_pool"], t["block_table"], t["seq_lens"])
@@ -91,11 +92,12 @@ def test_garbage_outside_valid_rows_ignored():
     assert ctx.read_device_errors() == 0
 
 
-def test_slot_layout_strides_identical():
+@pytest.mark.parametrize("bs", [16, 2])
+def test_slot_layout_strides_identical(bs):
     """The same cache in the slot layout [slot, K|V, kv_head, block, D]."""
     import torch
     import paged_gqa_decode_05_gb300 as pda
-    w = _w(seed=7, lens=(100, 257, 3))
+    w = _w(seed=7, bs=bs, lens=(100, 257, 3))
     ctx = context_for(w)
     base = _decode(ctx, w).cpu().float().numpy()
     nb, bs, Hkv, D = w.k_pool.shape
@@ -168,3 +170,25 @@ def test_invalid_arguments_rejected():
     with pytest.raises(pda.PdaError):  # batch > max_seqs
         ctx.decode(tb["q"], tb["k_pool"], tb["v_pool"], tb["block_table"], tb["seq_lens"])
     torch.cuda.synchronize()
+
+
+@pytest.mark.parametrize("bs", [2, 16])
+def test_padded_token_stride_identical(bs):
+    """Token rows padded by 8 elements (strides not multiples of D): block size
+    2 takes the 16-byte copy loader, 16 the TMA boxes; both match the dense pool."""
+    import torch
+    w = _w(seed=13, bs=bs, lens=(77, 300, 2))
+    ctx = context_for(w)
+    base = _decode(ctx, w).cpu().float().numpy()
+    nb, _, Hkv, D = w.k_pool.shape
+    row = Hkv * D + 8
+    def padded(pool):
+        a = np.zeros((nb, bs, row), dtype=np.uint16)
+        a[:, :, :Hkv * D] = pool.reshape(nb, bs, Hkv * D)
+        return dev(a.ravel())
+    t = upload(w)
+    out = ctx.decode(t["q"], padded(w.k_pool), padded(w.v_pool), t["block_table"], t["seq_lens"],
+                     strides=(bs * row, row, D), num_blocks=nb)
+    torch.cuda.synchronize()
+    assert ctx.read_device_errors() == 0
+    assert np.array_equal(out.cpu().float().numpy(), base)

@@ -45,7 +45,7 @@ def _lens(bs, extra=()):
 
 
 @pytest.mark.parametrize("D", [64, 128, 256])
-@pytest.mark.parametrize("bs", [8, 16, 32, 64])
+@pytest.mark.parametrize("bs", [1, 2, 4, 8, 16, 32, 64])
 @pytest.mark.parametrize("G", [1, 2, 4, 8])
 def test_shape_sweep(orc, D, bs, G):
     Hkv = 2 if G < 8 else 1
