@@ -55,6 +55,9 @@ class Oracle:
         lib.pdo_decode.restype = ctypes.c_int
         lib.pdo_decode.argtypes = [p, p, p, p, p, i32, i32, i32, i32, i32, i64, i32,
                                    i64, i64, i64, ctypes.c_double, p, i64, i32, p]
+        lib.pdo_decode_multi.restype = ctypes.c_int
+        lib.pdo_decode_multi.argtypes = [p, p, p, p, p, i32, i32, i32, i32, i32, i32, i64, i32,
+                                         i64, i64, i64, ctypes.c_double, i32, p]
         lib.pdo_gather.restype = ctypes.c_int
         lib.pdo_gather.argtypes = [p, p, p, p, i32, i32, i32, i32, i64, i32,
                                    i64, i64, i64, i32, i32, p, p]
@@ -105,6 +108,31 @@ class Oracle:
                                  int(max(1, n_threads)), self._ptr(out))
         if st != _OK:
             raise ValueError(f"oracle decode failed: {_ERRORS.get(st, st)}")
+        return out
+
+    def decode_multi(self, q, k_pool, v_pool, block_table, seq_lens, *, q_len: int, Hq: int,
+                     Hkv: int, D: int, block_size: int, scale: Optional[float] = None,
+                     strides: Optional[Sequence[int]] = None, n_threads: int = 1) -> np.ndarray:
+        """Causal multi-query outputs [B, q_len, Hq, D] (q is [B, q_len, Hq, D])."""
+        q = np.ascontiguousarray(q, dtype=np.uint16)
+        k_pool = np.ascontiguousarray(k_pool, dtype=np.uint16)
+        v_pool = np.ascontiguousarray(v_pool, dtype=np.uint16)
+        block_table = np.ascontiguousarray(block_table, dtype=np.int32)
+        seq_lens = np.ascontiguousarray(seq_lens, dtype=np.int32)
+        B = seq_lens.shape[0]
+        if strides is None:
+            strides = (block_size * Hkv * D, Hkv * D, D)
+        blk_s, tok_s, kvh_s = (int(x) for x in strides)
+        if scale is None:
+            scale = 1.0 / np.sqrt(D)
+        out = np.zeros((B, q_len, Hq, D), dtype=np.float64)
+        st = self.lib.pdo_decode_multi(self._ptr(q), self._ptr(k_pool), self._ptr(v_pool),
+                                       self._ptr(block_table), self._ptr(seq_lens), B, q_len, Hq,
+                                       Hkv, D, block_size, k_pool.size // blk_s,
+                                       block_table.shape[1], blk_s, tok_s, kvh_s, float(scale),
+                                       int(max(1, n_threads)), self._ptr(out))
+        if st != _OK:
+            raise ValueError(f"oracle multi-query decode failed: {_ERRORS.get(st, st)}")
         return out
 
     def gather(self, k_pool, v_pool, block_table, seq_lens, *, Hkv: int, D: int,

@@ -72,3 +72,39 @@ def decode(q, k_pool, v_pool, block_table, seq_lens, *, Hq: int, Hkv: int, D: in
                 for d in range(D):
                     out[b][h][d] = math.fsum(w[t] * vs[t][d] for t in range(n)) / z
     return out
+
+
+def decode_multi(q, k_pool, v_pool, block_table, seq_lens, *, q_len: int, Hq: int, Hkv: int,
+                 D: int, block_size: int, scale: Optional[float] = None,
+                 strides: Optional[Sequence[int]] = None) -> List[List[List[List[float]]]]:
+    """out[b][i][h][d] for q as [B][q_len][Hq][D] bits: query i is token
+    seq_lens[b] - q_len + i and sees every token up to and including itself."""
+    if strides is None:
+        strides = (block_size * Hkv * D, Hkv * D, D)
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    G = Hq // Hkv
+    out = []
+    for b in range(len(seq_lens)):
+        L = int(seq_lens[b])
+        rows = []
+        for i in range(q_len):
+            visible = max(0, L - q_len + 1 + i)
+            heads = []
+            for g in range(Hkv):
+                ks, vs = gather_rows(k_pool, v_pool, block_table[b], visible, g, block_size,
+                                     strides, D)
+                for h in range(g * G, g * G + G):
+                    if visible == 0:
+                        heads.append([0.0] * D)
+                        continue
+                    qv = [bf16_value(q[b][i][h][d]) for d in range(D)]
+                    scores = [scale * math.fsum(qv[d] * k[d] for d in range(D)) for k in ks]
+                    top = max(scores)
+                    w = [math.exp(x - top) for x in scores]
+                    z = math.fsum(w)
+                    heads.append([math.fsum(w[t] * vs[t][d] for t in range(visible)) / z
+                                  for d in range(D)])
+            rows.append(heads)
+        out.append(rows)
+    return out

@@ -65,18 +65,18 @@ static int64_t token_block(const problem* P, int32_t b, int32_t t) {
     return blk;
 }
 
-static int attend_one(const problem* P, int32_t b, int32_t h, double* out) {
+/* Attention of query row qrow (q head h) over tokens 0..n-1 of sequence b. */
+static int attend_prefix(const problem* P, int32_t b, int32_t h, int32_t n,
+                         const uint16_t* qrow, double* out) {
     const int32_t D = P->D;
     const int32_t G = P->Hq / P->Hkv;
     const int32_t kvh = h / G;
-    const int32_t n = P->seq_lens[b];
     if (n < 0 || (int64_t)n > (int64_t)P->max_blocks * P->bs) return PDO_ERR_SEQLEN;
     for (int32_t d = 0; d < D; ++d) out[d] = 0.0;
     if (n == 0) return PDO_OK;
 
     double* s = (double*)malloc(sizeof(double) * (size_t)n);
     if (!s) return PDO_ERR_NOMEM;
-    const uint16_t* qrow = P->q + ((int64_t)b * P->Hq + h) * D;
 
     /* scores */
     for (int32_t t = 0; t < n; ++t) {
@@ -104,17 +104,37 @@ static int attend_one(const problem* P, int32_t b, int32_t h, double* out) {
     return PDO_OK;
 }
 
+static int attend_one(const problem* P, int32_t b, int32_t h, double* out) {
+    const uint16_t* qrow = P->q + ((int64_t)b * P->Hq + h) * P->D;
+    return attend_prefix(P, b, h, P->seq_lens[b], qrow, out);
+}
+
 typedef struct {
     const problem* P;
     const int32_t* pairs;
     int64_t begin, end;
     double* out;
     int status;
+    int32_t q_len;  /* > 0: multi-query job over (b, i, h) rows */
 } job;
 
 static void* run_job(void* arg) {
     job* j = (job*)arg;
     j->status = PDO_OK;
+    if (j->q_len > 0) {  /* row i = (b, qi, h) of the [B, q_len, Hq] output */
+        const problem* P = j->P;
+        for (int64_t i = j->begin; i < j->end; ++i) {
+            const int32_t h = (int32_t)(i % P->Hq);
+            const int32_t qi = (int32_t)((i / P->Hq) % j->q_len);
+            const int32_t b = (int32_t)(i / ((int64_t)P->Hq * j->q_len));
+            int32_t n = P->seq_lens[b] - j->q_len + 1 + qi;
+            if (n < 0) n = 0;
+            const uint16_t* qrow = P->q + i * P->D;
+            int st = attend_prefix(P, b, h, n, qrow, j->out + i * P->D);
+            if (st != PDO_OK) { j->status = st; return NULL; }
+        }
+        return NULL;
+    }
     for (int64_t i = j->begin; i < j->end; ++i) {
         int32_t b, h;
         if (j->pairs) { b = j->pairs[2 * i]; h = j->pairs[2 * i + 1]; }
@@ -125,6 +145,9 @@ static void* run_job(void* arg) {
     }
     return NULL;
 }
+
+static int run_jobs(const problem* P, const int32_t* pairs, int64_t total, int32_t q_len,
+                    int32_t n_threads, double* out);
 
 int pdo_decode(const uint16_t* q, const uint16_t* k_pool, const uint16_t* v_pool,
                const int32_t* block_table, const int32_t* seq_lens,
@@ -141,18 +164,25 @@ int pdo_decode(const uint16_t* q, const uint16_t* k_pool, const uint16_t* v_pool
     int64_t total = pairs ? n_pairs : (int64_t)B * Hq;
     if (total < 0) return PDO_ERR_ARG;
     if (total == 0) return PDO_OK;
+
+    return run_jobs(&P, pairs, total, 0, n_threads, out);
+}
+
+/* Runs `total` output rows on n_threads threads (the calling thread included). */
+static int run_jobs(const problem* P, const int32_t* pairs, int64_t total, int32_t q_len,
+                    int32_t n_threads, double* out) {
     if (n_threads < 1) n_threads = 1;
     if ((int64_t)n_threads > total) n_threads = (int32_t)total;
-
     job* jobs = (job*)calloc((size_t)n_threads, sizeof(job));
     pthread_t* tids = (pthread_t*)calloc((size_t)n_threads, sizeof(pthread_t));
     if (!jobs || !tids) { free(jobs); free(tids); return PDO_ERR_NOMEM; }
     for (int32_t i = 0; i < n_threads; ++i) {
-        jobs[i].P = &P;
+        jobs[i].P = P;
         jobs[i].pairs = pairs;
         jobs[i].begin = total * i / n_threads;
         jobs[i].end = total * (i + 1) / n_threads;
         jobs[i].out = out;
+        jobs[i].q_len = q_len;
     }
     int started = 0;
     for (int32_t i = 1; i < n_threads; ++i) {
@@ -163,11 +193,27 @@ int pdo_decode(const uint16_t* q, const uint16_t* k_pool, const uint16_t* v_pool
     /* jobs that could not get a thread run here */
     for (int32_t i = started + 1; i < n_threads; ++i) run_job(&jobs[i]);
     for (int32_t i = 1; i <= started; ++i) pthread_join(tids[i], NULL);
-    st = PDO_OK;
+    int st = PDO_OK;
     for (int32_t i = 0; i < n_threads; ++i) if (jobs[i].status != PDO_OK) { st = jobs[i].status; break; }
     free(jobs);
     free(tids);
     return st;
+}
+
+int pdo_decode_multi(const uint16_t* q, const uint16_t* k_pool, const uint16_t* v_pool,
+                     const int32_t* block_table, const int32_t* seq_lens,
+                     int32_t B, int32_t q_len, int32_t Hq, int32_t Hkv, int32_t D,
+                     int32_t block_size, int64_t num_blocks, int32_t max_blocks,
+                     int64_t blk_stride, int64_t tok_stride, int64_t kvh_stride,
+                     double scale, int32_t n_threads, double* out) {
+    problem P = {q, k_pool, v_pool, block_table, seq_lens, B, Hq, Hkv, D, block_size,
+                 num_blocks, max_blocks, blk_stride, tok_stride, kvh_stride, scale};
+    int st = check_problem(&P);
+    if (st != PDO_OK) return st;
+    if (!out || q_len < 1) return PDO_ERR_ARG;
+    const int64_t total = (int64_t)B * q_len * Hq;
+    if (total == 0) return PDO_OK;
+    return run_jobs(&P, NULL, total, q_len, n_threads, out);
 }
 
 int pdo_gather(const uint16_t* k_pool, const uint16_t* v_pool,

@@ -74,6 +74,23 @@ int pdo_decode(const uint16_t* q, const uint16_t* k_pool, const uint16_t* v_pool
                int32_t n_threads, double* out);
 
 /*
+ * Multi-query (causal) decode: q and out are [B, q_len, Hq, D]; seq_lens[b]
+ * counts the whole sequence including its last q_len tokens, which are the
+ * queries.  Query i of sequence b sits at position seq_lens[b] - q_len + i
+ * and attends to tokens 0 .. seq_lens[b] - q_len + i (a causal mask aligned
+ * to the end of the sequence; AstrAI "CUDA Kernels", Python Wrappers,
+ * is_causal).  A sequence shorter than q_len gives query i the tokens
+ * 0 .. max(seq_lens[b] - q_len + i, -1) (none for negative limits: a zero row).
+ * out is [B][q_len][Hq][D] doubles.
+ */
+int pdo_decode_multi(const uint16_t* q, const uint16_t* k_pool, const uint16_t* v_pool,
+                     const int32_t* block_table, const int32_t* seq_lens,
+                     int32_t B, int32_t q_len, int32_t Hq, int32_t Hkv, int32_t D,
+                     int32_t block_size, int64_t num_blocks, int32_t max_blocks,
+                     int64_t blk_stride, int64_t tok_stride, int64_t kvh_stride,
+                     double scale, int32_t n_threads, double* out);
+
+/*
  * The block-table gather on its own: copies the K and V rows of sequence b,
  * KV head kvh, tokens 0..seq_lens[b]-1 in order, into k_rows / v_rows
  * ([seq_lens[b]][D] bf16 bits each).

@@ -294,6 +294,70 @@ def pin_slot_layout_strides(orc):
     assert np.array_equal(out, base)
 
 
+# --------------------------------------------------------------------------- multi-query (causal)
+
+def _multi(seed, q_len, B=2, Hq=4, Hkv=2, D=8, bs=4, lens=(9, 14)):
+    w = _small(seed, B=B, Hq=Hq, Hkv=Hkv, D=D, bs=bs, lens=lens)
+    rng = np.random.default_rng(seed)
+    q = bf16_bits(rng.standard_normal((B, q_len, Hq, D)).astype(np.float32))
+    return w, q
+
+
+def _run_multi(orc, w, q, q_len, **kw):
+    return orc.decode_multi(q, w.k_pool, w.v_pool, w.block_table, w.seq_lens, q_len=q_len,
+                            Hq=w.Hq, Hkv=w.Hkv, D=w.D, block_size=w.block_size, **kw)
+
+
+def pin_multi_worked_example(orc):
+    with open(GOLDEN) as f:
+        data = json.load(f)
+    for ex in data["multi_query_examples"]:
+        scale = math.log(3.0) if ex["scale"] == "ln3" else float(ex["scale"])
+        out = orc.decode_multi(_bits(ex["q"]), _bits(ex["k_pool"]), _bits(ex["v_pool"]),
+                               np.asarray(ex["block_table"], np.int32),
+                               np.asarray(ex["seq_lens"], np.int32), q_len=ex["q_len"],
+                               Hq=ex["Hq"], Hkv=ex["Hkv"], D=ex["D"], block_size=ex["block_size"],
+                               scale=scale)
+        np.testing.assert_allclose(out, np.asarray(ex["expected"]), rtol=0, atol=1e-13,
+                                   err_msg=ex["name"])
+
+
+def pin_multi_sdpa_causal(orc):
+    """fp64 SDPA with an explicit end-aligned causal mask on a gathered copy."""
+    import torch
+    import torch.nn.functional as F
+    for seed, (q_len, Hq, Hkv, bs, lens) in enumerate([(3, 4, 2, 4, (7, 13)), (5, 8, 1, 2, (5, 9)),
+                                                       (2, 6, 3, 16, (40, 2))]):
+        w, q = _multi(300 + seed, q_len, Hq=Hq, Hkv=Hkv, D=16, bs=bs, lens=lens)
+        out = _run_multi(orc, w, q, q_len)
+        for b in range(w.B):
+            k, v = _dense_kv(w, b)
+            L = int(w.seq_lens[b])
+            qq = torch.from_numpy(bf16_to_f32(q[b]).astype(np.float64)).permute(1, 0, 2)[None]
+            kt = torch.from_numpy(k).permute(1, 0, 2).repeat_interleave(w.G, dim=0)[None]
+            vt = torch.from_numpy(v).permute(1, 0, 2).repeat_interleave(w.G, dim=0)[None]
+            pos = L - q_len + np.arange(q_len)
+            mask = torch.from_numpy(np.arange(L)[None, :] <= pos[:, None])
+            ref = F.scaled_dot_product_attention(qq, kt, vt, attn_mask=mask,
+                                                 scale=1.0 / math.sqrt(w.D))
+            np.testing.assert_allclose(out[b], ref[0].permute(1, 0, 2).numpy(), rtol=0, atol=1e-12)
+
+
+def pin_multi_brute_force(orc):
+    w, q = _multi(310, 3, Hq=4, Hkv=2, D=6, bs=3, lens=(8, 2))
+    ref = brute.decode_multi(q.tolist(), w.k_pool.ravel().tolist(), w.v_pool.ravel().tolist(),
+                             w.block_table.tolist(), w.seq_lens.tolist(), q_len=3, Hq=w.Hq,
+                             Hkv=w.Hkv, D=w.D, block_size=w.block_size)
+    np.testing.assert_allclose(_run_multi(orc, w, q, 3), np.asarray(ref), rtol=0, atol=1e-12)
+
+
+def pin_multi_single_query_is_decode(orc):
+    w, q = _multi(320, 1, lens=(11, 5))
+    out = _run_multi(orc, w, q, 1)
+    w.q = q[:, 0]
+    assert np.array_equal(out[:, 0], _run(orc, w))
+
+
 PINS: Dict[str, Callable] = {name: fn for name, fn in globals().items() if name.startswith("pin_")}
 
 

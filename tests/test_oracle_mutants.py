@@ -20,9 +20,15 @@ MUTANTS = {
     "no normalisation": ("out[d] /= z;", "out[d] /= 1.0;"),
     "values used as keys": ("const uint16_t* krow = P->k_pool +", "const uint16_t* krow = P->v_pool +"),
     "keys used as values": ("const uint16_t* vrow = P->v_pool +", "const uint16_t* vrow = P->k_pool +"),
-    "q row of the kv head": ("((int64_t)b * P->Hq + h) * D", "((int64_t)b * P->Hq + kvh) * D"),
-    "last token dropped": ("const int32_t n = P->seq_lens[b];",
-                           "const int32_t n = P->seq_lens[b] > 1 ? P->seq_lens[b] - 1 : P->seq_lens[b];"),
+    "q row of the kv head": ("P->q + ((int64_t)b * P->Hq + h) * P->D",
+                             "P->q + ((int64_t)b * P->Hq + h / (P->Hq / P->Hkv)) * P->D"),
+    "last token dropped": ("return attend_prefix(P, b, h, P->seq_lens[b], qrow, out);",
+                           "return attend_prefix(P, b, h, P->seq_lens[b] > 1 ? P->seq_lens[b] - 1 : "
+                           "P->seq_lens[b], qrow, out);"),
+    "causal limit off by one": ("int32_t n = P->seq_lens[b] - j->q_len + 1 + qi;",
+                                "int32_t n = P->seq_lens[b] - j->q_len + qi;"),
+    "every query uses the first q row": ("const uint16_t* qrow = P->q + i * P->D;",
+                                         "const uint16_t* qrow = P->q + (i - (int64_t)qi * P->Hq) * P->D;"),
     "slot from block index": ("return blk * P->blk_stride + (int64_t)slot * P->tok_stride",
                               "return blk * P->blk_stride + (int64_t)(slot / 2) * P->tok_stride"),
     "bf16 widened as low half": ("uint32_t u = ((uint32_t)bits) << 16;", "uint32_t u = ((uint32_t)bits) << 15;"),
