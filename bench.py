@@ -50,6 +50,8 @@ def parse_args():
     ap.add_argument("--workload", default="8b")
     ap.add_argument("--block-size", type=int, default=0,
                     help="redraw the workload with this block size (e.g. 1 for token pages)")
+    ap.add_argument("--q-len", type=int, default=1,
+                    help="causal queries per sequence (pda_decode_multi) instead of one")
     ap.add_argument("--layout", choices=["paged", "contiguous"], default="paged",
                     help="contiguous: the same cache copied to [B, S, Hkv, D] and decoded "
                          "with pda_decode_contiguous")
@@ -223,7 +225,8 @@ def run_reference(args):
             "ms_per_step": cb["sec_per_call"] * 1e3, "us_per_call": cb["sec_per_call"] * 1e6,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic (seeded N(0,1) bf16 inputs)",
-            "config": {**w.describe(), "workload": w.name, "kv_layout": args.layout, "runs_on": "host CPU cores"},
+            "config": {**w.describe(), "workload": w.name, "kv_layout": args.layout,
+                   "q_len": args.q_len, "runs_on": "host CPU cores"},
             "cpu_baseline": {k: cb[k] for k in ("value", "unit", "cores", "kind", "sample")},
             "e2e": {"value": cb["value"], "unit": "GB/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
@@ -252,7 +255,10 @@ def run_ours(args):
     w = workloads.WORKLOADS[args.workload]()
     if args.block_size:
         w = workloads.with_block_size(w, args.block_size)
-    bytes_per_call = w.algorithmic_bytes()
+    if args.q_len > 1:
+        w.q = workloads.multi_queries(w, args.q_len)
+    # K+V of valid tokens once, q in and out (q_len rows each)
+    bytes_per_call = w.algorithmic_bytes() + (args.q_len - 1) * 2 * w.B * w.Hq * w.D * 2
     props = torch.cuda.get_device_properties(dev)
     l2 = int(getattr(props, "L2_cache_size", 129 * 2 ** 20))
     input_bytes = (w.q.nbytes + w.k_pool.nbytes + w.v_pool.nbytes + w.block_table.nbytes
@@ -272,9 +278,10 @@ def run_ours(args):
         host = {"q": w.q, "k_pool": w.k_pool, "v_pool": w.v_pool, "block_table": w.block_table,
                 "seq_lens": w.seq_lens}
     sets = [{k: to_dev(v) for k, v in host.items()} for _ in range(n_sets)]
-    outs = [torch.empty((w.B, w.Hq, w.D), device=dev, dtype=torch.bfloat16) for _ in range(n_sets)]
-    ctx = pda.Context(max_seqs=w.B, num_q_heads=w.Hq, num_kv_heads=w.Hkv, head_dim=w.D,
-                      block_size=w.block_size)
+    outs = [torch.empty(tuple(sets[0]["q"].shape), device=dev, dtype=torch.bfloat16)
+            for _ in range(n_sets)]
+    ctx = pda.Context(max_seqs=w.B * args.q_len, num_q_heads=w.Hq, num_kv_heads=w.Hkv,
+                      head_dim=w.D, block_size=w.block_size)
     stream = torch.cuda.current_stream()
 
     counter = [0]
@@ -284,7 +291,10 @@ def run_ours(args):
         i = counter[0]
         counter[0] += 1
         s = sets[i % n_sets]
-        if args.layout == "contiguous":
+        if args.q_len > 1:
+            ctx.decode_multi(s["q"], s["k_pool"], s["v_pool"], s["block_table"], s["seq_lens"],
+                             out=outs[i % n_sets])
+        elif args.layout == "contiguous":
             ctx.decode_contiguous(s["q"], s["k_pool"], s["v_pool"], s["seq_lens"],
                                   out=outs[i % n_sets])
         else:
@@ -357,7 +367,7 @@ def run_ours(args):
     if not (args.no_e2e or args.quick):
         pinned = {k: torch.from_numpy(v.view(np.int16) if v.dtype == np.uint16 else v).pin_memory()
                   for k, v in host.items()}
-        out_host = torch.empty((w.B, w.Hq, w.D), dtype=torch.bfloat16).pin_memory()
+        out_host = torch.empty(tuple(outs[0].shape), dtype=torch.bfloat16).pin_memory()
         dst = sets[0]
         h2d = sum(t.numel() * t.element_size() for t in pinned.values())
         d2h = out_host.numel() * out_host.element_size()
@@ -367,7 +377,10 @@ def run_ours(args):
             for k, t in pinned.items():
                 d = dst[k].view(torch.int16) if dst[k].dtype == torch.bfloat16 else dst[k]
                 d.copy_(t, non_blocking=True)
-            if args.layout == "contiguous":
+            if args.q_len > 1:
+                ctx.decode_multi(dst["q"], dst["k_pool"], dst["v_pool"], dst["block_table"],
+                                 dst["seq_lens"], out=outs[0])
+            elif args.layout == "contiguous":
                 ctx.decode_contiguous(dst["q"], dst["k_pool"], dst["v_pool"], dst["seq_lens"],
                                       out=outs[0])
             else:
@@ -411,6 +424,7 @@ def run_ours(args):
         "dtype": "bf16",
         "data": "synthetic: seeded N(0,1) q/K/V rounded to bf16, shuffled block table",
         "config": {**w.describe(), "workload": w.name, "kv_layout": args.layout,
+                   "q_len": args.q_len,
                    "l2": f"inputs larger than L2 ({input_bytes / 1e6:.0f} MB per set, "
                          f"{n_sets} sets rotated, L2 {l2 / 2 ** 20:.0f} MiB)",
                    "parallelism": "replicas" if world > 1 else "single GPU",

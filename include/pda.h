@@ -185,6 +185,27 @@ pda_status pda_decode_contiguous(pda_ctx* ctx, const pda_bf16* q, const pda_bf16
                                  pda_bf16* out, pda_stream stream);
 
 /*
+ * Multi-query decode with a causal mask (speculative verify, short prefill
+ * chunks) -- [CK] Overview (attn_paged_decode / attn_paged_prefill) and
+ * Python Wrappers (is_causal).  The last q_len tokens of each sequence are the
+ * queries: query i of sequence b is token seq_lens[b] - q_len + i and attends
+ * to tokens 0 .. seq_lens[b] - q_len + i of the paged cache (which already
+ * holds the new tokens' K/V).  A sequence shorter than q_len gives its first
+ * queries fewer (or no) tokens; no tokens give a zero row.
+ *   q, out   [batch, q_len, Hq, D] bf16, dense.
+ *   seq_lens [batch] total tokens per sequence (device).
+ *   batch * q_len <= max_seqs; other arguments as pda_decode.
+ * Each query row is split like a sequence of its own; rows of one sequence
+ * read the same blocks at nearly the same time, so the repeated reads come
+ * mostly from L2.
+ */
+pda_status pda_decode_multi(pda_ctx* ctx, const pda_bf16* q, const pda_bf16* k_pool,
+                            const pda_bf16* v_pool, int64_t num_blocks,
+                            const int32_t* block_table, int32_t max_blocks,
+                            const int32_t* seq_lens, int32_t batch, int32_t q_len, float scale,
+                            pda_bf16* out, pda_stream stream);
+
+/*
  * Tiled lifecycle, step 1 -- [TA] begin_step: resets the running state of
  * sequences 0..num_seqs-1 to (m, l, o) = (-inf, 0, 0).  num_seqs > max_seqs
  * is PDA_ERR_INVALID_ARG.

@@ -89,6 +89,7 @@ def lib() -> ctypes.CDLL:
         "pda_decode_strided": (I32, [P, P, P, P, I64, I64, I64, I64, P, I32, P, I32, F, P, P]),
         "pda_decode_f32": (I32, [P, P, P, P, I64, I64, I64, I64, P, I32, P, I32, F, P, P]),
         "pda_decode_contiguous": (I32, [P, P, P, P, I32, P, I32, F, P, P]),
+        "pda_decode_multi": (I32, [P, P, P, P, I64, P, I32, P, I32, I32, F, P, P]),
         "pda_begin_step": (I32, [P, I32, P]),
         "pda_step_tile": (I32, [P, P, P, P, I64, P, P, P, I32, I64, I64, I64, F, P]),
         "pda_finalize": (I32, [P, P, I32, P]),
@@ -289,6 +290,28 @@ class Context:
                                         ts_, hs_, _ptr(block_table), int(block_table.shape[1]),
                                         _ptr(seq_lens), B, self._scale(scale), _ptr(out),
                                         _stream(stream)))
+        return out
+
+    def decode_multi(self, q, k_pool, v_pool, block_table, seq_lens, scale: Optional[float] = None,
+                     out=None, stream=None):
+        """Causal multi-query decode: q [B, q_len, Hq, D] are each sequence's last q_len
+        tokens; query i sees tokens up to seq_lens[b] - q_len + i.  Returns [B, q_len, Hq, D]."""
+        torch = _torch()
+        d = self.dims
+        B = int(seq_lens.shape[0])
+        if q.dim() != 4 or q.shape[0] != B or q.shape[2:] != (d.num_q_heads, d.head_dim):
+            raise ValueError("q must be [B, q_len, Hq, D]")
+        self._bf16(q, "q")
+        self._i32(block_table, "block_table", 2)
+        self._i32(seq_lens, "seq_lens", 1)
+        (bs_, ts_, hs_), nblk = self._pool(k_pool, v_pool, None, None)
+        if out is None:
+            out = torch.empty_like(q)
+        self._bf16(out, "out", tuple(q.shape))
+        _check(lib().pda_decode_multi(self._ctx, _ptr(q), _ptr(k_pool), _ptr(v_pool), nblk,
+                                      _ptr(block_table), int(block_table.shape[1]), _ptr(seq_lens),
+                                      B, int(q.shape[1]), self._scale(scale), _ptr(out),
+                                      _stream(stream)))
         return out
 
     def decode_contiguous(self, q, k, v, seq_lens, scale: Optional[float] = None, out=None,

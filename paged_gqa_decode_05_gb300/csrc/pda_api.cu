@@ -171,13 +171,18 @@ struct RunArgs {
     pda_bf16* dbg_v;
     cudaStream_t stream;
     bool contiguous = false;  // no table: block b*table_stride + j (contiguous cache)
+    int32_t q_len = 1;        // causal queries per sequence (q, out: [batch, q_len, Hq, D])
 };
 
 pda_status run(pda_ctx* ctx, const RunArgs& r) {
     if (!ctx) return fail(PDA_ERR_INVALID_ARG, "ctx is NULL");
     const pda_dims& d = ctx->dims;
-    if (r.batch < 0 || r.batch > d.max_seqs)
-        return fail(PDA_ERR_INVALID_ARG, "batch %d outside [0, max_seqs=%d]", r.batch, d.max_seqs);
+    if (r.q_len < 1 || r.q_len > std::min(pda::kMaxLaunchBatch, ctx->split_ctas))
+        return fail(PDA_ERR_INVALID_ARG, "q_len %d outside [1, %d]", r.q_len,
+                    std::min(pda::kMaxLaunchBatch, ctx->split_ctas));
+    if (r.batch < 0 || (int64_t)r.batch * r.q_len > d.max_seqs)
+        return fail(PDA_ERR_INVALID_ARG, "batch %d x q_len %d outside [0, max_seqs=%d]", r.batch,
+                    r.q_len, d.max_seqs);
     if (r.batch == 0) return PDA_OK;
     pda_status st = check_pool(ctx, r.pool);
     if (st != PDA_OK) return st;
@@ -215,20 +220,26 @@ pda_status run(pda_ctx* ctx, const RunArgs& r) {
     const int32_t Hq = d.num_q_heads, Hkv = d.num_kv_heads, D = d.head_dim;
     const bool timing = ctx->ev_begin && ctx->ev_split && ctx->ev_end && r.mode == pda::kOneShot;
     const int64_t dbg_row_tokens = (int64_t)r.table_stride * d.block_size;
-    for (int32_t c0 = 0; c0 < r.batch; c0 += pda::kMaxLaunchBatch) {
-        const int32_t cb = std::min(pda::kMaxLaunchBatch, r.batch - c0);
+    // Launch over query rows: batch * q_len "sequences", chunked on whole
+    // sequences (a chunk holds all q_len queries of each of its sequences).
+    const int32_t rows_total = r.batch * r.q_len;
+    const int32_t chunk_rows = (pda::kMaxLaunchBatch / r.q_len) * r.q_len;
+    for (int32_t c0 = 0; c0 < rows_total; c0 += chunk_rows) {
+        const int32_t cb = std::min(chunk_rows, rows_total - c0);
+        const int32_t s0 = c0 / r.q_len;  // first table row / length of the chunk
         p.q = r.q ? r.q + (int64_t)c0 * Hq * D : nullptr;
-        p.table = r.contiguous ? nullptr : r.table + (int64_t)c0 * r.table_stride;
-        p.lens = r.lens + c0;
-        p.last_valid = r.last_valid ? r.last_valid + c0 : nullptr;
+        p.table = r.contiguous ? nullptr : r.table + (int64_t)s0 * r.table_stride;
+        p.lens = r.lens + s0;
+        p.q_len = r.q_len;
+        p.last_valid = r.last_valid ? r.last_valid + s0 : nullptr;
         p.out = r.out ? r.out + (int64_t)c0 * Hq * D : nullptr;
         p.out_f32 = r.out_f32 ? r.out_f32 + (int64_t)c0 * Hq * D : nullptr;
         p.part_o = ctx->part_o;
         p.part_ml = ctx->part_ml;
         p.pfx = ctx->pfx;
         p.err = ctx->err;
-        p.dbg_k = r.dbg_k ? r.dbg_k + (int64_t)c0 * Hkv * dbg_row_tokens * D : nullptr;
-        p.dbg_v = r.dbg_v ? r.dbg_v + (int64_t)c0 * Hkv * dbg_row_tokens * D : nullptr;
+        p.dbg_k = r.dbg_k ? r.dbg_k + (int64_t)s0 * Hkv * dbg_row_tokens * D : nullptr;
+        p.dbg_v = r.dbg_v ? r.dbg_v + (int64_t)s0 * Hkv * dbg_row_tokens * D : nullptr;
         p.num_blocks = r.pool.num_blocks;
         p.k_base = r.pool.k;
         p.v_base = r.pool.v;
@@ -274,6 +285,7 @@ pda_status run(pda_ctx* ctx, const RunArgs& r) {
         mp.G = ctx->G;
         mp.D = D;
         mp.split_ctas = ctx->split_ctas;
+        mp.q_len = r.q_len;
         e = pda::launch_merge(r.mode, mp, !timing, r.stream);
         if (e != cudaSuccess) return cuda_fail(e, "merge kernel launch");
         if (timing && (e = cudaEventRecord(ctx->ev_end, r.stream)) != cudaSuccess)
@@ -613,6 +625,20 @@ PDA_EXPORT pda_status pda_decode_contiguous(pda_ctx* ctx, const pda_bf16* q, con
     if (batch > pda::kMaxLaunchBatch)
         return fail(PDA_ERR_INVALID_ARG, "contiguous decode carries at most %d sequences per call",
                     pda::kMaxLaunchBatch);
+    return run(ctx, r);
+}
+
+PDA_EXPORT pda_status pda_decode_multi(pda_ctx* ctx, const pda_bf16* q, const pda_bf16* k_pool,
+                                       const pda_bf16* v_pool, int64_t num_blocks,
+                                       const int32_t* block_table, int32_t max_blocks,
+                                       const int32_t* seq_lens, int32_t batch, int32_t q_len,
+                                       float scale, pda_bf16* out, pda_stream stream) {
+    if (!ctx) return fail(PDA_ERR_INVALID_ARG, "ctx is NULL");
+    int64_t s[3];
+    pda_paged_strides(&ctx->dims, s);
+    RunArgs r = {pda::kOneShot, q, {k_pool, v_pool, num_blocks, s[0], s[1], s[2]},
+                 block_table, max_blocks, seq_lens, 0, nullptr, batch, scale, out, nullptr,
+                 nullptr, nullptr, (cudaStream_t)stream, false, q_len};
     return run(ctx, r);
 }
 

@@ -60,14 +60,38 @@ struct Cfg {
 
 // Entry idx of sequence b's block list: the table row, or, for a contiguous
 // cache [B, S, Hkv, D] (no table), block b * (S / bs) + idx.
+// With Q = q_len > 1 queries per sequence the launch's sequences are query
+// rows ordered query-major: row s is query s / Bs of sequence s % Bs
+// (Bs = B / Q real sequences), so each query index forms one plan group.
+__device__ __forceinline__ int table_row(const SplitParams& p, int s) {
+    return p.q_len > 1 ? s % (p.B / p.q_len) : s;
+}
+
+// Row of q and out ([Bs, Q, Hq, D]) that launch sequence s reads and writes.
+__device__ __forceinline__ int64_t qo_row(const SplitParams& p, int s) {
+    if (p.q_len <= 1) return s;
+    const int Bs = p.B / p.q_len;
+    return (int64_t)(s % Bs) * p.q_len + s / Bs;
+}
+
 __device__ __forceinline__ int32_t table_entry(const SplitParams& p, int b, int idx) {
-    if (p.table == nullptr) return b * p.table_stride + idx;
-    return p.table[(int64_t)b * p.table_stride + idx];
+    const int row = table_row(p, b);
+    if (p.table == nullptr) return row * p.table_stride + idx;
+    return p.table[(int64_t)row * p.table_stride + idx];
+}
+
+// Tokens seen by launch sequence s: its length, or for query i of a sequence
+// of length L the causal prefix L - q_len + 1 + i (at least 0).
+__device__ __forceinline__ int32_t seq_tokens(const SplitParams& p, int s) {
+    if (p.q_len <= 1) return p.lens[s];
+    const int Bs = p.B / p.q_len;
+    const int32_t len = p.lens[s % Bs] - p.q_len + 1 + s / Bs;
+    return len < 0 ? 0 : len;
 }
 
 // Blocks of sequence b, validated and clamped (flags bad lengths).
 __device__ __forceinline__ int32_t seq_blocks(const SplitParams& p, int b) {
-    int32_t len = p.lens[b];
+    int32_t len = p.lens_are_blocks ? p.lens[b] : seq_tokens(p, b);
     if (p.lens_are_blocks) {
         if (len < 0 || len > p.table_stride) {
             atomicOr(p.err, PDA_DEVERR_BAD_LENGTH_);
@@ -98,7 +122,7 @@ __device__ __forceinline__ int32_t last_block_slots(const SplitParams& p, int b,
         }
         return v;
     }
-    int32_t v = p.lens[b] - (nb - 1) * p.bs;
+    int32_t v = seq_tokens(p, b) - (nb - 1) * p.bs;
     return v > p.bs ? p.bs : v;
 }
 
@@ -144,7 +168,9 @@ __device__ __forceinline__ void run_producer(const SplitParams& p, uint32_t base
     constexpr int S = C::kStages;
     const uint32_t full0 = base_s + L.bars, empty0 = full0 + 8 * S;
     const bool leader = lane == 0;
-    const uint64_t pol = policy_evict_first();
+    // K/V are read once: evict them first.  With several query groups each
+    // block is read once per group at nearly the same time; keep it normal.
+    const uint64_t pol = p.q_len > 1 ? policy_evict_normal() : policy_evict_first();
     const int bs = p.bs, Hkv = p.Hkv;
     const int NB = kStageTokens / bs;
 
@@ -216,7 +242,7 @@ __device__ __forceinline__ void run_producer(const SplitParams& p, uint32_t base
             const uint32_t bytes = kv_bytes + (load_q ? (uint32_t)(p.G * D * 2) : 0u);
             mbar_arrive_expect_tx(full, bytes);
             if (load_q) {
-                const uint16_t* src = p.q + ((int64_t)b * p.Hq + (int64_t)kvh * p.G) * D;
+                const uint16_t* src = p.q + (qo_row(p, b) * p.Hq + (int64_t)kvh * p.G) * D;
                 bulk_load(sV + C::kTileBytes, src, (uint32_t)(p.G * D * 2), full);
             }
         }
@@ -584,7 +610,7 @@ __device__ __forceinline__ void run_consumer(const SplitParams& p, uint32_t base
             if (!consumer_sync(cbar, cphase, p.err, abort_flag)) break;
             const int ct = warp * 32 + lane;
             const bool direct = MODE == kOneShot && (m.flags & kWholeUnit);
-            const int64_t out_base = ((int64_t)m.b * p.Hq + (int64_t)m.kvh * G) * D;
+            const int64_t out_base = (qo_row(p, m.b) * p.Hq + (int64_t)m.kvh * G) * D;
             for (int idx = ct; idx < G * D; idx += kConsumerWarps * 32) {
                 const int h = idx / D, d = idx - h * D;
                 float M = kNegInf;
@@ -663,9 +689,12 @@ __global__ void __maxnreg__(Cfg<D>::kMaxRegs) split_kernel(const __grid_constant
     build_prefix(p, pfx, scan);  // ends with __syncthreads (also publishes the barriers)
     if (blockIdx.x == 0 && MODE != kGather)
         for (int i = tid; i <= p.B; i += kThreads) p.pfx[i] = pfx[i];
-    const int64_t W = (int64_t)pfx[p.B] * p.Hkv;
-    const int64_t P = gridDim.x;
-    const int64_t begin = cta_begin(blockIdx.x, W, P), end = cta_begin(blockIdx.x + 1, W, P);
+    int64_t begin, end;
+    {
+        const int64_t Q = p.q_len > 1 ? p.q_len : 1;
+        const GroupRange gr = group_of_cta(blockIdx.x, pfx, p.B, Q, p.Hkv, gridDim.x);
+        group_cta_range(gr, blockIdx.x, &begin, &end);
+    }
 
     if (warp == kConsumerWarps) {
         run_producer<D, MODE>(p, base_s, L, pfx, meta, &abort_flag, begin, end, lane);
@@ -701,7 +730,9 @@ __global__ void __launch_bounds__(kMaxGroup * 256 / 4) merge_kernel(const MergeP
     const int n4 = G * D / 4;
     const int i4 = threadIdx.x;
     const int32_t lo = p.pfx[b], nb = p.pfx[b + 1] - lo;
-    const int64_t q0 = (int64_t)b * p.Hq + (int64_t)kvh * G;  // first q head of the unit
+    const int Q = p.q_len > 1 ? p.q_len : 1;
+    const int64_t row = Q > 1 ? (int64_t)(b % (p.B / Q)) * Q + b / (p.B / Q) : b;
+    const int64_t q0 = row * p.Hq + (int64_t)kvh * G;  // first output row of the unit
     const bool active = i4 < n4;  // the block is rounded up to whole warps
     const int h = active ? (4 * i4) / D : 0;
     if (nb == 0) {
@@ -711,9 +742,10 @@ __global__ void __launch_bounds__(kMaxGroup * 256 / 4) merge_kernel(const MergeP
         }
         return;
     }
-    const int64_t W = (int64_t)p.pfx[p.B] * p.Hkv, P = p.split_ctas;
+    const GroupRange gr = group_of_seq(b, p.pfx, p.B, Q, p.Hkv, p.split_ctas);
     const int64_t su = (int64_t)lo * p.Hkv + (int64_t)kvh * nb, eu = su + nb;
-    const int64_t cf = cta_of_block(su, W, P), cl = cta_of_block(eu - 1, W, P);
+    const int64_t cf = gr.g * gr.Pg + cta_of_block(su - gr.F0, gr.W, gr.Pg);
+    const int64_t cl = gr.g * gr.Pg + cta_of_block(eu - 1 - gr.F0, gr.W, gr.Pg);
     if (MODE == kOneShot && cf == cl) return;  // written by the split kernel
     float M = kNegInf, Ls = 0.f;
     float4 Os = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -733,7 +765,8 @@ __global__ void __launch_bounds__(kMaxGroup * 256 / 4) merge_kernel(const MergeP
             li[k] = 0.f;
             oi[k] = make_float4(0.f, 0.f, 0.f, 0.f);
             if (c > cl) continue;
-            const int64_t cb = cta_begin(c, W, P), ce = cta_begin(c + 1, W, P);
+            int64_t cb, ce;
+            group_cta_range(gr, c, &cb, &ce);
             if ((cb > su ? cb : su) >= (ce < eu ? ce : eu)) continue;  // no share of this unit
             const int64_t slot = u + c;
             mi[k] = p.part_ml[(slot * G + h) * 2];

@@ -57,6 +57,8 @@ struct SplitParams {
                                  // (block sizes below 8); 2: 16-byte cp.async rows
     int64_t row_blk, row_tok, row_kvh;  // strides in rows of D elements (gather4)
     int32_t lens_are_blocks;
+    int32_t q_len;               // causal queries per sequence; with q_len > 1 launch
+                                 // sequence s is query s / (B/q_len) of row s % (B/q_len)
     int32_t B, Hq, Hkv, G, bs;
     int32_t dbg_row_tokens;      // tokens per (b, kvh) row of the gather output
     float scale_log2;            // softmax scale * log2(e)
@@ -73,6 +75,7 @@ struct MergeParams {
     float* o_state;
     int32_t B, Hq, Hkv, G, D;
     int32_t split_ctas;
+    int32_t q_len;               // as SplitParams::q_len
 };
 
 struct SmemLayout {

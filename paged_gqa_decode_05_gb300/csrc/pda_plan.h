@@ -28,6 +28,47 @@ PDA_HD int64_t cta_begin(int64_t c, int64_t W, int64_t P) { return c * W / P; }
 // with floor(c*W/P) <= s, i.e. floor(((s+1)*P - 1) / W).
 PDA_HD int64_t cta_of_block(int64_t s, int64_t W, int64_t P) { return ((s + 1) * P - 1) / W; }
 
+// Grouped split, for several causal queries per sequence: the launch's B
+// sequences form Q equal groups (group g = sequences [g*B/Q, (g+1)*B/Q), in
+// the same sequence order), each walked by its own P/Q CTAs over its own
+// flattened range [F_g, F_{g+1}), F_g = pfx[g*B/Q]*Hkv.  Every group visits
+// the same (sequence, kv head, block) positions at nearly the same time.
+// With Q = 1 this is the plain split above.  CTAs past Q*(P/Q) stay idle.
+struct GroupRange {
+    int64_t F0;   // first flattened block of the group
+    int64_t W;    // blocks of the group
+    int64_t Pg;   // CTAs of the group
+    int64_t g;    // group index (>= Q for an idle CTA)
+};
+
+template <typename Pfx>
+PDA_HD GroupRange group_of_cta(int64_t c, const Pfx& pfx, int64_t B, int64_t Q, int64_t Hkv,
+                               int64_t P) {
+    GroupRange r;
+    r.Pg = P / Q;
+    r.g = c / r.Pg;
+    if (r.g >= Q) { r.F0 = 0; r.W = 0; return r; }
+    const int64_t Bg = B / Q;
+    r.F0 = (int64_t)pfx[r.g * Bg] * Hkv;
+    r.W = (int64_t)pfx[(r.g + 1) * Bg] * Hkv - r.F0;
+    return r;
+}
+
+template <typename Pfx>
+PDA_HD GroupRange group_of_seq(int64_t s, const Pfx& pfx, int64_t B, int64_t Q, int64_t Hkv,
+                               int64_t P) {
+    const int64_t Bg = B / Q;
+    return group_of_cta((s / Bg) * (P / Q), pfx, B, Q, Hkv, P);
+}
+
+// Flattened range [begin, end) of CTA c within its group (empty when idle).
+PDA_HD void group_cta_range(const GroupRange& r, int64_t c, int64_t* begin, int64_t* end) {
+    if (r.W == 0) { *begin = *end = r.F0; return; }
+    const int64_t cl = c - r.g * r.Pg;
+    *begin = r.F0 + cta_begin(cl, r.W, r.Pg);
+    *end = r.F0 + cta_begin(cl + 1, r.W, r.Pg);
+}
+
 // Blocks needed for a length in tokens.
 PDA_HD int32_t blocks_for_tokens(int32_t len, int32_t block_size) {
     return len <= 0 ? 0 : (len + block_size - 1) / block_size;

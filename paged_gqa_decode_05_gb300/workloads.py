@@ -222,6 +222,13 @@ def with_block_size(w: Workload, block_size: int) -> Workload:
                          block_size=block_size, seq_lens=w.seq_lens, seed=w.seed)
 
 
+def multi_queries(w: Workload, q_len: int) -> np.ndarray:
+    """Seeded N(0,1) bf16 queries [B, q_len, Hq, D] for a causal multi-query
+    decode over the workload's cache (the cache is unchanged)."""
+    rng = np.random.Generator(np.random.PCG64(np.random.SeedSequence([w.seed, 13, q_len])))
+    return _normal_bits(rng, (w.B, q_len, w.Hq, w.D))
+
+
 def contiguous_kv(w: Workload, max_seq_len: Optional[int] = None):
     """The workload's cache copied to the contiguous layout [B, S, Hkv, D]
     (S = max_seq_len, default the longest sequence rounded up to a block),
