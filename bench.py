@@ -89,14 +89,18 @@ def peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+# The files the split and merge kernels are compiled from (host-only files
+# such as pda_api.cu do not change the kernels' traffic).
+KERNEL_SOURCES = ("pda_kernels.cuh", "pda_ptx.cuh", "pda_params.h", "pda_plan.h",
+                  "pda_kernels_d64.cu", "pda_kernels_d128.cu", "pda_kernels_d256.cu")
+
+
 def kernel_source_hash() -> str:
-    import glob
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "paged_gqa_decode_05_gb300", "csrc")
-    for p in sorted(glob.glob(os.path.join(csrc, "*"))):
-        if p.endswith((".cu", ".cuh", ".h")):
-            with open(p, "rb") as f:
-                h.update(f.read())
+    for name in KERNEL_SOURCES:
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(f.read())
     return h.hexdigest()[:16]
 
 

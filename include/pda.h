@@ -281,6 +281,16 @@ pda_status pda_read_device_errors(pda_ctx* ctx, uint32_t* flags, int32_t clear,
                                   pda_stream stream);
 
 /*
+ * Failure-detection check: launches one CTA that waits on a barrier phase
+ * nothing completes, through the same bounded wait every decode kernel uses
+ * for its TMA and consumer barriers.  After limit_ns (1 us .. 2 s) the wait
+ * gives up, PDA_DEVERR_TIMEOUT is set in the context's flags and the kernel
+ * returns; the context stays usable.  Read the flag with
+ * pda_read_device_errors().
+ */
+pda_status pda_check_wait_timeout(pda_ctx* ctx, int64_t limit_ns, pda_stream stream);
+
+/*
  * Timing hook: when the three events (cudaEvent_t) are non-NULL, every later
  * one-shot decode records ev_begin before its split kernel, ev_split after it
  * and ev_end after the merge kernel, on the call's stream; NULLs turn it off.

@@ -97,6 +97,7 @@ def lib() -> ctypes.CDLL:
         "pda_debug_gather": (I32, [P, P, P, I64, I64, I64, I64, P, I32, P, I32, P, P, P]),
         "pda_read_device_errors": (I32, [P, ctypes.POINTER(ctypes.c_uint32), I32, P]),
         "pda_set_timing_events": (I32, [P, P, P, P]),
+        "pda_check_wait_timeout": (I32, [P, I64, P]),
         "pda_get_launch_info": (I32, [P, ctypes.POINTER(LaunchInfo)]),
         "pda_plan_units": (I32, [P, I32, I32, I32, I32, I32, P, P, ctypes.POINTER(I64)]),
     }
@@ -395,6 +396,11 @@ class Context:
         if st not in (OK, ERR_DEVICE_DATA):
             _check(st)
         return int(flags.value)
+
+    def check_wait_timeout(self, limit_ns: int = 20_000_000, stream=None) -> int:
+        """Runs a bounded wait that cannot complete; returns the device flags after it."""
+        _check(lib().pda_check_wait_timeout(self._ctx, int(limit_ns), _stream(stream)))
+        return self.read_device_errors(stream=stream)
 
     def set_timing_events(self, ev_begin=None, ev_split=None, ev_end=None) -> None:
         h = [None if e is None else e.cuda_event for e in (ev_begin, ev_split, ev_end)]

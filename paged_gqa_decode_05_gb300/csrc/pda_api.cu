@@ -16,7 +16,7 @@
 #include <string>
 
 #include "pda.h"
-#include "pda_params.h"
+#include "pda_launch.h"
 
 #define PDA_EXPORT extern "C" __attribute__((visibility("default")))
 
@@ -555,6 +555,14 @@ PDA_EXPORT pda_status pda_read_device_errors(pda_ctx* ctx, uint32_t* flags, int3
     *flags = v;
     if (v) return fail(PDA_ERR_DEVICE_DATA, "device error flags 0x%x", v);
     return PDA_OK;
+}
+
+PDA_EXPORT pda_status pda_check_wait_timeout(pda_ctx* ctx, int64_t limit_ns, pda_stream stream) {
+    if (!ctx) return fail(PDA_ERR_INVALID_ARG, "ctx is NULL");
+    if (limit_ns < 1000 || limit_ns > 2000000000LL)
+        return fail(PDA_ERR_INVALID_ARG, "limit_ns %lld outside [1 us, 2 s]", (long long)limit_ns);
+    cudaError_t e = pda::launch_wait_timeout_probe(ctx->err, (uint64_t)limit_ns, (cudaStream_t)stream);
+    return e == cudaSuccess ? PDA_OK : cuda_fail(e, "wait probe launch");
 }
 
 PDA_EXPORT pda_status pda_set_timing_events(pda_ctx* ctx, void* ev_begin, void* ev_split, void* ev_end) {

@@ -2,6 +2,7 @@
 // split kernel.
 #define PDA_DEFINE_AUX_KERNELS
 #include "pda_kernels.cuh"
+#include "pda_launch.h"
 
 namespace pda {
 
@@ -77,4 +78,25 @@ cudaError_t launch_finalize(const float* l, const float* o, uint16_t* out, float
     return cudaGetLastError();
 }
 
+}  // namespace pda
+
+namespace pda {
+// Failure-detection check: waits on an mbarrier phase that nothing completes,
+// with the same bounded wait the decode kernels use; the wait gives up after
+// limit_ns, sets the timeout flag and the kernel returns.
+__global__ void wait_timeout_probe_kernel(uint32_t* err, uint64_t limit_ns) {
+    __shared__ __align__(8) uint64_t bar;
+    const uint32_t b = smem_u32(&bar);
+    if (threadIdx.x == 0) {
+        mbar_init(b, 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+    if (!mbar_wait_bounded(b, 0, limit_ns) && threadIdx.x == 0) atomicOr(err, PDA_DEVERR_TIMEOUT_);
+}
+
+cudaError_t launch_wait_timeout_probe(uint32_t* err, uint64_t limit_ns, cudaStream_t stream) {
+    wait_timeout_probe_kernel<<<1, 32, 0, stream>>>(err, limit_ns);
+    return cudaGetLastError();
+}
 }  // namespace pda

@@ -1,0 +1,21 @@
+// pda_launch.h -- host-side launch entry points of the kernels (defined in
+// pda_kernels_d*.cu and pda_launch.cu), called by the C API.
+#pragma once
+
+#include "pda_params.h"
+
+namespace pda {
+
+// Entry points defined per head_dim (pda_kernels_d*.cu).
+int split_stages(int D);
+const void* split_kernel_fn(int D, int mode);
+cudaError_t launch_split(int D, int mode, const SplitParams& p, int grid, size_t smem,
+                         cudaStream_t stream);
+cudaError_t launch_merge(int mode, const MergeParams& p, bool pdl, cudaStream_t stream);
+cudaError_t launch_reset_state(float* m, float* l, float* o, int64_t n_q, int32_t D,
+                               cudaStream_t stream);
+cudaError_t launch_wait_timeout_probe(uint32_t* err, uint64_t limit_ns, cudaStream_t stream);
+cudaError_t launch_finalize(const float* l, const float* o, uint16_t* out, float* out_f32,
+                            int64_t n_q, int32_t D, cudaStream_t stream);
+
+}  // namespace pda

@@ -1,6 +1,5 @@
-// pda_params.h -- kernel parameter blocks, shared-memory layout and the
-// launch entry points the host API calls (one translation unit per head_dim
-// defines them).
+// pda_params.h -- kernel parameter blocks and the shared-memory layout of the
+// split kernel (shared by the kernels and the host API).
 #pragma once
 
 #include <cuda.h>
@@ -100,16 +99,5 @@ PDA_HD SmemLayout smem_layout(int D, int stages, int G, int B) {
     L.total = off + 1024u;
     return L;
 }
-
-// Entry points defined per head_dim (pda_kernels_d*.cu).
-int split_stages(int D);
-const void* split_kernel_fn(int D, int mode);
-cudaError_t launch_split(int D, int mode, const SplitParams& p, int grid, size_t smem,
-                         cudaStream_t stream);
-cudaError_t launch_merge(int mode, const MergeParams& p, bool pdl, cudaStream_t stream);
-cudaError_t launch_reset_state(float* m, float* l, float* o, int64_t n_q, int32_t D,
-                               cudaStream_t stream);
-cudaError_t launch_finalize(const float* l, const float* o, uint16_t* out, float* out_f32,
-                            int64_t n_q, int32_t D, cudaStream_t stream);
 
 }  // namespace pda

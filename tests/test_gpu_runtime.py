@@ -1,0 +1,77 @@
+"""Runtime properties on the GPU: CUDA-graph capture of a decode, the bounded
+waits' failure path, and streams."""
+import numpy as np
+import pytest
+
+from gpu_util import context_for, upload
+from paged_gqa_decode_05_gb300 import workloads
+
+pytestmark = pytest.mark.gpu
+
+
+def _w():
+    return workloads.make_workload("rt", B=6, Hq=16, Hkv=4, D=128, block_size=16,
+                                   seq_lens=[1000, 5, 0, 333, 4096, 77], seed=21)
+
+
+def test_decode_captured_in_cuda_graph():
+    import torch
+    w = _w()
+    ctx = context_for(w)
+    t = upload(w)
+    eager = ctx.decode(t["q"], t["k_pool"], t["v_pool"], t["block_table"], t["seq_lens"]).clone()
+    out = torch.zeros_like(eager)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):  # warm-up on the capture stream
+        ctx.decode(t["q"], t["k_pool"], t["v_pool"], t["block_table"], t["seq_lens"], out=out)
+    torch.cuda.current_stream().wait_stream(s)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        ctx.decode(t["q"], t["k_pool"], t["v_pool"], t["block_table"], t["seq_lens"], out=out)
+    out.zero_()
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    assert np.array_equal(out.float().cpu().numpy(), eager.float().cpu().numpy())
+    # replay reads the current contents of the captured buffers
+    t["q"].mul_(-1)
+    g.replay()
+    flipped = ctx.decode(t["q"], t["k_pool"], t["v_pool"], t["block_table"], t["seq_lens"])
+    torch.cuda.synchronize()
+    assert np.array_equal(out.float().cpu().numpy(), flipped.float().cpu().numpy())
+
+
+def test_bounded_wait_reports_timeout_and_context_stays_usable():
+    import torch
+    import paged_gqa_decode_05_gb300 as pda
+    w = _w()
+    ctx = context_for(w)
+    assert ctx.read_device_errors() == 0
+    flags = ctx.check_wait_timeout(limit_ns=20_000_000)  # a wait nothing completes, 20 ms
+    assert flags & pda.DEVERR_TIMEOUT
+    assert ctx.read_device_errors() == 0  # cleared by the previous read
+    t = upload(w)
+    out = ctx.decode(t["q"], t["k_pool"], t["v_pool"], t["block_table"], t["seq_lens"])
+    torch.cuda.synchronize()
+    assert ctx.read_device_errors() == 0
+    assert torch.isfinite(out.float()).all()
+
+
+def test_two_contexts_on_two_streams():
+    import torch
+    w = _w()
+    t = upload(w)
+    a_ctx, b_ctx = context_for(w), context_for(w)
+    ref = a_ctx.decode(t["q"], t["k_pool"], t["v_pool"], t["block_table"], t["seq_lens"]).clone()
+    sa, sb = torch.cuda.Stream(), torch.cuda.Stream()
+    sa.wait_stream(torch.cuda.current_stream())
+    sb.wait_stream(torch.cuda.current_stream())
+    outs = []
+    for ctx, s in ((a_ctx, sa), (b_ctx, sb)):
+        with torch.cuda.stream(s):
+            outs.append(ctx.decode(t["q"], t["k_pool"], t["v_pool"], t["block_table"],
+                                   t["seq_lens"]))
+    torch.cuda.synchronize()
+    for o in outs:
+        assert np.array_equal(o.float().cpu().numpy(), ref.float().cpu().numpy())
