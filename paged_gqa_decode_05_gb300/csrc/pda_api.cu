@@ -220,20 +220,25 @@ pda_status run(pda_ctx* ctx, const RunArgs& r) {
     const int32_t Hq = d.num_q_heads, Hkv = d.num_kv_heads, D = d.head_dim;
     const bool timing = ctx->ev_begin && ctx->ev_split && ctx->ev_end && r.mode == pda::kOneShot;
     const int64_t dbg_row_tokens = (int64_t)r.table_stride * d.block_size;
-    // Launch over query rows: batch * q_len "sequences", chunked on whole
-    // sequences (a chunk holds all q_len queries of each of its sequences).
-    const int32_t rows_total = r.batch * r.q_len;
-    const int32_t chunk_rows = (pda::kMaxLaunchBatch / r.q_len) * r.q_len;
+    // Causal multi-query: qp queries of a sequence share one launch row (the
+    // MMA's N = qp*G <= 8); a sequence has Qr rows.  The launch is over
+    // batch * Qr rows, chunked on whole sequences.
+    const int32_t qp = r.q_len > 1 ? std::max(1, std::min(r.q_len, pda::kMaxGroup / ctx->G)) : 1;
+    const int32_t Qr = (r.q_len + qp - 1) / qp;
+    const int32_t rows_total = r.batch * Qr;
+    const int32_t chunk_rows = (pda::kMaxLaunchBatch / Qr) * Qr;
     for (int32_t c0 = 0; c0 < rows_total; c0 += chunk_rows) {
         const int32_t cb = std::min(chunk_rows, rows_total - c0);
-        const int32_t s0 = c0 / r.q_len;  // first table row / length of the chunk
-        p.q = r.q ? r.q + (int64_t)c0 * Hq * D : nullptr;
+        const int32_t s0 = c0 / Qr;  // first sequence of the chunk
+        p.q = r.q ? r.q + (int64_t)s0 * r.q_len * Hq * D : nullptr;
         p.table = r.contiguous ? nullptr : r.table + (int64_t)s0 * r.table_stride;
         p.lens = r.lens + s0;
         p.q_len = r.q_len;
+        p.qp = qp;
+        p.rows_per_slot = qp * ctx->G;
         p.last_valid = r.last_valid ? r.last_valid + s0 : nullptr;
-        p.out = r.out ? r.out + (int64_t)c0 * Hq * D : nullptr;
-        p.out_f32 = r.out_f32 ? r.out_f32 + (int64_t)c0 * Hq * D : nullptr;
+        p.out = r.out ? r.out + (int64_t)s0 * r.q_len * Hq * D : nullptr;
+        p.out_f32 = r.out_f32 ? r.out_f32 + (int64_t)s0 * r.q_len * Hq * D : nullptr;
         p.part_o = ctx->part_o;
         p.part_ml = ctx->part_ml;
         p.pfx = ctx->pfx;
@@ -276,9 +281,9 @@ pda_status run(pda_ctx* ctx, const RunArgs& r) {
         mp.pfx = ctx->pfx;
         mp.out = p.out;
         mp.out_f32 = p.out_f32;
-        mp.m_state = ctx->m_state + (int64_t)c0 * Hq;
-        mp.l_state = ctx->l_state + (int64_t)c0 * Hq;
-        mp.o_state = ctx->o_state + (int64_t)c0 * Hq * D;
+        mp.m_state = ctx->m_state + (int64_t)s0 * Hq;  // tiled path (q_len 1)
+        mp.l_state = ctx->l_state + (int64_t)s0 * Hq;
+        mp.o_state = ctx->o_state + (int64_t)s0 * Hq * D;
         mp.B = cb;
         mp.Hq = Hq;
         mp.Hkv = Hkv;
@@ -286,6 +291,8 @@ pda_status run(pda_ctx* ctx, const RunArgs& r) {
         mp.D = D;
         mp.split_ctas = ctx->split_ctas;
         mp.q_len = r.q_len;
+        mp.qp = qp;
+        mp.rows_per_slot = qp * ctx->G;
         e = pda::launch_merge(r.mode, mp, !timing, r.stream);
         if (e != cudaSuccess) return cuda_fail(e, "merge kernel launch");
         if (timing && (e = cudaEventRecord(ctx->ev_end, r.stream)) != cudaSuccess)
@@ -419,8 +426,9 @@ PDA_EXPORT pda_status pda_create(const pda_dims* dims, pda_ctx** out_ctx) {
 
     const int64_t nq = (int64_t)dims->max_seqs * dims->num_q_heads;
     struct { void** ptr; size_t bytes; } allocs[] = {
-        {(void**)&ctx->part_o, (size_t)ctx->slots * ctx->G * D * sizeof(float)},
-        {(void**)&ctx->part_ml, (size_t)ctx->slots * ctx->G * 2 * sizeof(float)},
+        // partial states: up to kMaxGroup q rows per slot (packed multi-query rows)
+        {(void**)&ctx->part_o, (size_t)ctx->slots * pda::kMaxGroup * D * sizeof(float)},
+        {(void**)&ctx->part_ml, (size_t)ctx->slots * pda::kMaxGroup * 2 * sizeof(float)},
         {(void**)&ctx->pfx, (size_t)(pda::kMaxLaunchBatch + 1) * sizeof(int32_t)},
         {(void**)&ctx->err, sizeof(uint32_t)},
         {(void**)&ctx->m_state, (size_t)nq * sizeof(float)},

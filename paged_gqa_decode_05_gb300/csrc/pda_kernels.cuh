@@ -60,32 +60,49 @@ struct Cfg {
 
 // Entry idx of sequence b's block list: the table row, or, for a contiguous
 // cache [B, S, Hkv, D] (no table), block b * (S / bs) + idx.
-// With Q = q_len > 1 queries per sequence the launch's sequences are query
-// rows ordered query-major: row s is query s / Bs of sequence s % Bs
-// (Bs = B / Q real sequences), so each query index forms one plan group.
-__device__ __forceinline__ int table_row(const SplitParams& p, int s) {
-    return p.q_len > 1 ? s % (p.B / p.q_len) : s;
+// Causal multi-query decode packs qp queries of a sequence into one launch
+// row (the MMA's N = qp*G columns: column n is query n / G, head n % G).  A
+// sequence has Qr = ceil(q_len / qp) rows, ordered row-major over the batch:
+// launch sequence s is row s / Bs of sequence s % Bs (Bs = B / Qr), which
+// makes each row index one group of the split plan.  Plain decode: Qr = 1.
+struct RowInfo {
+    int b;      // sequence (table row, lens index)
+    int first;  // first query of the row
+    int cnt;    // queries in the row
+};
+
+__device__ __forceinline__ int rows_per_seq(const SplitParams& p) {
+    return p.q_len > 1 ? (p.q_len + p.qp - 1) / p.qp : 1;
 }
 
-// Row of q and out ([Bs, Q, Hq, D]) that launch sequence s reads and writes.
-__device__ __forceinline__ int64_t qo_row(const SplitParams& p, int s) {
-    if (p.q_len <= 1) return s;
-    const int Bs = p.B / p.q_len;
-    return (int64_t)(s % Bs) * p.q_len + s / Bs;
+__device__ __forceinline__ RowInfo row_info(const SplitParams& p, int s) {
+    RowInfo r;
+    if (p.q_len <= 1) { r.b = s; r.first = 0; r.cnt = 1; return r; }
+    const int Bs = p.B / rows_per_seq(p);
+    r.b = s % Bs;
+    r.first = (s / Bs) * p.qp;
+    r.cnt = min(p.qp, p.q_len - r.first);
+    return r;
 }
 
-__device__ __forceinline__ int32_t table_entry(const SplitParams& p, int b, int idx) {
-    const int row = table_row(p, b);
+// Element offset of q/out row (query qi of sequence b, q head h).
+__device__ __forceinline__ int64_t qo_offset(const SplitParams& p, int b, int qi, int h, int D) {
+    const int ql = p.q_len > 1 ? p.q_len : 1;
+    return (((int64_t)b * ql + qi) * p.Hq + h) * D;
+}
+
+__device__ __forceinline__ int32_t table_entry(const SplitParams& p, int s, int idx) {
+    const int row = row_info(p, s).b;
     if (p.table == nullptr) return row * p.table_stride + idx;
     return p.table[(int64_t)row * p.table_stride + idx];
 }
 
-// Tokens seen by launch sequence s: its length, or for query i of a sequence
-// of length L the causal prefix L - q_len + 1 + i (at least 0).
+// Tokens read for launch sequence s: its length, or for a row of causal
+// queries the prefix its last query sees, L - q_len + first + cnt (>= 0).
 __device__ __forceinline__ int32_t seq_tokens(const SplitParams& p, int s) {
     if (p.q_len <= 1) return p.lens[s];
-    const int Bs = p.B / p.q_len;
-    const int32_t len = p.lens[s % Bs] - p.q_len + 1 + s / Bs;
+    const RowInfo r = row_info(p, s);
+    const int32_t len = p.lens[r.b] - p.q_len + r.first + r.cnt;
     return len < 0 ? 0 : len;
 }
 
@@ -170,7 +187,7 @@ __device__ __forceinline__ void run_producer(const SplitParams& p, uint32_t base
     const bool leader = lane == 0;
     // K/V are read once: evict them first.  With several query groups each
     // block is read once per group at nearly the same time; keep it normal.
-    const uint64_t pol = p.q_len > 1 ? policy_evict_normal() : policy_evict_first();
+    const uint64_t pol = rows_per_seq(p) > 1 ? policy_evict_normal() : policy_evict_first();
     const int bs = p.bs, Hkv = p.Hkv;
     const int NB = kStageTokens / bs;
 
@@ -231,7 +248,9 @@ __device__ __forceinline__ void run_producer(const SplitParams& p, uint32_t base
             m.flags = (seg_begin ? kSegBegin : 0) | (seg_end ? kSegEnd : 0) | (whole ? kWholeUnit : 0);
             m.slot = b * Hkv + kvh + (int)blockIdx.x;
             m.j0 = j;
-            m.pad0 = m.pad1 = 0;
+            const RowInfo ri = row_info(p, b);
+            m.lim = p.q_len > 1 ? p.lens[ri.b] - p.q_len + ri.first : 0x7fffffff;
+            m.nr = ri.cnt * p.G;
             meta[stage] = m;
             const bool load_q = seg_begin && MODE != kGather;
             const int rows = (n - 1) * bs + lastv;
@@ -239,12 +258,13 @@ __device__ __forceinline__ void run_producer(const SplitParams& p, uint32_t base
                 p.row_gather == 0 ? (uint32_t)n * 2u * (uint32_t)bs * D * 2u
                 : p.row_gather == 1 ? (uint32_t)((rows + 3) >> 2) * 2u * 4u * D * 2u
                                     : 0u;  // cp.async completions arrive instead
-            const uint32_t bytes = kv_bytes + (load_q ? (uint32_t)(p.G * D * 2) : 0u);
+            const uint32_t bytes = kv_bytes + (load_q ? (uint32_t)(m.nr * D * 2) : 0u);
             mbar_arrive_expect_tx(full, bytes);
-            if (load_q) {
-                const uint16_t* src = p.q + (qo_row(p, b) * p.Hq + (int64_t)kvh * p.G) * D;
-                bulk_load(sV + C::kTileBytes, src, (uint32_t)(p.G * D * 2), full);
-            }
+            if (load_q)  // the G q rows of kv head kvh for each packed query
+                for (int k = 0; k < ri.cnt; ++k)
+                    bulk_load(sV + C::kTileBytes + (uint32_t)(k * p.G * D * 2),
+                              p.q + qo_offset(p, ri.b, ri.first + k, kvh * p.G, D),
+                              (uint32_t)(p.G * D * 2), full);
         }
         __syncwarp();
         if (p.row_gather == 1) {
@@ -450,6 +470,7 @@ __device__ __forceinline__ void run_consumer(const SplitParams& p, uint32_t base
     const int g = lane >> 2, t = lane & 3;
     const int r0 = warp * 16;
     const int G = p.G;
+    const bool causal = p.q_len > 1;
     const float sl2 = p.scale_log2;
     // ldmatrix row addresses: QK reads K as the A operand (rows = tokens),
     // PV reads V transposed as the A operand (rows of V = tokens = k index).
@@ -498,7 +519,7 @@ __device__ __forceinline__ void run_consumer(const SplitParams& p, uint32_t base
 #pragma unroll
                 for (int kk = 0; kk < KS; ++kk) {
                     o[kk][0] = o[kk][1] = o[kk][2] = o[kk][3] = 0.f;
-                    if (g < G) {
+                    if (g < m.nr) {
                         const uint8_t* r = sq + (size_t)(g * D + 16 * kk + 2 * t) * 2;
                         qf[kk][0] = *reinterpret_cast<const uint32_t*>(r);
                         qf[kk][1] = *reinterpret_cast<const uint32_t*>(r + 16);
@@ -530,6 +551,14 @@ __device__ __forceinline__ void run_consumer(const SplitParams& p, uint32_t base
                 float s3 = ((acc[0][3] + acc[1][3]) + (acc[2][3] + acc[3][3])) * sl2;
                 if (r0 + g >= m.n_valid) { s0 = kNegInf; s1 = kNegInf; }
                 if (r0 + g + 8 >= m.n_valid) { s2 = kNegInf; s3 = kNegInf; }
+                if (causal) {  // column n = query n / G may not see the later tokens
+                    const int pos = m.j0 * p.bs + r0 + g;
+                    const int lim0 = m.lim + (2 * t) / G, lim1 = m.lim + (2 * t + 1) / G;
+                    if (pos > lim0) s0 = kNegInf;
+                    if (pos > lim1) s1 = kNegInf;
+                    if (pos + 8 > lim0) s2 = kNegInf;
+                    if (pos + 8 > lim1) s3 = kNegInf;
+                }
                 // column max over the 16 tokens (lanes sharing t)
                 float x0 = fmaxf(s0, s2), x1 = fmaxf(s1, s3);
 #pragma unroll
@@ -589,20 +618,21 @@ __device__ __forceinline__ void run_consumer(const SplitParams& p, uint32_t base
             }
             if (!consumer_sync(cbar, cphase, p.err, abort_flag)) break;  // all reads of the stage done
             const int h0 = 2 * t, h1 = 2 * t + 1;
+            const int NR = m.nr;  // q rows of the unit
             if (g == 0) {
-                if (h0 < G) { st_m[warp * kMaxGroup + h0] = m0; st_l[warp * kMaxGroup + h0] = l0; }
-                if (h1 < G) { st_m[warp * kMaxGroup + h1] = m1; st_l[warp * kMaxGroup + h1] = l1; }
+                if (h0 < NR) { st_m[warp * kMaxGroup + h0] = m0; st_l[warp * kMaxGroup + h0] = l0; }
+                if (h1 < NR) { st_m[warp * kMaxGroup + h1] = m1; st_l[warp * kMaxGroup + h1] = l1; }
             }
 #pragma unroll
             for (int mt = 0; mt < KS; ++mt) {
                 const int d = 16 * mt + g;
-                if (h0 < G) {
-                    float* r = st_o + (size_t)(warp * G + h0) * (D + 4);
+                if (h0 < NR) {
+                    float* r = st_o + (size_t)(warp * NR + h0) * (D + 4);
                     r[d] = o[mt][0];
                     r[d + 8] = o[mt][2];
                 }
-                if (h1 < G) {
-                    float* r = st_o + (size_t)(warp * G + h1) * (D + 4);
+                if (h1 < NR) {
+                    float* r = st_o + (size_t)(warp * NR + h1) * (D + 4);
                     r[d] = o[mt][1];
                     r[d + 8] = o[mt][3];
                 }
@@ -610,9 +640,10 @@ __device__ __forceinline__ void run_consumer(const SplitParams& p, uint32_t base
             if (!consumer_sync(cbar, cphase, p.err, abort_flag)) break;
             const int ct = warp * 32 + lane;
             const bool direct = MODE == kOneShot && (m.flags & kWholeUnit);
-            const int64_t out_base = (qo_row(p, m.b) * p.Hq + (int64_t)m.kvh * G) * D;
-            for (int idx = ct; idx < G * D; idx += kConsumerWarps * 32) {
-                const int h = idx / D, d = idx - h * D;
+            const RowInfo ri = row_info(p, m.b);
+            const int SR = p.rows_per_slot > 0 ? p.rows_per_slot : G;  // rows per partial slot
+            for (int idx = ct; idx < NR * D; idx += kConsumerWarps * 32) {
+                const int h = idx / D, d = idx - h * D;  // h: q row of the unit
                 float M = kNegInf;
 #pragma unroll
                 for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, st_m[w * kMaxGroup + h]);
@@ -622,18 +653,19 @@ __device__ __forceinline__ void run_consumer(const SplitParams& p, uint32_t base
                     for (int w = 0; w < kConsumerWarps; ++w) {
                         const float f = ex2(st_m[w * kMaxGroup + h] - M);
                         Ls += st_l[w * kMaxGroup + h] * f;
-                        Os += st_o[(size_t)(w * G + h) * (D + 4) + d] * f;
+                        Os += st_o[(size_t)(w * NR + h) * (D + 4) + d] * f;
                     }
                 }
                 if (direct) {
                     const float r = Ls > 0.f ? Os / Ls : 0.f;
-                    if (p.out_f32) p.out_f32[out_base + idx] = r;
-                    else p.out[out_base + idx] = __bfloat16_as_ushort(__float2bfloat16_rn(r));
+                    const int64_t o = qo_offset(p, ri.b, ri.first + h / G, m.kvh * G + h % G, D) + d;
+                    if (p.out_f32) p.out_f32[o] = r;
+                    else p.out[o] = __bfloat16_as_ushort(__float2bfloat16_rn(r));
                 } else {
-                    p.part_o[(int64_t)m.slot * G * D + idx] = Os;
+                    p.part_o[((int64_t)m.slot * SR + h) * D + d] = Os;
                     if (d == 0) {
-                        p.part_ml[((int64_t)m.slot * G + h) * 2] = M;
-                        p.part_ml[((int64_t)m.slot * G + h) * 2 + 1] = Ls;
+                        p.part_ml[((int64_t)m.slot * SR + h) * 2] = M;
+                        p.part_ml[((int64_t)m.slot * SR + h) * 2 + 1] = Ls;
                     }
                 }
             }
@@ -691,8 +723,7 @@ __global__ void __maxnreg__(Cfg<D>::kMaxRegs) split_kernel(const __grid_constant
         for (int i = tid; i <= p.B; i += kThreads) p.pfx[i] = pfx[i];
     int64_t begin, end;
     {
-        const int64_t Q = p.q_len > 1 ? p.q_len : 1;
-        const GroupRange gr = group_of_cta(blockIdx.x, pfx, p.B, Q, p.Hkv, gridDim.x);
+        const GroupRange gr = group_of_cta(blockIdx.x, pfx, p.B, rows_per_seq(p), p.Hkv, gridDim.x);
         group_cta_range(gr, blockIdx.x, &begin, &end);
     }
 
@@ -725,34 +756,43 @@ __global__ void __launch_bounds__(kMaxGroup * 256 / 4) merge_kernel(const MergeP
     pdl_launch_dependents();  // the next call's split kernel may start its set-up
     pdl_wait_primary();
     const int u = blockIdx.x;
-    const int b = u / p.Hkv, kvh = u - b * p.Hkv;
+    const int b = u / p.Hkv, kvh = u - b * p.Hkv;  // b: launch sequence (pfx index)
     const int G = p.G, D = p.D;
-    const int n4 = G * D / 4;
+    // the row's sequence, first packed query and query count (plain: b, 0, 1)
+    const int ql = p.q_len > 1 ? p.q_len : 1;
+    const int Qr = ql > 1 ? (ql + p.qp - 1) / p.qp : 1;
+    const int Bs = p.B / Qr;
+    const int seq = Qr > 1 ? b % Bs : b;
+    const int first = ql > 1 ? (b / Bs) * p.qp : 0;
+    const int cnt = ql > 1 ? min(p.qp, ql - first) : 1;
+    const int NR = cnt * G;  // q rows of the unit
+    const int SR = p.rows_per_slot > 0 ? p.rows_per_slot : G;
+    const int n4 = NR * D / 4;
     const int i4 = threadIdx.x;
     const int32_t lo = p.pfx[b], nb = p.pfx[b + 1] - lo;
-    const int Q = p.q_len > 1 ? p.q_len : 1;
-    const int64_t row = Q > 1 ? (int64_t)(b % (p.B / Q)) * Q + b / (p.B / Q) : b;
-    const int64_t q0 = row * p.Hq + (int64_t)kvh * G;  // first output row of the unit
     const bool active = i4 < n4;  // the block is rounded up to whole warps
     const int h = active ? (4 * i4) / D : 0;
+    const int d4 = 4 * i4 - h * D;
+    // output row of unit row h: query first + h / G, q head kvh*G + h % G
+    const int64_t orow = ((int64_t)seq * ql + first + h / G) * p.Hq + (int64_t)kvh * G + h % G;
     if (nb == 0) {
         if (MODE == kOneShot && active) {
-            if (p.out_f32) reinterpret_cast<float4*>(p.out_f32 + q0 * D)[i4] = make_float4(0.f, 0.f, 0.f, 0.f);
-            else reinterpret_cast<uint2*>(p.out + q0 * D)[i4] = make_uint2(0u, 0u);
+            if (p.out_f32) *reinterpret_cast<float4*>(p.out_f32 + orow * D + d4) = make_float4(0.f, 0.f, 0.f, 0.f);
+            else *reinterpret_cast<uint2*>(p.out + orow * D + d4) = make_uint2(0u, 0u);
         }
         return;
     }
-    const GroupRange gr = group_of_seq(b, p.pfx, p.B, Q, p.Hkv, p.split_ctas);
+    const GroupRange gr = group_of_seq(b, p.pfx, p.B, Qr, p.Hkv, p.split_ctas);
     const int64_t su = (int64_t)lo * p.Hkv + (int64_t)kvh * nb, eu = su + nb;
     const int64_t cf = gr.g * gr.Pg + cta_of_block(su - gr.F0, gr.W, gr.Pg);
     const int64_t cl = gr.g * gr.Pg + cta_of_block(eu - 1 - gr.F0, gr.W, gr.Pg);
     if (MODE == kOneShot && cf == cl) return;  // written by the split kernel
     float M = kNegInf, Ls = 0.f;
     float4 Os = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (MODE == kTiled && active) {
-        M = p.m_state[q0 + h];
-        Ls = p.l_state[q0 + h];
-        Os = reinterpret_cast<const float4*>(p.o_state + q0 * D)[i4];
+    if (MODE == kTiled && active) {  // plain decode rows: orow = (b*Hq + kvh*G + h)
+        M = p.m_state[orow];
+        Ls = p.l_state[orow];
+        Os = *reinterpret_cast<const float4*>(p.o_state + orow * D + d4);
     }
     constexpr int kBatch = 8;
     for (int64_t c0 = cf; active && c0 <= cl; c0 += kBatch) {
@@ -769,9 +809,9 @@ __global__ void __launch_bounds__(kMaxGroup * 256 / 4) merge_kernel(const MergeP
             group_cta_range(gr, c, &cb, &ce);
             if ((cb > su ? cb : su) >= (ce < eu ? ce : eu)) continue;  // no share of this unit
             const int64_t slot = u + c;
-            mi[k] = p.part_ml[(slot * G + h) * 2];
-            li[k] = p.part_ml[(slot * G + h) * 2 + 1];
-            oi[k] = reinterpret_cast<const float4*>(p.part_o + slot * G * D)[i4];
+            mi[k] = p.part_ml[(slot * SR + h) * 2];
+            li[k] = p.part_ml[(slot * SR + h) * 2 + 1];
+            oi[k] = *reinterpret_cast<const float4*>(p.part_o + (slot * SR + h) * D + d4);
         }
 #pragma unroll
         for (int k = 0; k < kBatch; ++k) merge_in(M, Ls, Os, mi[k], li[k], oi[k]);
@@ -781,22 +821,22 @@ __global__ void __launch_bounds__(kMaxGroup * 256 / 4) merge_kernel(const MergeP
         const float4 v = Ls > 0.f ? make_float4(Os.x / Ls, Os.y / Ls, Os.z / Ls, Os.w / Ls)
                                   : make_float4(0.f, 0.f, 0.f, 0.f);
         if (p.out_f32) {
-            reinterpret_cast<float4*>(p.out_f32 + q0 * D)[i4] = v;
+            *reinterpret_cast<float4*>(p.out_f32 + orow * D + d4) = v;
         } else {
             uint2 w;
             w.x = pack_bf16x2(v.x, v.y);
             w.y = pack_bf16x2(v.z, v.w);
-            reinterpret_cast<uint2*>(p.out + q0 * D)[i4] = w;
+            *reinterpret_cast<uint2*>(p.out + orow * D + d4) = w;
         }
     } else {
         // every thread of head h computed the same (M, Ls); the first one
         // stores them after all threads of the head have read the old values
         __syncthreads();
         if (!active) return;
-        reinterpret_cast<float4*>(p.o_state + q0 * D)[i4] = Os;
-        if ((4 * i4) % D == 0) {
-            p.m_state[q0 + h] = M;
-            p.l_state[q0 + h] = Ls;
+        *reinterpret_cast<float4*>(p.o_state + orow * D + d4) = Os;
+        if (d4 == 0) {
+            p.m_state[orow] = M;
+            p.l_state[orow] = Ls;
         }
     }
 }

@@ -46,7 +46,8 @@ cudaError_t launch_split(int D, int mode, const SplitParams& p, int grid, size_t
 cudaError_t launch_merge(int mode, const MergeParams& p, bool pdl, cudaStream_t stream) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(p.B * p.Hkv), 1, 1);
-    const int n4 = p.G * p.D / 4;  // one thread per 4 outputs of a unit
+    const int rows = p.rows_per_slot > 0 ? p.rows_per_slot : p.G;  // q rows of a unit, at most
+    const int n4 = rows * p.D / 4;  // one thread per 4 outputs of a unit
     cfg.blockDim = dim3((unsigned)((n4 + 31) / 32 * 32), 1, 1);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = stream;

@@ -27,7 +27,8 @@ struct StageMeta {
     int32_t flags;    // kSegBegin | kSegEnd | kWholeUnit | kDone
     int32_t slot;     // partial-state slot of the segment (u + c)
     int32_t j0;       // index of the stage's first block within the sequence
-    int32_t pad0, pad1;
+    int32_t lim;      // causal limit of the row's first query (token index)
+    int32_t nr;       // q rows of the unit (packed queries x G)
 };
 enum MetaFlags : int32_t { kSegBegin = 1, kSegEnd = 2, kWholeUnit = 4, kDone = 8 };
 
@@ -56,8 +57,9 @@ struct SplitParams {
                                  // (block sizes below 8); 2: 16-byte cp.async rows
     int64_t row_blk, row_tok, row_kvh;  // strides in rows of D elements (gather4)
     int32_t lens_are_blocks;
-    int32_t q_len;               // causal queries per sequence; with q_len > 1 launch
-                                 // sequence s is query s / (B/q_len) of row s % (B/q_len)
+    int32_t q_len;               // causal queries per sequence (0 or 1: plain decode)
+    int32_t qp;                  // queries packed into one launch row (MMA N = qp*G <= 8)
+    int32_t rows_per_slot;       // rows of a partial-state slot (0: G)
     int32_t B, Hq, Hkv, G, bs;
     int32_t dbg_row_tokens;      // tokens per (b, kvh) row of the gather output
     float scale_log2;            // softmax scale * log2(e)
@@ -74,7 +76,9 @@ struct MergeParams {
     float* o_state;
     int32_t B, Hq, Hkv, G, D;
     int32_t split_ctas;
-    int32_t q_len;               // as SplitParams::q_len
+    int32_t q_len;               // as SplitParams
+    int32_t qp;
+    int32_t rows_per_slot;
 };
 
 struct SmemLayout {
