@@ -189,7 +189,7 @@ pda_status run(pda_ctx* ctx, const RunArgs& r) {
     if (r.mode != pda::kGather) {
         if (!r.q || !aligned(r.q, 16)) return fail(PDA_ERR_INVALID_ARG, "q must be non-NULL and 16-byte aligned");
     }
-    if (r.mode == pda::kOneShot) {
+    if (pda::writes_output(r.mode)) {
         if (r.out_f32 ? !aligned(r.out_f32, 16) : (!r.out || !aligned(r.out, 16)))
             return fail(PDA_ERR_INVALID_ARG, "out must be non-NULL and 16-byte aligned");
     }
@@ -218,7 +218,7 @@ pda_status run(pda_ctx* ctx, const RunArgs& r) {
     }
 
     const int32_t Hq = d.num_q_heads, Hkv = d.num_kv_heads, D = d.head_dim;
-    const bool timing = ctx->ev_begin && ctx->ev_split && ctx->ev_end && r.mode == pda::kOneShot;
+    const bool timing = ctx->ev_begin && ctx->ev_split && ctx->ev_end && pda::writes_output(r.mode);
     const int64_t dbg_row_tokens = (int64_t)r.table_stride * d.block_size;
     // Causal multi-query: qp queries of a sequence share one launch row (the
     // MMA's N = qp*G <= 8); a sequence has Qr rows.  The launch is over
@@ -406,7 +406,7 @@ PDA_EXPORT pda_status pda_create(const pda_dims* dims, pda_ctx** out_ctx) {
         return fail(PDA_ERR_UNSUPPORTED, "needs %d bytes of shared memory per CTA (device allows %d)",
                     ctx->smem_max, (int)prop.sharedMemPerBlockOptin);
     }
-    for (int mode = 0; mode < 3; ++mode) {
+    for (int mode = 0; mode < pda::kNumModes; ++mode) {
         e = cudaFuncSetAttribute(pda::split_kernel_fn(D, mode), cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  ctx->smem_max);
         if (e == cudaSuccess)
@@ -652,7 +652,9 @@ PDA_EXPORT pda_status pda_decode_multi(pda_ctx* ctx, const pda_bf16* q, const pd
     if (!ctx) return fail(PDA_ERR_INVALID_ARG, "ctx is NULL");
     int64_t s[3];
     pda_paged_strides(&ctx->dims, s);
-    RunArgs r = {pda::kOneShot, q, {k_pool, v_pool, num_blocks, s[0], s[1], s[2]},
+    // one query per sequence is plain decode; more take the causal kernels
+    RunArgs r = {q_len > 1 ? pda::kMulti : pda::kOneShot, q,
+                 {k_pool, v_pool, num_blocks, s[0], s[1], s[2]},
                  block_table, max_blocks, seq_lens, 0, nullptr, batch, scale, out, nullptr,
                  nullptr, nullptr, (cudaStream_t)stream, false, q_len};
     return run(ctx, r);

@@ -64,21 +64,26 @@ struct Cfg {
 // row (the MMA's N = qp*G columns: column n is query n / G, head n % G).  A
 // sequence has Qr = ceil(q_len / qp) rows, ordered row-major over the batch:
 // launch sequence s is row s / Bs of sequence s % Bs (Bs = B / Qr), which
-// makes each row index one group of the split plan.  Plain decode: Qr = 1.
+// makes each row index one group of the split plan.  Plain decode (MQ false,
+// every mode but kMulti): Qr = 1 and row s is sequence s, fixed at compile
+// time so the single-query kernels carry none of the packing arithmetic.
 struct RowInfo {
     int b;      // sequence (table row, lens index)
     int first;  // first query of the row
     int cnt;    // queries in the row
 };
 
+template <bool MQ>
 __device__ __forceinline__ int rows_per_seq(const SplitParams& p) {
-    return p.q_len > 1 ? (p.q_len + p.qp - 1) / p.qp : 1;
+    if constexpr (!MQ) return 1;
+    else return (p.q_len + p.qp - 1) / p.qp;
 }
 
+template <bool MQ>
 __device__ __forceinline__ RowInfo row_info(const SplitParams& p, int s) {
     RowInfo r;
-    if (p.q_len <= 1) { r.b = s; r.first = 0; r.cnt = 1; return r; }
-    const int Bs = p.B / rows_per_seq(p);
+    if constexpr (!MQ) { r.b = s; r.first = 0; r.cnt = 1; return r; }
+    const int Bs = p.B / rows_per_seq<MQ>(p);
     r.b = s % Bs;
     r.first = (s / Bs) * p.qp;
     r.cnt = min(p.qp, p.q_len - r.first);
@@ -86,29 +91,33 @@ __device__ __forceinline__ RowInfo row_info(const SplitParams& p, int s) {
 }
 
 // Element offset of q/out row (query qi of sequence b, q head h).
+template <bool MQ>
 __device__ __forceinline__ int64_t qo_offset(const SplitParams& p, int b, int qi, int h, int D) {
-    const int ql = p.q_len > 1 ? p.q_len : 1;
+    const int ql = MQ ? p.q_len : 1;
     return (((int64_t)b * ql + qi) * p.Hq + h) * D;
 }
 
+template <bool MQ>
 __device__ __forceinline__ int32_t table_entry(const SplitParams& p, int s, int idx) {
-    const int row = row_info(p, s).b;
+    const int row = row_info<MQ>(p, s).b;
     if (p.table == nullptr) return row * p.table_stride + idx;
     return p.table[(int64_t)row * p.table_stride + idx];
 }
 
 // Tokens read for launch sequence s: its length, or for a row of causal
 // queries the prefix its last query sees, L - q_len + first + cnt (>= 0).
+template <bool MQ>
 __device__ __forceinline__ int32_t seq_tokens(const SplitParams& p, int s) {
-    if (p.q_len <= 1) return p.lens[s];
-    const RowInfo r = row_info(p, s);
+    if constexpr (!MQ) return p.lens[s];
+    const RowInfo r = row_info<MQ>(p, s);
     const int32_t len = p.lens[r.b] - p.q_len + r.first + r.cnt;
     return len < 0 ? 0 : len;
 }
 
 // Blocks of sequence b, validated and clamped (flags bad lengths).
+template <bool MQ>
 __device__ __forceinline__ int32_t seq_blocks(const SplitParams& p, int b) {
-    int32_t len = p.lens_are_blocks ? p.lens[b] : seq_tokens(p, b);
+    int32_t len = p.lens_are_blocks ? p.lens[b] : seq_tokens<MQ>(p, b);
     if (p.lens_are_blocks) {
         if (len < 0 || len > p.table_stride) {
             atomicOr(p.err, PDA_DEVERR_BAD_LENGTH_);
@@ -129,6 +138,7 @@ __device__ __forceinline__ int32_t seq_blocks(const SplitParams& p, int b) {
 }
 
 // Valid slots of sequence b's last block (1..bs).
+template <bool MQ>
 __device__ __forceinline__ int32_t last_block_slots(const SplitParams& p, int b, int32_t nb) {
     if (p.lens_are_blocks) {
         if (p.last_valid == nullptr) return p.bs;
@@ -139,17 +149,18 @@ __device__ __forceinline__ int32_t last_block_slots(const SplitParams& p, int b,
         }
         return v;
     }
-    int32_t v = seq_tokens(p, b) - (nb - 1) * p.bs;
+    int32_t v = seq_tokens<MQ>(p, b) - (nb - 1) * p.bs;
     return v > p.bs ? p.bs : v;
 }
 
 // Exclusive prefix of blocks per sequence into shared pfx[0..B].
+template <bool MQ>
 __device__ __forceinline__ void build_prefix(const SplitParams& p, int32_t* pfx, int32_t* scan) {
     const int tid = threadIdx.x;
     const int per = (p.B + kThreads - 1) / kThreads;
     const int lo = min(p.B, tid * per), hi = min(p.B, lo + per);
     int32_t sum = 0;
-    for (int b = lo; b < hi; ++b) sum += seq_blocks(p, b);
+    for (int b = lo; b < hi; ++b) sum += seq_blocks<MQ>(p, b);
     scan[tid] = sum;
     __syncthreads();
     if (tid == 0) {
@@ -165,7 +176,7 @@ __device__ __forceinline__ void build_prefix(const SplitParams& p, int32_t* pfx,
     int32_t run = scan[tid];
     for (int b = lo; b < hi; ++b) {
         pfx[b] = run;
-        run += seq_blocks(p, b);
+        run += seq_blocks<MQ>(p, b);
     }
     __syncthreads();
 }
@@ -183,11 +194,13 @@ __device__ __forceinline__ void run_producer(const SplitParams& p, uint32_t base
     // the barrier operations and the TMA copies.
     using C = Cfg<D>;
     constexpr int S = C::kStages;
+    constexpr bool MQ = MODE == kMulti;
     const uint32_t full0 = base_s + L.bars, empty0 = full0 + 8 * S;
     const bool leader = lane == 0;
-    // K/V are read once: evict them first.  With several query groups each
-    // block is read once per group at nearly the same time; keep it normal.
-    const uint64_t pol = rows_per_seq(p) > 1 ? policy_evict_normal() : policy_evict_first();
+    // K/V are read once: evict them first.  With several query rows per
+    // sequence each block is read once per row at nearly the same time; keep
+    // it normal.
+    const uint64_t pol = rows_per_seq<MQ>(p) > 1 ? policy_evict_normal() : policy_evict_first();
     const int bs = p.bs, Hkv = p.Hkv;
     const int NB = kStageTokens / bs;
 
@@ -212,8 +225,8 @@ __device__ __forceinline__ void run_producer(const SplitParams& p, uint32_t base
         kvh = (int)(rem / nb);
         j = (int32_t)(rem % nb);
         win = j;
-        id0 = win + lane < nb ? table_entry(p, b, win + lane) : 0;
-        id1 = win + 32 + lane < nb ? table_entry(p, b, win + 32 + lane) : 0;
+        id0 = win + lane < nb ? table_entry<MQ>(p, b, win + lane) : 0;
+        id1 = win + 32 + lane < nb ? table_entry<MQ>(p, b, win + 32 + lane) : 0;
     }
     bool seg_begin = true;
     bool whole = false;
@@ -222,15 +235,15 @@ __device__ __forceinline__ void run_producer(const SplitParams& p, uint32_t base
         if (stop) { ok = false; break; }
         if (p.row_gather && win != j) {  // up to 64 blocks per stage: reload the window
             win = j;
-            id0 = win + lane < nb ? table_entry(p, b, win + lane) : 0;
-            id1 = win + 32 + lane < nb ? table_entry(p, b, win + 32 + lane) : 0;
+            id0 = win + lane < nb ? table_entry<MQ>(p, b, win + lane) : 0;
+            id1 = win + 32 + lane < nb ? table_entry<MQ>(p, b, win + 32 + lane) : 0;
         }
         const int32_t n = (int32_t)min((int64_t)min(NB, nb - j), end - pos);
         const bool unit_end = (j + n == nb);
         const bool seg_end = unit_end || (pos + n == end);
         if (seg_begin) whole = (j == 0) && ((int64_t)pfx[b] * Hkv + (int64_t)(kvh + 1) * nb <= end);
 
-        const int32_t lastv = unit_end ? last_block_slots(p, b, nb) : bs;
+        const int32_t lastv = unit_end ? last_block_slots<MQ>(p, b, nb) : bs;
 
         bool got = true;
         if (leader) got = mbar_wait_bounded(empty0 + 8 * stage, phase ^ 1u, kWaitLimitNs);
@@ -248,9 +261,9 @@ __device__ __forceinline__ void run_producer(const SplitParams& p, uint32_t base
             m.flags = (seg_begin ? kSegBegin : 0) | (seg_end ? kSegEnd : 0) | (whole ? kWholeUnit : 0);
             m.slot = b * Hkv + kvh + (int)blockIdx.x;
             m.j0 = j;
-            const RowInfo ri = row_info(p, b);
-            m.lim = p.q_len > 1 ? p.lens[ri.b] - p.q_len + ri.first : 0x7fffffff;
-            m.nr = ri.cnt * p.G;
+            const RowInfo ri = row_info<MQ>(p, b);
+            m.lim = MQ ? p.lens[ri.b] - p.q_len + ri.first : 0x7fffffff;
+            m.nr = MQ ? ri.cnt * p.G : p.G;
             meta[stage] = m;
             const bool load_q = seg_begin && MODE != kGather;
             const int rows = (n - 1) * bs + lastv;
@@ -260,11 +273,17 @@ __device__ __forceinline__ void run_producer(const SplitParams& p, uint32_t base
                                     : 0u;  // cp.async completions arrive instead
             const uint32_t bytes = kv_bytes + (load_q ? (uint32_t)(m.nr * D * 2) : 0u);
             mbar_arrive_expect_tx(full, bytes);
-            if (load_q)  // the G q rows of kv head kvh for each packed query
-                for (int k = 0; k < ri.cnt; ++k)
-                    bulk_load(sV + C::kTileBytes + (uint32_t)(k * p.G * D * 2),
-                              p.q + qo_offset(p, ri.b, ri.first + k, kvh * p.G, D),
+            if (load_q) {  // the G q rows of kv head kvh for each packed query
+                if constexpr (MQ) {
+                    for (int k = 0; k < ri.cnt; ++k)
+                        bulk_load(sV + C::kTileBytes + (uint32_t)(k * p.G * D * 2),
+                                  p.q + qo_offset<MQ>(p, ri.b, ri.first + k, kvh * p.G, D),
+                                  (uint32_t)(p.G * D * 2), full);
+                } else {
+                    bulk_load(sV + C::kTileBytes, p.q + qo_offset<MQ>(p, b, 0, kvh * p.G, D),
                               (uint32_t)(p.G * D * 2), full);
+                }
+            }
         }
         __syncwarp();
         if (p.row_gather == 1) {
@@ -361,14 +380,14 @@ __device__ __forceinline__ void run_producer(const SplitParams& p, uint32_t base
             nb = b < p.B ? pfx[b + 1] - pfx[b] : 0;
             if (pos < end) {
                 win = 0;
-                id0 = lane < nb ? table_entry(p, b, lane) : 0;
-                id1 = 32 + lane < nb ? table_entry(p, b, 32 + lane) : 0;
+                id0 = lane < nb ? table_entry<MQ>(p, b, lane) : 0;
+                id1 = 32 + lane < nb ? table_entry<MQ>(p, b, 32 + lane) : 0;
             }
         } else if (j - win >= 32) {
             // first half consumed: slide the window and fetch the next 32 ids
             win += 32;
             id0 = id1;
-            id1 = win + 32 + lane < nb ? table_entry(p, b, win + 32 + lane) : 0;
+            id1 = win + 32 + lane < nb ? table_entry<MQ>(p, b, win + 32 + lane) : 0;
         }
         if (++stage == S) { stage = 0; phase ^= 1u; }
     }
@@ -469,8 +488,8 @@ __device__ __forceinline__ void run_consumer(const SplitParams& p, uint32_t base
     const uint32_t full0 = base_s + L.bars, empty0 = full0 + 8 * S;
     const int g = lane >> 2, t = lane & 3;
     const int r0 = warp * 16;
+    constexpr bool MQ = MODE == kMulti;
     const int G = p.G;
-    const bool causal = p.q_len > 1;
     const float sl2 = p.scale_log2;
     // ldmatrix row addresses: QK reads K as the A operand (rows = tokens),
     // PV reads V transposed as the A operand (rows of V = tokens = k index).
@@ -519,7 +538,7 @@ __device__ __forceinline__ void run_consumer(const SplitParams& p, uint32_t base
 #pragma unroll
                 for (int kk = 0; kk < KS; ++kk) {
                     o[kk][0] = o[kk][1] = o[kk][2] = o[kk][3] = 0.f;
-                    if (g < m.nr) {
+                    if (g < (MQ ? m.nr : G)) {
                         const uint8_t* r = sq + (size_t)(g * D + 16 * kk + 2 * t) * 2;
                         qf[kk][0] = *reinterpret_cast<const uint32_t*>(r);
                         qf[kk][1] = *reinterpret_cast<const uint32_t*>(r + 16);
@@ -551,7 +570,7 @@ __device__ __forceinline__ void run_consumer(const SplitParams& p, uint32_t base
                 float s3 = ((acc[0][3] + acc[1][3]) + (acc[2][3] + acc[3][3])) * sl2;
                 if (r0 + g >= m.n_valid) { s0 = kNegInf; s1 = kNegInf; }
                 if (r0 + g + 8 >= m.n_valid) { s2 = kNegInf; s3 = kNegInf; }
-                if (causal) {  // column n = query n / G may not see the later tokens
+                if constexpr (MQ) {  // column n = query n / G may not see the later tokens
                     const int pos = m.j0 * p.bs + r0 + g;
                     const int lim0 = m.lim + (2 * t) / G, lim1 = m.lim + (2 * t + 1) / G;
                     if (pos > lim0) s0 = kNegInf;
@@ -618,7 +637,7 @@ __device__ __forceinline__ void run_consumer(const SplitParams& p, uint32_t base
             }
             if (!consumer_sync(cbar, cphase, p.err, abort_flag)) break;  // all reads of the stage done
             const int h0 = 2 * t, h1 = 2 * t + 1;
-            const int NR = m.nr;  // q rows of the unit
+            const int NR = MQ ? m.nr : G;  // q rows of the unit
             if (g == 0) {
                 if (h0 < NR) { st_m[warp * kMaxGroup + h0] = m0; st_l[warp * kMaxGroup + h0] = l0; }
                 if (h1 < NR) { st_m[warp * kMaxGroup + h1] = m1; st_l[warp * kMaxGroup + h1] = l1; }
@@ -639,9 +658,9 @@ __device__ __forceinline__ void run_consumer(const SplitParams& p, uint32_t base
             }
             if (!consumer_sync(cbar, cphase, p.err, abort_flag)) break;
             const int ct = warp * 32 + lane;
-            const bool direct = MODE == kOneShot && (m.flags & kWholeUnit);
-            const RowInfo ri = row_info(p, m.b);
-            const int SR = p.rows_per_slot > 0 ? p.rows_per_slot : G;  // rows per partial slot
+            const bool direct = writes_output(MODE) && (m.flags & kWholeUnit);
+            const RowInfo ri = row_info<MQ>(p, m.b);
+            const int SR = MQ ? p.rows_per_slot : G;  // rows per partial slot
             for (int idx = ct; idx < NR * D; idx += kConsumerWarps * 32) {
                 const int h = idx / D, d = idx - h * D;  // h: q row of the unit
                 float M = kNegInf;
@@ -658,7 +677,8 @@ __device__ __forceinline__ void run_consumer(const SplitParams& p, uint32_t base
                 }
                 if (direct) {
                     const float r = Ls > 0.f ? Os / Ls : 0.f;
-                    const int64_t o = qo_offset(p, ri.b, ri.first + h / G, m.kvh * G + h % G, D) + d;
+                    const int64_t o = MQ ? qo_offset<MQ>(p, ri.b, ri.first + h / G, m.kvh * G + h % G, D) + d
+                                         : qo_offset<MQ>(p, m.b, 0, m.kvh * G, D) + idx;
                     if (p.out_f32) p.out_f32[o] = r;
                     else p.out[o] = __bfloat16_as_ushort(__float2bfloat16_rn(r));
                 } else {
@@ -718,12 +738,13 @@ __global__ void __maxnreg__(Cfg<D>::kMaxRegs) split_kernel(const __grid_constant
         prefetch_tensormap(&p.tm_v);
     }
     pdl_wait_primary();
-    build_prefix(p, pfx, scan);  // ends with __syncthreads (also publishes the barriers)
+    build_prefix<MODE == kMulti>(p, pfx, scan);  // ends with __syncthreads (also publishes the barriers)
     if (blockIdx.x == 0 && MODE != kGather)
         for (int i = tid; i <= p.B; i += kThreads) p.pfx[i] = pfx[i];
     int64_t begin, end;
     {
-        const GroupRange gr = group_of_cta(blockIdx.x, pfx, p.B, rows_per_seq(p), p.Hkv, gridDim.x);
+        const GroupRange gr = group_of_cta(blockIdx.x, pfx, p.B, rows_per_seq<MODE == kMulti>(p), p.Hkv,
+                                           gridDim.x);
         group_cta_range(gr, blockIdx.x, &begin, &end);
     }
 
@@ -757,16 +778,20 @@ __global__ void __launch_bounds__(kMaxGroup * 256 / 4) merge_kernel(const MergeP
     pdl_wait_primary();
     const int u = blockIdx.x;
     const int b = u / p.Hkv, kvh = u - b * p.Hkv;  // b: launch sequence (pfx index)
+    constexpr bool MQ = MODE == kMulti;
     const int G = p.G, D = p.D;
     // the row's sequence, first packed query and query count (plain: b, 0, 1)
-    const int ql = p.q_len > 1 ? p.q_len : 1;
-    const int Qr = ql > 1 ? (ql + p.qp - 1) / p.qp : 1;
-    const int Bs = p.B / Qr;
-    const int seq = Qr > 1 ? b % Bs : b;
-    const int first = ql > 1 ? (b / Bs) * p.qp : 0;
-    const int cnt = ql > 1 ? min(p.qp, ql - first) : 1;
+    const int ql = MQ ? p.q_len : 1;
+    int Qr = 1, seq = b, first = 0, cnt = 1;
+    if constexpr (MQ) {
+        Qr = (ql + p.qp - 1) / p.qp;
+        const int Bs = p.B / Qr;
+        seq = b % Bs;
+        first = (b / Bs) * p.qp;
+        cnt = min(p.qp, ql - first);
+    }
     const int NR = cnt * G;  // q rows of the unit
-    const int SR = p.rows_per_slot > 0 ? p.rows_per_slot : G;
+    const int SR = MQ ? p.rows_per_slot : G;
     const int n4 = NR * D / 4;
     const int i4 = threadIdx.x;
     const int32_t lo = p.pfx[b], nb = p.pfx[b + 1] - lo;
@@ -774,9 +799,10 @@ __global__ void __launch_bounds__(kMaxGroup * 256 / 4) merge_kernel(const MergeP
     const int h = active ? (4 * i4) / D : 0;
     const int d4 = 4 * i4 - h * D;
     // output row of unit row h: query first + h / G, q head kvh*G + h % G
-    const int64_t orow = ((int64_t)seq * ql + first + h / G) * p.Hq + (int64_t)kvh * G + h % G;
+    const int64_t orow = MQ ? ((int64_t)seq * ql + first + h / G) * p.Hq + (int64_t)kvh * G + h % G
+                            : (int64_t)b * p.Hq + (int64_t)kvh * G + h;
     if (nb == 0) {
-        if (MODE == kOneShot && active) {
+        if (writes_output(MODE) && active) {
             if (p.out_f32) *reinterpret_cast<float4*>(p.out_f32 + orow * D + d4) = make_float4(0.f, 0.f, 0.f, 0.f);
             else *reinterpret_cast<uint2*>(p.out + orow * D + d4) = make_uint2(0u, 0u);
         }
@@ -786,7 +812,7 @@ __global__ void __launch_bounds__(kMaxGroup * 256 / 4) merge_kernel(const MergeP
     const int64_t su = (int64_t)lo * p.Hkv + (int64_t)kvh * nb, eu = su + nb;
     const int64_t cf = gr.g * gr.Pg + cta_of_block(su - gr.F0, gr.W, gr.Pg);
     const int64_t cl = gr.g * gr.Pg + cta_of_block(eu - 1 - gr.F0, gr.W, gr.Pg);
-    if (MODE == kOneShot && cf == cl) return;  // written by the split kernel
+    if (writes_output(MODE) && cf == cl) return;  // written by the split kernel
     float M = kNegInf, Ls = 0.f;
     float4 Os = make_float4(0.f, 0.f, 0.f, 0.f);
     if (MODE == kTiled && active) {  // plain decode rows: orow = (b*Hq + kvh*G + h)
@@ -816,7 +842,7 @@ __global__ void __launch_bounds__(kMaxGroup * 256 / 4) merge_kernel(const MergeP
 #pragma unroll
         for (int k = 0; k < kBatch; ++k) merge_in(M, Ls, Os, mi[k], li[k], oi[k]);
     }
-    if (MODE == kOneShot) {
+    if (writes_output(MODE)) {
         if (!active) return;
         const float4 v = Ls > 0.f ? make_float4(Os.x / Ls, Os.y / Ls, Os.z / Ls, Os.w / Ls)
                                   : make_float4(0.f, 0.f, 0.f, 0.f);

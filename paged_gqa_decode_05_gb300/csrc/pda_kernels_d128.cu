@@ -9,6 +9,7 @@ const void* split_kernel_fn_d128(int mode) {
         case kOneShot: return reinterpret_cast<const void*>(&split_kernel<128, kOneShot>);
         case kTiled: return reinterpret_cast<const void*>(&split_kernel<128, kTiled>);
         case kGather: return reinterpret_cast<const void*>(&split_kernel<128, kGather>);
+        case kMulti: return reinterpret_cast<const void*>(&split_kernel<128, kMulti>);
         default: return nullptr;
     }
 }
@@ -33,6 +34,7 @@ cudaError_t launch_split_d128(int mode, const SplitParams& p, int grid, size_t s
         case kOneShot: return cudaLaunchKernelEx(&cfg, split_kernel<128, kOneShot>, p);
         case kTiled: return cudaLaunchKernelEx(&cfg, split_kernel<128, kTiled>, p);
         case kGather: return cudaLaunchKernelEx(&cfg, split_kernel<128, kGather>, p);
+        case kMulti: return cudaLaunchKernelEx(&cfg, split_kernel<128, kMulti>, p);
         default: return cudaErrorInvalidValue;
     }
 }

@@ -9,6 +9,7 @@ const void* split_kernel_fn_d256(int mode) {
         case kOneShot: return reinterpret_cast<const void*>(&split_kernel<256, kOneShot>);
         case kTiled: return reinterpret_cast<const void*>(&split_kernel<256, kTiled>);
         case kGather: return reinterpret_cast<const void*>(&split_kernel<256, kGather>);
+        case kMulti: return reinterpret_cast<const void*>(&split_kernel<256, kMulti>);
         default: return nullptr;
     }
 }
@@ -33,6 +34,7 @@ cudaError_t launch_split_d256(int mode, const SplitParams& p, int grid, size_t s
         case kOneShot: return cudaLaunchKernelEx(&cfg, split_kernel<256, kOneShot>, p);
         case kTiled: return cudaLaunchKernelEx(&cfg, split_kernel<256, kTiled>, p);
         case kGather: return cudaLaunchKernelEx(&cfg, split_kernel<256, kGather>, p);
+        case kMulti: return cudaLaunchKernelEx(&cfg, split_kernel<256, kMulti>, p);
         default: return cudaErrorInvalidValue;
     }
 }

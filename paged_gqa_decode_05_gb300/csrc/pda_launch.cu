@@ -58,6 +58,7 @@ cudaError_t launch_merge(int mode, const MergeParams& p, bool pdl, cudaStream_t 
     cfg.numAttrs = pdl ? 1 : 0;
     if (mode == kOneShot) return cudaLaunchKernelEx(&cfg, merge_kernel<kOneShot>, p);
     if (mode == kTiled) return cudaLaunchKernelEx(&cfg, merge_kernel<kTiled>, p);
+    if (mode == kMulti) return cudaLaunchKernelEx(&cfg, merge_kernel<kMulti>, p);
     return cudaErrorInvalidValue;
 }
 

@@ -17,7 +17,13 @@ constexpr int kHalfBytes = kStageTokens * 128;           // 64 rows of one 64-co
 constexpr int kMaxLaunchBatch = 1024;                    // sequences per kernel launch
 constexpr int kMaxGroup = 8;                             // q heads per kv head (n8 MMA)
 
-enum Mode : int { kOneShot = 0, kTiled = 1, kGather = 2 };
+// kOneShot: decode, output written; kTiled: fold a tile into the running
+// state; kGather: copy the staged rows out (loader check); kMulti: causal
+// multi-query decode, output written (the other modes see one query per
+// sequence, known at compile time).
+enum Mode : int { kOneShot = 0, kTiled = 1, kGather = 2, kMulti = 3 };
+constexpr int kNumModes = 4;
+__host__ __device__ constexpr bool writes_output(int mode) { return mode == kOneShot || mode == kMulti; }
 
 // Per-stage record the producer writes before arming the stage's barrier.
 struct StageMeta {

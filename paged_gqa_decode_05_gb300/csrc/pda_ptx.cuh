@@ -1,6 +1,6 @@
 // pda_ptx.cuh -- thin inline-PTX wrappers for sm_103a used by the decode kernels:
-// mbarriers with bounded waits, TMA tensor/bulk copies, ldmatrix / movmatrix,
-// bf16 mma.sync, ex2, named barriers and programmatic dependent launch.
+// mbarriers with bounded waits, TMA tensor/bulk copies, cp.async, ldmatrix /
+// movmatrix, bf16 mma.sync, ex2 and programmatic dependent launch.
 #pragma once
 
 #include <cuda.h>
@@ -180,10 +180,6 @@ __device__ __forceinline__ float bf16_lo(uint32_t x) { return __uint_as_float(x 
 __device__ __forceinline__ float bf16_hi(uint32_t x) { return __uint_as_float(x & 0xFFFF0000u); }
 
 // ---------------------------------------------------------------- sync / PDL
-
-__device__ __forceinline__ void named_barrier(uint32_t id, uint32_t threads) {
-    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
-}
 
 __device__ __forceinline__ void pdl_launch_dependents() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
