@@ -188,10 +188,14 @@ __device__ __forceinline__ void run_producer(const SplitParams& p, uint32_t base
                                              const int32_t* pfx, StageMeta* meta,
                                              volatile int* abort_flag, int64_t begin, int64_t end,
                                              int lane) {
-    // The whole warp walks the plan in lockstep: every lane keeps two block
-    // ids of a 64-entry window of the current sequence's table row (loaded
-    // one window ahead, so table reads never stall the copies), lane 0 issues
-    // the barrier operations and the TMA copies.
+    // The whole warp walks the plan in lockstep; lane 0 issues the barrier
+    // operations, the lanes issue the copies.  Block ids come from registers,
+    // loaded well before they are used so that table reads do not stall the
+    // copies: w[0..3] hold the 128-entry window [win, win + 128) of the
+    // current table row (lane i of w[k]: entry win + 32k + i), f[] the first
+    // 128 entries of the current sequence's row (the next kv head starts
+    // there) and n[] those of the next non-empty sequence, loaded one unit
+    // ahead together with its last block's valid slots.
     using C = Cfg<D>;
     constexpr int S = C::kStages;
     constexpr bool MQ = MODE == kMulti;
@@ -212,7 +216,35 @@ __device__ __forceinline__ void run_producer(const SplitParams& p, uint32_t base
     int64_t pos = begin;
     int b = 0, kvh = 0;
     int32_t j = 0, nb = 0;
-    int32_t win = 0, id0 = 0, id1 = 0;
+    int32_t win = 0;
+    int32_t w[4], f[4], nx[4];
+    int32_t lv = bs, nlv = bs;  // valid slots of the last block: this / next sequence
+    int bn = p.B;               // next non-empty sequence
+#pragma unroll
+    for (int k = 0; k < 4; ++k) w[k] = f[k] = nx[k] = 0;
+    // entries [from, from + 128) of sequence s's row (nbs blocks), lane-strided
+    auto load_ids = [&](int32_t* dst, int s, int32_t from, int32_t nbs) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int32_t e = from + 32 * k + lane;
+            dst[k] = e < nbs ? table_entry<MQ>(p, s, e) : 0;
+        }
+    };
+    auto next_seq = [&](int s) {
+        do { ++s; } while (s < p.B && pfx[s + 1] == pfx[s]);
+        return s;
+    };
+    // The id of window entry idx (lane-varying).  A stage reads entries
+    // j - win .. j - win + n - 1 < 64: the blocks per stage NB = 64 / bs is a
+    // power of two, j - win stays a multiple of NB (the window starts at a
+    // segment start or a unit start and slides by 64) and n <= NB.  So only
+    // w[0] and w[1] are read; w[2] and w[3], loaded at a slide, are first read
+    // a whole window later, after the next slide has moved them down.
+    auto win_id = [&](int idx) {
+        const int32_t a = __shfl_sync(0xffffffffu, w[0], idx & 31);
+        const int32_t c = __shfl_sync(0xffffffffu, w[1], idx & 31);
+        return idx < 32 ? a : c;
+    };
     if (pos < end) {
         int lo = 0, hi = p.B - 1;  // largest b with pfx[b]*Hkv <= pos
         while (lo < hi) {
@@ -225,25 +257,32 @@ __device__ __forceinline__ void run_producer(const SplitParams& p, uint32_t base
         kvh = (int)(rem / nb);
         j = (int32_t)(rem % nb);
         win = j;
-        id0 = win + lane < nb ? table_entry<MQ>(p, b, win + lane) : 0;
-        id1 = win + 32 + lane < nb ? table_entry<MQ>(p, b, win + 32 + lane) : 0;
+        load_ids(w, b, win, nb);
+        if (win == 0) {
+#pragma unroll
+            for (int k = 0; k < 4; ++k) f[k] = w[k];
+        } else {
+            load_ids(f, b, 0, nb);
+        }
+        lv = last_block_slots<MQ>(p, b, nb);
+        bn = next_seq(b);
+        if (bn < p.B) {
+            const int32_t nbn = pfx[bn + 1] - pfx[bn];
+            load_ids(nx, bn, 0, nbn);
+            nlv = last_block_slots<MQ>(p, bn, nbn);
+        }
     }
     bool seg_begin = true;
     bool whole = false;
     while (pos < end) {
         const int stop = __shfl_sync(0xffffffffu, leader ? *abort_flag : 0, 0);
         if (stop) { ok = false; break; }
-        if (p.row_gather && win != j) {  // up to 64 blocks per stage: reload the window
-            win = j;
-            id0 = win + lane < nb ? table_entry<MQ>(p, b, win + lane) : 0;
-            id1 = win + 32 + lane < nb ? table_entry<MQ>(p, b, win + 32 + lane) : 0;
-        }
         const int32_t n = (int32_t)min((int64_t)min(NB, nb - j), end - pos);
         const bool unit_end = (j + n == nb);
         const bool seg_end = unit_end || (pos + n == end);
         if (seg_begin) whole = (j == 0) && ((int64_t)pfx[b] * Hkv + (int64_t)(kvh + 1) * nb <= end);
 
-        const int32_t lastv = unit_end ? last_block_slots<MQ>(p, b, nb) : bs;
+        const int32_t lastv = unit_end ? lv : bs;
 
         bool got = true;
         if (leader) got = mbar_wait_bounded(empty0 + 8 * stage, phase ^ 1u, kWaitLimitNs);
@@ -302,9 +341,7 @@ __device__ __forceinline__ void run_producer(const SplitParams& p, uint32_t base
                 for (int k = 0; k < 4; ++k) {
                     const int t = min(4 * g + k, rows - 1);
                     const int i = t >> lbs;  // block of the stage (< 64)
-                    const int32_t a = __shfl_sync(0xffffffffu, id0, i & 31);
-                    const int32_t cc = __shfl_sync(0xffffffffu, id1, i & 31);
-                    int32_t id = i < 32 ? a : cc;
+                    int32_t id = win_id(j - win + i);
                     if (o < groups * H && (id < 0 || (int64_t)id >= p.num_blocks)) {
                         atomicOr(p.err, PDA_DEVERR_BAD_BLOCK_ID_);
                         id = 0;
@@ -330,11 +367,10 @@ __device__ __forceinline__ void run_producer(const SplitParams& p, uint32_t base
             const uint16_t* vb = p.v_base + (int64_t)kvh * p.kvh_s + c * 8;
             for (int t0 = 0; t0 < rows; t0 += RPI) {
                 const int t = t0 + sub;
-                const int i = t >> lbs;  // block of the stage (< 64)
-                const int32_t a = __shfl_sync(0xffffffffu, id0, i & 31);
-                const int32_t cc = __shfl_sync(0xffffffffu, id1, i & 31);
+                const int i = min(t, rows - 1) >> lbs;  // block of the stage (< 64)
+                const int32_t wid = win_id(j - win + i);
                 if (t < rows) {
-                    int32_t id = i < 32 ? a : cc;
+                    int32_t id = wid;
                     if (id < 0 || (int64_t)id >= p.num_blocks) {
                         atomicOr(p.err, PDA_DEVERR_BAD_BLOCK_ID_);
                         id = 0;
@@ -348,14 +384,11 @@ __device__ __forceinline__ void run_producer(const SplitParams& p, uint32_t base
             }
             cp_async_mbar_arrive_noinc(full);
         } else
-        // lane i copies block i of the stage (its id comes from the window;
-        // j + i - win < 40 by the window rule below)
+        // lane i copies block i of the stage (its id comes from the window)
         {
-            const int idx = j + lane - win;
-            const int32_t a = __shfl_sync(0xffffffffu, id0, idx & 31);
-            const int32_t c = __shfl_sync(0xffffffffu, id1, idx & 31);
+            const int32_t wid = win_id(j - win + min(lane, n - 1));
             if (lane < n) {
-                int32_t id = idx < 32 ? a : c;
+                int32_t id = wid;
                 if (id < 0 || (int64_t)id >= p.num_blocks) {
                     atomicOr(p.err, PDA_DEVERR_BAD_BLOCK_ID_);
                     id = 0;  // stays in bounds; the flag marks the result invalid
@@ -373,21 +406,37 @@ __device__ __forceinline__ void run_producer(const SplitParams& p, uint32_t base
         seg_begin = seg_end;
         if (unit_end) {
             j = 0;
-            if (++kvh == Hkv) {
+            win = 0;
+            if (++kvh == Hkv) {  // next sequence: its ids were loaded a unit ago
                 kvh = 0;
-                do { ++b; } while (b < p.B && pfx[b + 1] == pfx[b]);
+                b = bn;
+                nb = b < p.B ? pfx[b + 1] - pfx[b] : 0;
+#pragma unroll
+                for (int k = 0; k < 4; ++k) w[k] = f[k] = nx[k];
+                lv = nlv;
+                if (b < p.B && pos < end) {
+                    bn = next_seq(b);
+                    if (bn < p.B) {
+                        const int32_t nbn = pfx[bn + 1] - pfx[bn];
+                        load_ids(nx, bn, 0, nbn);
+                        nlv = last_block_slots<MQ>(p, bn, nbn);
+                    }
+                }
+            } else {  // next kv head of the same sequence: the same row again
+#pragma unroll
+                for (int k = 0; k < 4; ++k) w[k] = f[k];
             }
-            nb = b < p.B ? pfx[b + 1] - pfx[b] : 0;
-            if (pos < end) {
-                win = 0;
-                id0 = lane < nb ? table_entry<MQ>(p, b, lane) : 0;
-                id1 = 32 + lane < nb ? table_entry<MQ>(p, b, 32 + lane) : 0;
+        } else if (j - win >= 64) {
+            // first half consumed: slide by 64 and fetch the 64 entries after
+            // the window (needed no sooner than the next stage)
+            win += 64;
+            w[0] = w[2];
+            w[1] = w[3];
+#pragma unroll
+            for (int k = 2; k < 4; ++k) {
+                const int32_t e = win + 32 * k + lane;
+                w[k] = e < nb ? table_entry<MQ>(p, b, e) : 0;
             }
-        } else if (j - win >= 32) {
-            // first half consumed: slide the window and fetch the next 32 ids
-            win += 32;
-            id0 = id1;
-            id1 = win + 32 + lane < nb ? table_entry<MQ>(p, b, win + 32 + lane) : 0;
         }
         if (++stage == S) { stage = 0; phase ^= 1u; }
     }
