@@ -104,20 +104,33 @@ __device__ __forceinline__ int32_t table_entry(const SplitParams& p, int s, int 
     return p.table[(int64_t)row * p.table_stride + idx];
 }
 
-// Tokens read for launch sequence s: its length, or for a row of causal
-// queries the prefix its last query sees, L - q_len + first + cnt (>= 0).
+// The length entry of launch sequence s (tokens; blocks in tiled steps).
 template <bool MQ>
-__device__ __forceinline__ int32_t seq_tokens(const SplitParams& p, int s) {
-    if constexpr (!MQ) return p.lens[s];
+__device__ __forceinline__ int32_t len_entry(const SplitParams& p, int s) {
+    return p.lens[row_info<MQ>(p, s).b];
+}
+
+// Tokens read for launch sequence s with length entry L: L itself, or for a
+// row of causal queries the prefix its last query sees, L - q_len + first +
+// cnt (>= 0).
+template <bool MQ>
+__device__ __forceinline__ int32_t tokens_of(const SplitParams& p, int s, int32_t L) {
+    if constexpr (!MQ) return L;
     const RowInfo r = row_info<MQ>(p, s);
-    const int32_t len = p.lens[r.b] - p.q_len + r.first + r.cnt;
+    const int32_t len = L - p.q_len + r.first + r.cnt;
     return len < 0 ? 0 : len;
 }
 
-// Blocks of sequence b, validated and clamped (flags bad lengths).
 template <bool MQ>
-__device__ __forceinline__ int32_t seq_blocks(const SplitParams& p, int b) {
-    int32_t len = p.lens_are_blocks ? p.lens[b] : seq_tokens<MQ>(p, b);
+__device__ __forceinline__ int32_t seq_tokens(const SplitParams& p, int s) {
+    return tokens_of<MQ>(p, s, len_entry<MQ>(p, s));
+}
+
+// Blocks of sequence b with length entry L, validated and clamped (flags
+// bad lengths).
+template <bool MQ>
+__device__ __forceinline__ int32_t blocks_of(const SplitParams& p, int b, int32_t L) {
+    int32_t len = p.lens_are_blocks ? L : tokens_of<MQ>(p, b, L);
     if (p.lens_are_blocks) {
         if (len < 0 || len > p.table_stride) {
             atomicOr(p.err, PDA_DEVERR_BAD_LENGTH_);
@@ -153,31 +166,45 @@ __device__ __forceinline__ int32_t last_block_slots(const SplitParams& p, int b,
     return v > p.bs ? p.bs : v;
 }
 
-// Exclusive prefix of blocks per sequence into shared pfx[0..B].
+// Exclusive prefix of blocks per sequence into shared pfx[0..B] (B <= 1024).
+// Thread t owns sequences [t*per, t*per + per): it loads all their length
+// entries at once (one memory round trip), stores their block counts in pfx,
+// and the per-thread sums are scanned with warp shuffles and the warp totals.
 template <bool MQ>
 __device__ __forceinline__ void build_prefix(const SplitParams& p, int32_t* pfx, int32_t* scan) {
-    const int tid = threadIdx.x;
-    const int per = (p.B + kThreads - 1) / kThreads;
+    constexpr int kPer = (kMaxLaunchBatch + kThreads - 1) / kThreads;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int per = (p.B + kThreads - 1) / kThreads;  // <= kPer
     const int lo = min(p.B, tid * per), hi = min(p.B, lo + per);
+    int32_t L[kPer];
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) L[k] = lo + k < hi ? len_entry<MQ>(p, lo + k) : 0;
     int32_t sum = 0;
-    for (int b = lo; b < hi; ++b) sum += seq_blocks<MQ>(p, b);
-    scan[tid] = sum;
+#pragma unroll
+    for (int k = 0; k < kPer; ++k)
+        if (lo + k < hi) {
+            const int32_t v = blocks_of<MQ>(p, lo + k, L[k]);
+            pfx[lo + k] = v;
+            sum += v;
+        }
+    int32_t x = sum;  // inclusive scan within the warp
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int32_t y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) scan[warp] = x;
     __syncthreads();
-    if (tid == 0) {
-        int32_t run = 0;
-        for (int i = 0; i < kThreads; ++i) {
-            const int32_t v = scan[i];
-            scan[i] = run;
+    int32_t run = x - sum;
+    for (int w = 0; w < warp; ++w) run += scan[w];
+    if (tid == kThreads - 1) pfx[p.B] = run + sum;
+#pragma unroll
+    for (int k = 0; k < kPer; ++k)
+        if (lo + k < hi) {
+            const int32_t v = pfx[lo + k];
+            pfx[lo + k] = run;
             run += v;
         }
-        pfx[p.B] = run;
-    }
-    __syncthreads();
-    int32_t run = scan[tid];
-    for (int b = lo; b < hi; ++b) {
-        pfx[b] = run;
-        run += seq_blocks<MQ>(p, b);
-    }
     __syncthreads();
 }
 

@@ -102,7 +102,7 @@ PDA_HD SmemLayout smem_layout(int D, int stages, int G, int B) {
     L.bars = off;  off += 2u * stages * 8u;
     L.cbar = off;  off += 8u;
     L.meta = off;  off += (uint32_t)stages * (uint32_t)sizeof(StageMeta);
-    L.scan = off;  off += kThreads * 4u;
+    L.scan = off;  off += 32u;  // one int per warp (block-prefix scan)
     L.st_m = off;  off += kConsumerWarps * kMaxGroup * 4u;
     L.st_l = off;  off += kConsumerWarps * kMaxGroup * 4u;
     L.pfx = off;   off += (uint32_t)(B + 1) * 4u;
