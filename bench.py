@@ -212,9 +212,20 @@ def cpu_oracle_timing(w, budget_s: float = 10.0):
     frac = (n if pairs is not None else total_pairs) / total_pairs
     sec_per_call = elapsed / reps / frac  # scaled to the whole workload
     gbs = w.algorithmic_bytes() / sec_per_call / 1e9
+    # the same oracle on one thread, over a smaller sample of the same outputs
+    n1 = int(min(total_pairs, max(1, budget_s / 4 / max(per_pair * threads, 1e-9))))
+    pick1 = np.sort(rng.choice(total_pairs, size=n1, replace=False))
+    pairs1 = np.stack([pick1 // w.Hq, pick1 % w.Hq], axis=1).astype(np.int32)
+    t = time.perf_counter()
+    orc.decode(*args, **{**kw, "n_threads": 1}, pairs=pairs1)
+    sec1 = (time.perf_counter() - t) * total_pairs / n1
     return {"value": gbs, "unit": "GB/s", "cores": threads, "kind": "oracle",
             "sample": f"{desc}; fp64 C oracle, {reps} repetition(s), scaled to the full call",
-            "sec_per_call": sec_per_call}
+            "sec_per_call": sec_per_call,
+            "single_thread": {"value": w.algorithmic_bytes() / sec1 / 1e9, "unit": "GB/s",
+                              "sec_per_call": sec1,
+                              "sample": f"{n1} of {total_pairs} (b, q-head) outputs, one thread, "
+                                        "scaled to the full call"}}
 
 
 def run_reference(args):
@@ -231,7 +242,8 @@ def run_reference(args):
             "data": "synthetic (seeded N(0,1) bf16 inputs)",
             "config": {**w.describe(), "workload": w.name, "kv_layout": args.layout,
                    "q_len": args.q_len, "runs_on": "host CPU cores"},
-            "cpu_baseline": {k: cb[k] for k in ("value", "unit", "cores", "kind", "sample")},
+            "cpu_baseline": {k: cb[k] for k in ("value", "unit", "cores", "kind", "sample",
+                                                "single_thread")},
             "e2e": {"value": cb["value"], "unit": "GB/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -366,6 +378,50 @@ def run_ours(args):
     if ctx.read_device_errors() != 0:
         raise RuntimeError("device error flags set during timing")
 
+    # --- per-call distribution: an event pair around each call (events between
+    # calls stop the next call's early launch, so these are isolated calls)
+    per_call = None
+    if not args.quick:
+        n_pc = max(50, min(args.steps, 200))
+        pc = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(n_pc)]
+        for a, b in pc:
+            a.record(stream)
+            step()
+            b.record(stream)
+        torch.cuda.synchronize()
+        us = sorted(a.elapsed_time(b) * 1e3 for a, b in pc)
+        per_call = {"median": statistics.median(us), "p10": us[int(0.1 * (n_pc - 1))],
+                    "p90": us[int(0.9 * (n_pc - 1))], "calls": n_pc,
+                    "note": "isolated calls, inputs rotated (L2 cold)"}
+
+    # --- L2-warm number (same inputs every call) for the workloads that fit in L2
+    l2_warm = None
+    if not args.quick and input_bytes < l2 // 2:
+        s0, o0 = sets[0], outs[0]
+
+        def warm_step():
+            if args.q_len > 1:
+                ctx.decode_multi(s0["q"], s0["k_pool"], s0["v_pool"], s0["block_table"],
+                                 s0["seq_lens"], out=o0)
+            elif args.layout == "contiguous":
+                ctx.decode_contiguous(s0["q"], s0["k_pool"], s0["v_pool"], s0["seq_lens"], out=o0)
+            else:
+                ctx.decode(s0["q"], s0["k_pool"], s0["v_pool"], s0["block_table"], s0["seq_lens"],
+                           out=o0)
+
+        for _ in range(5):
+            warm_step()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(args.steps):
+            warm_step()
+        b.record(stream)
+        torch.cuda.synchronize()
+        warm_us = a.elapsed_time(b) * 1e3 / args.steps
+        l2_warm = {"us_per_call": warm_us, "GB/s": bytes_per_call / (warm_us * 1e-6) / 1e9,
+                   "note": "L2-warm: one input set reused every call (labelled; not the metric)"}
+
     # --- end to end: pinned host inputs copied in, output copied back, each step
     e2e = None
     if not (args.no_e2e or args.quick):
@@ -436,16 +492,25 @@ def run_ours(args):
                    "stages": info["stages"], "algorithmic_bytes_per_call": bytes_per_call},
         "roofline": {"bound": "hbm", "kernel": "split_kernel", "achieved": achieved, "peak": peak,
                      "peak_kind": f"{peak_kind} hbm_gbs (STREAM-style copy)", "unit": "GB/s",
-                     "frac": achieved / peak, "traffic": recorded_traffic(args.workload),
+                     "frac": achieved / peak,
+                     # the ncu record holds the default configuration of each workload
+                     "traffic": (recorded_traffic(args.workload)
+                                 if (args.block_size == 0 and args.layout == "paged"
+                                     and args.q_len == 1) else None),
                      "split_us": split_avg * 1e3, "merge_us": merge_avg * 1e3},
         "gpu_launches": 2 * args.steps,
         "clocks": clocks,
     }
+    if per_call is not None:
+        line["per_call_us"] = per_call
+    if l2_warm is not None:
+        line["l2_warm"] = l2_warm
     if e2e is not None:
         line["e2e"] = e2e
     if rank == 0 and world == 1 and not (args.no_cpu_baseline or args.quick):
         cb = cpu_oracle_timing(w)
-        line["cpu_baseline"] = {k: cb[k] for k in ("value", "unit", "cores", "kind", "sample")}
+        line["cpu_baseline"] = {k: cb[k] for k in ("value", "unit", "cores", "kind", "sample",
+                                                   "single_thread")}
     if rank == 0:
         print(json.dumps(line), flush=True)
     ctx.close()
