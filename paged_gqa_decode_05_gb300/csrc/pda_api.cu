@@ -64,6 +64,7 @@ struct pda_ctx {
     int device = 0;
     int num_sms = 0;
     int stages = 0;
+    int stage_rows = 64;  // split-kernel shape: KV rows per stage
     int ctas_per_sm = 0;
     int split_ctas = 0;
     int smem_max = 0;
@@ -264,12 +265,12 @@ pda_status run(pda_ctx* ctx, const RunArgs& r) {
         p.bs = d.block_size;
         p.dbg_row_tokens = (int32_t)dbg_row_tokens;
         p.scale_log2 = scale_log2;
-        const size_t smem = pda::smem_layout(D, ctx->stages, ctx->G, cb).total;
+        const size_t smem = pda::smem_layout(D, ctx->stage_rows, ctx->stages, ctx->G, cb).total;
 
         cudaError_t e;
         if (timing && c0 == 0 && (e = cudaEventRecord(ctx->ev_begin, r.stream)) != cudaSuccess)
             return cuda_fail(e, "cudaEventRecord");
-        e = pda::launch_split(D, r.mode, p, ctx->split_ctas, smem, r.stream);
+        e = pda::launch_split(D, ctx->stage_rows, r.mode, p, ctx->split_ctas, smem, r.stream);
         if (e != cudaSuccess) return cuda_fail(e, "split kernel launch");
         if (r.mode == pda::kGather) continue;
         if (timing && (e = cudaEventRecord(ctx->ev_split, r.stream)) != cudaSuccess)
@@ -398,26 +399,29 @@ PDA_EXPORT pda_status pda_create(const pda_dims* dims, pda_ctx** out_ctx) {
     ctx->device = dev;
     ctx->num_sms = prop.multiProcessorCount;
     const int D = dims->head_dim;
-    ctx->stages = pda::split_stages(D);
+    ctx->stage_rows = pda::stage_tokens(D, dims->block_size);
+    ctx->stages = pda::split_stages(D, ctx->stage_rows);
     const int chunk_b = std::min(dims->max_seqs, pda::kMaxLaunchBatch);
-    ctx->smem_max = (int)pda::smem_layout(D, ctx->stages, ctx->G, chunk_b).total;
+    ctx->smem_max = (int)pda::smem_layout(D, ctx->stage_rows, ctx->stages, ctx->G, chunk_b).total;
     if (ctx->smem_max > (int)prop.sharedMemPerBlockOptin) {
         delete ctx;
         return fail(PDA_ERR_UNSUPPORTED, "needs %d bytes of shared memory per CTA (device allows %d)",
                     ctx->smem_max, (int)prop.sharedMemPerBlockOptin);
     }
     for (int mode = 0; mode < pda::kNumModes; ++mode) {
-        e = cudaFuncSetAttribute(pda::split_kernel_fn(D, mode), cudaFuncAttributeMaxDynamicSharedMemorySize,
+        e = cudaFuncSetAttribute(pda::split_kernel_fn(D, ctx->stage_rows, mode),
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  ctx->smem_max);
         if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(pda::split_kernel_fn(D, mode),
+            e = cudaFuncSetAttribute(pda::split_kernel_fn(D, ctx->stage_rows, mode),
                                      cudaFuncAttributePreferredSharedMemoryCarveout,
                                      cudaSharedmemCarveoutMaxShared);
         if (e != cudaSuccess) { delete ctx; return cuda_fail(e, "cudaFuncSetAttribute"); }
     }
     int per_sm = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, pda::split_kernel_fn(D, pda::kOneShot),
-                                                      pda::kThreads, ctx->smem_max);
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm,
+                                                      pda::split_kernel_fn(D, ctx->stage_rows, pda::kOneShot),
+                                                      pda::split_threads(ctx->stage_rows), ctx->smem_max);
     if (e != cudaSuccess) { delete ctx; return cuda_fail(e, "occupancy query"); }
     if (per_sm < 1) { delete ctx; return fail(PDA_ERR_UNSUPPORTED, "split kernel does not fit on an SM"); }
     ctx->ctas_per_sm = per_sm;
@@ -588,7 +592,7 @@ PDA_EXPORT pda_status pda_get_launch_info(const pda_ctx* ctx, pda_launch_info* i
     info->num_sms = ctx->num_sms;
     info->stages = ctx->stages;
     info->smem_bytes = ctx->smem_max;
-    info->stage_tokens = pda::kStageTokens;
+    info->stage_tokens = ctx->stage_rows;
     info->partial_slots = ctx->slots;
     return PDA_OK;
 }
@@ -730,9 +734,10 @@ PDA_EXPORT pda_status pda_decode_noalloc(const pda_bf16* q, const pda_bf16* k_po
         num_sms = nd.num_sms;
     }
 
-    const int stages = pda::split_stages(D);
-    const size_t smem = pda::smem_layout(D, stages, G, batch).total;
-    const void* split_fn = pda::split_kernel_fn(D, pda::kOneShot);
+    const int rows = pda::stage_tokens(D, block_size);  // split-kernel shape
+    const int stages = pda::split_stages(D, rows);
+    const size_t smem = pda::smem_layout(D, rows, stages, G, batch).total;
+    const void* split_fn = pda::split_kernel_fn(D, rows, pda::kOneShot);
     // The attribute is per function and device and other contexts may have
     // set a smaller value, so it is set on every call (no allocation).
     if ((e = cudaFuncSetAttribute(split_fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) != cudaSuccess ||
@@ -740,7 +745,8 @@ PDA_EXPORT pda_status pda_decode_noalloc(const pda_bf16* q, const pda_bf16* k_po
                                   cudaSharedmemCarveoutMaxShared)) != cudaSuccess)
         return cuda_fail(e, "cudaFuncSetAttribute");
     int per_sm = 0;
-    if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, split_fn, pda::kThreads, smem)) != cudaSuccess)
+    if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, split_fn, pda::split_threads(rows), smem)) !=
+        cudaSuccess)
         return cuda_fail(e, "occupancy query");
     if (per_sm < 1) return fail(PDA_ERR_UNSUPPORTED, "split kernel does not fit on an SM");
     const int split_ctas = per_sm * num_sms;
@@ -793,7 +799,7 @@ PDA_EXPORT pda_status pda_decode_noalloc(const pda_bf16* q, const pda_bf16* k_po
     p.G = G;
     p.bs = block_size;
     p.scale_log2 = scale_log2;
-    if ((e = pda::launch_split(D, pda::kOneShot, p, split_ctas, smem, s)) != cudaSuccess)
+    if ((e = pda::launch_split(D, rows, pda::kOneShot, p, split_ctas, smem, s)) != cudaSuccess)
         return cuda_fail(e, "split kernel launch");
     pda::MergeParams mp;
     std::memset(&mp, 0, sizeof mp);

@@ -7,7 +7,8 @@
 //     head into a ring of shared-memory stages with one 5-D TMA tensor copy
 //     per block and pool (128-byte swizzle), plus the group's q rows with one
 //     bulk copy at the start of each segment.  Stage completion is tracked by mbarriers.
-//   * warps 0..3 consume a stage of 64 rows, 16 rows each.  The GQA group
+//   * ST/16 consumer warps read a stage of ST rows (64; 32 for head_dim 256
+//     with blocks of at most 32 tokens), 16 rows each.  The GQA group
 //     (G <= 8 q heads of one kv head) shares every K/V load: S^T = K q^T is a
 //     16x8 tile per warp (mma.sync m16n8k16, tokens as M, heads as N), the
 //     online-softmax update runs on the accumulator fragments (warp-shuffle
@@ -47,15 +48,29 @@ constexpr uint64_t kWaitLimitNs = 2000000000ull;  // each mbarrier wait gives up
 #ifndef PDA_STAGES_D256
 #define PDA_STAGES_D256 3
 #endif
+// 32-row stages (head_dim 256, block sizes below 8).
+#ifndef PDA_STAGES_D256_ST32
+#define PDA_STAGES_D256_ST32 3
+#endif
 
-template <int D>
+// Register cap of the split kernel (see split_kernel).
+constexpr int split_max_regs(int D) { return D == 256 ? 255 : 168; }
+
+template <int D, int ST>
 struct Cfg {
+    static constexpr int kST = ST;                       // KV rows per stage (64 or 32)
+    static constexpr int kLogST = ST == 64 ? 6 : 5;
+    static constexpr int kConsumerWarps = ST / 16;       // 16 rows each
+    static constexpr int kThreads = (kConsumerWarps + 1) * 32;  // + the producer warp
     static constexpr int kHalves = D / 64;               // 64-column swizzled slabs per row
+    static constexpr int kHalfBytes = ST * 128;          // ST rows of one slab
     static constexpr int kTileBytes = kHalves * kHalfBytes;
     static constexpr int kStageBytes = 2 * kTileBytes + 16 * D;
-    static constexpr int kStages = D == 64 ? PDA_STAGES_D64 : (D == 128 ? PDA_STAGES_D128 : PDA_STAGES_D256);
+    static constexpr int kStages = D == 64 ? PDA_STAGES_D64
+                                 : D == 128 ? PDA_STAGES_D128
+                                 : ST == 32 ? PDA_STAGES_D256_ST32 : PDA_STAGES_D256;
     static constexpr int kKSteps = D / 16;
-    static constexpr int kMaxRegs = D == 256 ? 255 : 168;
+    static_assert(ST == 64 || ST == 32, "stage rows");
 };
 
 // Entry idx of sequence b's block list: the table row, or, for a contiguous
@@ -170,7 +185,7 @@ __device__ __forceinline__ int32_t last_block_slots(const SplitParams& p, int b,
 // Thread t owns sequences [t*per, t*per + per): it loads all their length
 // entries at once (one memory round trip), stores their block counts in pfx,
 // and the per-thread sums are scanned with warp shuffles and the warp totals.
-template <bool MQ>
+template <bool MQ, int kThreads>
 __device__ __forceinline__ void build_prefix(const SplitParams& p, int32_t* pfx, int32_t* scan) {
     constexpr int kPer = (kMaxLaunchBatch + kThreads - 1) / kThreads;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -210,7 +225,7 @@ __device__ __forceinline__ void build_prefix(const SplitParams& p, int32_t* pfx,
 
 // ------------------------------------------------------------------ producer
 
-template <int D, int MODE>
+template <int D, int ST, int MODE>
 __device__ __forceinline__ void run_producer(const SplitParams& p, uint32_t base_s, const SmemLayout& L,
                                              const int32_t* pfx, StageMeta* meta,
                                              volatile int* abort_flag, int64_t begin, int64_t end,
@@ -223,7 +238,7 @@ __device__ __forceinline__ void run_producer(const SplitParams& p, uint32_t base
     // 128 entries of the current sequence's row (the next kv head starts
     // there) and n[] those of the next non-empty sequence, loaded one unit
     // ahead together with its last block's valid slots.
-    using C = Cfg<D>;
+    using C = Cfg<D, ST>;
     constexpr int S = C::kStages;
     constexpr bool MQ = MODE == kMulti;
     const uint32_t full0 = base_s + L.bars, empty0 = full0 + 8 * S;
@@ -233,7 +248,7 @@ __device__ __forceinline__ void run_producer(const SplitParams& p, uint32_t base
     // it normal.
     const uint64_t pol = rows_per_seq<MQ>(p) > 1 ? policy_evict_normal() : policy_evict_first();
     const int bs = p.bs, Hkv = p.Hkv;
-    const int NB = kStageTokens / bs;
+    const int NB = C::kST / bs;  // blocks per stage (the host keeps bs <= ST)
 
     int stage = 0;
     uint32_t phase = 0;
@@ -355,19 +370,19 @@ __device__ __forceinline__ void run_producer(const SplitParams& p, uint32_t base
         if (p.row_gather == 1) {
             // Rows of small blocks, 4 per TMA gather4 copy of one 64-column slab:
             // group g covers stage rows 4g..4g+3 (the tail repeats the last row,
-            // which the consumers mask), written as one 64-row block.
+            // which the consumers mask), written as one ST-row block.
             constexpr int H = C::kHalves;
             const int lbs = 31 - __clz(bs);
             const int rows = (n - 1) * bs + lastv;
             const int groups = (rows + 3) >> 2;
-            for (int o0 = 0; o0 < 16 * H; o0 += 32) {
+            for (int o0 = 0; o0 < (C::kST / 4) * H; o0 += 32) {
                 const int o = o0 + lane;
                 const int g = o / H, h = o - g * H;
                 int32_t r[4];
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
                     const int t = min(4 * g + k, rows - 1);
-                    const int i = t >> lbs;  // block of the stage (< 64)
+                    const int i = t >> lbs;  // block of the stage (< ST)
                     int32_t id = win_id(j - win + i);
                     if (o < groups * H && (id < 0 || (int64_t)id >= p.num_blocks)) {
                         atomicOr(p.err, PDA_DEVERR_BAD_BLOCK_ID_);
@@ -377,14 +392,14 @@ __device__ __forceinline__ void run_producer(const SplitParams& p, uint32_t base
                                      (int64_t)kvh * p.row_kvh);
                 }
                 if (o < groups * H) {
-                    const uint32_t dst = (uint32_t)h * kHalfBytes + (uint32_t)(4 * g) * 128u;
+                    const uint32_t dst = (uint32_t)h * C::kHalfBytes + (uint32_t)(4 * g) * 128u;
                     tma_gather4(sK + dst, &p.tm_k, h * 64, r[0], r[1], r[2], r[3], full, pol);
                     tma_gather4(sV + dst, &p.tm_v, h * 64, r[0], r[1], r[2], r[3], full, pol);
                 }
             }
         } else if (p.row_gather == 2) {
             // Rows of small blocks: 16-byte cp.async chunks, CH per row, written
-            // in the layout of one 64-row block ([slab][row][128 B], swizzled).
+            // in the layout of one ST-row block ([slab][row][128 B], swizzled).
             constexpr int CH = D / 8;
             constexpr int RPI = 32 / CH;  // rows per pass of the warp
             const int c = lane % CH, sub = lane / CH;
@@ -394,7 +409,7 @@ __device__ __forceinline__ void run_producer(const SplitParams& p, uint32_t base
             const uint16_t* vb = p.v_base + (int64_t)kvh * p.kvh_s + c * 8;
             for (int t0 = 0; t0 < rows; t0 += RPI) {
                 const int t = t0 + sub;
-                const int i = min(t, rows - 1) >> lbs;  // block of the stage (< 64)
+                const int i = min(t, rows - 1) >> lbs;  // block of the stage (< ST)
                 const int32_t wid = win_id(j - win + i);
                 if (t < rows) {
                     int32_t id = wid;
@@ -403,7 +418,7 @@ __device__ __forceinline__ void run_producer(const SplitParams& p, uint32_t base
                         id = 0;
                     }
                     const int64_t off = (int64_t)id * p.blk_s + (int64_t)(t & (bs - 1)) * p.tok_s;
-                    const uint32_t dst = (uint32_t)(c >> 3) * kHalfBytes + (uint32_t)t * 128u +
+                    const uint32_t dst = (uint32_t)(c >> 3) * C::kHalfBytes + (uint32_t)t * 128u +
                                          (uint32_t)(((c & 7) ^ (t & 7)) << 4);
                     cp_async_16(sK + dst, kb + off);
                     cp_async_16(sV + dst, vb + off);
@@ -505,12 +520,12 @@ __device__ __forceinline__ uint32_t row_off(int t, int lbs) {
 // bits, and 0 * NaN would poison the P.V product).
 template <int D>
 __device__ __forceinline__ void zero_rows(uint32_t sV, int from, int to, int lbs, int lane) {
-    using C = Cfg<D>;
+    constexpr int kHalves = D / 64;
     const uint32_t hs = (uint32_t)(128 << lbs);
-    const int units = (to - from) * C::kHalves * 8;
+    const int units = (to - from) * kHalves * 8;
     for (int u = lane; u < units; u += 32) {
-        const int r = from + u / (C::kHalves * 8);
-        const int rem = u % (C::kHalves * 8);
+        const int r = from + u / (kHalves * 8);
+        const int rem = u % (kHalves * 8);
         const uint32_t a = sV + row_off<D>(r, lbs) + (uint32_t)(rem >> 3) * hs + ((rem & 7) << 4);
         asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(a), "r"(0) : "memory");
     }
@@ -520,15 +535,15 @@ template <int D>
 __device__ __forceinline__ void gather_rows(const SplitParams& p, uint32_t base_s, const uint8_t* base,
                                             uint32_t sK, uint32_t sV, const StageMeta& m, int r0,
                                             int lbs, int lane) {
-    using C = Cfg<D>;
+    constexpr int kHalves = D / 64;
     const uint32_t hs = (uint32_t)(128 << lbs);
     const int rows = min(16, m.n_valid - r0);
     if (rows <= 0) return;
-    const int units = rows * C::kHalves * 8;
+    const int units = rows * kHalves * 8;
     const int64_t row0 = ((int64_t)m.b * p.Hkv + m.kvh) * p.dbg_row_tokens + (int64_t)m.j0 * p.bs + r0;
     for (int u = lane; u < units; u += 32) {
-        const int r = u / (C::kHalves * 8);
-        const int rem = u % (C::kHalves * 8);
+        const int r = u / (kHalves * 8);
+        const int rem = u % (kHalves * 8);
         const int h = rem >> 3, c = rem & 7;
         const int rr = r0 + r;
         const uint32_t off = row_off<D>(rr, lbs) + (uint32_t)h * hs + (uint32_t)((c ^ (rr & 7)) << 4);
@@ -554,11 +569,11 @@ __device__ __forceinline__ bool consumer_sync(uint32_t cbar, uint32_t& cphase, u
     return ok;
 }
 
-template <int D, int MODE>
+template <int D, int ST, int MODE>
 __device__ __forceinline__ void run_consumer(const SplitParams& p, uint32_t base_s, uint8_t* base,
                                              const SmemLayout& L, const StageMeta* meta,
                                              volatile int* abort_flag, int warp, int lane) {
-    using C = Cfg<D>;
+    using C = Cfg<D, ST>;
     constexpr int S = C::kStages;
     constexpr int KS = C::kKSteps;
     const uint32_t full0 = base_s + L.bars, empty0 = full0 + 8 * S;
@@ -574,7 +589,7 @@ __device__ __forceinline__ void run_consumer(const SplitParams& p, uint32_t base
     const int pv_row = r0 + (lane & 7) + ((lane >> 4) << 3);
     const int pv_cpar = (lane >> 3) & 1;
     const int sw = lane & 7;  // == row & 7 for both
-    const int lbs = p.row_gather ? 6 : 31 - __clz(p.bs);  // smem block = 64 rows when gathered
+    const int lbs = p.row_gather ? C::kLogST : 31 - __clz(p.bs);  // gathered rows: one ST-row block
     const uint32_t hs = (uint32_t)(128 << lbs);  // bytes between 64-column slabs of a block
     const uint32_t qk_off = row_off<D>(qk_row, lbs);
     const uint32_t pv_off = row_off<D>(pv_row, lbs);
@@ -737,15 +752,15 @@ __device__ __forceinline__ void run_consumer(const SplitParams& p, uint32_t base
             const bool direct = writes_output(MODE) && (m.flags & kWholeUnit);
             const RowInfo ri = row_info<MQ>(p, m.b);
             const int SR = MQ ? p.rows_per_slot : G;  // rows per partial slot
-            for (int idx = ct; idx < NR * D; idx += kConsumerWarps * 32) {
+            for (int idx = ct; idx < NR * D; idx += C::kConsumerWarps * 32) {
                 const int h = idx / D, d = idx - h * D;  // h: q row of the unit
                 float M = kNegInf;
 #pragma unroll
-                for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, st_m[w * kMaxGroup + h]);
+                for (int w = 0; w < C::kConsumerWarps; ++w) M = fmaxf(M, st_m[w * kMaxGroup + h]);
                 float Ls = 0.f, Os = 0.f;
                 if (M != kNegInf) {
 #pragma unroll
-                    for (int w = 0; w < kConsumerWarps; ++w) {
+                    for (int w = 0; w < C::kConsumerWarps; ++w) {
                         const float f = ex2(st_m[w * kMaxGroup + h] - M);
                         Ls += st_l[w * kMaxGroup + h] * f;
                         Os += st_o[(size_t)(w * NR + h) * (D + 4) + d] * f;
@@ -780,15 +795,17 @@ __device__ __forceinline__ void run_consumer(const SplitParams& p, uint32_t base
 // many bytes in flight as one 4-stage ring, and a second set of consumer warps
 // hides the MMA/shuffle latency), which needs each 16K-register quarter of the
 // SM to hold 3 of the 10 warps: at most 168 registers per thread.  D = 256
-// runs one CTA per SM.
-template <int D, int MODE>
-__global__ void __maxnreg__(Cfg<D>::kMaxRegs) split_kernel(const __grid_constant__ SplitParams p) {
+// runs one CTA per SM; with 32-row stages (block sizes below 8) a CTA has two
+// consumer warps and one producer warp, and two CTAs share an SM.
+template <int D, int ST, int MODE>
+__global__ void __maxnreg__(split_max_regs(D)) split_kernel(const __grid_constant__ SplitParams p) {
+    using C = Cfg<D, ST>;
     extern __shared__ uint8_t smem_raw[];
     __shared__ int abort_flag;
     const uint32_t raw_s = smem_u32(smem_raw);
     const uint32_t base_s = (raw_s + 1023u) & ~1023u;
     uint8_t* base = smem_raw + (base_s - raw_s);
-    const SmemLayout L = smem_layout(D, Cfg<D>::kStages, p.G, p.B);
+    const SmemLayout L = smem_layout(D, ST, C::kStages, p.G, p.B);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     int32_t* pfx = reinterpret_cast<int32_t*>(base + L.pfx);
     int32_t* scan = reinterpret_cast<int32_t*>(base + L.scan);
@@ -799,24 +816,24 @@ __global__ void __maxnreg__(Cfg<D>::kMaxRegs) split_kernel(const __grid_constant
     // finishes, and read no global memory before it has completed.
     if (MODE != kGather) pdl_launch_dependents();
     if (tid == 0) {
-        for (int s = 0; s < Cfg<D>::kStages; ++s) {
+        for (int s = 0; s < C::kStages; ++s) {
             // full: the producer's arrive (+ one cp.async arrival per lane when
             // rows are copied with cp.async); empty: one arrival per consumer warp
             mbar_init(base_s + L.bars + 8 * s, p.row_gather == 2 ? 33 : 1);
-            mbar_init(base_s + L.bars + 8 * (Cfg<D>::kStages + s), kConsumerWarps);
+            mbar_init(base_s + L.bars + 8 * (C::kStages + s), C::kConsumerWarps);
         }
-        mbar_init(base_s + L.cbar, kConsumerWarps * 32);
+        mbar_init(base_s + L.cbar, C::kConsumerWarps * 32);
         fence_mbar_init();
         abort_flag = 0;
     }
-    if (tid == kConsumerWarps * 32) {
+    if (tid == C::kConsumerWarps * 32) {
         prefetch_tensormap(&p.tm_k);
         prefetch_tensormap(&p.tm_v);
     }
     pdl_wait_primary();
-    build_prefix<MODE == kMulti>(p, pfx, scan);  // ends with __syncthreads (also publishes the barriers)
+    build_prefix<MODE == kMulti, C::kThreads>(p, pfx, scan);  // ends with __syncthreads (also publishes the barriers)
     if (blockIdx.x == 0 && MODE != kGather)
-        for (int i = tid; i <= p.B; i += kThreads) p.pfx[i] = pfx[i];
+        for (int i = tid; i <= p.B; i += C::kThreads) p.pfx[i] = pfx[i];
     int64_t begin, end;
     {
         const GroupRange gr = group_of_cta(blockIdx.x, pfx, p.B, rows_per_seq<MODE == kMulti>(p), p.Hkv,
@@ -824,11 +841,11 @@ __global__ void __maxnreg__(Cfg<D>::kMaxRegs) split_kernel(const __grid_constant
         group_cta_range(gr, blockIdx.x, &begin, &end);
     }
 
-    if (warp == kConsumerWarps) {
-        run_producer<D, MODE>(p, base_s, L, pfx, meta, &abort_flag, begin, end, lane);
+    if (warp == C::kConsumerWarps) {
+        run_producer<D, ST, MODE>(p, base_s, L, pfx, meta, &abort_flag, begin, end, lane);
         return;
     }
-    run_consumer<D, MODE>(p, base_s, base, L, meta, &abort_flag, warp, lane);
+    run_consumer<D, ST, MODE>(p, base_s, base, L, meta, &abort_flag, warp, lane);
 }
 
 // Merge of split partial states: one CTA per (sequence, kv head) unit, one
@@ -940,6 +957,42 @@ __global__ void __launch_bounds__(kMaxGroup * 256 / 4) merge_kernel(const MergeP
             p.m_state[orow] = M;
             p.l_state[orow] = Ls;
         }
+    }
+}
+
+// Host side of one split-kernel shape: its entry points by mode and its
+// launch (programmatic stream serialization: the prologue may overlap the
+// previous kernel; the kernel waits with griddepcontrol.wait before reading
+// global memory).
+template <int D, int ST>
+const void* split_fn_of(int mode) {
+    switch (mode) {
+        case kOneShot: return reinterpret_cast<const void*>(&split_kernel<D, ST, kOneShot>);
+        case kTiled: return reinterpret_cast<const void*>(&split_kernel<D, ST, kTiled>);
+        case kGather: return reinterpret_cast<const void*>(&split_kernel<D, ST, kGather>);
+        case kMulti: return reinterpret_cast<const void*>(&split_kernel<D, ST, kMulti>);
+        default: return nullptr;
+    }
+}
+
+template <int D, int ST>
+cudaError_t launch_split_of(int mode, const SplitParams& p, int grid, size_t smem, cudaStream_t stream) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid, 1, 1);
+    cfg.blockDim = dim3(Cfg<D, ST>::kThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    switch (mode) {
+        case kOneShot: return cudaLaunchKernelEx(&cfg, split_kernel<D, ST, kOneShot>, p);
+        case kTiled: return cudaLaunchKernelEx(&cfg, split_kernel<D, ST, kTiled>, p);
+        case kGather: return cudaLaunchKernelEx(&cfg, split_kernel<D, ST, kGather>, p);
+        case kMulti: return cudaLaunchKernelEx(&cfg, split_kernel<D, ST, kMulti>, p);
+        default: return cudaErrorInvalidValue;
     }
 }
 

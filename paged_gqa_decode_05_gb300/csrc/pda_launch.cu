@@ -7,38 +7,38 @@
 namespace pda {
 
 #define PDA_DECLARE_D(D)                                                                     \
-    const void* split_kernel_fn_d##D(int mode);                                             \
-    int split_stages_d##D();                                                                 \
-    cudaError_t launch_split_d##D(int mode, const SplitParams& p, int grid, size_t smem,     \
-                                  cudaStream_t stream);
+    const void* split_kernel_fn_d##D(int st, int mode);                                     \
+    int split_stages_d##D(int st);                                                           \
+    cudaError_t launch_split_d##D(int st, int mode, const SplitParams& p, int grid,          \
+                                  size_t smem, cudaStream_t stream);
 PDA_DECLARE_D(64)
 PDA_DECLARE_D(128)
 PDA_DECLARE_D(256)
 
-int split_stages(int D) {
+int split_stages(int D, int st) {
     switch (D) {
-        case 64: return split_stages_d64();
-        case 128: return split_stages_d128();
-        case 256: return split_stages_d256();
+        case 64: return split_stages_d64(st);
+        case 128: return split_stages_d128(st);
+        case 256: return split_stages_d256(st);
         default: return 0;
     }
 }
 
-const void* split_kernel_fn(int D, int mode) {
+const void* split_kernel_fn(int D, int st, int mode) {
     switch (D) {
-        case 64: return split_kernel_fn_d64(mode);
-        case 128: return split_kernel_fn_d128(mode);
-        case 256: return split_kernel_fn_d256(mode);
+        case 64: return split_kernel_fn_d64(st, mode);
+        case 128: return split_kernel_fn_d128(st, mode);
+        case 256: return split_kernel_fn_d256(st, mode);
         default: return nullptr;
     }
 }
 
-cudaError_t launch_split(int D, int mode, const SplitParams& p, int grid, size_t smem,
+cudaError_t launch_split(int D, int st, int mode, const SplitParams& p, int grid, size_t smem,
                          cudaStream_t stream) {
     switch (D) {
-        case 64: return launch_split_d64(mode, p, grid, smem, stream);
-        case 128: return launch_split_d128(mode, p, grid, smem, stream);
-        case 256: return launch_split_d256(mode, p, grid, smem, stream);
+        case 64: return launch_split_d64(st, mode, p, grid, smem, stream);
+        case 128: return launch_split_d128(st, mode, p, grid, smem, stream);
+        case 256: return launch_split_d256(st, mode, p, grid, smem, stream);
         default: return cudaErrorInvalidValue;
     }
 }

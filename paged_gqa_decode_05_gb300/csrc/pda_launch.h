@@ -7,9 +7,10 @@
 namespace pda {
 
 // Entry points defined per head_dim (pda_kernels_d*.cu).
-int split_stages(int D);
-const void* split_kernel_fn(int D, int mode);
-cudaError_t launch_split(int D, int mode, const SplitParams& p, int grid, size_t smem,
+// st: stage rows of the split kernel's shape (stage_tokens(D, block_size)).
+int split_stages(int D, int st);
+const void* split_kernel_fn(int D, int st, int mode);
+cudaError_t launch_split(int D, int st, int mode, const SplitParams& p, int grid, size_t smem,
                          cudaStream_t stream);
 cudaError_t launch_merge(int mode, const MergeParams& p, bool pdl, cudaStream_t stream);
 cudaError_t launch_reset_state(float* m, float* l, float* o, int64_t n_q, int32_t D,

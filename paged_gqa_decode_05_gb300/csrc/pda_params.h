@@ -10,12 +10,21 @@
 
 namespace pda {
 
-constexpr int kConsumerWarps = 4;                        // compute warps per CTA
-constexpr int kThreads = (kConsumerWarps + 1) * 32;      // + one TMA producer warp
-constexpr int kStageTokens = 64;                         // KV rows per pipeline stage
-constexpr int kHalfBytes = kStageTokens * 128;           // 64 rows of one 64-column slab
+// Split-kernel shape: a pipeline stage holds ST KV rows, read by ST / 16
+// consumer warps of 16 rows; one more warp is the TMA producer.  ST = 64,
+// except for head_dim 256 with block sizes below 8: there the producer copies
+// rows (4 per gather4 copy, or 16-byte cp.async) and is bound by its
+// instruction rate, and with 64-row stages only one CTA (one producer) fits
+// on an SM; ST = 32 fits two.  (For head_dim 128, already two CTAs per SM,
+// 32-row stages were measured slower.)
+constexpr int kMaxConsumerWarps = 4;
 constexpr int kMaxLaunchBatch = 1024;                    // sequences per kernel launch
 constexpr int kMaxGroup = 8;                             // q heads per kv head (n8 MMA)
+
+PDA_HD int consumer_warps(int st) { return st / 16; }
+PDA_HD int split_threads(int st) { return (st / 16 + 1) * 32; }
+// Stage rows for a head size and block size.
+PDA_HD int stage_tokens(int D, int block_size) { return D == 256 && block_size < 8 ? 32 : 64; }
 
 // kOneShot: decode, output written; kTiled: fold a tile into the running
 // state; kGather: copy the staged rows out (loader check); kMulti: causal
@@ -91,20 +100,24 @@ struct SmemLayout {
     uint32_t bars, cbar, meta, scan, st_m, st_l, pfx, total;
 };
 
-PDA_HD uint32_t stage_bytes(int D) { return 2u * (uint32_t)(D / 64) * kHalfBytes + 16u * D; }
+// K and V tiles of ST rows plus the group's q rows (up to 8 x D bf16).
+PDA_HD uint32_t stage_bytes(int D, int st) {
+    return 2u * (uint32_t)(D / 64) * (uint32_t)st * 128u + 16u * D;
+}
 
 // Dynamic shared memory of the split kernel (the +1024 pays for aligning the
 // base to the 128-byte-swizzle atom).  The segment epilogue stages its o tiles
-// (4 warps x G x (D+4) floats <= 2 * 64 * D * 2 bytes) in the finished stage.
-PDA_HD SmemLayout smem_layout(int D, int stages, int G, int B) {
+// (ST/16 warps x 8 rows x (D+4) floats <= 2 * ST * D * 2 bytes) in the
+// finished stage.
+PDA_HD SmemLayout smem_layout(int D, int st, int stages, int G, int B) {
     SmemLayout L;
-    uint32_t off = (uint32_t)stages * stage_bytes(D);
+    uint32_t off = (uint32_t)stages * stage_bytes(D, st);
     L.bars = off;  off += 2u * stages * 8u;
     L.cbar = off;  off += 8u;
     L.meta = off;  off += (uint32_t)stages * (uint32_t)sizeof(StageMeta);
     L.scan = off;  off += 32u;  // one int per warp (block-prefix scan)
-    L.st_m = off;  off += kConsumerWarps * kMaxGroup * 4u;
-    L.st_l = off;  off += kConsumerWarps * kMaxGroup * 4u;
+    L.st_m = off;  off += kMaxConsumerWarps * kMaxGroup * 4u;
+    L.st_l = off;  off += kMaxConsumerWarps * kMaxGroup * 4u;
     L.pfx = off;   off += (uint32_t)(B + 1) * 4u;
     L.total = off + 1024u;
     return L;
