@@ -913,20 +913,24 @@ __global__ void __launch_bounds__(kMaxGroup * 256 / 4) merge_kernel(const MergeP
         Ls = p.l_state[orow];
         Os = *reinterpret_cast<const float4*>(p.o_state + orow * D + d4);
     }
+    // The slots to merge, in CTA order: with W >= Pg every CTA range is
+    // non-empty, so the CTAs cf..cl all hold part of the unit; with W < Pg a
+    // CTA holds at most one block, so the slots are the owners of the unit's
+    // nb blocks, taken in block order.
+    const bool every = gr.W >= gr.Pg;
+    const int64_t n_slots = every ? cl - cf + 1 : eu - su;
     constexpr int kBatch = 8;
-    for (int64_t c0 = cf; active && c0 <= cl; c0 += kBatch) {
+    for (int64_t i0 = 0; active && i0 < n_slots; i0 += kBatch) {
         float mi[kBatch], li[kBatch];
         float4 oi[kBatch];
 #pragma unroll
         for (int k = 0; k < kBatch; ++k) {
-            const int64_t c = c0 + k;
+            const int64_t i = i0 + k;
             mi[k] = kNegInf;
             li[k] = 0.f;
             oi[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (c > cl) continue;
-            int64_t cb, ce;
-            group_cta_range(gr, c, &cb, &ce);
-            if ((cb > su ? cb : su) >= (ce < eu ? ce : eu)) continue;  // no share of this unit
+            if (i >= n_slots) continue;
+            const int64_t c = every ? cf + i : gr.g * gr.Pg + cta_of_block(su + i - gr.F0, gr.W, gr.Pg);
             const int64_t slot = u + c;
             mi[k] = p.part_ml[(slot * SR + h) * 2];
             li[k] = p.part_ml[(slot * SR + h) * 2 + 1];

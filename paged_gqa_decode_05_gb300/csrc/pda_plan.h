@@ -21,12 +21,19 @@
 
 namespace pda {
 
+// floor(a / b) for a >= 0, b > 0.  Operands that fit in 32 bits take the
+// 32-bit division: a 64-bit division is a long instruction sequence on the GPU.
+PDA_HD int64_t div_floor(int64_t a, int64_t b) {
+    if (((uint64_t)a | (uint64_t)b) <= 0xffffffffull) return (int64_t)((uint32_t)a / (uint32_t)b);
+    return a / b;
+}
+
 // First flattened block of CTA c.
-PDA_HD int64_t cta_begin(int64_t c, int64_t W, int64_t P) { return c * W / P; }
+PDA_HD int64_t cta_begin(int64_t c, int64_t W, int64_t P) { return div_floor(c * W, P); }
 
 // The CTA whose range contains flattened block s (0 <= s < W): the largest c
 // with floor(c*W/P) <= s, i.e. floor(((s+1)*P - 1) / W).
-PDA_HD int64_t cta_of_block(int64_t s, int64_t W, int64_t P) { return ((s + 1) * P - 1) / W; }
+PDA_HD int64_t cta_of_block(int64_t s, int64_t W, int64_t P) { return div_floor((s + 1) * P - 1, W); }
 
 // Grouped split, for several causal queries per sequence: the launch's B
 // sequences form Q equal groups (group g = sequences [g*B/Q, (g+1)*B/Q), in
@@ -45,10 +52,10 @@ template <typename Pfx>
 PDA_HD GroupRange group_of_cta(int64_t c, const Pfx& pfx, int64_t B, int64_t Q, int64_t Hkv,
                                int64_t P) {
     GroupRange r;
-    r.Pg = P / Q;
-    r.g = c / r.Pg;
+    r.Pg = div_floor(P, Q);
+    r.g = div_floor(c, r.Pg);
     if (r.g >= Q) { r.F0 = 0; r.W = 0; return r; }
-    const int64_t Bg = B / Q;
+    const int64_t Bg = div_floor(B, Q);
     r.F0 = (int64_t)pfx[r.g * Bg] * Hkv;
     r.W = (int64_t)pfx[(r.g + 1) * Bg] * Hkv - r.F0;
     return r;
@@ -57,8 +64,8 @@ PDA_HD GroupRange group_of_cta(int64_t c, const Pfx& pfx, int64_t B, int64_t Q, 
 template <typename Pfx>
 PDA_HD GroupRange group_of_seq(int64_t s, const Pfx& pfx, int64_t B, int64_t Q, int64_t Hkv,
                                int64_t P) {
-    const int64_t Bg = B / Q;
-    return group_of_cta((s / Bg) * (P / Q), pfx, B, Q, Hkv, P);
+    const int64_t Bg = div_floor(B, Q);
+    return group_of_cta(div_floor(s, Bg) * div_floor(P, Q), pfx, B, Q, Hkv, P);
 }
 
 // Flattened range [begin, end) of CTA c within its group (empty when idle).

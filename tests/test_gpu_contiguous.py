@@ -10,7 +10,8 @@ from paged_gqa_decode_05_gb300 import workloads
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("D,bs,G", [(128, 16, 4), (64, 32, 8), (256, 8, 2), (128, 64, 1)])
+@pytest.mark.parametrize("D,bs,G", [(128, 16, 4), (64, 32, 8), (256, 8, 2), (128, 64, 1),
+                                    (256, 2, 4)])
 def test_contiguous_matches_oracle_and_identity_table(D, bs, G):
     import torch
     lens = [0, 1, bs + 3, 900, 4 * 64 + 1, 2048]

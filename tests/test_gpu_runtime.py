@@ -75,3 +75,17 @@ def test_two_contexts_on_two_streams():
     torch.cuda.synchronize()
     for o in outs:
         assert np.array_equal(o.float().cpu().numpy(), ref.float().cpu().numpy())
+
+
+@pytest.mark.parametrize("D,bs,rows,per_sm", [(128, 16, 64, 2), (64, 16, 64, 2), (256, 16, 64, 1),
+                                              (256, 64, 64, 1), (256, 4, 32, 2), (256, 1, 32, 2)])
+def test_split_kernel_shape(D, bs, rows, per_sm):
+    """Stage rows and CTAs per SM as designed: two CTAs per SM at head size
+    <= 128; at 256 one, or two with 32-row stages for block sizes below 8."""
+    import paged_gqa_decode_05_gb300 as pda
+    ctx = pda.Context(max_seqs=32, num_q_heads=32, num_kv_heads=8, head_dim=D, block_size=bs)
+    info = ctx.launch_info()
+    assert info["stage_tokens"] == rows
+    assert info["ctas_per_sm"] == per_sm
+    assert info["split_ctas"] == per_sm * info["num_sms"]
+    ctx.close()

@@ -49,7 +49,8 @@ def run_tiled(ctx, w, tiles, t, scale=None):
 
 
 @pytest.mark.parametrize("D,bs,G,cap", [(128, 16, 4, 8), (64, 32, 8, 3), (256, 16, 2, 16),
-                                        (128, 8, 1, 64), (128, 1, 4, 200), (64, 4, 8, 33)])
+                                        (128, 8, 1, 64), (128, 1, 4, 200), (64, 4, 8, 33),
+                                        (256, 4, 4, 40), (256, 1, 8, 100)])
 def test_tiled_matches_oneshot_and_oracle(D, bs, G, cap):
     import torch
     rng = np.random.default_rng(D + bs + G)
