@@ -15,7 +15,9 @@ Prints ONE JSON line (rank 0).  ``--impl reference`` times the CPU oracle
 
 Timing: CUDA events on the launching stream around exactly K back-to-back
 calls after W warm-up calls; inputs are larger than L2 and rotate between
-copies at distinct addresses.  A second pass records events between the two
+copies at distinct addresses.  The K calls are captured once in a CUDA graph
+and replayed (the host's per-call launch cost would otherwise bound the small
+workloads); the same calls launched one by one are timed too (``loop``).  A second pass records events between the two
 kernels of each call (which disables the merge kernel's early launch) to time
 the split kernel alone for the roofline.  ``e2e`` repeats the calls with the
 inputs copied from pinned host memory and the output copied back every step.
@@ -55,6 +57,9 @@ def parse_args():
     ap.add_argument("--layout", choices=["paged", "contiguous"], default="paged",
                     help="contiguous: the same cache copied to [B, S, Hkv, D] and decoded "
                          "with pda_decode_contiguous")
+    ap.add_argument("--no-graph", action="store_true",
+                    help="time the K calls launched one by one from Python instead of replaying "
+                         "them from a CUDA graph")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--quick", action="store_true",
@@ -335,16 +340,40 @@ def run_ours(args):
         step(i); i += 1
         if i % 64 == 0:
             torch.cuda.synchronize()
+    graph = None
+    if not args.no_graph:
+        # the K calls, with their input-set rotation, captured once
+        graph = torch.cuda.CUDAGraph()
+        cap = torch.cuda.Stream(device=dev)
+        cap.wait_stream(stream)
+        with torch.cuda.stream(cap):
+            with torch.cuda.graph(graph, stream=cap):
+                for k in range(args.steps):
+                    step(k)
+        stream.wait_stream(cap)
+        graph.replay()  # warm
+        torch.cuda.synchronize()
     barrier()
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
-    for k in range(args.steps):
-        step(k)
+    if graph is not None:
+        graph.replay()
+    else:
+        for k in range(args.steps):
+            step(k)
     e1.record(stream)
     torch.cuda.synchronize()
     barrier()
     ms_total = e0.elapsed_time(e1)
+    # the same calls launched one by one from Python (host launch cost included)
+    a_l, b_l = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a_l.record(stream)
+    for k in range(args.steps):
+        step(k)
+    b_l.record(stream)
+    torch.cuda.synchronize()
+    loop_us = a_l.elapsed_time(b_l) * 1e3 / args.steps
     pad_end = time.time() + pad_s
     while time.time() < pad_end:
         step(i); i += 1
@@ -412,10 +441,26 @@ def run_ours(args):
 
         for _ in range(5):
             warm_step()
+        torch.cuda.synchronize()
+        warm_graph = None
+        if not args.no_graph:
+            warm_graph = torch.cuda.CUDAGraph()
+            cap = torch.cuda.Stream(device=dev)
+            cap.wait_stream(stream)
+            with torch.cuda.stream(cap):
+                with torch.cuda.graph(warm_graph, stream=cap):
+                    for _ in range(args.steps):
+                        warm_step()
+            stream.wait_stream(cap)
+            warm_graph.replay()
+            torch.cuda.synchronize()
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(stream)
-        for _ in range(args.steps):
-            warm_step()
+        if warm_graph is not None:
+            warm_graph.replay()
+        else:
+            for _ in range(args.steps):
+                warm_step()
         b.record(stream)
         torch.cuda.synchronize()
         warm_us = a.elapsed_time(b) * 1e3 / args.steps
@@ -477,6 +522,7 @@ def run_ours(args):
         "warmup": args.warmup,
         "ms_per_step": ms_step,
         "us_per_call": ms_step * 1e3,
+        "loop_us_per_call": loop_us,
         "pct_of_hbm_peak": 100.0 * value / (world * peak),
         "higher_is_better": True,
         "scaling": "weak",
@@ -488,6 +534,8 @@ def run_ours(args):
                    "l2": f"inputs larger than L2 ({input_bytes / 1e6:.0f} MB per set, "
                          f"{n_sets} sets rotated, L2 {l2 / 2 ** 20:.0f} MiB)",
                    "parallelism": "replicas" if world > 1 else "single GPU",
+                   "launch": ("K calls replayed from one CUDA graph" if graph is not None
+                              else "K calls launched one by one"),
                    "split_ctas": info["split_ctas"], "ctas_per_sm": info["ctas_per_sm"],
                    "stages": info["stages"], "algorithmic_bytes_per_call": bytes_per_call},
         "roofline": {"bound": "hbm", "kernel": "split_kernel", "achieved": achieved, "peak": peak,
