@@ -165,19 +165,26 @@ __device__ __forceinline__ int32_t blocks_of(const SplitParams& p, int b, int32_
     return nb;
 }
 
-// Valid slots of sequence b's last block (1..bs).
+// The entry the valid-slot count of sequence b's last block comes from: its
+// length entry, or in tiled steps its last_valid entry (bs when none given).
+// Loaded apart from its use so that the load's latency overlaps other loads.
 template <bool MQ>
-__device__ __forceinline__ int32_t last_block_slots(const SplitParams& p, int b, int32_t nb) {
+__device__ __forceinline__ int32_t last_entry(const SplitParams& p, int b) {
+    if (p.lens_are_blocks) return p.last_valid ? p.last_valid[b] : p.bs;
+    return len_entry<MQ>(p, b);
+}
+
+// Valid slots of sequence b's last block (1..bs) from its last_entry e.
+template <bool MQ>
+__device__ __forceinline__ int32_t last_block_slots(const SplitParams& p, int b, int32_t nb, int32_t e) {
     if (p.lens_are_blocks) {
-        if (p.last_valid == nullptr) return p.bs;
-        int32_t v = p.last_valid[b];
-        if (v < 1 || v > p.bs) {
+        if (e < 1 || e > p.bs) {
             atomicOr(p.err, PDA_DEVERR_BAD_LENGTH_);
-            v = v < 1 ? 1 : p.bs;
+            e = e < 1 ? 1 : p.bs;
         }
-        return v;
+        return e;
     }
-    int32_t v = seq_tokens<MQ>(p, b) - (nb - 1) * p.bs;
+    const int32_t v = tokens_of<MQ>(p, b, e) - (nb - 1) * p.bs;
     return v > p.bs ? p.bs : v;
 }
 
@@ -236,8 +243,8 @@ __device__ __forceinline__ void run_producer(const SplitParams& p, uint32_t base
     // copies: w[0..3] hold the 128-entry window [win, win + 128) of the
     // current table row (lane i of w[k]: entry win + 32k + i), f[] the first
     // 128 entries of the current sequence's row (the next kv head starts
-    // there) and n[] those of the next non-empty sequence, loaded one unit
-    // ahead together with its last block's valid slots.
+    // there) and nx[] those of the next non-empty sequence, loaded one unit
+    // ahead together with the entry its last block's valid slots come from.
     using C = Cfg<D, ST>;
     constexpr int S = C::kStages;
     constexpr bool MQ = MODE == kMulti;
@@ -260,7 +267,8 @@ __device__ __forceinline__ void run_producer(const SplitParams& p, uint32_t base
     int32_t j = 0, nb = 0;
     int32_t win = 0;
     int32_t w[4], f[4], nx[4];
-    int32_t lv = bs, nlv = bs;  // valid slots of the last block: this / next sequence
+    int32_t lv = bs;   // valid slots of this sequence's last block
+    int32_t nle = 0;   // the next sequence's last_entry, loaded a unit ahead
     int bn = p.B;               // next non-empty sequence
 #pragma unroll
     for (int k = 0; k < 4; ++k) w[k] = f[k] = nx[k] = 0;
@@ -299,6 +307,10 @@ __device__ __forceinline__ void run_producer(const SplitParams& p, uint32_t base
         kvh = (int)(rem / nb);
         j = (int32_t)(rem % nb);
         win = j;
+        // every load first (one round trip), their uses after
+        bn = next_seq(b);
+        const int32_t e_cur = last_entry<MQ>(p, b);
+        nle = bn < p.B ? last_entry<MQ>(p, bn) : 0;
         load_ids(w, b, win, nb);
         if (win == 0) {
 #pragma unroll
@@ -306,13 +318,8 @@ __device__ __forceinline__ void run_producer(const SplitParams& p, uint32_t base
         } else {
             load_ids(f, b, 0, nb);
         }
-        lv = last_block_slots<MQ>(p, b, nb);
-        bn = next_seq(b);
-        if (bn < p.B) {
-            const int32_t nbn = pfx[bn + 1] - pfx[bn];
-            load_ids(nx, bn, 0, nbn);
-            nlv = last_block_slots<MQ>(p, bn, nbn);
-        }
+        if (bn < p.B) load_ids(nx, bn, 0, pfx[bn + 1] - pfx[bn]);
+        lv = last_block_slots<MQ>(p, b, nb, e_cur);
     }
     bool seg_begin = true;
     bool whole = false;
@@ -455,13 +462,12 @@ __device__ __forceinline__ void run_producer(const SplitParams& p, uint32_t base
                 nb = b < p.B ? pfx[b + 1] - pfx[b] : 0;
 #pragma unroll
                 for (int k = 0; k < 4; ++k) w[k] = f[k] = nx[k];
-                lv = nlv;
                 if (b < p.B && pos < end) {
+                    lv = last_block_slots<MQ>(p, b, nb, nle);
                     bn = next_seq(b);
                     if (bn < p.B) {
-                        const int32_t nbn = pfx[bn + 1] - pfx[bn];
-                        load_ids(nx, bn, 0, nbn);
-                        nlv = last_block_slots<MQ>(p, bn, nbn);
+                        nle = last_entry<MQ>(p, bn);
+                        load_ids(nx, bn, 0, pfx[bn + 1] - pfx[bn]);
                     }
                 }
             } else {  // next kv head of the same sequence: the same row again
@@ -887,7 +893,13 @@ __global__ void __launch_bounds__(kMaxGroup * 256 / 4) merge_kernel(const MergeP
     const int SR = MQ ? p.rows_per_slot : G;
     const int n4 = NR * D / 4;
     const int i4 = threadIdx.x;
-    const int32_t lo = p.pfx[b], nb = p.pfx[b + 1] - lo;
+    // Every prefix entry needed, loaded together (one round trip): the unit's
+    // sequence and the bounds of its row group (group_of_seq, written out).
+    const int64_t Bg = div_floor(p.B, Qr);
+    const int64_t grp = div_floor(b, Bg);
+    const int32_t lo = p.pfx[b], hi = p.pfx[b + 1];
+    const int32_t g_lo = p.pfx[grp * Bg], g_hi = p.pfx[(grp + 1) * Bg];
+    const int32_t nb = hi - lo;
     const bool active = i4 < n4;  // the block is rounded up to whole warps
     const int h = active ? (4 * i4) / D : 0;
     const int d4 = 4 * i4 - h * D;
@@ -901,7 +913,11 @@ __global__ void __launch_bounds__(kMaxGroup * 256 / 4) merge_kernel(const MergeP
         }
         return;
     }
-    const GroupRange gr = group_of_seq(b, p.pfx, p.B, Qr, p.Hkv, p.split_ctas);
+    GroupRange gr;
+    gr.Pg = div_floor(p.split_ctas, Qr);
+    gr.g = grp;
+    gr.F0 = (int64_t)g_lo * p.Hkv;
+    gr.W = (int64_t)g_hi * p.Hkv - gr.F0;
     const int64_t su = (int64_t)lo * p.Hkv + (int64_t)kvh * nb, eu = su + nb;
     const int64_t cf = gr.g * gr.Pg + cta_of_block(su - gr.F0, gr.W, gr.Pg);
     const int64_t cl = gr.g * gr.Pg + cta_of_block(eu - 1 - gr.F0, gr.W, gr.Pg);
