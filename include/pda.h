@@ -30,7 +30,10 @@
  *     set a flag read by pda_read_device_errors().
  *   - All state belongs to the pda_ctx.  Calls on one context must be
  *     ordered (one stream, or explicit events); use one context per
- *     concurrent stream.
+ *     concurrent stream.  A context also keeps the TMA descriptors of the
+ *     last KV pool it read (pointers, block count and strides); a call with
+ *     another pool re-encodes them, so neither calls nor host threads may
+ *     share a context concurrently.
  *   - Errors: every call returns a pda_status; pda_last_error() gives the
  *     message of the last failed call on the calling thread.
  */
@@ -79,8 +82,10 @@ enum {
  *                  64, 128 and 256.
  *   block_size     tokens per KV block: 1, 2, 4, 8, 16, 32 or 64 in this build
  *                  (from 8 up, one TMA copy per block and pool; below 8 the
- *                  rows are gathered with 16-byte copies).  block_size 1 is
- *                  the token-granular page of [CK] Attention Backend.
+ *                  rows are gathered, four per TMA gather4 copy when the pool
+ *                  strides are multiples of head_dim, else with 16-byte
+ *                  copies).  block_size 1 is the token-granular page of [CK]
+ *                  Attention Backend.
  *   tile_capacity  most block ids per sequence in one pda_step_tile call.
  */
 typedef struct pda_dims {

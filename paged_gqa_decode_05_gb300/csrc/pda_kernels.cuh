@@ -1,20 +1,21 @@
 // pda_kernels.cuh -- split-KV paged GQA decode kernels for sm_103a.
 //
 // Split kernel (one persistent CTA per resident slot; grid = SMs x CTAs/SM):
-//   * warp 4, lane 0 is the producer: it walks the CTA's share of the
+//   * the last warp is the producer: it walks the CTA's share of the
 //     flattened (sequence, kv head, block) space (pda_plan.h), looks every
 //     block up in the block table and copies whole K/V block rows of one kv
 //     head into a ring of shared-memory stages with one 5-D TMA tensor copy
-//     per block and pool (128-byte swizzle), plus the group's q rows with one
-//     bulk copy at the start of each segment.  Stage completion is tracked by mbarriers.
+//     per block and pool (128-byte swizzle; rows gathered for block sizes
+//     below 8), plus the group's q rows with one bulk copy at the start of
+//     each segment.  Stage completion is tracked by mbarriers.
 //   * ST/16 consumer warps read a stage of ST rows (64; 32 for head_dim 256
-//     with blocks of at most 32 tokens), 16 rows each.  The GQA group
+//     with block sizes below 8), 16 rows each.  The GQA group
 //     (G <= 8 q heads of one kv head) shares every K/V load: S^T = K q^T is a
 //     16x8 tile per warp (mma.sync m16n8k16, tokens as M, heads as N), the
 //     online-softmax update runs on the accumulator fragments (warp-shuffle
 //     max over tokens), P is transposed in registers (movmatrix) and
 //     O^T += V^T P^T accumulates over D in 16-row slabs.
-//   * at the end of a segment the four warp states are merged in shared
+//   * at the end of a segment the consumer warps' states are merged in shared
 //     memory; a segment that covers its whole unit writes bf16 o / l
 //     directly, others write an fp32 partial (m, l, o) state.
 // Merge kernel: combines the partial states of every unit split across CTAs
@@ -721,7 +722,7 @@ __device__ __forceinline__ void run_consumer(const SplitParams& p, uint32_t base
             }
         }
         if (MODE != kGather && (m.flags & kSegEnd)) {
-            // ---- merge the four warp states of this segment.  The o tiles are
+            // ---- merge the consumer warps' states of this segment.  The o tiles are
             // staged in this stage's own K/V memory (the stage is released only
             // after the merge), which keeps shared memory for deeper rings.
             float* st_m = reinterpret_cast<float*>(base + L.st_m);
@@ -797,10 +798,11 @@ __device__ __forceinline__ void run_consumer(const SplitParams& p, uint32_t base
 
 // ------------------------------------------------------------------ kernels
 
-// Register cap: for D <= 128 two CTAs share an SM (two 2-stage rings keep as
-// many bytes in flight as one 4-stage ring, and a second set of consumer warps
-// hides the MMA/shuffle latency), which needs each 16K-register quarter of the
-// SM to hold 3 of the 10 warps: at most 168 registers per thread.  D = 256
+// Register cap: for D <= 128 two CTAs share an SM (two 3-stage rings keep as
+// many bytes in flight as one 6-stage ring, and a second set of consumer warps
+// hides the MMA/shuffle latency; measured 4 % faster than one CTA with six
+// stages), which needs each 16K-register quarter of the SM to hold 3 of the
+// 10 warps: at most 168 registers per thread.  D = 256
 // runs one CTA per SM; with 32-row stages (block sizes below 8) a CTA has two
 // consumer warps and one producer warp, and two CTAs share an SM.
 template <int D, int ST, int MODE>
