@@ -101,11 +101,16 @@ KERNEL_SOURCES = ("pda_kernels.cuh", "pda_ptx.cuh", "pda_params.h", "pda_plan.h"
 
 
 def kernel_source_hash() -> str:
+    """Hash of the kernel sources with // comments, trailing blanks and empty
+    lines dropped, so that a change to comments alone keeps the record."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "paged_gqa_decode_05_gb300", "csrc")
     for name in KERNEL_SOURCES:
-        with open(os.path.join(csrc, name), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(csrc, name), encoding="utf-8") as f:
+            for line in f:
+                code = line.split("//", 1)[0].rstrip()
+                if code:
+                    h.update(code.encode() + b"\n")
     return h.hexdigest()[:16]
 
 
