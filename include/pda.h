@@ -252,6 +252,39 @@ pda_status pda_finalize(pda_ctx* ctx, pda_bf16* out, int32_t num_seqs, pda_strea
 pda_status pda_finalize_f32(pda_ctx* ctx, float* out, int32_t num_seqs, pda_stream stream);
 
 /*
+ * Partial states from several contexts -- context-parallel decode, where each
+ * context (one per GPU, say) folds a shard of every sequence's blocks with
+ * the tiled lifecycle.  [CK] Overview: split-KV partial states combined by a
+ * merge; [TA] module comment: the running state (m, l, o).
+ *
+ * pda_export_state copies the running state of sequences [0, num_seqs) into
+ * caller-owned DEVICE buffers m, l [num_seqs*Hq] and o [num_seqs*Hq*D] (fp32,
+ * 4-byte aligned), in natural-log units of the scaled scores:
+ *   m = max_t s_t,  l = sum_t exp(s_t - m),  o = sum_t exp(s_t - m) v_t,
+ * s_t = scale * q . K_t over the tokens folded so far ((-inf, 0, 0) when
+ * none).  num_seqs must be <= max_seqs.
+ *
+ * pda_merge_states combines n_parts (>= 1) such states per (sequence, q head)
+ * row, laid out part-major: m_parts, l_parts [n_parts][num_seqs*Hq] and
+ * o_parts [n_parts][num_seqs*Hq*D] (DEVICE; o_parts 16-byte aligned):
+ *   M = max_i m_i,  L = sum_i l_i exp(m_i - M),  O = sum_i o_i exp(m_i - M),
+ *   out[s, h, :] = bf16(O / L)   (0 when L == 0)
+ * into out [num_seqs, Hq, D] (16-byte aligned).  States whose token sets
+ * partition a sequence merge to the decode over all of them.
+ * pda_merge_states_f32 writes O / L in fp32.  Moving states between devices
+ * (an all-gather of Hq*(D+2)*4 bytes per sequence and part) is the caller's;
+ * the Python binding has one over torch.distributed (gather_states).
+ */
+pda_status pda_export_state(pda_ctx* ctx, int32_t num_seqs, float* m, float* l, float* o,
+                            pda_stream stream);
+pda_status pda_merge_states(pda_ctx* ctx, int32_t n_parts, int32_t num_seqs, const float* m_parts,
+                            const float* l_parts, const float* o_parts, pda_bf16* out,
+                            pda_stream stream);
+pda_status pda_merge_states_f32(pda_ctx* ctx, int32_t n_parts, int32_t num_seqs,
+                                const float* m_parts, const float* l_parts, const float* o_parts,
+                                float* out, pda_stream stream);
+
+/*
  * One-shot decode writing the fp32 quotient o / l instead of bf16 (same
  * arguments as pda_decode_strided; out is [batch, Hq, D] float).  Used to
  * compare the one-shot and tiled paths before output rounding.

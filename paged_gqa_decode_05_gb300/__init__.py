@@ -28,8 +28,8 @@ import os
 from typing import Optional, Sequence, Tuple
 
 __all__ = ["Context", "PdaError", "lib", "library_path", "check_dims", "paged_strides",
-           "slot_strides", "plan_units", "DEVERR_BAD_BLOCK_ID", "DEVERR_BAD_LENGTH",
-           "DEVERR_TIMEOUT"]
+           "slot_strides", "plan_units", "gather_states", "DEVERR_BAD_BLOCK_ID",
+           "DEVERR_BAD_LENGTH", "DEVERR_TIMEOUT"]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _LIBPATH = os.path.join(_HERE, "libpda.so")
@@ -94,6 +94,9 @@ def lib() -> ctypes.CDLL:
         "pda_step_tile": (I32, [P, P, P, P, I64, P, P, P, I32, I64, I64, I64, F, P]),
         "pda_finalize": (I32, [P, P, I32, P]),
         "pda_finalize_f32": (I32, [P, P, I32, P]),
+        "pda_export_state": (I32, [P, I32, P, P, P, P]),
+        "pda_merge_states": (I32, [P, I32, I32, P, P, P, P, P]),
+        "pda_merge_states_f32": (I32, [P, I32, I32, P, P, P, P, P]),
         "pda_debug_gather": (I32, [P, P, P, I64, I64, I64, I64, P, I32, P, I32, P, P, P]),
         "pda_read_device_errors": (I32, [P, ctypes.POINTER(ctypes.c_uint32), I32, P]),
         "pda_set_timing_events": (I32, [P, P, P, P]),
@@ -369,6 +372,42 @@ class Context:
         _check(fn(self._ctx, _ptr(out), int(num_seqs), _stream(stream)))
         return out
 
+    # -- partial states across contexts (context-parallel decode)
+    def export_state(self, num_seqs: int, stream=None):
+        """The running (m, l, o) of sequences [0, num_seqs) as fp32 tensors
+        [num_seqs, Hq], [num_seqs, Hq], [num_seqs, Hq, D]; m in natural-log units
+        of the scaled scores, l = sum exp(s - m), o = sum exp(s - m) v."""
+        torch = _torch()
+        d = self.dims
+        m = torch.empty((num_seqs, d.num_q_heads), device=self.device, dtype=torch.float32)
+        l = torch.empty_like(m)
+        o = torch.empty((num_seqs, d.num_q_heads, d.head_dim), device=self.device,
+                        dtype=torch.float32)
+        _check(lib().pda_export_state(self._ctx, int(num_seqs), _ptr(m), _ptr(l), _ptr(o),
+                                      _stream(stream)))
+        return m, l, o
+
+    def merge_states(self, m_parts, l_parts, o_parts, out=None, out_dtype=None, stream=None):
+        """o / l of P exported states per (sequence, q head): m_parts, l_parts
+        [P, S, Hq], o_parts [P, S, Hq, D] (fp32, CUDA) -> [S, Hq, D]."""
+        torch = _torch()
+        d = self.dims
+        P_, S = int(m_parts.shape[0]), int(m_parts.shape[1])
+        for t, name, shape in ((m_parts, "m_parts", (P_, S, d.num_q_heads)),
+                               (l_parts, "l_parts", (P_, S, d.num_q_heads)),
+                               (o_parts, "o_parts", (P_, S, d.num_q_heads, d.head_dim))):
+            if t.dtype != torch.float32 or not t.is_cuda or not t.is_contiguous() or \
+                    tuple(t.shape) != shape:
+                raise ValueError(f"{name} must be a contiguous float32 CUDA tensor of shape {shape}")
+        f32 = out_dtype == torch.float32
+        if out is None:
+            out = torch.empty((S, d.num_q_heads, d.head_dim), device=self.device,
+                              dtype=torch.float32 if f32 else torch.bfloat16)
+        fn = lib().pda_merge_states_f32 if f32 else lib().pda_merge_states
+        _check(fn(self._ctx, P_, S, _ptr(m_parts), _ptr(l_parts), _ptr(o_parts), _ptr(out),
+                  _stream(stream)))
+        return out
+
     # -- checks and hooks
     def debug_gather(self, k_pool, v_pool, block_table, seq_lens, strides=None, num_blocks=None,
                      stream=None):
@@ -405,6 +444,22 @@ class Context:
     def set_timing_events(self, ev_begin=None, ev_split=None, ev_end=None) -> None:
         h = [None if e is None else e.cuda_event for e in (ev_begin, ev_split, ev_end)]
         _check(lib().pda_set_timing_events(self._ctx, *h))
+
+
+def gather_states(m, l, o, group=None):
+    """All-gathers one exported state (m, l, o) per rank over a torch.distributed
+    process group into part-major stacks [world, ...] (rank order), ready for
+    Context.merge_states.  Tensors stay on their device (NCCL for CUDA tensors)."""
+    torch = _torch()
+    import torch.distributed as dist
+    world = dist.get_world_size(group)
+    out = []
+    for t in (m, l, o):
+        t = t.contiguous()
+        parts = [torch.empty_like(t) for _ in range(world)]
+        dist.all_gather(parts, t, group=group)
+        out.append(torch.stack(parts))
+    return tuple(out)
 
 
 def default_scale(head_dim: int) -> float:

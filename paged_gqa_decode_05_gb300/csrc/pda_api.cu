@@ -564,6 +564,57 @@ PDA_EXPORT pda_status pda_finalize_f32(pda_ctx* ctx, float* out, int32_t num_seq
     return finalize_impl(ctx, nullptr, out, num_seqs, stream);
 }
 
+PDA_EXPORT pda_status pda_export_state(pda_ctx* ctx, int32_t num_seqs, float* m, float* l, float* o,
+                                       pda_stream stream) {
+    if (!ctx) return fail(PDA_ERR_INVALID_ARG, "ctx is NULL");
+    if (num_seqs < 0 || num_seqs > ctx->dims.max_seqs)
+        return fail(PDA_ERR_INVALID_ARG, "num_seqs %d outside [0, max_seqs=%d]", num_seqs,
+                    ctx->dims.max_seqs);
+    if (num_seqs == 0) return PDA_OK;
+    if (!m || !l || !o || !aligned(m, 4) || !aligned(l, 4) || !aligned(o, 4))
+        return fail(PDA_ERR_INVALID_ARG, "m / l / o must be non-NULL and 4-byte aligned");
+    const cudaError_t e = pda::launch_export_state(ctx->m_state, ctx->l_state, ctx->o_state, m, l, o,
+                                                   (int64_t)num_seqs * ctx->dims.num_q_heads,
+                                                   ctx->dims.head_dim, (cudaStream_t)stream);
+    return e == cudaSuccess ? PDA_OK : cuda_fail(e, "state export launch");
+}
+
+namespace {
+
+pda_status merge_states_impl(pda_ctx* ctx, int32_t n_parts, int32_t num_seqs, const float* m_parts,
+                             const float* l_parts, const float* o_parts, pda_bf16* out, float* out_f32,
+                             pda_stream stream) {
+    if (!ctx) return fail(PDA_ERR_INVALID_ARG, "ctx is NULL");
+    if (n_parts < 1 || num_seqs < 0)
+        return fail(PDA_ERR_INVALID_ARG, "n_parts %d must be >= 1 and num_seqs %d >= 0", n_parts, num_seqs);
+    if (num_seqs == 0) return PDA_OK;
+    if (!m_parts || !l_parts || !o_parts || !aligned(m_parts, 4) || !aligned(l_parts, 4) ||
+        !aligned(o_parts, 16))
+        return fail(PDA_ERR_INVALID_ARG,
+                    "m_parts / l_parts must be 4-byte and o_parts 16-byte aligned, non-NULL");
+    if (out_f32 ? !aligned(out_f32, 16) : (!out || !aligned(out, 16)))
+        return fail(PDA_ERR_INVALID_ARG, "out must be non-NULL and 16-byte aligned");
+    const cudaError_t e = pda::launch_merge_states(
+        m_parts, l_parts, o_parts, n_parts, (int64_t)num_seqs * ctx->dims.num_q_heads, ctx->dims.head_dim,
+        out, out_f32, (cudaStream_t)stream);
+    return e == cudaSuccess ? PDA_OK : cuda_fail(e, "state merge launch");
+}
+
+}  // namespace
+
+PDA_EXPORT pda_status pda_merge_states(pda_ctx* ctx, int32_t n_parts, int32_t num_seqs,
+                                       const float* m_parts, const float* l_parts, const float* o_parts,
+                                       pda_bf16* out, pda_stream stream) {
+    return merge_states_impl(ctx, n_parts, num_seqs, m_parts, l_parts, o_parts, out, nullptr, stream);
+}
+
+PDA_EXPORT pda_status pda_merge_states_f32(pda_ctx* ctx, int32_t n_parts, int32_t num_seqs,
+                                           const float* m_parts, const float* l_parts,
+                                           const float* o_parts, float* out, pda_stream stream) {
+    if (!out && num_seqs > 0) return fail(PDA_ERR_INVALID_ARG, "out is NULL");
+    return merge_states_impl(ctx, n_parts, num_seqs, m_parts, l_parts, o_parts, nullptr, out, stream);
+}
+
 PDA_EXPORT pda_status pda_debug_gather(pda_ctx* ctx, const pda_bf16* k_pool, const pda_bf16* v_pool,
                                        int64_t num_blocks, int64_t blk_stride, int64_t tok_stride,
                                        int64_t kvh_stride, const int32_t* block_table,

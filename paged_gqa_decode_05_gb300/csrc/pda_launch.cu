@@ -101,4 +101,23 @@ cudaError_t launch_wait_timeout_probe(uint32_t* err, uint64_t limit_ns, cudaStre
     wait_timeout_probe_kernel<<<1, 32, 0, stream>>>(err, limit_ns);
     return cudaGetLastError();
 }
+cudaError_t launch_export_state(const float* m2, const float* l, const float* o, float* m_out,
+                                float* l_out, float* o_out, int64_t n_q, int32_t D, cudaStream_t stream) {
+    if (n_q <= 0) return cudaSuccess;
+    const int64_t n = n_q * D;
+    const int grid = (int)((n + 255) / 256 < 4096 ? (n + 255) / 256 : 4096);
+    export_state_kernel<<<grid, 256, 0, stream>>>(m2, l, o, m_out, l_out, o_out, n_q, D);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_merge_states(const float* m_parts, const float* l_parts, const float* o_parts,
+                                int32_t n_parts, int64_t n_q, int32_t D, uint16_t* out, float* out_f32,
+                                cudaStream_t stream) {
+    if (n_q <= 0) return cudaSuccess;
+    const int64_t n4 = n_q * D / 4;
+    const int grid = (int)((n4 + 255) / 256 < 4096 ? (n4 + 255) / 256 : 4096);
+    merge_states_kernel<<<grid, 256, 0, stream>>>(m_parts, l_parts, o_parts, n_parts, n_q, D, out, out_f32);
+    return cudaGetLastError();
+}
+
 }  // namespace pda

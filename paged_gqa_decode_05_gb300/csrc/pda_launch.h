@@ -18,5 +18,10 @@ cudaError_t launch_reset_state(float* m, float* l, float* o, int64_t n_q, int32_
 cudaError_t launch_wait_timeout_probe(uint32_t* err, uint64_t limit_ns, cudaStream_t stream);
 cudaError_t launch_finalize(const float* l, const float* o, uint16_t* out, float* out_f32,
                             int64_t n_q, int32_t D, cudaStream_t stream);
+cudaError_t launch_export_state(const float* m2, const float* l, const float* o, float* m_out,
+                                float* l_out, float* o_out, int64_t n_q, int32_t D, cudaStream_t stream);
+cudaError_t launch_merge_states(const float* m_parts, const float* l_parts, const float* o_parts,
+                                int32_t n_parts, int64_t n_q, int32_t D, uint16_t* out, float* out_f32,
+                                cudaStream_t stream);
 
 }  // namespace pda
