@@ -1,7 +1,6 @@
 // Merge, state-reset and finalize kernels, and the head_dim dispatch of the
 // split kernel.
-#define PDA_DEFINE_AUX_KERNELS
-#include "pda_kernels.cuh"
+#include "pda_aux.cuh"
 #include "pda_launch.h"
 
 namespace pda {
