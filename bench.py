@@ -54,6 +54,9 @@ def parse_args():
                     help="redraw the workload with this block size (e.g. 1 for token pages)")
     ap.add_argument("--q-len", type=int, default=1,
                     help="causal queries per sequence (pda_decode_multi) instead of one")
+    ap.add_argument("--tiles", type=int, default=0,
+                    help="decode with the tiled lifecycle instead: begin_step, this many "
+                         "step_tile calls (each 1/T of every sequence's blocks), finalize")
     ap.add_argument("--layout", choices=["paged", "contiguous"], default="paged",
                     help="contiguous: the same cache copied to [B, S, Hkv, D] and decoded "
                          "with pda_decode_contiguous")
@@ -306,9 +309,41 @@ def run_ours(args):
     sets = [{k: to_dev(v) for k, v in host.items()} for _ in range(n_sets)]
     outs = [torch.empty(tuple(sets[0]["q"].shape), device=dev, dtype=torch.bfloat16)
             for _ in range(n_sets)]
+    tiles = []
+    tile_cap = 64
+    if args.tiles > 0:
+        # tile i holds blocks [i*cap, (i+1)*cap) of every sequence (fewer at the end)
+        nbs = -(-w.seq_lens.astype(np.int64) // w.block_size)
+        tile_cap = max(1, int(-(-int(nbs.max()) // args.tiles)))
+        for i in range(args.tiles):
+            blocks = np.zeros((w.B, tile_cap), dtype=np.int32)
+            counts = np.zeros(w.B, dtype=np.int32)
+            last = np.full(w.B, w.block_size, dtype=np.int32)
+            for b in range(w.B):
+                lo, hi = min(i * tile_cap, int(nbs[b])), min((i + 1) * tile_cap, int(nbs[b]))
+                blocks[b, :hi - lo] = w.block_table[b, lo:hi]
+                counts[b] = hi - lo
+                if hi == nbs[b] and hi > lo:
+                    last[b] = int(w.seq_lens[b]) - (hi - 1) * w.block_size
+            tiles.append((to_dev(blocks), to_dev(counts), to_dev(last)))
     ctx = pda.Context(max_seqs=w.B * args.q_len, num_q_heads=w.Hq, num_kv_heads=w.Hkv,
-                      head_dim=w.D, block_size=w.block_size)
+                      head_dim=w.D, block_size=w.block_size, tile_capacity=tile_cap)
     stream = torch.cuda.current_stream()
+
+    def call(s, out):
+        """One decode of input set s into out through the public API."""
+        if args.tiles > 0:
+            ctx.begin_step(w.B)
+            for blocks, counts, last in tiles:
+                ctx.step_tile(s["q"], s["k_pool"], s["v_pool"], blocks, counts, last)
+            ctx.finalize(w.B, out=out)
+        elif args.q_len > 1:
+            ctx.decode_multi(s["q"], s["k_pool"], s["v_pool"], s["block_table"], s["seq_lens"],
+                             out=out)
+        elif args.layout == "contiguous":
+            ctx.decode_contiguous(s["q"], s["k_pool"], s["v_pool"], s["seq_lens"], out=out)
+        else:
+            ctx.decode(s["q"], s["k_pool"], s["v_pool"], s["block_table"], s["seq_lens"], out=out)
 
     counter = [0]
 
@@ -316,16 +351,7 @@ def run_ours(args):
         # consecutive calls always read a different input set (L2 is never warm)
         i = counter[0]
         counter[0] += 1
-        s = sets[i % n_sets]
-        if args.q_len > 1:
-            ctx.decode_multi(s["q"], s["k_pool"], s["v_pool"], s["block_table"], s["seq_lens"],
-                             out=outs[i % n_sets])
-        elif args.layout == "contiguous":
-            ctx.decode_contiguous(s["q"], s["k_pool"], s["v_pool"], s["seq_lens"],
-                                  out=outs[i % n_sets])
-        else:
-            ctx.decode(s["q"], s["k_pool"], s["v_pool"], s["block_table"], s["seq_lens"],
-                       out=outs[i % n_sets])
+        call(sets[i % n_sets], outs[i % n_sets])
 
     for i in range(max(3, args.warmup)):
         step(i)
@@ -393,7 +419,8 @@ def run_ours(args):
     ms_step = max_over_ranks(ms_total / args.steps, dev)
 
     # --- kernel timing pass: events between the split and merge kernels
-    n_timed = 0 if args.quick else args.steps
+    # (one-shot calls only; a tiled step is timed as a whole)
+    n_timed = 0 if (args.quick or args.tiles > 0) else args.steps
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
             torch.cuda.Event(enable_timing=True)) for _ in range(n_timed)]
     for k in range(n_timed):
@@ -435,14 +462,7 @@ def run_ours(args):
         s0, o0 = sets[0], outs[0]
 
         def warm_step():
-            if args.q_len > 1:
-                ctx.decode_multi(s0["q"], s0["k_pool"], s0["v_pool"], s0["block_table"],
-                                 s0["seq_lens"], out=o0)
-            elif args.layout == "contiguous":
-                ctx.decode_contiguous(s0["q"], s0["k_pool"], s0["v_pool"], s0["seq_lens"], out=o0)
-            else:
-                ctx.decode(s0["q"], s0["k_pool"], s0["v_pool"], s0["block_table"], s0["seq_lens"],
-                           out=o0)
+            call(s0, o0)
 
         for _ in range(5):
             warm_step()
@@ -487,15 +507,7 @@ def run_ours(args):
             for k, t in pinned.items():
                 d = dst[k].view(torch.int16) if dst[k].dtype == torch.bfloat16 else dst[k]
                 d.copy_(t, non_blocking=True)
-            if args.q_len > 1:
-                ctx.decode_multi(dst["q"], dst["k_pool"], dst["v_pool"], dst["block_table"],
-                                 dst["seq_lens"], out=outs[0])
-            elif args.layout == "contiguous":
-                ctx.decode_contiguous(dst["q"], dst["k_pool"], dst["v_pool"], dst["seq_lens"],
-                                      out=outs[0])
-            else:
-                ctx.decode(dst["q"], dst["k_pool"], dst["v_pool"], dst["block_table"],
-                           dst["seq_lens"], out=outs[0])
+            call(dst, outs[0])
             out_host.copy_(outs[0], non_blocking=True)
 
         for _ in range(2):
@@ -516,7 +528,11 @@ def run_ours(args):
 
     peak, peak_kind = peaks()
     value = world * bytes_per_call / (ms_step * 1e-3) / 1e9
-    achieved = bytes_per_call / (split_avg * 1e-3) / 1e9
+    if args.tiles > 0 or args.quick:  # no split-kernel events: the whole call
+        split_avg = merge_avg = float("nan")
+        achieved = bytes_per_call / (ms_step * 1e-3) / 1e9
+    else:
+        achieved = bytes_per_call / (split_avg * 1e-3) / 1e9
     info = ctx.launch_info()
     line = {
         "metric": METRIC,
@@ -535,7 +551,7 @@ def run_ours(args):
         "dtype": "bf16",
         "data": "synthetic: seeded N(0,1) q/K/V rounded to bf16, shuffled block table",
         "config": {**w.describe(), "workload": w.name, "kv_layout": args.layout,
-                   "q_len": args.q_len,
+                   "q_len": args.q_len, "tiles": args.tiles,
                    "l2": f"inputs larger than L2 ({input_bytes / 1e6:.0f} MB per set, "
                          f"{n_sets} sets rotated, L2 {l2 / 2 ** 20:.0f} MiB)",
                    "parallelism": "replicas" if world > 1 else "single GPU",
@@ -543,15 +559,19 @@ def run_ours(args):
                               else "K calls launched one by one"),
                    "split_ctas": info["split_ctas"], "ctas_per_sm": info["ctas_per_sm"],
                    "stages": info["stages"], "algorithmic_bytes_per_call": bytes_per_call},
-        "roofline": {"bound": "hbm", "kernel": "split_kernel", "achieved": achieved, "peak": peak,
+        "roofline": {"bound": "hbm",
+                     "kernel": ("split_kernel" if not (args.tiles > 0 or args.quick)
+                                else "whole call (split kernel not timed apart)"),
+                     "achieved": achieved, "peak": peak,
                      "peak_kind": f"{peak_kind} hbm_gbs (STREAM-style copy)", "unit": "GB/s",
                      "frac": achieved / peak,
                      # the ncu record holds the default configuration of each workload
                      "traffic": (recorded_traffic(args.workload)
                                  if (args.block_size == 0 and args.layout == "paged"
-                                     and args.q_len == 1) else None),
-                     "split_us": split_avg * 1e3, "merge_us": merge_avg * 1e3},
-        "gpu_launches": 2 * args.steps,
+                                     and args.q_len == 1 and args.tiles == 0) else None),
+                     "split_us": None if math.isnan(split_avg) else split_avg * 1e3,
+                     "merge_us": None if math.isnan(merge_avg) else merge_avg * 1e3},
+        "gpu_launches": (2 + 2 * args.tiles if args.tiles > 0 else 2) * args.steps,
         "clocks": clocks,
     }
     if per_call is not None:
