@@ -4,7 +4,7 @@ import numpy as np
 import pytest
 
 import oracle
-from gpu_util import assert_close_to_oracle, context_for, dev, host_f64, upload
+from gpu_util import context_for, dev, host_f64, upload
 from paged_gqa_decode_05_gb300 import workloads
 from paged_gqa_decode_05_gb300.workloads import bf16_bits, bf16_to_f32, make_workload
 
@@ -56,12 +56,11 @@ def test_block_permutation_bit_identical():
     k2[perm] = w.k_pool; v2[perm] = w.v_pool
     w.k_pool, w.v_pool, w.block_table = k2, v2, perm[w.block_table].astype(np.int32)
     again = _decode(ctx, w)
-    assert np.array_equal(base.view(dtype=base.dtype).cpu().float().numpy(),
-                          again.cpu().float().numpy())
+    assert np.array_equal(base.cpu().float().numpy(), again.cpu().float().numpy())
 
 
 def test_deterministic():
-    w = workloads.ragged() if False else _w(seed=5, lens=(4096, 333, 17, 2049))
+    w = _w(seed=5, lens=(4096, 333, 17, 2049))
     ctx = context_for(w)
     a = _decode(ctx, w).clone()
     b = _decode(ctx, w)

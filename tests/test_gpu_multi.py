@@ -17,7 +17,7 @@ def _ctx(w, q_len):
 
 @pytest.mark.parametrize("D,bs,G,q_len", [(128, 16, 4, 4), (64, 32, 8, 2), (256, 8, 2, 7),
                                           (128, 1, 4, 3), (128, 16, 1, 16), (256, 4, 2, 5),
-                                          (256, 2, 8, 3)])
+                                          (256, 2, 8, 3), (64, 16, 2, 9), (128, 32, 8, 5)])
 def test_multi_matches_oracle(D, bs, G, q_len):
     import torch
     lens = [q_len, 1, q_len + bs, 900, 2 * 64 + 5, 3000]
