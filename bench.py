@@ -8,19 +8,24 @@ batch (split kernel + merge kernel).  Default workload: the 8B-style batch
 (B=32, Hq=32, Hkv=8, D=128, block 16, 4096 tokens each; 537 MB moved per call).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--workload 8b|1b|wide|ragged|tiny]
+                  [--workload 8b|1b|wide|ragged|tiny] [--block-size BS]
+                  [--q-len Q] [--layout paged|contiguous] [--tiles T]
+                  [--no-graph] [--no-e2e] [--no-cpu-baseline] [--quick]
 
 Prints ONE JSON line (rank 0).  ``--impl reference`` times the CPU oracle
 (the fp64 definition) on this host's cores instead of the GPU path.
+``--q-len`` decodes Q causal queries per sequence, ``--layout contiguous``
+the same cache as [B, S, Hkv, D], ``--tiles`` through the tiled lifecycle.
 
 Timing: CUDA events on the launching stream around exactly K back-to-back
 calls after W warm-up calls; inputs are larger than L2 and rotate between
 copies at distinct addresses.  The K calls are captured once in a CUDA graph
 and replayed (the host's per-call launch cost would otherwise bound the small
-workloads); the same calls launched one by one are timed too (``loop``).  A second pass records events between the two
-kernels of each call (which disables the merge kernel's early launch) to time
-the split kernel alone for the roofline.  ``e2e`` repeats the calls with the
-inputs copied from pinned host memory and the output copied back every step.
+workloads); the same calls launched one by one are timed too (``loop``).  A
+second pass records events between the two kernels of each call (which
+disables the merge kernel's early launch) to time the split kernel alone for
+the roofline.  ``e2e`` repeats the calls with the inputs copied from pinned
+host memory and the output copied back every step.
 """
 from __future__ import annotations
 
