@@ -666,8 +666,10 @@ __device__ __forceinline__ void run_consumer(const SplitParams& p, uint32_t base
                 float s1 = ((acc[0][1] + acc[1][1]) + (acc[2][1] + acc[3][1])) * sl2;
                 float s2 = ((acc[0][2] + acc[1][2]) + (acc[2][2] + acc[3][2])) * sl2;
                 float s3 = ((acc[0][3] + acc[1][3]) + (acc[2][3] + acc[3][3])) * sl2;
-                if (r0 + g >= m.n_valid) { s0 = kNegInf; s1 = kNegInf; }
-                if (r0 + g + 8 >= m.n_valid) { s2 = kNegInf; s3 = kNegInf; }
+                if (m.n_valid < C::kST) {  // a stage that ends mid-way: mask the rows past it
+                    if (r0 + g >= m.n_valid) { s0 = kNegInf; s1 = kNegInf; }
+                    if (r0 + g + 8 >= m.n_valid) { s2 = kNegInf; s3 = kNegInf; }
+                }
                 if constexpr (MQ) {  // column n = query n / G may not see the later tokens
                     const int pos = m.j0 * p.bs + r0 + g;
                     const int lim0 = m.lim + (2 * t) / G, lim1 = m.lim + (2 * t + 1) / G;
@@ -696,9 +698,10 @@ __device__ __forceinline__ void run_consumer(const SplitParams& p, uint32_t base
                 const uint32_t px = pack_bf16x2(p0, p1), py = pack_bf16x2(p2, p3);
                 const uint32_t qx = pack_bf16x2(p0 - bf16_lo(px), p1 - bf16_hi(px));
                 const uint32_t qy = pack_bf16x2(p2 - bf16_lo(py), p3 - bf16_hi(py));
-                // l sums exactly the weights that multiply V
-                l0 = l0 * a0 + ((bf16_lo(px) + bf16_lo(qx)) + (bf16_lo(py) + bf16_lo(qy)));
-                l1 = l1 * a1 + ((bf16_hi(px) + bf16_hi(qx)) + (bf16_hi(py) + bf16_hi(qy)));
+                // l sums the fp32 weights; the ones that multiply V (hi + lo)
+                // equal them to about 2^-17 relative
+                l0 = l0 * a0 + (p0 + p2);
+                l1 = l1 * a1 + (p1 + p3);
                 m0 = n0;
                 m1 = n1;
                 if (!__all_sync(0xffffffffu, a0 == 1.f && a1 == 1.f)) {
