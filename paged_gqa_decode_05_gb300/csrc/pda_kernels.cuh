@@ -651,21 +651,23 @@ __device__ __forceinline__ void run_consumer(const SplitParams& p, uint32_t base
                     zero_rows<D>(sV, m.n_valid, r0 + 16, lbs, lane);
                     __syncwarp();
                 }
-                // S^T (16 tokens x 8 heads) = K q^T in four independent chains
-                float acc[4][4];
+                // S^T (16 tokens x 8 heads) = K q^T in two independent chains
+                // (more chains shorten the MMA dependency but cost adds to combine;
+                // fewer instructions measured faster)
+                float acc[2][4];
 #pragma unroll
-                for (int ch = 0; ch < 4; ++ch) acc[ch][0] = acc[ch][1] = acc[ch][2] = acc[ch][3] = 0.f;
+                for (int ch = 0; ch < 2; ++ch) acc[ch][0] = acc[ch][1] = acc[ch][2] = acc[ch][3] = 0.f;
 #pragma unroll
                 for (int kk = 0; kk < KS; ++kk) {
                     uint32_t a[4];
                     const int cc = (((kk & 3) << 1) + qk_cpar) ^ sw;
                     ldsm_x4(sK + qk_off + (uint32_t)(kk >> 2) * hs + (cc << 4), a);
-                    mma_16816(acc[kk & 3], a, qf[kk][0], qf[kk][1]);
+                    mma_16816(acc[kk & 1], a, qf[kk][0], qf[kk][1]);
                 }
-                float s0 = ((acc[0][0] + acc[1][0]) + (acc[2][0] + acc[3][0])) * sl2;
-                float s1 = ((acc[0][1] + acc[1][1]) + (acc[2][1] + acc[3][1])) * sl2;
-                float s2 = ((acc[0][2] + acc[1][2]) + (acc[2][2] + acc[3][2])) * sl2;
-                float s3 = ((acc[0][3] + acc[1][3]) + (acc[2][3] + acc[3][3])) * sl2;
+                float s0 = (acc[0][0] + acc[1][0]) * sl2;
+                float s1 = (acc[0][1] + acc[1][1]) * sl2;
+                float s2 = (acc[0][2] + acc[1][2]) * sl2;
+                float s3 = (acc[0][3] + acc[1][3]) * sl2;
                 if (m.n_valid < C::kST) {  // a stage that ends mid-way: mask the rows past it
                     if (r0 + g >= m.n_valid) { s0 = kNegInf; s1 = kNegInf; }
                     if (r0 + g + 8 >= m.n_valid) { s2 = kNegInf; s3 = kNegInf; }
