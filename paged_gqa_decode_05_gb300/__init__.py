@@ -296,6 +296,30 @@ class Context:
                                         _stream(stream)))
         return out
 
+    def bind_decode(self, q, k_pool, v_pool, block_table, seq_lens, out,
+                    scale: Optional[float] = None, strides: Optional[Sequence[int]] = None,
+                    num_blocks: Optional[int] = None, stream=None):
+        """Validates one decode's tensors once and returns a zero-argument callable
+        that reruns it (the same buffers, their contents free to change between
+        calls) with only the C call: for decode loops over persistent buffers
+        that do not use CUDA graphs.  The callable keeps the tensors and this
+        context alive, launches on the stream current at binding (or `stream`),
+        and raises once the context is closed."""
+        d = self.dims
+        B = int(seq_lens.shape[0])
+        self._bf16(q, "q", (B, d.num_q_heads, d.head_dim))
+        self._i32(block_table, "block_table", 2)
+        self._i32(seq_lens, "seq_lens", 1)
+        if block_table.shape[0] != B:
+            raise ValueError("block_table must have one row per sequence")
+        self._bf16(out, "out", (B, d.num_q_heads, d.head_dim))
+        (bs_, ts_, hs_), nblk = self._pool(k_pool, v_pool, strides, num_blocks)
+        args = (_ptr(q), _ptr(k_pool), _ptr(v_pool), nblk, bs_, ts_, hs_, _ptr(block_table),
+                int(block_table.shape[1]), _ptr(seq_lens), B, self._scale(scale), _ptr(out),
+                _stream(stream))
+        return _Bound(self, lib().pda_decode_strided, args,
+                      (q, k_pool, v_pool, block_table, seq_lens, out))
+
     def decode_multi(self, q, k_pool, v_pool, block_table, seq_lens, scale: Optional[float] = None,
                      out=None, stream=None):
         """Causal multi-query decode: q [B, q_len, Hq, D] are each sequence's last q_len
@@ -444,6 +468,21 @@ class Context:
     def set_timing_events(self, ev_begin=None, ev_split=None, ev_end=None) -> None:
         h = [None if e is None else e.cuda_event for e in (ev_begin, ev_split, ev_end)]
         _check(lib().pda_set_timing_events(self._ctx, *h))
+
+
+class _Bound:
+    """A decode with its arguments marshalled once (Context.bind_decode)."""
+
+    __slots__ = ("_owner", "_fn", "_args", "_keep")
+
+    def __init__(self, owner, fn, args, keep):
+        self._owner, self._fn, self._args, self._keep = owner, fn, args, keep
+
+    def __call__(self) -> None:
+        ctx = self._owner._ctx
+        if not ctx:
+            raise PdaError(ERR_INVALID_ARG, "the context of this bound decode is closed")
+        _check(self._fn(ctx, *self._args))
 
 
 def gather_states(m, l, o, group=None):

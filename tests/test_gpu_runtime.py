@@ -89,3 +89,27 @@ def test_split_kernel_shape(D, bs, rows, per_sm):
     assert info["ctas_per_sm"] == per_sm
     assert info["split_ctas"] == per_sm * info["num_sms"]
     ctx.close()
+
+
+def test_bound_decode_matches_decode_and_tracks_contents():
+    """A decode bound once reruns on the same buffers: it follows their current
+    contents, matches decode bit for bit, and refuses to run after close."""
+    import torch
+    import paged_gqa_decode_05_gb300 as pda
+    w = _w()
+    ctx = context_for(w)
+    t = upload(w)
+    out = torch.empty((w.B, w.Hq, w.D), device="cuda", dtype=torch.bfloat16)
+    run = ctx.bind_decode(t["q"], t["k_pool"], t["v_pool"], t["block_table"], t["seq_lens"], out)
+    run()
+    ref = ctx.decode(t["q"], t["k_pool"], t["v_pool"], t["block_table"], t["seq_lens"])
+    torch.cuda.synchronize()
+    assert torch.equal(out, ref)
+    t["q"].mul_(-1.0)  # new contents, same buffer
+    run()
+    ref2 = ctx.decode(t["q"], t["k_pool"], t["v_pool"], t["block_table"], t["seq_lens"])
+    torch.cuda.synchronize()
+    assert torch.equal(out, ref2) and not torch.equal(ref, ref2)
+    ctx.close()
+    with pytest.raises(pda.PdaError):
+        run()
