@@ -113,13 +113,6 @@ __device__ __forceinline__ int64_t qo_offset(const SplitParams& p, int b, int qi
     return (((int64_t)b * ql + qi) * p.Hq + h) * D;
 }
 
-template <bool MQ>
-__device__ __forceinline__ int32_t table_entry(const SplitParams& p, int s, int idx) {
-    const int row = row_info<MQ>(p, s).b;
-    if (p.table == nullptr) return row * p.table_stride + idx;
-    return p.table[(int64_t)row * p.table_stride + idx];
-}
-
 // The length entry of launch sequence s (tokens; blocks in tiled steps).
 template <bool MQ>
 __device__ __forceinline__ int32_t len_entry(const SplitParams& p, int s) {
@@ -271,14 +264,23 @@ __device__ __forceinline__ void run_producer(const SplitParams& p, uint32_t base
     int32_t lv = bs;   // valid slots of this sequence's last block
     int32_t nle = 0;   // the next sequence's last_entry, loaded a unit ahead
     int bn = p.B;               // next non-empty sequence
+    // The launch rows of b and bn (multi-query: table row, first query, query
+    // count) and b's causal limit, computed once per sequence, not per stage.
+    RowInfo ri = row_info<MQ>(p, 0), rn = ri;
+    int32_t lim = 0x7fffffff;
 #pragma unroll
     for (int k = 0; k < 4; ++k) w[k] = f[k] = nx[k] = 0;
-    // entries [from, from + 128) of sequence s's row (nbs blocks), lane-strided
-    auto load_ids = [&](int32_t* dst, int s, int32_t from, int32_t nbs) {
+    // entry idx of table row `row` (contiguous cache: block row * stride + idx)
+    auto table_at = [&](int row, int32_t idx) -> int32_t {
+        if (p.table == nullptr) return row * p.table_stride + idx;
+        return p.table[(int64_t)row * p.table_stride + idx];
+    };
+    // entries [from, from + 128) of table row `row` (nbs blocks), lane-strided
+    auto load_ids = [&](int32_t* dst, int row, int32_t from, int32_t nbs) {
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
             const int32_t e = from + 32 * k + lane;
-            dst[k] = e < nbs ? table_entry<MQ>(p, s, e) : 0;
+            dst[k] = e < nbs ? table_at(row, e) : 0;
         }
     };
     auto next_seq = [&](int s) {
@@ -310,17 +312,20 @@ __device__ __forceinline__ void run_producer(const SplitParams& p, uint32_t base
         win = j;
         // every load first (one round trip), their uses after
         bn = next_seq(b);
+        ri = row_info<MQ>(p, b);
+        rn = bn < p.B ? row_info<MQ>(p, bn) : ri;
         const int32_t e_cur = last_entry<MQ>(p, b);
         nle = bn < p.B ? last_entry<MQ>(p, bn) : 0;
-        load_ids(w, b, win, nb);
+        load_ids(w, ri.b, win, nb);
         if (win == 0) {
 #pragma unroll
             for (int k = 0; k < 4; ++k) f[k] = w[k];
         } else {
-            load_ids(f, b, 0, nb);
+            load_ids(f, ri.b, 0, nb);
         }
-        if (bn < p.B) load_ids(nx, bn, 0, pfx[bn + 1] - pfx[bn]);
+        if (bn < p.B) load_ids(nx, rn.b, 0, pfx[bn + 1] - pfx[bn]);
         lv = last_block_slots<MQ>(p, b, nb, e_cur);
+        if constexpr (MQ) lim = e_cur - p.q_len + ri.first;
     }
     bool seg_begin = true;
     bool whole = false;
@@ -350,8 +355,7 @@ __device__ __forceinline__ void run_producer(const SplitParams& p, uint32_t base
             m.flags = (seg_begin ? kSegBegin : 0) | (seg_end ? kSegEnd : 0) | (whole ? kWholeUnit : 0);
             m.slot = b * Hkv + kvh + (int)blockIdx.x;
             m.j0 = j;
-            const RowInfo ri = row_info<MQ>(p, b);
-            m.lim = MQ ? p.lens[ri.b] - p.q_len + ri.first : 0x7fffffff;
+            m.lim = lim;
             m.nr = MQ ? ri.cnt * p.G : p.G;
             meta[stage] = m;
             const bool load_q = seg_begin && MODE != kGather;
@@ -464,11 +468,14 @@ __device__ __forceinline__ void run_producer(const SplitParams& p, uint32_t base
 #pragma unroll
                 for (int k = 0; k < 4; ++k) w[k] = f[k] = nx[k];
                 if (b < p.B && pos < end) {
+                    ri = rn;
                     lv = last_block_slots<MQ>(p, b, nb, nle);
+                    if constexpr (MQ) lim = nle - p.q_len + ri.first;
                     bn = next_seq(b);
                     if (bn < p.B) {
+                        rn = row_info<MQ>(p, bn);
                         nle = last_entry<MQ>(p, bn);
-                        load_ids(nx, bn, 0, pfx[bn + 1] - pfx[bn]);
+                        load_ids(nx, rn.b, 0, pfx[bn + 1] - pfx[bn]);
                     }
                 }
             } else {  // next kv head of the same sequence: the same row again
@@ -484,7 +491,7 @@ __device__ __forceinline__ void run_producer(const SplitParams& p, uint32_t base
 #pragma unroll
             for (int k = 2; k < 4; ++k) {
                 const int32_t e = win + 32 * k + lane;
-                w[k] = e < nb ? table_entry<MQ>(p, b, e) : 0;
+                w[k] = e < nb ? table_at(ri.b, e) : 0;
             }
         }
         if (++stage == S) { stage = 0; phase ^= 1u; }
