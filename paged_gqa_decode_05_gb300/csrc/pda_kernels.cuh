@@ -74,8 +74,6 @@ struct Cfg {
     static_assert(ST == 64 || ST == 32, "stage rows");
 };
 
-// Entry idx of sequence b's block list: the table row, or, for a contiguous
-// cache [B, S, Hkv, D] (no table), block b * (S / bs) + idx.
 // Causal multi-query decode packs qp queries of a sequence into one launch
 // row (the MMA's N = qp*G columns: column n is query n / G, head n % G).  A
 // sequence has Qr = ceil(q_len / qp) rows, ordered row-major over the batch:
@@ -596,6 +594,9 @@ __device__ __forceinline__ void run_consumer(const SplitParams& p, uint32_t base
     constexpr bool MQ = MODE == kMulti;
     const int G = p.G;
     const float sl2 = p.scale_log2;
+    // multi-query: the queries of this lane's two score columns (column n is
+    // query n / G of the row), fixed for the whole launch
+    const int qc0 = MQ ? (2 * t) / G : 0, qc1 = MQ ? (2 * t + 1) / G : 0;
     // ldmatrix row addresses: QK reads K as the A operand (rows = tokens),
     // PV reads V transposed as the A operand (rows of V = tokens = k index).
     const int qk_row = r0 + (lane & 7) + (((lane >> 3) & 1) << 3);
@@ -680,12 +681,15 @@ __device__ __forceinline__ void run_consumer(const SplitParams& p, uint32_t base
                     if (r0 + g + 8 >= m.n_valid) { s2 = kNegInf; s3 = kNegInf; }
                 }
                 if constexpr (MQ) {  // column n = query n / G may not see the later tokens
-                    const int pos = m.j0 * p.bs + r0 + g;
-                    const int lim0 = m.lim + (2 * t) / G, lim1 = m.lim + (2 * t + 1) / G;
-                    if (pos > lim0) s0 = kNegInf;
-                    if (pos > lim1) s1 = kNegInf;
-                    if (pos + 8 > lim0) s2 = kNegInf;
-                    if (pos + 8 > lim1) s3 = kNegInf;
+                    const int pos0 = m.j0 * p.bs + r0;  // the warp's first token
+                    if (pos0 + 15 > m.lim) {  // only rows past the row's first query's limit
+                        const int pos = pos0 + g;
+                        const int lim0 = m.lim + qc0, lim1 = m.lim + qc1;
+                        if (pos > lim0) s0 = kNegInf;
+                        if (pos > lim1) s1 = kNegInf;
+                        if (pos + 8 > lim0) s2 = kNegInf;
+                        if (pos + 8 > lim1) s3 = kNegInf;
+                    }
                 }
                 // column max over the 16 tokens (lanes sharing t)
                 float x0 = fmaxf(s0, s2), x1 = fmaxf(s1, s3);
