@@ -340,7 +340,8 @@ pda_status pda_set_timing_events(pda_ctx* ctx, void* ev_begin, void* ev_split, v
 /*
  * Describes the launch the context would make (host only, after pda_create):
  * split-kernel CTAs (a multiple of the SM count), CTAs per SM, pipeline
- * stages, dynamic shared memory bytes per CTA and partial-state slots.
+ * stages, dynamic shared memory bytes per CTA, partial-state slots and the
+ * plan's unit cost (see pda_plan_units).
  */
 typedef struct pda_launch_info {
     int32_t split_ctas;
@@ -350,25 +351,33 @@ typedef struct pda_launch_info {
     int32_t smem_bytes;
     int32_t stage_tokens;
     int64_t partial_slots;
+    int32_t unit_cost;
 } pda_launch_info;
 pda_status pda_get_launch_info(const pda_ctx* ctx, pda_launch_info* info);
 
 /*
  * The split plan on its own (host only; no GPU needed).  The decode kernel
- * walks the flattened index space of W = Hkv * sum_b nb_b blocks, ordered
- * (sequence, kv head, block), with nb_b = ceil(max(len_b, 0) / block_size)
- * (or the tile count when blocks_given != 0).  CTA c takes blocks
- * [floor(c*W/P), floor((c+1)*W/P)).  For unit u = b*Hkv + g this reports the
- * first and last CTA touching it (-1, -1 when it has no blocks); a CTA's
- * partial state for unit u goes to slot u + c.
+ * walks the flattened index space of W = Hkv * sum_b nv_b plan blocks,
+ * ordered (sequence, kv head, block): a unit with nb_b blocks,
+ * nb_b = ceil(max(len_b, 0) / block_size) (or the tile count when
+ * blocks_given != 0), spans nv_b = nb_b + unit_cost positions (0 when
+ * nb_b = 0), its blocks first.  The unit cost stands for the fixed work of a
+ * segment, so that CTAs covering many short units get fewer blocks; a
+ * context's value is in pda_launch_info.unit_cost (one stage of blocks).
+ * CTA c takes positions [floor(c*W/P), floor((c+1)*W/P)).  For unit
+ * u = b*Hkv + g this reports the first and last CTA holding one of its
+ * blocks (-1, -1 when it has none); a CTA's partial state for unit u goes to
+ * slot u + c.
  *   lens        [batch] host int32 (tokens, or block counts).
+ *   unit_cost   >= 0.
  *   first_cta,
  *   last_cta    [batch*Hkv] outputs.
  *   total_blocks receives W.
  */
 pda_status pda_plan_units(const int32_t* lens, int32_t batch, int32_t blocks_given,
                           int32_t block_size, int32_t num_kv_heads, int32_t split_ctas,
-                          int32_t* first_cta, int32_t* last_cta, int64_t* total_blocks);
+                          int32_t unit_cost, int32_t* first_cta, int32_t* last_cta,
+                          int64_t* total_blocks);
 
 /*
  * One-shot decode that allocates nothing -- no counterpart on the pages; it

@@ -56,7 +56,7 @@ class LaunchInfo(ctypes.Structure):
     _fields_ = [("split_ctas", ctypes.c_int32), ("ctas_per_sm", ctypes.c_int32),
                 ("num_sms", ctypes.c_int32), ("stages", ctypes.c_int32),
                 ("smem_bytes", ctypes.c_int32), ("stage_tokens", ctypes.c_int32),
-                ("partial_slots", ctypes.c_int64)]
+                ("partial_slots", ctypes.c_int64), ("unit_cost", ctypes.c_int32)]
 
 
 _LIB: Optional[ctypes.CDLL] = None
@@ -102,7 +102,7 @@ def lib() -> ctypes.CDLL:
         "pda_set_timing_events": (I32, [P, P, P, P]),
         "pda_check_wait_timeout": (I32, [P, I64, P]),
         "pda_get_launch_info": (I32, [P, ctypes.POINTER(LaunchInfo)]),
-        "pda_plan_units": (I32, [P, I32, I32, I32, I32, I32, P, P, ctypes.POINTER(I64)]),
+        "pda_plan_units": (I32, [P, I32, I32, I32, I32, I32, I32, P, P, ctypes.POINTER(I64)]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(L, name)
@@ -149,8 +149,9 @@ def slot_strides(**kw) -> Tuple[int, int, int]:
 
 
 def plan_units(lens: Sequence[int], *, block_size: int, num_kv_heads: int, split_ctas: int,
-               blocks_given: bool = False):
-    """(first_cta, last_cta, total_blocks) of the split plan (host only)."""
+               blocks_given: bool = False, unit_cost: int = 0):
+    """(first_cta, last_cta, total_blocks) of the split plan (host only); a
+    context's unit_cost is in its launch_info()."""
     import numpy as np
     lens = np.ascontiguousarray(lens, dtype=np.int32)
     n = lens.shape[0] * num_kv_heads
@@ -158,7 +159,7 @@ def plan_units(lens: Sequence[int], *, block_size: int, num_kv_heads: int, split
     last = np.zeros(max(n, 1), dtype=np.int32)
     total = ctypes.c_int64()
     _check(lib().pda_plan_units(lens.ctypes.data, lens.shape[0], int(blocks_given), block_size,
-                                num_kv_heads, split_ctas, first.ctypes.data, last.ctypes.data,
+                                num_kv_heads, split_ctas, unit_cost, first.ctypes.data, last.ctypes.data,
                                 ctypes.byref(total)))
     return first[:n], last[:n], int(total.value)
 

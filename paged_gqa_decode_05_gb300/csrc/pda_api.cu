@@ -286,6 +286,7 @@ pda_status run(pda_ctx* ctx, const RunArgs& r) {
         p.Hkv = Hkv;
         p.G = ctx->G;
         p.bs = d.block_size;
+        p.unit_cost = pda::unit_cost_blocks(ctx->stage_rows, d.block_size, r.mode == pda::kMulti);
         p.dbg_row_tokens = (int32_t)dbg_row_tokens;
         p.scale_log2 = scale_log2;
         const size_t smem = pda::smem_layout(D, ctx->stage_rows, ctx->stages, ctx->G, cb).total;
@@ -313,6 +314,7 @@ pda_status run(pda_ctx* ctx, const RunArgs& r) {
         mp.Hkv = Hkv;
         mp.G = ctx->G;
         mp.D = D;
+        mp.unit_cost = p.unit_cost;
         mp.split_ctas = ctx->split_ctas;
         mp.q_len = r.q_len;
         mp.qp = qp;
@@ -668,34 +670,38 @@ PDA_EXPORT pda_status pda_get_launch_info(const pda_ctx* ctx, pda_launch_info* i
     info->smem_bytes = ctx->smem_max;
     info->stage_tokens = ctx->stage_rows;
     info->partial_slots = ctx->slots;
+    info->unit_cost = pda::unit_cost_blocks(ctx->stage_rows, ctx->dims.block_size, false);
     return PDA_OK;
 }
 
 PDA_EXPORT pda_status pda_plan_units(const int32_t* lens, int32_t batch, int32_t blocks_given,
                                      int32_t block_size, int32_t num_kv_heads, int32_t split_ctas,
-                                     int32_t* first_cta, int32_t* last_cta, int64_t* total_blocks) {
-    if (batch < 0 || block_size < 1 || num_kv_heads < 1 || split_ctas < 1 ||
+                                     int32_t unit_cost, int32_t* first_cta, int32_t* last_cta,
+                                     int64_t* total_blocks) {
+    if (batch < 0 || block_size < 1 || num_kv_heads < 1 || split_ctas < 1 || unit_cost < 0 ||
         (batch > 0 && (!lens || !first_cta || !last_cta)) || !total_blocks)
         return fail(PDA_ERR_INVALID_ARG, "bad plan arguments");
+    auto blocks = [&](int32_t b) {
+        return blocks_given ? std::max(lens[b], 0) : pda::blocks_for_tokens(lens[b], block_size);
+    };
     int64_t sum = 0;
-    for (int32_t b = 0; b < batch; ++b)
-        sum += blocks_given ? std::max(lens[b], 0) : pda::blocks_for_tokens(lens[b], block_size);
+    for (int32_t b = 0; b < batch; ++b) sum += pda::plan_blocks(blocks(b), unit_cost);
     const int64_t W = sum * num_kv_heads, P = split_ctas;
     *total_blocks = W;
     int64_t pfx = 0;
     for (int32_t b = 0; b < batch; ++b) {
-        const int32_t nb = blocks_given ? std::max(lens[b], 0) : pda::blocks_for_tokens(lens[b], block_size);
+        const int32_t nb = blocks(b), nv = pda::plan_blocks(nb, unit_cost);
         for (int32_t g = 0; g < num_kv_heads; ++g) {
             const int64_t u = (int64_t)b * num_kv_heads + g;
             if (nb == 0) {
                 first_cta[u] = last_cta[u] = -1;
                 continue;
             }
-            const int64_t su = pfx * num_kv_heads + (int64_t)g * nb;
+            const int64_t su = pfx * num_kv_heads + (int64_t)g * nv;
             first_cta[u] = (int32_t)pda::cta_of_block(su, W, P);
             last_cta[u] = (int32_t)pda::cta_of_block(su + nb - 1, W, P);
         }
-        pfx += nb;
+        pfx += nv;
     }
     return PDA_OK;
 }
@@ -872,6 +878,7 @@ PDA_EXPORT pda_status pda_decode_noalloc(const pda_bf16* q, const pda_bf16* k_po
     p.Hkv = num_kv_heads;
     p.G = G;
     p.bs = block_size;
+    p.unit_cost = pda::unit_cost_blocks(rows, block_size, false);
     p.scale_log2 = scale_log2;
     if ((e = pda::launch_split(D, rows, pda::kOneShot, p, split_ctas, smem, s)) != cudaSuccess)
         return cuda_fail(e, "split kernel launch");
@@ -886,6 +893,7 @@ PDA_EXPORT pda_status pda_decode_noalloc(const pda_bf16* q, const pda_bf16* k_po
     mp.Hkv = num_kv_heads;
     mp.G = G;
     mp.D = D;
+    mp.unit_cost = p.unit_cost;
     mp.split_ctas = split_ctas;
     if ((e = pda::launch_merge(pda::kOneShot, mp, true, s)) != cudaSuccess)
         return cuda_fail(e, "merge kernel launch");

@@ -180,9 +180,10 @@ __device__ __forceinline__ int32_t last_block_slots(const SplitParams& p, int b,
     return v > p.bs ? p.bs : v;
 }
 
-// Exclusive prefix of blocks per sequence into shared pfx[0..B] (B <= 1024).
+// Exclusive prefix of plan blocks per sequence (blocks plus the unit cost)
+// into shared pfx[0..B] (B <= 1024).
 // Thread t owns sequences [t*per, t*per + per): it loads all their length
-// entries at once (one memory round trip), stores their block counts in pfx,
+// entries at once (one memory round trip), stores their plan blocks in pfx,
 // and the per-thread sums are scanned with warp shuffles and the warp totals.
 template <bool MQ, int kThreads>
 __device__ __forceinline__ void build_prefix(const SplitParams& p, int32_t* pfx, int32_t* scan) {
@@ -197,7 +198,7 @@ __device__ __forceinline__ void build_prefix(const SplitParams& p, int32_t* pfx,
 #pragma unroll
     for (int k = 0; k < kPer; ++k)
         if (lo + k < hi) {
-            const int32_t v = blocks_of<MQ>(p, lo + k, L[k]);
+            const int32_t v = plan_blocks(blocks_of<MQ>(p, lo + k, L[k]), p.unit_cost);
             pfx[lo + k] = v;
             sum += v;
         }
@@ -256,7 +257,7 @@ __device__ __forceinline__ void run_producer(const SplitParams& p, uint32_t base
 
     int64_t pos = begin;
     int b = 0, kvh = 0;
-    int32_t j = 0, nb = 0;
+    int32_t j = 0, nb = 0, nv = 0;  // j: block of the unit; nb blocks, nv plan blocks
     int32_t win = 0;
     int32_t w[4], f[4], nx[4];
     int32_t lv = bs;   // valid slots of this sequence's last block
@@ -303,10 +304,11 @@ __device__ __forceinline__ void run_producer(const SplitParams& p, uint32_t base
             if ((int64_t)pfx[mid] * Hkv <= pos) lo = mid; else hi = mid - 1;
         }
         b = lo;
-        nb = pfx[b + 1] - pfx[b];
+        nv = pfx[b + 1] - pfx[b];
+        nb = real_blocks(nv, p.unit_cost);
         const int64_t rem = pos - (int64_t)pfx[b] * Hkv;
-        kvh = (int)(rem / nb);
-        j = (int32_t)(rem % nb);
+        kvh = (int)(rem / nv);
+        j = (int32_t)(rem % nv);  // may lie in the unit's cost tail (j >= nb)
         win = j;
         // every load first (one round trip), their uses after
         bn = next_seq(b);
@@ -321,19 +323,55 @@ __device__ __forceinline__ void run_producer(const SplitParams& p, uint32_t base
         } else {
             load_ids(f, ri.b, 0, nb);
         }
-        if (bn < p.B) load_ids(nx, rn.b, 0, pfx[bn + 1] - pfx[bn]);
+        if (bn < p.B) load_ids(nx, rn.b, 0, real_blocks(pfx[bn + 1] - pfx[bn], p.unit_cost));
         lv = last_block_slots<MQ>(p, b, nb, e_cur);
         if constexpr (MQ) lim = e_cur - p.q_len + ri.first;
     }
+    // Past a unit's last block: skip its cost tail and move to the next unit
+    // (the next kv head reuses the row's first ids; the next sequence's ids
+    // were loaded a unit ago).
+    auto next_unit = [&]() {
+        pos += nv - j;
+        j = 0;
+        win = 0;
+        if (++kvh == Hkv) {
+            kvh = 0;
+            b = bn;
+            nv = b < p.B ? pfx[b + 1] - pfx[b] : 0;
+            nb = real_blocks(nv, p.unit_cost);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) w[k] = f[k] = nx[k];
+            if (b < p.B && pos < end) {
+                ri = rn;
+                lv = last_block_slots<MQ>(p, b, nb, nle);
+                if constexpr (MQ) lim = nle - p.q_len + ri.first;
+                bn = next_seq(b);
+                if (bn < p.B) {
+                    rn = row_info<MQ>(p, bn);
+                    nle = last_entry<MQ>(p, bn);
+                    load_ids(nx, rn.b, 0, real_blocks(pfx[bn + 1] - pfx[bn], p.unit_cost));
+                }
+            }
+        } else {
+#pragma unroll
+            for (int k = 0; k < 4; ++k) w[k] = f[k];
+        }
+    };
     bool seg_begin = true;
     bool whole = false;
     while (pos < end) {
         const int stop = __shfl_sync(0xffffffffu, leader ? *abort_flag : 0, 0);
         if (stop) { ok = false; break; }
+        if (j >= nb) {  // the unit's last block is issued (or the range starts in its tail)
+            if (b >= p.B) break;  // no units left (not reached: end <= the plan's size)
+            next_unit();
+            continue;
+        }
         const int32_t n = (int32_t)min((int64_t)min(NB, nb - j), end - pos);
         const bool unit_end = (j + n == nb);
         const bool seg_end = unit_end || (pos + n == end);
-        if (seg_begin) whole = (j == 0) && ((int64_t)pfx[b] * Hkv + (int64_t)(kvh + 1) * nb <= end);
+        if (seg_begin)
+            whole = (j == 0) && ((int64_t)pfx[b] * Hkv + (int64_t)kvh * nv + nb <= end);
 
         const int32_t lastv = unit_end ? lv : bs;
 
@@ -456,31 +494,7 @@ __device__ __forceinline__ void run_producer(const SplitParams& p, uint32_t base
         pos += n;
         j += n;
         seg_begin = seg_end;
-        if (unit_end) {
-            j = 0;
-            win = 0;
-            if (++kvh == Hkv) {  // next sequence: its ids were loaded a unit ago
-                kvh = 0;
-                b = bn;
-                nb = b < p.B ? pfx[b + 1] - pfx[b] : 0;
-#pragma unroll
-                for (int k = 0; k < 4; ++k) w[k] = f[k] = nx[k];
-                if (b < p.B && pos < end) {
-                    ri = rn;
-                    lv = last_block_slots<MQ>(p, b, nb, nle);
-                    if constexpr (MQ) lim = nle - p.q_len + ri.first;
-                    bn = next_seq(b);
-                    if (bn < p.B) {
-                        rn = row_info<MQ>(p, bn);
-                        nle = last_entry<MQ>(p, bn);
-                        load_ids(nx, rn.b, 0, pfx[bn + 1] - pfx[bn]);
-                    }
-                }
-            } else {  // next kv head of the same sequence: the same row again
-#pragma unroll
-                for (int k = 0; k < 4; ++k) w[k] = f[k];
-            }
-        } else if (j - win >= 64) {
+        if (!unit_end && j - win >= 64) {
             // first half consumed: slide by 64 and fetch the 64 entries after
             // the window (needed no sooner than the next stage)
             win += 64;
@@ -917,7 +931,7 @@ __global__ void __launch_bounds__(kMaxGroup * 256 / 4) merge_kernel(const MergeP
     const int64_t grp = div_floor(b, Bg);
     const int32_t lo = p.pfx[b], hi = p.pfx[b + 1];
     const int32_t g_lo = p.pfx[grp * Bg], g_hi = p.pfx[(grp + 1) * Bg];
-    const int32_t nb = hi - lo;
+    const int32_t nb = real_blocks(hi - lo, p.unit_cost);
     const bool active = i4 < n4;  // the block is rounded up to whole warps
     const int h = active ? (4 * i4) / D : 0;
     const int d4 = 4 * i4 - h * D;
@@ -936,7 +950,8 @@ __global__ void __launch_bounds__(kMaxGroup * 256 / 4) merge_kernel(const MergeP
     gr.g = grp;
     gr.F0 = (int64_t)g_lo * p.Hkv;
     gr.W = (int64_t)g_hi * p.Hkv - gr.F0;
-    const int64_t su = (int64_t)lo * p.Hkv + (int64_t)kvh * nb, eu = su + nb;
+    // the unit's blocks: the first nb of its hi - lo plan blocks
+    const int64_t su = (int64_t)lo * p.Hkv + (int64_t)kvh * (hi - lo), eu = su + nb;
     const int64_t cf = gr.g * gr.Pg + cta_of_block(su - gr.F0, gr.W, gr.Pg);
     const int64_t cl = gr.g * gr.Pg + cta_of_block(eu - 1 - gr.F0, gr.W, gr.Pg);
     if (writes_output(MODE) && cf == cl) return;  // written by the split kernel

@@ -59,7 +59,7 @@ struct SplitParams {
     float* out_f32;              // [B, Hq, D] fp32 instead of out when non-null
     float* part_o;               // [slots, G, D]
     float* part_ml;              // [slots, G, 2] (m in base-2 units, l)
-    int32_t* pfx;                // [B+1] block prefix, written by CTA 0 for the merge
+    int32_t* pfx;                // [B+1] plan-block prefix, written by CTA 0 for the merge
     uint32_t* err;               // device error flags
     uint16_t* dbg_k;             // gather check outputs
     uint16_t* dbg_v;
@@ -76,6 +76,7 @@ struct SplitParams {
     int32_t qp;                  // queries packed into one launch row (MMA N = qp*G <= 8)
     int32_t rows_per_slot;       // rows of a partial-state slot (0: G)
     int32_t B, Hq, Hkv, G, bs;
+    int32_t unit_cost;           // plan blocks added to every non-empty unit
     int32_t dbg_row_tokens;      // tokens per (b, kvh) row of the gather output
     float scale_log2;            // softmax scale * log2(e)
 };
@@ -90,6 +91,7 @@ struct MergeParams {
     float* l_state;
     float* o_state;
     int32_t B, Hq, Hkv, G, D;
+    int32_t unit_cost;           // as SplitParams
     int32_t split_ctas;
     int32_t q_len;               // as SplitParams
     int32_t qp;

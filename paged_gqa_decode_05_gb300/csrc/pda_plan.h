@@ -1,14 +1,19 @@
 // pda_plan.h -- the split plan shared by the host API and the kernels.
 //
-// The work of one call is the flattened index space of W blocks ordered
+// The work of one call is the flattened index space of W plan blocks ordered
 // (sequence b, kv head g, block j): unit u = b*Hkv + g owns the W-range
-// [pfx[b]*Hkv + g*nb_b, pfx[b]*Hkv + (g+1)*nb_b), where nb_b is the number of
-// blocks of sequence b and pfx its exclusive prefix sum.  A grid of P CTAs
-// splits the range evenly: CTA c takes [floor(c*W/P), floor((c+1)*W/P)).  Each
-// maximal run of one unit inside one CTA's range is a "segment" with its own
-// online-softmax state; the state of the segment of unit u in CTA c is stored
-// in slot u + c, which is unique because moving to the next segment always
-// advances u, c or both.
+// [pfx[b]*Hkv + g*nv_b, pfx[b]*Hkv + (g+1)*nv_b), where nv_b = nb_b + c for a
+// sequence of nb_b > 0 blocks (0 for an empty one) and pfx is the exclusive
+// prefix sum of nv.  The first nb_b positions of a unit are its blocks; the c
+// after them are a cost placeholder read by nobody: every segment takes a
+// fixed time beyond its blocks (its partial last stage, the consumer warps'
+// state merge and store, the next unit's q rows), and counting that cost in
+// the plan gives a CTA that covers many short units fewer blocks.  A grid of
+// P CTAs splits the range evenly: CTA c takes [floor(c*W/P),
+// floor((c+1)*W/P)).  Each maximal run of one unit's blocks inside one CTA's
+// range is a "segment" with its own online-softmax state; the state of the
+// segment of unit u in CTA c is stored in slot u + c, which is unique because
+// moving to the next segment always advances u, c or both.
 #pragma once
 
 #include <stdint.h>
@@ -75,6 +80,27 @@ PDA_HD void group_cta_range(const GroupRange& r, int64_t c, int64_t* begin, int6
     *begin = r.F0 + cta_begin(cl, r.W, r.Pg);
     *end = r.F0 + cta_begin(cl + 1, r.W, r.Pg);
 }
+
+// Plan blocks c added to every non-empty unit: a segment's fixed cost in
+// quarter stages, measured per loader (each value the fastest of a sweep on
+// ragged and uniform batches).  TMA block boxes: two stages.  Row gathers of
+// blocks below 8 tokens, whose stages take longer: half a stage.  Causal
+// multi-query rows, whose CTAs cover about q_len times more segments and
+// read most stages from L2: four stages.
+constexpr int32_t kUnitCostX4 = 8;
+constexpr int32_t kUnitCostGatherX4 = 2;
+constexpr int32_t kUnitCostMultiX4 = 16;
+PDA_HD int32_t unit_cost_blocks(int32_t stage_rows, int32_t block_size, bool multi_query) {
+    const int32_t nb = stage_rows / block_size;
+    const int32_t x4 = multi_query ? kUnitCostMultiX4 : block_size < 8 ? kUnitCostGatherX4 : kUnitCostX4;
+    return (nb < 1 ? 1 : nb) * x4 / 4;
+}
+
+// Plan blocks of a unit with nb blocks.
+PDA_HD int32_t plan_blocks(int32_t nb, int32_t unit_cost) { return nb > 0 ? nb + unit_cost : 0; }
+
+// Blocks of a unit with nv plan blocks.
+PDA_HD int32_t real_blocks(int32_t nv, int32_t unit_cost) { return nv > 0 ? nv - unit_cost : 0; }
 
 // Blocks needed for a length in tokens.
 PDA_HD int32_t blocks_for_tokens(int32_t len, int32_t block_size) {
