@@ -47,7 +47,7 @@
 extern "C" {
 #endif
 
-#define PDA_ABI_VERSION 1
+#define PDA_ABI_VERSION 2
 
 typedef struct pda_ctx pda_ctx;
 typedef void* pda_stream;      /* cudaStream_t */

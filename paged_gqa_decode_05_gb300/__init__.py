@@ -60,6 +60,7 @@ class LaunchInfo(ctypes.Structure):
 
 
 _LIB: Optional[ctypes.CDLL] = None
+ABI_VERSION = 2  # PDA_ABI_VERSION of include/pda.h that these signatures follow
 
 
 def library_path() -> str:
@@ -108,6 +109,9 @@ def lib() -> ctypes.CDLL:
         fn = getattr(L, name)
         fn.restype = res
         fn.argtypes = args
+    if L.pda_abi_version() != ABI_VERSION:
+        raise RuntimeError(f"{_LIBPATH} has ABI version {L.pda_abi_version()}, this binding "
+                           f"expects {ABI_VERSION}: rebuild it")
     _LIB = L
     return L
 
