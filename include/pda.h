@@ -153,7 +153,8 @@ void pda_destroy(pda_ctx* ctx);
  *   out          [batch, Hq, D] bf16, written completely.
  *   batch        0 .. max_seqs (0 returns PDA_OK without launching).
  * The work is split over the flattened (sequence, kv head, block) space so
- * every SM gets an equal share, whatever the lengths; no host copy of
+ * every SM gets an equal share (its blocks plus a fixed cost per unit it
+ * covers; see pda_plan_units), whatever the lengths; no host copy of
  * seq_lens is needed and the call can be captured in a CUDA graph.
  */
 pda_status pda_decode(pda_ctx* ctx, const pda_bf16* q, const pda_bf16* k_pool,

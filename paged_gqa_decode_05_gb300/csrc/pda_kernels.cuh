@@ -128,11 +128,6 @@ __device__ __forceinline__ int32_t tokens_of(const SplitParams& p, int s, int32_
     return len < 0 ? 0 : len;
 }
 
-template <bool MQ>
-__device__ __forceinline__ int32_t seq_tokens(const SplitParams& p, int s) {
-    return tokens_of<MQ>(p, s, len_entry<MQ>(p, s));
-}
-
 // Blocks of sequence b with length entry L, validated and clamped (flags
 // bad lengths).
 template <bool MQ>
@@ -926,7 +921,7 @@ __global__ void __launch_bounds__(kMaxGroup * 256 / 4) merge_kernel(const MergeP
     const int n4 = NR * D / 4;
     const int i4 = threadIdx.x;
     // Every prefix entry needed, loaded together (one round trip): the unit's
-    // sequence and the bounds of its row group (group_of_seq, written out).
+    // sequence and the bounds of its row group (group_of_cta's, written out).
     const int64_t Bg = div_floor(p.B, Qr);
     const int64_t grp = div_floor(b, Bg);
     const int32_t lo = p.pfx[b], hi = p.pfx[b + 1];

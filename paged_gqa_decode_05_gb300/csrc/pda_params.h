@@ -21,7 +21,6 @@ constexpr int kMaxConsumerWarps = 4;
 constexpr int kMaxLaunchBatch = 1024;                    // sequences per kernel launch
 constexpr int kMaxGroup = 8;                             // q heads per kv head (n8 MMA)
 
-PDA_HD int consumer_warps(int st) { return st / 16; }
 PDA_HD int split_threads(int st) { return (st / 16 + 1) * 32; }
 // Stage rows for a head size and block size.
 PDA_HD int stage_tokens(int D, int block_size) { return D == 256 && block_size < 8 ? 32 : 64; }

@@ -66,13 +66,6 @@ PDA_HD GroupRange group_of_cta(int64_t c, const Pfx& pfx, int64_t B, int64_t Q, 
     return r;
 }
 
-template <typename Pfx>
-PDA_HD GroupRange group_of_seq(int64_t s, const Pfx& pfx, int64_t B, int64_t Q, int64_t Hkv,
-                               int64_t P) {
-    const int64_t Bg = div_floor(B, Q);
-    return group_of_cta(div_floor(s, Bg) * div_floor(P, Q), pfx, B, Q, Hkv, P);
-}
-
 // Flattened range [begin, end) of CTA c within its group (empty when idle).
 PDA_HD void group_cta_range(const GroupRange& r, int64_t c, int64_t* begin, int64_t* end) {
     if (r.W == 0) { *begin = *end = r.F0; return; }
