@@ -187,6 +187,18 @@ struct RunArgs {
     int32_t q_len = 1;        // causal queries per sequence (q, out: [batch, q_len, Hq, D])
 };
 
+// The kernels keep a launch's plan-block prefix in int32: up to
+// kMaxLaunchBatch rows of at most table_width + unit_cost plan blocks each.
+pda_status check_plan_size(int64_t rows, int32_t table_width, int32_t unit_cost) {
+    const int64_t most = std::min<int64_t>(rows, pda::kMaxLaunchBatch) * ((int64_t)table_width + unit_cost);
+    if (most > 0x7fffffffLL)
+        return fail(PDA_ERR_INVALID_ARG,
+                    "block table width %d is too large: %lld rows per launch could hold %lld "
+                    "blocks, more than a 32-bit prefix holds",
+                    table_width, (long long)std::min<int64_t>(rows, pda::kMaxLaunchBatch), (long long)most);
+    return PDA_OK;
+}
+
 pda_status run(pda_ctx* ctx, const RunArgs& r) {
     if (!ctx) return fail(PDA_ERR_INVALID_ARG, "ctx is NULL");
     const pda_dims& d = ctx->dims;
@@ -213,6 +225,9 @@ pda_status run(pda_ctx* ctx, const RunArgs& r) {
         return fail(PDA_ERR_INVALID_ARG, "table / length arrays must be non-NULL and 4-byte aligned");
     if (r.table_stride < 1)
         return fail(PDA_ERR_INVALID_ARG, "block table width must be >= 1 (got %d)", r.table_stride);
+    st = check_plan_size((int64_t)r.batch * r.q_len, r.table_stride,
+                         pda::unit_cost_blocks(ctx->stage_rows, d.block_size, r.mode == pda::kMulti));
+    if (st != PDA_OK) return st;
     float scale_log2 = 0.f;
     st = check_scale(r.scale, d.head_dim, &scale_log2);
     if (st != PDA_OK) return st;
@@ -847,6 +862,8 @@ PDA_EXPORT pda_status pda_decode_noalloc(const pda_bf16* q, const pda_bf16* k_po
     if (!block_table || !seq_lens || !aligned(block_table, 4) || !aligned(seq_lens, 4))
         return fail(PDA_ERR_INVALID_ARG, "block_table / seq_lens must be non-NULL and 4-byte aligned");
     if (max_blocks < 1) return fail(PDA_ERR_INVALID_ARG, "max_blocks must be >= 1");
+    if ((st = check_plan_size(batch, max_blocks, pda::unit_cost_blocks(rows, block_size, false))) != PDA_OK)
+        return st;
     PoolArgs pool = {k_pool, v_pool, num_blocks, (int64_t)block_size * num_kv_heads * head_dim,
                      (int64_t)num_kv_heads * head_dim, (int64_t)head_dim};
     pda_ctx shape;  // only the dims are read by the helpers below

@@ -171,6 +171,29 @@ def test_invalid_arguments_rejected():
     torch.cuda.synchronize()
 
 
+def test_table_too_wide_for_int32_plan_rejected():
+    """A launch's plan-block prefix is int32: a table width that could overflow
+    it for the batch is refused on the host, before anything is launched (the
+    table pointer is never read)."""
+    import torch
+    import paged_gqa_decode_05_gb300 as pda
+    w = _w(seed=13, lens=(10, 20))
+    ctx = pda.Context(max_seqs=1024, num_q_heads=w.Hq, num_kv_heads=w.Hkv, head_dim=w.D,
+                      block_size=w.block_size)
+    t = upload(w)
+    q = torch.zeros((1024, w.Hq, w.D), dtype=torch.bfloat16, device="cuda")
+    lens = torch.ones(1024, dtype=torch.int32, device="cuda")
+    out = torch.empty_like(q)
+    L = pda.lib()
+    width = 1 << 21  # 1024 rows x (2^21 + unit cost) plan blocks > 2^31 - 1
+    st = L.pda_decode(ctx._ctx, q.data_ptr(), t["k_pool"].data_ptr(), t["v_pool"].data_ptr(),
+                      int(w.k_pool.shape[0]), t["block_table"].data_ptr(), width, lens.data_ptr(),
+                      1024, float("nan"), out.data_ptr(), None)
+    assert st == pda.ERR_INVALID_ARG
+    assert b"too large" in L.pda_last_error()
+    torch.cuda.synchronize()
+
+
 @pytest.mark.parametrize("bs", [2, 16])
 def test_padded_token_stride_identical(bs):
     """Token rows padded by 8 elements (strides not multiples of D): block size
