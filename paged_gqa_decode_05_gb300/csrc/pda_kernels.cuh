@@ -282,7 +282,7 @@ __device__ __forceinline__ void run_producer(const SplitParams& p, uint32_t base
         return s;
     };
     // The id of window entry idx (lane-varying).  A stage reads entries
-    // j - win .. j - win + n - 1 < 64: the blocks per stage NB = 64 / bs is a
+    // j - win .. j - win + n - 1 < 64: the blocks per stage NB = ST / bs is a
     // power of two, j - win stays a multiple of NB (the window starts at a
     // segment start or a unit start and slides by 64) and n <= NB.  So only
     // w[0] and w[1] are read; w[2] and w[3], loaded at a slide, are first read
