@@ -47,7 +47,7 @@
 extern "C" {
 #endif
 
-#define PDA_ABI_VERSION 2
+#define PDA_ABI_VERSION 3
 
 typedef struct pda_ctx pda_ctx;
 typedef void* pda_stream;      /* cudaStream_t */
@@ -395,20 +395,25 @@ pda_status pda_plan_units(const int32_t* lens, int32_t batch, int32_t blocks_giv
  * until the process exits.
  *
  * Arguments and layout are those of pda_decode (default pool layout
- * [num_blocks, block_size, Hkv, D]); the sizes that pda_create would take
- * come as arguments.  device_flags is an optional device word that receives
- * PDA_DEVERR_* bits (the caller zeroes it); with NULL the flags go to the
- * scratch, where they are cleared at the start of every call and not
- * reported.
+ * [num_blocks, block_size, Hkv, D], every block size pda_check_dims
+ * accepts); the sizes that pda_create would take come as arguments, and the
+ * call launches the same kernels, with the same loader for the block size,
+ * as a context would.  device_flags is a required device word (4-byte
+ * aligned) that receives PDA_DEVERR_* bits; the caller zeroes it and reads
+ * it after the call has run.  A kernel that met a bad block id or length, or
+ * whose bounded wait gave up (its output is then not valid), says so there;
+ * NULL is refused so that no failure goes unreported.
  *
  * Rules: a call whose scratch need exceeds PDA_NOALLOC_SCRATCH_BYTES returns
  * PDA_ERR_INVALID_ARG with the size in pda_last_error(); batch is limited
  * to 1024 sequences.  The first call on each device finds the scratch's
- * device address and sets kernel attributes there: make that first call
- * before any stream capture.  All calls share the one scratch array and keep
- * the last call's contents: two calls that can overlap on the GPU (different
- * streams without ordering, or several threads) race and corrupt each
- * other's results, so order them on one stream.
+ * device address and sets the split kernels' shared-memory attributes there
+ * (to the same values pda_create sets): make that first call before any
+ * stream capture.  All calls share the one scratch array and keep the last
+ * call's contents (every call rewrites what it reads, so nothing needs
+ * clearing): two calls that can overlap on the GPU (different streams
+ * without ordering, or several threads) race and corrupt each other's
+ * results, so order them on one stream.
  */
 #define PDA_NOALLOC_SCRATCH_BYTES (4u << 20)
 pda_status pda_decode_noalloc(const pda_bf16* q, const pda_bf16* k_pool, const pda_bf16* v_pool,

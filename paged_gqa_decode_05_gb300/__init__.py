@@ -23,7 +23,6 @@ Tiled lifecycle (tiled_attention.rs: begin_step / step_tile / finalize)::
 from __future__ import annotations
 
 import ctypes
-import math
 import os
 from typing import Optional, Sequence, Tuple
 
@@ -60,7 +59,7 @@ class LaunchInfo(ctypes.Structure):
 
 
 _LIB: Optional[ctypes.CDLL] = None
-ABI_VERSION = 2  # PDA_ABI_VERSION of include/pda.h that these signatures follow
+ABI_VERSION = 3  # PDA_ABI_VERSION of include/pda.h that these signatures follow
 
 
 def library_path() -> str:
@@ -505,7 +504,3 @@ def gather_states(m, l, o, group=None):
         out.append(torch.stack(parts))
     return tuple(out)
 
-
-def default_scale(head_dim: int) -> float:
-    """1/sqrt(head_dim), the scale used when none is given."""
-    return 1.0 / math.sqrt(head_dim)

@@ -105,10 +105,9 @@ struct PoolArgs {
 // head's rows of one block: a single TMA copy per block and pool, landing in
 // shared memory as [slab][slot][128 bytes] with the 128-byte swizzle.  The
 // stride triple (block, token, kv head) places any row layout in this view.
-pda_status encode_pool(const pda_ctx* ctx, const void* base, const PoolArgs& a, CUtensorMap* tm) {
+pda_status encode_pool(const pda_dims& d, const void* base, const PoolArgs& a, CUtensorMap* tm) {
     auto enc = tensor_map_encoder();
     if (!enc) return fail(PDA_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
-    const pda_dims& d = ctx->dims;
     const cuuint64_t dims[5] = {64, (cuuint64_t)d.block_size, (cuuint64_t)(d.head_dim / 64),
                                 (cuuint64_t)d.num_kv_heads, (cuuint64_t)a.num_blocks};
     const cuuint64_t strides[4] = {(cuuint64_t)a.tok * 2, 128, (cuuint64_t)a.kvh * 2,
@@ -127,9 +126,8 @@ pda_status encode_pool(const pda_ctx* ctx, const void* base, const PoolArgs& a, 
 // For block sizes below 8: a 2-D view {D, rows} of a pool whose three strides
 // are multiples of D, box {64, 1}, for TMA gather4 (four rows per copy).
 // Returns false (no error) when the layout does not fit that view.
-bool encode_rows(const pda_ctx* ctx, const void* base, const PoolArgs& a, CUtensorMap* tm) {
+bool encode_rows(const pda_dims& d, const void* base, const PoolArgs& a, CUtensorMap* tm) {
     auto enc = tensor_map_encoder();
-    const pda_dims& d = ctx->dims;
     const int64_t D = d.head_dim;
     if (!enc || a.blk % D || a.tok % D || a.kvh % D) return false;
     const int64_t rows = (a.num_blocks - 1) * (a.blk / D) + (int64_t)(d.block_size - 1) * (a.tok / D) +
@@ -144,7 +142,7 @@ bool encode_rows(const pda_ctx* ctx, const void* base, const PoolArgs& a, CUtens
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-pda_status check_pool(const pda_ctx* ctx, const PoolArgs& a) {
+pda_status check_pool(const PoolArgs& a) {
     if (!a.k || !a.v) return fail(PDA_ERR_INVALID_ARG, "k_pool / v_pool must not be NULL");
     if (!aligned(a.k, 16) || !aligned(a.v, 16))
         return fail(PDA_ERR_INVALID_ARG, "k_pool / v_pool must be 16-byte aligned");
@@ -156,7 +154,63 @@ pda_status check_pool(const pda_ctx* ctx, const PoolArgs& a) {
             return fail(PDA_ERR_INVALID_ARG,
                         "pool strides must be positive multiples of 8 elements (got %lld, %lld, %lld)",
                         (long long)a.blk, (long long)a.tok, (long long)a.kvh);
-    (void)ctx;
+    return PDA_OK;
+}
+
+// The split kernel's KV loader for a pool, with its two tensor maps: one 5-D
+// box per block and pool for block sizes from 8 (row mode 0); below 8 the
+// rows are gathered, with TMA gather4 when the three strides are multiples of
+// D (row mode 1), else with 16-byte cp.async (row mode 2, maps unused).  The
+// consumers' shared-memory layout depends on this choice, so every launch
+// path takes it from here.
+pda_status encode_loader(const pda_dims& d, const PoolArgs& a, CUtensorMap* tk, CUtensorMap* tv,
+                         int32_t* row_mode) {
+    if (d.block_size >= 8) {
+        pda_status st = encode_pool(d, a.k, a, tk);
+        if (st == PDA_OK) st = encode_pool(d, a.v, a, tv);
+        *row_mode = 0;
+        return st;
+    }
+    *row_mode = encode_rows(d, a.k, a, tk) && encode_rows(d, a.v, a, tv) ? 1 : 2;
+    return PDA_OK;
+}
+
+// The pool fields of the split kernel's parameters for a loader row mode.
+void set_pool_params(pda::SplitParams& p, const pda_dims& d, const PoolArgs& a, int32_t row_mode) {
+    p.num_blocks = a.num_blocks;
+    p.k_base = a.k;
+    p.v_base = a.v;
+    p.blk_s = a.blk;
+    p.tok_s = a.tok;
+    p.kvh_s = a.kvh;
+    p.row_gather = row_mode;
+    p.row_blk = a.blk / d.head_dim;
+    p.row_tok = a.tok / d.head_dim;
+    p.row_kvh = a.kvh / d.head_dim;
+}
+
+// Dynamic shared memory allowed for a split-kernel shape: what a launch of a
+// full batch (kMaxLaunchBatch sequences) uses, so every caller sets the same
+// value and none lowers it below what another launches with.
+int split_smem_limit(int D, int st) {
+    return (int)pda::smem_layout(D, st, pda::split_stages(D, st), pda::kMaxGroup, pda::kMaxLaunchBatch).total;
+}
+
+// Sets the shared-memory attributes of every mode of a split-kernel shape on
+// the current device.
+pda_status set_split_attributes(int D, int st, int optin) {
+    const int limit = split_smem_limit(D, st);
+    if (limit > optin)
+        return fail(PDA_ERR_UNSUPPORTED, "needs %d bytes of shared memory per CTA (device allows %d)",
+                    limit, optin);
+    for (int mode = 0; mode < pda::kNumModes; ++mode) {
+        const void* fn = pda::split_kernel_fn(D, st, mode);
+        cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, limit);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                     cudaSharedmemCarveoutMaxShared);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
+    }
     return PDA_OK;
 }
 
@@ -209,7 +263,7 @@ pda_status run(pda_ctx* ctx, const RunArgs& r) {
         return fail(PDA_ERR_INVALID_ARG, "batch %d x q_len %d outside [0, max_seqs=%d]", r.batch,
                     r.q_len, d.max_seqs);
     if (r.batch == 0) return PDA_OK;
-    pda_status st = check_pool(ctx, r.pool);
+    pda_status st = check_pool(r.pool);
     if (st != PDA_OK) return st;
     if (r.mode != pda::kGather) {
         if (!r.q || !aligned(r.q, 16)) return fail(PDA_ERR_INVALID_ARG, "q must be non-NULL and 16-byte aligned");
@@ -239,16 +293,8 @@ pda_status run(pda_ctx* ctx, const RunArgs& r) {
     if (!(ctx->maps_valid && mk.k == key.k && mk.v == key.v && mk.num_blocks == key.num_blocks &&
           mk.blk == key.blk && mk.tok == key.tok && mk.kvh == key.kvh)) {
         ctx->maps_valid = false;
-        if (d.block_size >= 8) {
-            st = encode_pool(ctx, r.pool.k, r.pool, &ctx->map_k);
-            if (st != PDA_OK) return st;
-            st = encode_pool(ctx, r.pool.v, r.pool, &ctx->map_v);
-            if (st != PDA_OK) return st;
-            ctx->maps_row_mode = 0;
-        } else {
-            ctx->maps_row_mode = encode_rows(ctx, r.pool.k, r.pool, &ctx->map_k) &&
-                                 encode_rows(ctx, r.pool.v, r.pool, &ctx->map_v) ? 1 : 2;
-        }
+        st = encode_loader(d, r.pool, &ctx->map_k, &ctx->map_v, &ctx->maps_row_mode);
+        if (st != PDA_OK) return st;
         ctx->maps_key = key;
         ctx->maps_valid = true;
     }
@@ -284,16 +330,7 @@ pda_status run(pda_ctx* ctx, const RunArgs& r) {
         p.err = ctx->err;
         p.dbg_k = r.dbg_k ? r.dbg_k + (int64_t)s0 * Hkv * dbg_row_tokens * D : nullptr;
         p.dbg_v = r.dbg_v ? r.dbg_v + (int64_t)s0 * Hkv * dbg_row_tokens * D : nullptr;
-        p.num_blocks = r.pool.num_blocks;
-        p.k_base = r.pool.k;
-        p.v_base = r.pool.v;
-        p.blk_s = r.pool.blk;
-        p.tok_s = r.pool.tok;
-        p.kvh_s = r.pool.kvh;
-        p.row_gather = row_mode;
-        p.row_blk = r.pool.blk / d.head_dim;
-        p.row_tok = r.pool.tok / d.head_dim;
-        p.row_kvh = r.pool.kvh / d.head_dim;
+        set_pool_params(p, d, r.pool, row_mode);
         p.table_stride = r.table_stride;
         p.lens_are_blocks = r.lens_are_blocks;
         p.B = cb;
@@ -448,15 +485,9 @@ PDA_EXPORT pda_status pda_create(const pda_dims* dims, pda_ctx** out_ctx) {
         return fail(PDA_ERR_UNSUPPORTED, "needs %d bytes of shared memory per CTA (device allows %d)",
                     ctx->smem_max, (int)prop.sharedMemPerBlockOptin);
     }
-    for (int mode = 0; mode < pda::kNumModes; ++mode) {
-        e = cudaFuncSetAttribute(pda::split_kernel_fn(D, ctx->stage_rows, mode),
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 ctx->smem_max);
-        if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(pda::split_kernel_fn(D, ctx->stage_rows, mode),
-                                     cudaFuncAttributePreferredSharedMemoryCarveout,
-                                     cudaSharedmemCarveoutMaxShared);
-        if (e != cudaSuccess) { delete ctx; return cuda_fail(e, "cudaFuncSetAttribute"); }
+    if ((st = set_split_attributes(D, ctx->stage_rows, (int)prop.sharedMemPerBlockOptin)) != PDA_OK) {
+        delete ctx;
+        return st;
     }
     int per_sm = 0;
     e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm,
@@ -779,6 +810,34 @@ NoallocDevice g_noalloc_devices[64];
 
 size_t round256(size_t x) { return (x + 255) / 256 * 256; }
 
+// Once per device, with that device current: the scratch's device address,
+// the SM count, and the shared-memory attributes of every split-kernel shape
+// (the same values pda_create sets, so neither lowers the other's).
+pda_status noalloc_setup(int dev, NoallocDevice& nd) {
+    int major = 0, minor = 0, optin = 0;
+    cudaError_t e;
+    if ((e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&nd.num_sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+        return cuda_fail(e, "device attributes");
+    if (major != 10 || minor != 3)
+        return fail(PDA_ERR_NO_DEVICE, "device %d is sm_%d%d; this library is built for sm_103a", dev,
+                    major, minor);
+    if (!tensor_map_encoder()) return fail(PDA_ERR_CUDA, "cuTensorMapEncodeTiled is not available");
+    const int shapes[4][2] = {{64, 64}, {128, 64}, {256, 64}, {256, 32}};
+    for (const auto& sh : shapes) {
+        const pda_status st = set_split_attributes(sh[0], sh[1], optin);
+        if (st != PDA_OK) return st;
+    }
+    void* ptr = nullptr;
+    if ((e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch)) != cudaSuccess)
+        return cuda_fail(e, "cudaGetSymbolAddress(scratch)");
+    nd.scratch = static_cast<unsigned char*>(ptr);
+    nd.ready = true;
+    return PDA_OK;
+}
+
 }  // namespace
 
 PDA_EXPORT pda_status pda_decode_noalloc(const pda_bf16* q, const pda_bf16* k_pool,
@@ -794,11 +853,12 @@ PDA_EXPORT pda_status pda_decode_noalloc(const pda_bf16* q, const pda_bf16* k_po
     const pda_dims dims = {batch > 0 ? batch : 1, num_q_heads, num_kv_heads, head_dim, block_size, 1};
     pda_status st = pda_check_dims(&dims);
     if (st != PDA_OK) return st;
+    if (!device_flags || !aligned(device_flags, 4))
+        return fail(PDA_ERR_INVALID_ARG,
+                    "device_flags must be a non-NULL, 4-byte aligned device word (a call whose "
+                    "kernel gives up or meets a bad block id reports it there)");
     if (batch == 0) return PDA_OK;
-    if (device_flags && !aligned(device_flags, 4))
-        return fail(PDA_ERR_INVALID_ARG, "device_flags must be 4-byte aligned");
 
-    // Scratch need: flags word, block prefix, partial states (m, l) and o.
     const int G = num_q_heads / num_kv_heads, D = head_dim;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -810,35 +870,15 @@ PDA_EXPORT pda_status pda_decode_noalloc(const pda_bf16* q, const pda_bf16* k_po
     {
         std::lock_guard<std::mutex> lock(g_noalloc_mutex);
         NoallocDevice& nd = g_noalloc_devices[dev];
-        if (!nd.ready) {  // once per device, with that device current
-            int major = 0, minor = 0;
-            if ((e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess ||
-                (e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess ||
-                (e = cudaDeviceGetAttribute(&nd.num_sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
-                return cuda_fail(e, "device attributes");
-            if (major != 10 || minor != 3)
-                return fail(PDA_ERR_NO_DEVICE, "device %d is sm_%d%d; this library is built for sm_103a",
-                            dev, major, minor);
-            void* ptr = nullptr;
-            e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
-            if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(scratch)");
-            nd.scratch = static_cast<unsigned char*>(ptr);
-            nd.ready = true;
-        }
+        if (!nd.ready && (st = noalloc_setup(dev, nd)) != PDA_OK) return st;
         scratch = nd.scratch;
         num_sms = nd.num_sms;
     }
 
-    const int rows = pda::stage_tokens(D, block_size);  // split-kernel shape
+    const int rows = pda::stage_tokens(D, block_size);  // split-kernel shape, as pda_create picks it
     const int stages = pda::split_stages(D, rows);
     const size_t smem = pda::smem_layout(D, rows, stages, G, batch).total;
     const void* split_fn = pda::split_kernel_fn(D, rows, pda::kOneShot);
-    // The attribute is per function and device and other contexts may have
-    // set a smaller value, so it is set on every call (no allocation).
-    if ((e = cudaFuncSetAttribute(split_fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) != cudaSuccess ||
-        (e = cudaFuncSetAttribute(split_fn, cudaFuncAttributePreferredSharedMemoryCarveout,
-                                  cudaSharedmemCarveoutMaxShared)) != cudaSuccess)
-        return cuda_fail(e, "cudaFuncSetAttribute");
     int per_sm = 0;
     if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, split_fn, pda::split_threads(rows), smem)) !=
         cudaSuccess)
@@ -846,8 +886,9 @@ PDA_EXPORT pda_status pda_decode_noalloc(const pda_bf16* q, const pda_bf16* k_po
     if (per_sm < 1) return fail(PDA_ERR_UNSUPPORTED, "split kernel does not fit on an SM");
     const int split_ctas = per_sm * num_sms;
 
+    // Scratch: block prefix, partial states (m, l) and o, as a context's workspace.
     const int64_t slots = (int64_t)batch * num_kv_heads + split_ctas;
-    const size_t off_pfx = 256;
+    const size_t off_pfx = 0;
     const size_t off_ml = off_pfx + round256((size_t)(batch + 1) * sizeof(int32_t));
     const size_t off_o = off_ml + round256((size_t)slots * G * 2 * sizeof(float));
     const size_t need = off_o + (size_t)slots * G * D * sizeof(float);
@@ -862,24 +903,20 @@ PDA_EXPORT pda_status pda_decode_noalloc(const pda_bf16* q, const pda_bf16* k_po
     if (!block_table || !seq_lens || !aligned(block_table, 4) || !aligned(seq_lens, 4))
         return fail(PDA_ERR_INVALID_ARG, "block_table / seq_lens must be non-NULL and 4-byte aligned");
     if (max_blocks < 1) return fail(PDA_ERR_INVALID_ARG, "max_blocks must be >= 1");
-    if ((st = check_plan_size(batch, max_blocks, pda::unit_cost_blocks(rows, block_size, false))) != PDA_OK)
-        return st;
+    const int32_t unit_cost = pda::unit_cost_blocks(rows, block_size, false);
+    if ((st = check_plan_size(batch, max_blocks, unit_cost)) != PDA_OK) return st;
     PoolArgs pool = {k_pool, v_pool, num_blocks, (int64_t)block_size * num_kv_heads * head_dim,
                      (int64_t)num_kv_heads * head_dim, (int64_t)head_dim};
-    pda_ctx shape;  // only the dims are read by the helpers below
-    shape.dims = dims;
-    if ((st = check_pool(&shape, pool)) != PDA_OK) return st;
+    if ((st = check_pool(pool)) != PDA_OK) return st;
     float scale_log2 = 0.f;
     if ((st = check_scale(scale, D, &scale_log2)) != PDA_OK) return st;
 
     pda::SplitParams p;
     std::memset(&p, 0, sizeof p);
-    if ((st = encode_pool(&shape, k_pool, pool, &p.tm_k)) != PDA_OK) return st;
-    if ((st = encode_pool(&shape, v_pool, pool, &p.tm_v)) != PDA_OK) return st;
+    int32_t row_mode = 0;
+    if ((st = encode_loader(dims, pool, &p.tm_k, &p.tm_v, &row_mode)) != PDA_OK) return st;
+    set_pool_params(p, dims, pool, row_mode);
     cudaStream_t s = (cudaStream_t)stream;
-    uint32_t* err = device_flags ? device_flags : reinterpret_cast<uint32_t*>(scratch);
-    if (!device_flags && (e = cudaMemsetAsync(err, 0, sizeof(uint32_t), s)) != cudaSuccess)
-        return cuda_fail(e, "clearing the scratch flags");
     p.q = q;
     p.table = block_table;
     p.lens = seq_lens;
@@ -887,15 +924,17 @@ PDA_EXPORT pda_status pda_decode_noalloc(const pda_bf16* q, const pda_bf16* k_po
     p.part_o = reinterpret_cast<float*>(scratch + off_o);
     p.part_ml = reinterpret_cast<float*>(scratch + off_ml);
     p.pfx = reinterpret_cast<int32_t*>(scratch + off_pfx);
-    p.err = err;
-    p.num_blocks = num_blocks;
+    p.err = device_flags;
     p.table_stride = max_blocks;
     p.B = batch;
     p.Hq = num_q_heads;
     p.Hkv = num_kv_heads;
     p.G = G;
     p.bs = block_size;
-    p.unit_cost = pda::unit_cost_blocks(rows, block_size, false);
+    p.q_len = 1;
+    p.qp = 1;
+    p.rows_per_slot = G;
+    p.unit_cost = unit_cost;
     p.scale_log2 = scale_log2;
     if ((e = pda::launch_split(D, rows, pda::kOneShot, p, split_ctas, smem, s)) != cudaSuccess)
         return cuda_fail(e, "split kernel launch");
@@ -910,8 +949,11 @@ PDA_EXPORT pda_status pda_decode_noalloc(const pda_bf16* q, const pda_bf16* k_po
     mp.Hkv = num_kv_heads;
     mp.G = G;
     mp.D = D;
-    mp.unit_cost = p.unit_cost;
+    mp.unit_cost = unit_cost;
     mp.split_ctas = split_ctas;
+    mp.q_len = 1;
+    mp.qp = 1;
+    mp.rows_per_slot = G;
     if ((e = pda::launch_merge(pda::kOneShot, mp, true, s)) != cudaSuccess)
         return cuda_fail(e, "merge kernel launch");
     return PDA_OK;

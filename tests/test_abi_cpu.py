@@ -32,9 +32,9 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_version_and_status_strings(lib):
-    assert lib.pda_abi_version() == 2
+    assert lib.pda_abi_version() == 3
     hdr = open(HEADER).read()
-    assert int(re.search(r"#define PDA_ABI_VERSION (\d+)", hdr).group(1)) == pda.ABI_VERSION == 2
+    assert int(re.search(r"#define PDA_ABI_VERSION (\d+)", hdr).group(1)) == pda.ABI_VERSION == 3
     assert lib.pda_status_string(0) == b"ok"
     assert b"invalid" in lib.pda_status_string(1)
 
@@ -79,3 +79,37 @@ def test_calls_on_null_context_are_rejected(lib):
         pda.ERR_INVALID_ARG
     flags = ctypes.c_uint32()
     assert lib.pda_read_device_errors(None, ctypes.byref(flags), 1, None) == pda.ERR_INVALID_ARG
+
+
+def _noalloc(lib):
+    fn = lib.pda_decode_noalloc
+    P, I32, I64, F = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float
+    fn.restype = I32
+    fn.argtypes = [P, P, P, I64, P, I32, P, I32, I32, I32, I32, I32, F, P, P, P]
+    return fn
+
+
+def test_noalloc_host_checks(lib):
+    """The allocation-free decode refuses, before touching a device, a missing
+    flags word (a failure would otherwise go unreported), unsupported dims and
+    an oversized batch."""
+    fn = _noalloc(lib)
+    buf = ctypes.create_string_buffer(64)
+    addr = ctypes.addressof(buf) + (-ctypes.addressof(buf)) % 16
+    args = dict(q=addr, k=addr, v=addr, nb=1, table=addr, mb=1, lens=addr, batch=1, hq=8, hkv=2,
+                d=128, bs=16, scale=float("nan"), out=addr, flags=addr, stream=None)
+
+    def call(**kw):
+        a = {**args, **kw}
+        return fn(a["q"], a["k"], a["v"], a["nb"], a["table"], a["mb"], a["lens"], a["batch"],
+                  a["hq"], a["hkv"], a["d"], a["bs"], a["scale"], a["out"], a["flags"], a["stream"])
+
+    assert call(flags=None) == pda.ERR_INVALID_ARG
+    assert b"device_flags" in lib.pda_last_error()
+    assert call(flags=addr + 2) == pda.ERR_INVALID_ARG
+    assert call(d=96) == pda.ERR_UNSUPPORTED
+    assert call(bs=3) == pda.ERR_UNSUPPORTED
+    assert call(hkv=3) == pda.ERR_INVALID_ARG
+    assert call(batch=1025) == pda.ERR_INVALID_ARG
+    assert call(batch=-1) == pda.ERR_INVALID_ARG
+    assert call(batch=0) == pda.OK  # nothing to do, nothing launched
