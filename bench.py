@@ -10,12 +10,15 @@ batch (split kernel + merge kernel).  Default workload: the 8B-style batch
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                   [--workload 8b|1b|wide|ragged|tiny] [--block-size BS]
                   [--q-len Q] [--layout paged|contiguous] [--tiles T]
-                  [--no-graph] [--no-e2e] [--no-cpu-baseline] [--quick]
+                  [--no-graph] [--no-e2e] [--no-cpu-baseline] [--no-others] [--quick]
 
 Prints ONE JSON line (rank 0).  ``--impl reference`` times the CPU oracle
 (the fp64 definition) on this host's cores instead of the GPU path.
 ``--q-len`` decodes Q causal queries per sequence, ``--layout contiguous``
 the same cache as [B, S, Hkv, D], ``--tiles`` through the tiled lifecycle.
+The default run (the 8B batch, paged, one query) also times the other four
+named workloads (tiny, 1b, wide, ragged) the same way and adds them to its
+line as ``other_configs``; the headline value stays the 8B batch.
 
 Timing: CUDA events on the launching stream around exactly K back-to-back
 calls after W warm-up calls; inputs are larger than L2 and rotate between
@@ -70,6 +73,9 @@ def parse_args():
                          "them from a CUDA graph")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-others", action="store_true",
+                    help="skip timing the other named workloads (tiny, 1b, wide, ragged) that "
+                         "the default run adds to its line as other_configs")
     ap.add_argument("--quick", action="store_true",
                     help="only the W + K calls: no clock padding, kernel-timing pass, e2e or "
                          "CPU baseline (for profiler captures)")
@@ -265,6 +271,97 @@ def run_reference(args):
             "e2e": {"value": cb["value"], "unit": "GB/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
+
+
+OTHER_CONFIGS = ("tiny", "1b", "wide", "ragged")
+
+
+def time_other_config(name: str, dev, steps: int, warmup: int, peak: float):
+    """One of the other named decode workloads at its own shape, timed like the
+    headline: calls replayed from a CUDA graph with inputs larger than L2
+    rotated between copies, the split kernel alone with CUDA events around it,
+    and the L2-warm figure where the inputs fit in L2."""
+    import numpy as np
+    import torch
+
+    import paged_gqa_decode_05_gb300 as pda
+    from paged_gqa_decode_05_gb300 import workloads
+
+    w = workloads.WORKLOADS[name]()
+    nbytes = w.algorithmic_bytes()
+    l2 = int(getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 129 * 2 ** 20))
+    input_bytes = w.q.nbytes + w.k_pool.nbytes + w.v_pool.nbytes + w.block_table.nbytes + \
+        w.seq_lens.nbytes
+    n_sets = max(2, math.ceil(3 * l2 / max(input_bytes, 1)))
+
+    def to_dev(a):
+        if a.dtype == np.uint16:
+            return torch.from_numpy(a.view(np.int16)).to(dev).view(torch.bfloat16)
+        return torch.from_numpy(a).to(dev)
+
+    host = {"q": w.q, "k_pool": w.k_pool, "v_pool": w.v_pool, "block_table": w.block_table,
+            "seq_lens": w.seq_lens}
+    sets = [{k: to_dev(v) for k, v in host.items()} for _ in range(n_sets)]
+    outs = [torch.empty(tuple(sets[0]["q"].shape), device=dev, dtype=torch.bfloat16)
+            for _ in range(n_sets)]
+    ctx = pda.Context(max_seqs=w.B, num_q_heads=w.Hq, num_kv_heads=w.Hkv, head_dim=w.D,
+                      block_size=w.block_size)
+    stream = torch.cuda.current_stream()
+    counter = [0]
+
+    def step(s=None, o=None):
+        if s is None:
+            i = counter[0]
+            counter[0] += 1
+            s, o = sets[i % n_sets], outs[i % n_sets]
+        ctx.decode(s["q"], s["k_pool"], s["v_pool"], s["block_table"], s["seq_lens"], out=o)
+
+    def graph_us(fn):
+        for _ in range(max(3, warmup)):
+            fn()
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        cap = torch.cuda.Stream(device=dev)
+        cap.wait_stream(stream)
+        with torch.cuda.stream(cap):
+            with torch.cuda.graph(g, stream=cap):
+                for _ in range(steps):
+                    fn()
+        stream.wait_stream(cap)
+        g.replay()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        g.replay()
+        b.record(stream)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) * 1e3 / steps
+
+    us = graph_us(step)
+    evs = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(3)) for _ in range(steps)]
+    for k in range(steps):
+        for e in evs[k]:
+            e.record(stream)
+        ctx.set_timing_events(*evs[k])
+        step()
+    ctx.set_timing_events(None, None, None)
+    torch.cuda.synchronize()
+    split_us = statistics.mean(a.elapsed_time(b) for a, b, _ in evs) * 1e3
+    if ctx.read_device_errors() != 0:
+        raise RuntimeError(f"device error flags set while timing {name}")
+    r = {"workload": w.name, "algorithmic_bytes_per_call": nbytes, "us_per_call": us,
+         "GB/s": nbytes / (us * 1e-6) / 1e9, "frac": nbytes / (us * 1e-6) / 1e9 / peak,
+         "split_us": split_us, "split_GB/s": nbytes / (split_us * 1e-6) / 1e9,
+         "split_frac": nbytes / (split_us * 1e-6) / 1e9 / peak, "steps": steps,
+         "l2": f"{n_sets} input sets of {input_bytes / 1e6:.1f} MB rotated"}
+    if input_bytes < l2 // 2:
+        warm_us = graph_us(lambda: step(sets[0], outs[0]))
+        r["l2_warm"] = {"us_per_call": warm_us, "GB/s": nbytes / (warm_us * 1e-6) / 1e9,
+                        "note": "one input set reused every call (labelled; not the metric)"}
+    ctx.close()
+    del sets, outs
+    torch.cuda.empty_cache()
+    return r
 
 
 def run_ours(args):
@@ -575,7 +672,11 @@ def run_ours(args):
                                  if (args.block_size == 0 and args.layout == "paged"
                                      and args.q_len == 1 and args.tiles == 0) else None),
                      "split_us": None if math.isnan(split_avg) else split_avg * 1e3,
-                     "merge_us": None if math.isnan(merge_avg) else merge_avg * 1e3},
+                     "merge_us": None if math.isnan(merge_avg) else merge_avg * 1e3,
+                     "timing": ("split kernel timed alone: CUDA events recorded on its stream "
+                                "before and after it in every call, which also stops the "
+                                "merge kernel's early launch, so split_us is an isolated-kernel "
+                                "time (an upper bound of its share of a graph-replayed call)")},
         "gpu_launches": (2 + 2 * args.tiles if args.tiles > 0 else 2) * args.steps,
         "clocks": clocks,
     }
@@ -585,6 +686,12 @@ def run_ours(args):
         line["l2_warm"] = l2_warm
     if e2e is not None:
         line["e2e"] = e2e
+    default_config = (args.workload == "8b" and args.block_size == 0 and args.q_len == 1
+                      and args.tiles == 0 and args.layout == "paged")
+    if rank == 0 and not (args.quick or args.no_others) and default_config:
+        line["other_configs"] = {name: time_other_config(name, dev, max(10, min(args.steps, 50)),
+                                                         args.warmup, peak)
+                                 for name in OTHER_CONFIGS}
     if rank == 0 and world == 1 and not (args.no_cpu_baseline or args.quick):
         cb = cpu_oracle_timing(w)
         line["cpu_baseline"] = {k: cb[k] for k in ("value", "unit", "cores", "kind", "sample",
