@@ -4,8 +4,9 @@
 Metric: paged decode attention microseconds per call and achieved HBM GB/s
 (K + V + q + out bytes over the call's time) as a fraction of the measured
 HBM peak, on one GPU.  One "step" is one ``pda_decode`` call over the whole
-batch (split kernel + merge kernel).  Default workload: the 8B-style batch
-(B=32, Hq=32, Hkv=8, D=128, block 16, 4096 tokens each; 537 MB moved per call).
+batch (one kernel launch: the split pieces of a unit merge inside it).
+Default workload: the 8B-style batch (B=32, Hq=32, Hkv=8, D=128, block 16,
+4096 tokens each; 537 MB moved per call).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                   [--workload 8b|1b|wide|ragged|tiny] [--block-size BS]
@@ -25,9 +26,8 @@ calls after W warm-up calls; inputs are larger than L2 and rotate between
 copies at distinct addresses.  The K calls are captured once in a CUDA graph
 and replayed (the host's per-call launch cost would otherwise bound the small
 workloads); the same calls launched one by one are timed too (``loop``).  A
-second pass records events between the two kernels of each call (which
-disables the merge kernel's early launch) to time the split kernel alone for
-the roofline.  ``e2e`` repeats the calls with the inputs copied from pinned
+second pass records events around the kernel of each call (which stops the
+next call's early launch) to time the kernel alone for the roofline.  ``e2e`` repeats the calls with the inputs copied from pinned
 host memory and the output copied back every step.
 """
 from __future__ import annotations
@@ -108,7 +108,7 @@ def peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-# The files the split and merge kernels are compiled from (host-only files
+# The files the decode kernels are compiled from (host-only files
 # such as pda_api.cu do not change the kernels' traffic).
 KERNEL_SOURCES = ("pda_kernels.cuh", "pda_ptx.cuh", "pda_params.h", "pda_plan.h",
                   "pda_kernels_d64.cu", "pda_kernels_d128.cu", "pda_kernels_d256.cu")
@@ -520,7 +520,7 @@ def run_ours(args):
 
     ms_step = max_over_ranks(ms_total / args.steps, dev)
 
-    # --- kernel timing pass: events between the split and merge kernels
+    # --- kernel timing pass: events around the split kernel of each call
     # (one-shot calls only; a tiled step is timed as a whole)
     n_timed = 0 if (args.quick or args.tiles > 0) else args.steps
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
@@ -535,9 +535,7 @@ def run_ours(args):
     ctx.set_timing_events(None, None, None)
     torch.cuda.synchronize()
     split_ms = [a.elapsed_time(b) for a, b, _ in evs]
-    merge_ms = [b.elapsed_time(c) for _, b, c in evs]
     split_avg = statistics.mean(split_ms) if split_ms else float("nan")
-    merge_avg = statistics.mean(merge_ms) if merge_ms else float("nan")
     if ctx.read_device_errors() != 0:
         raise RuntimeError("device error flags set during timing")
 
@@ -631,7 +629,7 @@ def run_ours(args):
     peak, peak_kind = peaks()
     value = world * bytes_per_call / (ms_step * 1e-3) / 1e9
     if args.tiles > 0 or args.quick:  # no split-kernel events: the whole call
-        split_avg = merge_avg = float("nan")
+        split_avg = float("nan")
         achieved = bytes_per_call / (ms_step * 1e-3) / 1e9
     else:
         achieved = bytes_per_call / (split_avg * 1e-3) / 1e9
@@ -672,12 +670,12 @@ def run_ours(args):
                                  if (args.block_size == 0 and args.layout == "paged"
                                      and args.q_len == 1 and args.tiles == 0) else None),
                      "split_us": None if math.isnan(split_avg) else split_avg * 1e3,
-                     "merge_us": None if math.isnan(merge_avg) else merge_avg * 1e3,
                      "timing": ("split kernel timed alone: CUDA events recorded on its stream "
-                                "before and after it in every call, which also stops the "
-                                "merge kernel's early launch, so split_us is an isolated-kernel "
-                                "time (an upper bound of its share of a graph-replayed call)")},
-        "gpu_launches": (2 + 2 * args.tiles if args.tiles > 0 else 2) * args.steps,
+                                "before and after it in every call, which also stops the next "
+                                "call's early launch, so split_us is an isolated-kernel time "
+                                "(an upper bound of its share of a graph-replayed call)")},
+        # one split kernel per call; a tiled step: reset, one split kernel per tile, finalize
+        "gpu_launches": (2 + args.tiles if args.tiles > 0 else 1) * args.steps,
         "clocks": clocks,
     }
     if per_call is not None:

@@ -314,7 +314,10 @@ pda_status pda_debug_gather(pda_ctx* ctx, const pda_bf16* k_pool, const pda_bf16
 /*
  * Reads (and with clear != 0 resets) the device error flags of this context
  * (PDA_DEVERR_* bits).  Synchronises `stream`.  Returns PDA_ERR_DEVICE_DATA
- * when any flag was set, PDA_OK otherwise.
+ * when any flag was set, PDA_OK otherwise.  Clearing also zeroes the
+ * counters through which the pieces of a split unit find the one that merges
+ * them: a kernel that gave up (PDA_DEVERR_TIMEOUT) may leave them behind, and
+ * later calls are valid again only after a clearing read.
  */
 pda_status pda_read_device_errors(pda_ctx* ctx, uint32_t* flags, int32_t clear,
                                   pda_stream stream);
@@ -331,10 +334,11 @@ pda_status pda_check_wait_timeout(pda_ctx* ctx, int64_t limit_ns, pda_stream str
 
 /*
  * Timing hook: when the three events (cudaEvent_t) are non-NULL, every later
- * one-shot decode records ev_begin before its split kernel, ev_split after it
- * and ev_end after the merge kernel, on the call's stream; NULLs turn it off.
- * Recording an event between the kernels stops the merge kernel's early
- * (programmatic) launch, so timed calls measure each kernel on its own.
+ * one-shot decode records ev_begin before its kernel and ev_split and ev_end
+ * after it (a decode is one kernel launch: the split pieces of a unit merge
+ * inside it), on the call's stream; NULLs turn it off.  The events between
+ * calls stop the next call's early (programmatic) launch, so timed calls are
+ * measured on their own.
  */
 pda_status pda_set_timing_events(pda_ctx* ctx, void* ev_begin, void* ev_split, void* ev_end);
 

@@ -77,7 +77,8 @@ struct pda_ctx {
     int64_t slots = 0;
     float* part_o = nullptr;
     float* part_ml = nullptr;
-    int32_t* pfx = nullptr;
+    int32_t* unit_sync = nullptr;  // [chunk_b*Hkv][2] split-unit tickets and stored counts
+    int64_t unit_sync_bytes = 0;
     uint32_t* err = nullptr;
     float* m_state = nullptr;
     float* l_state = nullptr;
@@ -326,7 +327,10 @@ pda_status run(pda_ctx* ctx, const RunArgs& r) {
         p.out_f32 = r.out_f32 ? r.out_f32 + (int64_t)s0 * r.q_len * Hq * D : nullptr;
         p.part_o = ctx->part_o;
         p.part_ml = ctx->part_ml;
-        p.pfx = ctx->pfx;
+        p.unit_sync = ctx->unit_sync;
+        p.m_state = ctx->m_state + (int64_t)s0 * Hq;  // tiled path (q_len 1)
+        p.l_state = ctx->l_state + (int64_t)s0 * Hq;
+        p.o_state = ctx->o_state + (int64_t)s0 * Hq * D;
         p.err = ctx->err;
         p.dbg_k = r.dbg_k ? r.dbg_k + (int64_t)s0 * Hkv * dbg_row_tokens * D : nullptr;
         p.dbg_v = r.dbg_v ? r.dbg_v + (int64_t)s0 * Hkv * dbg_row_tokens * D : nullptr;
@@ -349,31 +353,8 @@ pda_status run(pda_ctx* ctx, const RunArgs& r) {
         e = pda::launch_split(D, ctx->stage_rows, r.mode, p, ctx->split_ctas, smem, r.stream);
         if (e != cudaSuccess) return cuda_fail(e, "split kernel launch");
         if (r.mode == pda::kGather) continue;
-        if (timing && (e = cudaEventRecord(ctx->ev_split, r.stream)) != cudaSuccess)
-            return cuda_fail(e, "cudaEventRecord");
-        pda::MergeParams mp;
-        std::memset(&mp, 0, sizeof mp);
-        mp.part_o = ctx->part_o;
-        mp.part_ml = ctx->part_ml;
-        mp.pfx = ctx->pfx;
-        mp.out = p.out;
-        mp.out_f32 = p.out_f32;
-        mp.m_state = ctx->m_state + (int64_t)s0 * Hq;  // tiled path (q_len 1)
-        mp.l_state = ctx->l_state + (int64_t)s0 * Hq;
-        mp.o_state = ctx->o_state + (int64_t)s0 * Hq * D;
-        mp.B = cb;
-        mp.Hq = Hq;
-        mp.Hkv = Hkv;
-        mp.G = ctx->G;
-        mp.D = D;
-        mp.unit_cost = p.unit_cost;
-        mp.split_ctas = ctx->split_ctas;
-        mp.q_len = r.q_len;
-        mp.qp = qp;
-        mp.rows_per_slot = qp * ctx->G;
-        e = pda::launch_merge(r.mode, mp, !timing, r.stream);
-        if (e != cudaSuccess) return cuda_fail(e, "merge kernel launch");
-        if (timing && (e = cudaEventRecord(ctx->ev_end, r.stream)) != cudaSuccess)
+        if (timing && ((e = cudaEventRecord(ctx->ev_split, r.stream)) != cudaSuccess ||
+                       (e = cudaEventRecord(ctx->ev_end, r.stream)) != cudaSuccess))
             return cuda_fail(e, "cudaEventRecord");
     }
     return PDA_OK;
@@ -446,7 +427,7 @@ PDA_EXPORT void pda_destroy(pda_ctx* ctx) {
     cudaDeviceSynchronize();
     cudaFree(ctx->part_o);
     cudaFree(ctx->part_ml);
-    cudaFree(ctx->pfx);
+    cudaFree(ctx->unit_sync);
     cudaFree(ctx->err);
     cudaFree(ctx->m_state);
     cudaFree(ctx->l_state);
@@ -504,7 +485,7 @@ PDA_EXPORT pda_status pda_create(const pda_dims* dims, pda_ctx** out_ctx) {
         // partial states: up to kMaxGroup q rows per slot (packed multi-query rows)
         {(void**)&ctx->part_o, (size_t)ctx->slots * pda::kMaxGroup * D * sizeof(float)},
         {(void**)&ctx->part_ml, (size_t)ctx->slots * pda::kMaxGroup * 2 * sizeof(float)},
-        {(void**)&ctx->pfx, (size_t)(pda::kMaxLaunchBatch + 1) * sizeof(int32_t)},
+        {(void**)&ctx->unit_sync, (size_t)chunk_b * dims->num_kv_heads * 2 * sizeof(int32_t)},
         {(void**)&ctx->err, sizeof(uint32_t)},
         {(void**)&ctx->m_state, (size_t)nq * sizeof(float)},
         {(void**)&ctx->l_state, (size_t)nq * sizeof(float)},
@@ -514,7 +495,9 @@ PDA_EXPORT pda_status pda_create(const pda_dims* dims, pda_ctx** out_ctx) {
         e = cudaMalloc(a.ptr, a.bytes);
         if (e != cudaSuccess) { pda_destroy(ctx); return cuda_fail(e, "cudaMalloc"); }
     }
-    if ((e = cudaMemset(ctx->err, 0, sizeof(uint32_t))) != cudaSuccess) {
+    ctx->unit_sync_bytes = (int64_t)chunk_b * dims->num_kv_heads * 2 * sizeof(int32_t);
+    if ((e = cudaMemset(ctx->err, 0, sizeof(uint32_t))) != cudaSuccess ||
+        (e = cudaMemset(ctx->unit_sync, 0, (size_t)ctx->unit_sync_bytes)) != cudaSuccess) {
         pda_destroy(ctx);
         return cuda_fail(e, "cudaMemset");
     }
@@ -682,7 +665,9 @@ PDA_EXPORT pda_status pda_read_device_errors(pda_ctx* ctx, uint32_t* flags, int3
     cudaError_t e = cudaMemcpyAsync(&v, ctx->err, sizeof v, cudaMemcpyDeviceToHost, s);
     if (e == cudaSuccess) e = cudaStreamSynchronize(s);
     if (e == cudaSuccess && clear) {
+        // a launch that gave up may have left split-unit counters behind
         e = cudaMemsetAsync(ctx->err, 0, sizeof(uint32_t), s);
+        if (e == cudaSuccess) e = cudaMemsetAsync(ctx->unit_sync, 0, (size_t)ctx->unit_sync_bytes, s);
         if (e == cudaSuccess) e = cudaStreamSynchronize(s);
     }
     if (e != cudaSuccess) return cuda_fail(e, "reading device error flags");
@@ -886,10 +871,11 @@ PDA_EXPORT pda_status pda_decode_noalloc(const pda_bf16* q, const pda_bf16* k_po
     if (per_sm < 1) return fail(PDA_ERR_UNSUPPORTED, "split kernel does not fit on an SM");
     const int split_ctas = per_sm * num_sms;
 
-    // Scratch: block prefix, partial states (m, l) and o, as a context's workspace.
+    // Scratch: split-unit counters, partial states (m, l) and o, as a context's workspace.
     const int64_t slots = (int64_t)batch * num_kv_heads + split_ctas;
-    const size_t off_pfx = 0;
-    const size_t off_ml = off_pfx + round256((size_t)(batch + 1) * sizeof(int32_t));
+    const size_t off_sync = 0;
+    const size_t sync_bytes = (size_t)batch * num_kv_heads * 2 * sizeof(int32_t);
+    const size_t off_ml = off_sync + round256(sync_bytes);
     const size_t off_o = off_ml + round256((size_t)slots * G * 2 * sizeof(float));
     const size_t need = off_o + (size_t)slots * G * D * sizeof(float);
     if (need > PDA_NOALLOC_SCRATCH_BYTES)
@@ -923,7 +909,7 @@ PDA_EXPORT pda_status pda_decode_noalloc(const pda_bf16* q, const pda_bf16* k_po
     p.out = out;
     p.part_o = reinterpret_cast<float*>(scratch + off_o);
     p.part_ml = reinterpret_cast<float*>(scratch + off_ml);
-    p.pfx = reinterpret_cast<int32_t*>(scratch + off_pfx);
+    p.unit_sync = reinterpret_cast<int32_t*>(scratch + off_sync);
     p.err = device_flags;
     p.table_stride = max_blocks;
     p.B = batch;
@@ -936,25 +922,10 @@ PDA_EXPORT pda_status pda_decode_noalloc(const pda_bf16* q, const pda_bf16* k_po
     p.rows_per_slot = G;
     p.unit_cost = unit_cost;
     p.scale_log2 = scale_log2;
+    // The counters start at zero (a launch that gave up may have left some behind).
+    if ((e = cudaMemsetAsync(scratch + off_sync, 0, sync_bytes, s)) != cudaSuccess)
+        return cuda_fail(e, "clearing the scratch counters");
     if ((e = pda::launch_split(D, rows, pda::kOneShot, p, split_ctas, smem, s)) != cudaSuccess)
         return cuda_fail(e, "split kernel launch");
-    pda::MergeParams mp;
-    std::memset(&mp, 0, sizeof mp);
-    mp.part_o = p.part_o;
-    mp.part_ml = p.part_ml;
-    mp.pfx = p.pfx;
-    mp.out = out;
-    mp.B = batch;
-    mp.Hq = num_q_heads;
-    mp.Hkv = num_kv_heads;
-    mp.G = G;
-    mp.D = D;
-    mp.unit_cost = unit_cost;
-    mp.split_ctas = split_ctas;
-    mp.q_len = 1;
-    mp.qp = 1;
-    mp.rows_per_slot = G;
-    if ((e = pda::launch_merge(pda::kOneShot, mp, true, s)) != cudaSuccess)
-        return cuda_fail(e, "merge kernel launch");
     return PDA_OK;
 }

@@ -17,9 +17,10 @@
 //     O^T += V^T P^T accumulates over D in 16-row slabs.
 //   * at the end of a segment the consumer warps' states are merged in shared
 //     memory; a segment that covers its whole unit writes bf16 o / l
-//     directly, others write an fp32 partial (m, l, o) state.
-// Merge kernel: combines the partial states of every unit split across CTAs
-// and writes o / l (one-shot), or folds them into the running state (tiled).
+//     directly (or folds its state into the running state, in tiled steps).
+//     The pieces of a unit split across CTAs draw tickets: all but the last
+//     store an fp32 partial (m, l, o) state and signal it; the last merges
+//     them with its own and writes o / l (or folds).  One launch per call.
 //
 // Method sources: tiled_attention.rs (spark_storage) for the (m, l, o) state,
 // its reset values and o / l finalize; AstrAI "CUDA Kernels" (Overview:
@@ -590,9 +591,27 @@ __device__ __forceinline__ bool consumer_sync(uint32_t cbar, uint32_t& cphase, u
     return ok;
 }
 
+// Combines a partial state (mi, li, oi) into (M, Ls, Os).
+__device__ __forceinline__ void merge_state(float& M, float& Ls, float4& Os, float mi, float li,
+                                            const float4& oi) {
+    const float Mn = fmaxf(M, mi);
+    if (Mn == kNegInf) return;  // both states empty
+    const float fa = ex2(M - Mn), fb = ex2(mi - Mn);
+    Ls = Ls * fa + li * fb;
+    Os.x = Os.x * fa + oi.x * fb;
+    Os.y = Os.y * fa + oi.y * fb;
+    Os.z = Os.z * fa + oi.z * fb;
+    Os.w = Os.w * fa + oi.w * fb;
+    M = Mn;
+}
+
+// Segment-end roles (see the epilogue in run_consumer).
+enum SegRole : int32_t { kRoleWhole = 0, kRoleStore = 1, kRoleMerge = 2, kRoleAbort = -1 };
+
 template <int D, int ST, int MODE>
 __device__ __forceinline__ void run_consumer(const SplitParams& p, uint32_t base_s, uint8_t* base,
                                              const SmemLayout& L, const StageMeta* meta,
+                                             const int32_t* pfx, const GroupRange& gr,
                                              volatile int* abort_flag, int warp, int lane) {
     using C = Cfg<D, ST>;
     constexpr int S = C::kStages;
@@ -631,6 +650,28 @@ __device__ __forceinline__ void run_consumer(const SplitParams& p, uint32_t base
     uint32_t cphase = 0;
     int stage = 0;
     uint32_t phase = 0;
+    int32_t ticket = 0;  // consumer thread 0: this piece's ticket for its split unit
+
+    if constexpr (writes_output(MODE)) {
+        // A unit with no tokens has no segment: its output rows are zero.  Such
+        // units are shared round-robin over the grid; the stores overlap the
+        // wait for the first stage.
+        const int ct = warp * 32 + lane;
+        for (int u = blockIdx.x; u < p.B * p.Hkv; u += gridDim.x) {
+            const int sq = u / p.Hkv, kvh = u - sq * p.Hkv;
+            if (pfx[sq + 1] != pfx[sq]) continue;
+            const RowInfo ri = row_info<MQ>(p, sq);
+            const int NR = ri.cnt * G;
+            for (int i4 = ct; i4 < NR * D / 4; i4 += C::kConsumerWarps * 32) {
+                const int h = (4 * i4) / D, d4 = 4 * i4 - h * D;
+                const int64_t o = MQ ? qo_offset<MQ>(p, ri.b, ri.first + h / G, kvh * G + h % G, D) + d4
+                                     : qo_offset<MQ>(p, sq, 0, kvh * G, D) + 4 * i4;
+                if (p.out_f32) *reinterpret_cast<float4*>(p.out_f32 + o) = make_float4(0.f, 0.f, 0.f, 0.f);
+                else *reinterpret_cast<uint2*>(p.out + o) = make_uint2(0u, 0u);
+            }
+        }
+    }
+
     while (true) {
         if (*abort_flag) break;
         if (!mbar_wait_bounded(full0 + 8 * stage, phase, kWaitLimitNs)) {
@@ -640,6 +681,11 @@ __device__ __forceinline__ void run_consumer(const SplitParams& p, uint32_t base
         }
         const StageMeta m = meta[stage];
         if (m.flags & kDone) break;
+        // The last stage of a piece of a split unit: take the piece's ticket now, so
+        // that the atomic's round trip overlaps this stage's math.  Tickets only
+        // assign roles: the piece that draws the last one merges all pieces.
+        if (MODE != kGather && warp == 0 && lane == 0 && (m.flags & kSegEnd) && !(m.flags & kWholeUnit))
+            ticket = atomicAdd(p.unit_sync + 2 * (m.b * p.Hkv + m.kvh), 1);
         const uint32_t sK = base_s + (uint32_t)stage * C::kStageBytes;
         const uint32_t sV = sK + C::kTileBytes;
 
@@ -747,11 +793,25 @@ __device__ __forceinline__ void run_consumer(const SplitParams& p, uint32_t base
             }
         }
         if (MODE != kGather && (m.flags & kSegEnd)) {
-            // ---- merge the consumer warps' states of this segment.  The o tiles are
-            // staged in this stage's own K/V memory (the stage is released only
-            // after the merge), which keeps shared memory for deeper rings.
+            // ---- segment end.  The consumer warps' states merge through this
+            // stage's own K/V memory (the stage is released only afterwards).
+            // Then, by role:
+            //   whole unit (the unit lies in this CTA): write o / l, or fold the
+            //     state into the running state (tiled steps);
+            //   piece of a split unit that did not draw the last ticket: store
+            //     the partial (m, l, o) in slot u + blockIdx.x and signal it with
+            //     a release increment of the unit's stored count;
+            //   piece that drew the last ticket: wait (bounded) until the other
+            //     pieces' partials are stored, merge them with its own state,
+            //     write o / l (or fold), and zero the unit's counters for the
+            //     next launch.
+            // The last-ticket piece only waits for pieces that have already
+            // drawn their tickets, i.e. are running towards their own store, so
+            // the wait cannot deadlock whichever CTAs are resident.
             float* st_m = reinterpret_cast<float*>(base + L.st_m);
             float* st_l = reinterpret_cast<float*>(base + L.st_l);
+            float* st_x = reinterpret_cast<float*>(base + L.st_x);  // old running m [8], l [8]
+            int32_t* st_role = reinterpret_cast<int32_t*>(st_x + 2 * kMaxGroup);
             float* st_o = reinterpret_cast<float*>(base + (sK - base_s));
 #pragma unroll
             for (int off = 4; off < 32; off <<= 1) {
@@ -779,40 +839,136 @@ __device__ __forceinline__ void run_consumer(const SplitParams& p, uint32_t base
                     r[d + 8] = o[mt][3];
                 }
             }
-            if (!consumer_sync(cbar, cphase, p.err, abort_flag)) break;
+            const bool whole = (m.flags & kWholeUnit) != 0;
+            const int u = m.b * p.Hkv + m.kvh;
+            UnitPieces pc;
+            pc.cf = 0; pc.su = 0; pc.n = 1; pc.every = true;
+            if (!whole) pc = unit_pieces(pfx, m.b, m.kvh, p.Hkv, p.unit_cost, gr);
             const int ct = warp * 32 + lane;
-            const bool direct = writes_output(MODE) && (m.flags & kWholeUnit);
+            if constexpr (MODE == kTiled) {
+                // the running state's (m, l) of the unit's rows, read before any is rewritten
+                if (ct < NR) {
+                    const int64_t row = (int64_t)m.b * p.Hq + (int64_t)m.kvh * G + ct;
+                    st_x[ct] = p.m_state[row];
+                    st_x[kMaxGroup + ct] = p.l_state[row];
+                }
+            }
+            if (ct == 0) {
+                int32_t role = whole ? kRoleWhole : ticket == pc.n - 1 ? kRoleMerge : kRoleStore;
+                if (role == kRoleMerge) {
+                    int32_t* cnt = p.unit_sync + 2 * u;
+                    bool ready = ld_acquire_gpu(cnt + 1) == pc.n - 1;
+                    if (!ready) {
+                        const uint64_t t0 = global_ns();
+                        while (!(ready = ld_acquire_gpu(cnt + 1) == pc.n - 1) && global_ns() - t0 <= kWaitLimitNs) {
+                        }
+                    }
+                    if (ready) {
+                        cnt[0] = 0;  // every piece has drawn and stored: reset for the next launch
+                        cnt[1] = 0;
+                    } else {
+                        atomicOr(p.err, PDA_DEVERR_TIMEOUT_);
+                        *abort_flag = 1;
+                        role = kRoleAbort;
+                    }
+                }
+                *st_role = role;
+            }
+            if (!consumer_sync(cbar, cphase, p.err, abort_flag)) break;
+            const int role = *st_role;
+            if (role == kRoleAbort) break;
             const RowInfo ri = row_info<MQ>(p, m.b);
             const int SR = MQ ? p.rows_per_slot : G;  // rows per partial slot
-            for (int idx = ct; idx < NR * D; idx += C::kConsumerWarps * 32) {
-                const int h = idx / D, d = idx - h * D;  // h: q row of the unit
+            for (int i4 = ct; i4 < NR * D / 4; i4 += C::kConsumerWarps * 32) {
+                const int h = (4 * i4) / D, d4 = 4 * i4 - h * D;  // h: q row of the unit
                 float M = kNegInf;
 #pragma unroll
                 for (int w = 0; w < C::kConsumerWarps; ++w) M = fmaxf(M, st_m[w * kMaxGroup + h]);
-                float Ls = 0.f, Os = 0.f;
+                float Ls = 0.f;
+                float4 Os = make_float4(0.f, 0.f, 0.f, 0.f);
                 if (M != kNegInf) {
 #pragma unroll
                     for (int w = 0; w < C::kConsumerWarps; ++w) {
                         const float f = ex2(st_m[w * kMaxGroup + h] - M);
+                        const float4 v = *reinterpret_cast<const float4*>(st_o + (size_t)(w * NR + h) * (D + 4) + d4);
                         Ls += st_l[w * kMaxGroup + h] * f;
-                        Os += st_o[(size_t)(w * NR + h) * (D + 4) + d] * f;
+                        Os.x += v.x * f; Os.y += v.y * f; Os.z += v.z * f; Os.w += v.w * f;
                     }
                 }
-                if (direct) {
-                    const float r = Ls > 0.f ? Os / Ls : 0.f;
-                    const int64_t o = MQ ? qo_offset<MQ>(p, ri.b, ri.first + h / G, m.kvh * G + h % G, D) + d
-                                         : qo_offset<MQ>(p, m.b, 0, m.kvh * G, D) + idx;
-                    if (p.out_f32) p.out_f32[o] = r;
-                    else p.out[o] = __bfloat16_as_ushort(__float2bfloat16_rn(r));
+                if (role == kRoleStore) {
+                    const int64_t r = (int64_t)(u + (int)blockIdx.x) * SR + h;
+                    *reinterpret_cast<float4*>(p.part_o + r * D + d4) = Os;
+                    if (d4 == 0) {
+                        p.part_ml[r * 2] = M;
+                        p.part_ml[r * 2 + 1] = Ls;
+                    }
+                    continue;
+                }
+                if (role == kRoleMerge) {
+                    // every piece in piece order (this piece's own state in its
+                    // place), so the result does not depend on which piece
+                    // finished last; the others' partials are loaded up to eight
+                    // per memory round trip
+                    float Mr = kNegInf, Lr = 0.f;
+                    float4 Or = make_float4(0.f, 0.f, 0.f, 0.f);
+                    for (int i0 = 0; i0 < pc.n; i0 += 8) {
+                        float mi[8], li[8];
+                        float4 oi[8];
+                        bool own[8];
+#pragma unroll
+                        for (int k = 0; k < 8; ++k) {
+                            mi[k] = kNegInf;
+                            li[k] = 0.f;
+                            oi[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+                            const int64_t c = piece_cta(pc, i0 + k, gr);
+                            own[k] = i0 + k < pc.n && c == (int64_t)blockIdx.x;
+                            if (i0 + k >= pc.n || own[k]) continue;
+                            const int64_t r = (u + c) * SR + h;
+                            mi[k] = ld_cg(p.part_ml + r * 2);
+                            li[k] = ld_cg(p.part_ml + r * 2 + 1);
+                            oi[k] = __ldcg(reinterpret_cast<const float4*>(p.part_o + r * D + d4));
+                        }
+#pragma unroll
+                        for (int k = 0; k < 8; ++k) {
+                            if (own[k]) merge_state(Mr, Lr, Or, M, Ls, Os);
+                            else merge_state(Mr, Lr, Or, mi[k], li[k], oi[k]);
+                        }
+                    }
+                    M = Mr;
+                    Ls = Lr;
+                    Os = Or;
+                }
+                if constexpr (MODE == kTiled) {
+                    // fold into the running state (plain decode rows: b*Hq + kvh*G + h)
+                    const int64_t row = (int64_t)m.b * p.Hq + (int64_t)m.kvh * G + h;
+                    float Mo = st_x[h], Lo = st_x[kMaxGroup + h];
+                    float4* so = reinterpret_cast<float4*>(p.o_state + row * D + d4);
+                    float4 Oo = *so;
+                    merge_state(Mo, Lo, Oo, M, Ls, Os);
+                    *so = Oo;
+                    if (d4 == 0) {
+                        p.m_state[row] = Mo;
+                        p.l_state[row] = Lo;
+                    }
                 } else {
-                    p.part_o[((int64_t)m.slot * SR + h) * D + d] = Os;
-                    if (d == 0) {
-                        p.part_ml[((int64_t)m.slot * SR + h) * 2] = M;
-                        p.part_ml[((int64_t)m.slot * SR + h) * 2 + 1] = Ls;
+                    const float4 v = Ls > 0.f ? make_float4(Os.x / Ls, Os.y / Ls, Os.z / Ls, Os.w / Ls)
+                                              : make_float4(0.f, 0.f, 0.f, 0.f);
+                    const int64_t o = MQ ? qo_offset<MQ>(p, ri.b, ri.first + h / G, m.kvh * G + h % G, D) + d4
+                                         : qo_offset<MQ>(p, m.b, 0, m.kvh * G, D) + 4 * i4;
+                    if (p.out_f32) {
+                        *reinterpret_cast<float4*>(p.out_f32 + o) = v;
+                    } else {
+                        uint2 w2;
+                        w2.x = pack_bf16x2(v.x, v.y);
+                        w2.y = pack_bf16x2(v.z, v.w);
+                        *reinterpret_cast<uint2*>(p.out + o) = w2;
                     }
                 }
             }
             if (!consumer_sync(cbar, cphase, p.err, abort_flag)) break;
+            // a stored piece signals after every consumer thread's stores (ordered
+            // before this thread's release by the consumer barrier)
+            if (role == kRoleStore && ct == 0) red_release_gpu_add(p.unit_sync + 2 * u + 1, 1);
             fence_proxy_async_smem();  // staging writes before the next TMA into this stage
         }
         __syncwarp();
@@ -844,9 +1000,10 @@ __global__ void __maxnreg__(split_max_regs(D)) split_kernel(const __grid_constan
     int32_t* scan = reinterpret_cast<int32_t*>(base + L.scan);
     StageMeta* meta = reinterpret_cast<StageMeta*>(base + L.meta);
 
-    // Programmatic dependent launch: let the merge kernel be scheduled now,
-    // set up barriers and descriptors while the previous kernel in the stream
-    // finishes, and read no global memory before it has completed.
+    // Programmatic dependent launch: let the next kernel in the stream be
+    // scheduled as CTAs of this one exit, set up barriers and descriptors
+    // while the previous kernel finishes, and read no global memory before it
+    // has completed.
     if (MODE != kGather) pdl_launch_dependents();
     if (tid == 0) {
         for (int s = 0; s < C::kStages; ++s) {
@@ -865,147 +1022,16 @@ __global__ void __maxnreg__(split_max_regs(D)) split_kernel(const __grid_constan
     }
     pdl_wait_primary();
     build_prefix<MODE == kMulti, C::kThreads>(p, pfx, scan);  // ends with __syncthreads (also publishes the barriers)
-    if (blockIdx.x == 0 && MODE != kGather)
-        for (int i = tid; i <= p.B; i += C::kThreads) p.pfx[i] = pfx[i];
     int64_t begin, end;
-    {
-        const GroupRange gr = group_of_cta(blockIdx.x, pfx, p.B, rows_per_seq<MODE == kMulti>(p), p.Hkv,
-                                           gridDim.x);
-        group_cta_range(gr, blockIdx.x, &begin, &end);
-    }
+    const GroupRange gr = group_of_cta(blockIdx.x, pfx, p.B, rows_per_seq<MODE == kMulti>(p), p.Hkv,
+                                       gridDim.x);
+    group_cta_range(gr, blockIdx.x, &begin, &end);
 
     if (warp == C::kConsumerWarps) {
         run_producer<D, ST, MODE>(p, base_s, L, pfx, meta, &abort_flag, begin, end, lane);
         return;
     }
-    run_consumer<D, ST, MODE>(p, base_s, base, L, meta, &abort_flag, warp, lane);
-}
-
-// Merge of split partial states: one CTA per (sequence, kv head) unit, one
-// thread per 4 consecutive outputs of the unit's G x D block.  The slots of
-// up to 8 CTAs are loaded together, so the merge costs one memory round trip
-// per 8 partial states.
-__device__ __forceinline__ void merge_in(float& M, float& Ls, float4& Os, float mi, float li,
-                                         const float4& oi) {
-    const float Mn = fmaxf(M, mi);
-    if (Mn == kNegInf) return;  // both states empty
-    const float fa = ex2(M - Mn), fb = ex2(mi - Mn);
-    Ls = Ls * fa + li * fb;
-    Os.x = Os.x * fa + oi.x * fb;
-    Os.y = Os.y * fa + oi.y * fb;
-    Os.z = Os.z * fa + oi.z * fb;
-    Os.w = Os.w * fa + oi.w * fb;
-    M = Mn;
-}
-
-template <int MODE>
-__global__ void __launch_bounds__(kMaxGroup * 256 / 4) merge_kernel(const MergeParams p) {
-    pdl_launch_dependents();  // the next call's split kernel may start its set-up
-    pdl_wait_primary();
-    const int u = blockIdx.x;
-    const int b = u / p.Hkv, kvh = u - b * p.Hkv;  // b: launch sequence (pfx index)
-    constexpr bool MQ = MODE == kMulti;
-    const int G = p.G, D = p.D;
-    // the row's sequence, first packed query and query count (plain: b, 0, 1)
-    const int ql = MQ ? p.q_len : 1;
-    int Qr = 1, seq = b, first = 0, cnt = 1;
-    if constexpr (MQ) {
-        Qr = (ql + p.qp - 1) / p.qp;
-        const int Bs = p.B / Qr;
-        seq = b % Bs;
-        first = (b / Bs) * p.qp;
-        cnt = min(p.qp, ql - first);
-    }
-    const int NR = cnt * G;  // q rows of the unit
-    const int SR = MQ ? p.rows_per_slot : G;
-    const int n4 = NR * D / 4;
-    const int i4 = threadIdx.x;
-    // Every prefix entry needed, loaded together (one round trip): the unit's
-    // sequence and the bounds of its row group (group_of_cta's, written out).
-    const int64_t Bg = div_floor(p.B, Qr);
-    const int64_t grp = div_floor(b, Bg);
-    const int32_t lo = p.pfx[b], hi = p.pfx[b + 1];
-    const int32_t g_lo = p.pfx[grp * Bg], g_hi = p.pfx[(grp + 1) * Bg];
-    const int32_t nb = real_blocks(hi - lo, p.unit_cost);
-    const bool active = i4 < n4;  // the block is rounded up to whole warps
-    const int h = active ? (4 * i4) / D : 0;
-    const int d4 = 4 * i4 - h * D;
-    // output row of unit row h: query first + h / G, q head kvh*G + h % G
-    const int64_t orow = MQ ? ((int64_t)seq * ql + first + h / G) * p.Hq + (int64_t)kvh * G + h % G
-                            : (int64_t)b * p.Hq + (int64_t)kvh * G + h;
-    if (nb == 0) {
-        if (writes_output(MODE) && active) {
-            if (p.out_f32) *reinterpret_cast<float4*>(p.out_f32 + orow * D + d4) = make_float4(0.f, 0.f, 0.f, 0.f);
-            else *reinterpret_cast<uint2*>(p.out + orow * D + d4) = make_uint2(0u, 0u);
-        }
-        return;
-    }
-    GroupRange gr;
-    gr.Pg = div_floor(p.split_ctas, Qr);
-    gr.g = grp;
-    gr.F0 = (int64_t)g_lo * p.Hkv;
-    gr.W = (int64_t)g_hi * p.Hkv - gr.F0;
-    // the unit's blocks: the first nb of its hi - lo plan blocks
-    const int64_t su = (int64_t)lo * p.Hkv + (int64_t)kvh * (hi - lo), eu = su + nb;
-    const int64_t cf = gr.g * gr.Pg + cta_of_block(su - gr.F0, gr.W, gr.Pg);
-    const int64_t cl = gr.g * gr.Pg + cta_of_block(eu - 1 - gr.F0, gr.W, gr.Pg);
-    if (writes_output(MODE) && cf == cl) return;  // written by the split kernel
-    float M = kNegInf, Ls = 0.f;
-    float4 Os = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (MODE == kTiled && active) {  // plain decode rows: orow = (b*Hq + kvh*G + h)
-        M = p.m_state[orow];
-        Ls = p.l_state[orow];
-        Os = *reinterpret_cast<const float4*>(p.o_state + orow * D + d4);
-    }
-    // The slots to merge, in CTA order: with W >= Pg every CTA range is
-    // non-empty, so the CTAs cf..cl all hold part of the unit; with W < Pg a
-    // CTA holds at most one block, so the slots are the owners of the unit's
-    // nb blocks, taken in block order.
-    const bool every = gr.W >= gr.Pg;
-    const int64_t n_slots = every ? cl - cf + 1 : eu - su;
-    constexpr int kBatch = 8;
-    for (int64_t i0 = 0; active && i0 < n_slots; i0 += kBatch) {
-        float mi[kBatch], li[kBatch];
-        float4 oi[kBatch];
-#pragma unroll
-        for (int k = 0; k < kBatch; ++k) {
-            const int64_t i = i0 + k;
-            mi[k] = kNegInf;
-            li[k] = 0.f;
-            oi[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (i >= n_slots) continue;
-            const int64_t c = every ? cf + i : gr.g * gr.Pg + cta_of_block(su + i - gr.F0, gr.W, gr.Pg);
-            const int64_t slot = u + c;
-            mi[k] = p.part_ml[(slot * SR + h) * 2];
-            li[k] = p.part_ml[(slot * SR + h) * 2 + 1];
-            oi[k] = *reinterpret_cast<const float4*>(p.part_o + (slot * SR + h) * D + d4);
-        }
-#pragma unroll
-        for (int k = 0; k < kBatch; ++k) merge_in(M, Ls, Os, mi[k], li[k], oi[k]);
-    }
-    if (writes_output(MODE)) {
-        if (!active) return;
-        const float4 v = Ls > 0.f ? make_float4(Os.x / Ls, Os.y / Ls, Os.z / Ls, Os.w / Ls)
-                                  : make_float4(0.f, 0.f, 0.f, 0.f);
-        if (p.out_f32) {
-            *reinterpret_cast<float4*>(p.out_f32 + orow * D + d4) = v;
-        } else {
-            uint2 w;
-            w.x = pack_bf16x2(v.x, v.y);
-            w.y = pack_bf16x2(v.z, v.w);
-            *reinterpret_cast<uint2*>(p.out + orow * D + d4) = w;
-        }
-    } else {
-        // every thread of head h computed the same (M, Ls); the first one
-        // stores them after all threads of the head have read the old values
-        __syncthreads();
-        if (!active) return;
-        *reinterpret_cast<float4*>(p.o_state + orow * D + d4) = Os;
-        if (d4 == 0) {
-            p.m_state[orow] = M;
-            p.l_state[orow] = Ls;
-        }
-    }
+    run_consumer<D, ST, MODE>(p, base_s, base, L, meta, pfx, gr, &abort_flag, warp, lane);
 }
 
 // Host side of one split-kernel shape: its entry points by mode and its

@@ -1,5 +1,5 @@
-// Merge, state-reset and finalize kernels, and the head_dim dispatch of the
-// split kernel.
+// State-reset, finalize, export and merge-states kernels, and the head_dim
+// dispatch of the split kernel.
 #include "pda_aux.cuh"
 #include "pda_launch.h"
 
@@ -40,25 +40,6 @@ cudaError_t launch_split(int D, int st, int mode, const SplitParams& p, int grid
         case 256: return launch_split_d256(st, mode, p, grid, smem, stream);
         default: return cudaErrorInvalidValue;
     }
-}
-
-cudaError_t launch_merge(int mode, const MergeParams& p, bool pdl, cudaStream_t stream) {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)(p.B * p.Hkv), 1, 1);
-    const int rows = p.rows_per_slot > 0 ? p.rows_per_slot : p.G;  // q rows of a unit, at most
-    const int n4 = rows * p.D / 4;  // one thread per 4 outputs of a unit
-    cfg.blockDim = dim3((unsigned)((n4 + 31) / 32 * 32), 1, 1);
-    cfg.dynamicSmemBytes = 0;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = pdl ? 1 : 0;
-    if (mode == kOneShot) return cudaLaunchKernelEx(&cfg, merge_kernel<kOneShot>, p);
-    if (mode == kTiled) return cudaLaunchKernelEx(&cfg, merge_kernel<kTiled>, p);
-    if (mode == kMulti) return cudaLaunchKernelEx(&cfg, merge_kernel<kMulti>, p);
-    return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_reset_state(float* m, float* l, float* o, int64_t n_q, int32_t D,

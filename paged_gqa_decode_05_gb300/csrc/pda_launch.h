@@ -12,7 +12,6 @@ int split_stages(int D, int st);
 const void* split_kernel_fn(int D, int st, int mode);
 cudaError_t launch_split(int D, int st, int mode, const SplitParams& p, int grid, size_t smem,
                          cudaStream_t stream);
-cudaError_t launch_merge(int mode, const MergeParams& p, bool pdl, cudaStream_t stream);
 cudaError_t launch_reset_state(float* m, float* l, float* o, int64_t n_q, int32_t D,
                                cudaStream_t stream);
 cudaError_t launch_wait_timeout_probe(uint32_t* err, uint64_t limit_ns, cudaStream_t stream);

@@ -58,7 +58,11 @@ struct SplitParams {
     float* out_f32;              // [B, Hq, D] fp32 instead of out when non-null
     float* part_o;               // [slots, G, D]
     float* part_ml;              // [slots, G, 2] (m in base-2 units, l)
-    int32_t* pfx;                // [B+1] plan-block prefix, written by CTA 0 for the merge
+    int32_t* unit_sync;          // [B*Hkv][2] per split unit: pieces that took a ticket, pieces
+                                 // whose partial state is stored (0 between launches)
+    float* m_state;              // tiled: running state [B*Hq], [B*Hq], [B*Hq*D]
+    float* l_state;
+    float* o_state;
     uint32_t* err;               // device error flags
     uint16_t* dbg_k;             // gather check outputs
     uint16_t* dbg_v;
@@ -80,25 +84,8 @@ struct SplitParams {
     float scale_log2;            // softmax scale * log2(e)
 };
 
-struct MergeParams {
-    const float* part_o;
-    const float* part_ml;
-    const int32_t* pfx;
-    uint16_t* out;
-    float* out_f32;
-    float* m_state;              // tiled: running state [B*Hq], [B*Hq], [B*Hq*D]
-    float* l_state;
-    float* o_state;
-    int32_t B, Hq, Hkv, G, D;
-    int32_t unit_cost;           // as SplitParams
-    int32_t split_ctas;
-    int32_t q_len;               // as SplitParams
-    int32_t qp;
-    int32_t rows_per_slot;
-};
-
 struct SmemLayout {
-    uint32_t bars, cbar, meta, scan, st_m, st_l, pfx, total;
+    uint32_t bars, cbar, meta, scan, st_m, st_l, st_x, pfx, total;
 };
 
 // K and V tiles of ST rows plus the group's q rows (up to 8 x D bf16).
@@ -119,6 +106,7 @@ PDA_HD SmemLayout smem_layout(int D, int st, int stages, int G, int B) {
     L.scan = off;  off += 32u;  // one int per warp (block-prefix scan)
     L.st_m = off;  off += kMaxConsumerWarps * kMaxGroup * 4u;
     L.st_l = off;  off += kMaxConsumerWarps * kMaxGroup * 4u;
+    L.st_x = off;  off += 2u * kMaxGroup * 4u + 16u;  // old running (m, l) of a unit's rows; role word
     L.pfx = off;   off += (uint32_t)(B + 1) * 4u;
     L.total = off + 1024u;
     return L;

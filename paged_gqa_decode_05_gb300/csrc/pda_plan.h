@@ -74,6 +74,28 @@ PDA_HD void group_cta_range(const GroupRange& r, int64_t c, int64_t* begin, int6
     *end = r.F0 + cta_begin(cl + 1, r.W, r.Pg);
 }
 
+// The pieces of a unit split across CTAs: the CTAs of its group that hold
+// its blocks (the cost positions after them belong to no piece).  With
+// W >= Pg every CTA range is non-empty, so the pieces are the CTAs cf .. cl
+// between the owners of the unit's first and last block; with W < Pg a CTA
+// holds at most one block, so piece i is the owner of block su + i.  The
+// piece in CTA c keeps its partial state in slot u + c.
+struct UnitPieces {
+    int64_t cf;   // CTA of the first piece
+    int64_t su;   // the unit's first flattened block
+    int32_t n;    // pieces (1: the unit lies in one CTA)
+    bool every;   // the pieces are the CTAs cf .. cf + n - 1
+};
+
+template <typename Pfx>
+PDA_HD UnitPieces unit_pieces(const Pfx& pfx, int64_t b, int64_t kvh, int64_t Hkv, int32_t unit_cost,
+                              const GroupRange& gr);
+
+// CTA of piece i of a unit.
+PDA_HD int64_t piece_cta(const UnitPieces& u, int64_t i, const GroupRange& gr) {
+    return u.every ? u.cf + i : gr.g * gr.Pg + cta_of_block(u.su + i - gr.F0, gr.W, gr.Pg);
+}
+
 // Plan blocks c added to every non-empty unit: a segment's fixed cost in
 // quarter stages, measured per loader (each value the fastest of a sweep on
 // ragged and uniform batches).  TMA block boxes: two stages.  Row gathers of
@@ -98,6 +120,21 @@ PDA_HD int32_t real_blocks(int32_t nv, int32_t unit_cost) { return nv > 0 ? nv -
 // Blocks needed for a length in tokens.
 PDA_HD int32_t blocks_for_tokens(int32_t len, int32_t block_size) {
     return len <= 0 ? 0 : (len + block_size - 1) / block_size;
+}
+
+template <typename Pfx>
+PDA_HD UnitPieces unit_pieces(const Pfx& pfx, int64_t b, int64_t kvh, int64_t Hkv, int32_t unit_cost,
+                              const GroupRange& gr) {
+    const int32_t lo = pfx[b], hi = pfx[b + 1];
+    const int32_t nb = real_blocks(hi - lo, unit_cost);
+    UnitPieces r;
+    r.su = (int64_t)lo * Hkv + kvh * (hi - lo);
+    const int64_t eu = r.su + nb;
+    r.cf = gr.g * gr.Pg + cta_of_block(r.su - gr.F0, gr.W, gr.Pg);
+    const int64_t cl = gr.g * gr.Pg + cta_of_block(eu - 1 - gr.F0, gr.W, gr.Pg);
+    r.every = gr.W >= gr.Pg;
+    r.n = (int32_t)(r.every ? cl - r.cf + 1 : nb);
+    return r;
 }
 
 }  // namespace pda

@@ -181,6 +181,23 @@ __device__ __forceinline__ float bf16_hi(uint32_t x) { return __uint_as_float(x 
 
 // ---------------------------------------------------------------- sync / PDL
 
+// Device-scope signalling between CTAs: a release increment (every write this
+// CTA ordered before it is visible to whoever acquires the new value) and an
+// acquire load.
+__device__ __forceinline__ void red_release_gpu_add(int32_t* p, int32_t v) {
+    asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ int32_t ld_acquire_gpu(const int32_t* p) {
+    int32_t v;
+    asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// A float written by another CTA of this grid, read from L2 (never a stale
+// line of this SM's L1).
+__device__ __forceinline__ float ld_cg(const float* p) { return __ldcg(p); }
+
 __device__ __forceinline__ void pdl_launch_dependents() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }

@@ -9,6 +9,10 @@ MEAN_ABS = 2e-3
 # The bar between the tiled and the one-shot path, both in fp32 before rounding.
 TILED_VS_ONESHOT = 1e-3
 
+# Achieved errors of every oracle comparison in this session (printed at the
+# end of the run by conftest.py; report only).
+ERROR_LOG: list = []
+
 
 def dev(a: np.ndarray):
     """numpy -> CUDA tensor; uint16 arrays are bf16 bit patterns."""
@@ -33,9 +37,45 @@ def context_for(w, max_seqs=None, tile_capacity=64):
                        head_dim=w.D, block_size=w.block_size, tile_capacity=tile_capacity)
 
 
-def assert_close_to_oracle(got: np.ndarray, ref: np.ndarray, what: str = ""):
+def bf16_ulp(x: np.ndarray) -> np.ndarray:
+    """Spacing of bf16 values (8 significant bits) around each |x| (0 at 0)."""
+    x = np.abs(np.asarray(x, dtype=np.float64))
+    e = np.frexp(x)[1]
+    return np.where(x > 0, np.ldexp(1.0, e - 8), 0.0)
+
+
+def bf16_rn(x: np.ndarray) -> np.ndarray:
+    """x rounded to the nearest bf16 value, ties to even (normal range)."""
+    x = np.asarray(x, dtype=np.float64)
+    q = bf16_ulp(x)
+    return np.where(q > 0, np.round(x / np.where(q > 0, q, 1.0)) * q, 0.0)
+
+
+def rounding_report(got: np.ndarray, ref: np.ndarray) -> dict:
+    """How the output relates to the correctly rounded oracle value:
+    the fraction equal to bf16_rn(ref), the largest distance from it in bf16
+    steps, and the largest error beyond the half step the output rounding
+    itself may cost (what the kernel's fp32 arithmetic added)."""
+    if got.size == 0:
+        return {"exact_frac": 1.0, "max_steps": 0.0, "excess": 0.0}
+    rn = bf16_rn(ref)
+    step = bf16_ulp(np.maximum(np.abs(got), np.abs(ref)))
+    dist = np.abs(got - rn)
+    steps = np.where(step > 0, dist / np.where(step > 0, step, 1.0), 0.0)
+    excess = np.abs(got - ref) - 0.5 * step
+    return {"exact_frac": float(np.mean(got == rn)), "max_steps": float(steps.max()),
+            "excess": float(max(excess.max(), 0.0))}
+
+
+def assert_close_to_oracle(got: np.ndarray, ref: np.ndarray, what: str = "", rounded: bool = True):
+    """The task's bar (max |err| <= 2e-2, mean |err| <= 2e-3).  The achieved
+    errors, and for bf16 outputs their relation to bf16_rn(ref), are logged."""
     err = np.abs(got - ref)
     assert np.all(np.isfinite(got)), f"{what}: non-finite output"
     mx, mean = float(err.max()) if err.size else 0.0, float(err.mean()) if err.size else 0.0
+    rec = {"what": what, "max": mx, "mean": mean}
+    if rounded:
+        rec.update(rounding_report(got, ref))
+    ERROR_LOG.append(rec)
     assert mx <= MAX_ABS and mean <= MEAN_ABS, f"{what}: max|err|={mx:.3e} mean|err|={mean:.3e}"
     return mx, mean

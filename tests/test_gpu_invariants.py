@@ -214,3 +214,70 @@ def test_padded_token_stride_identical(bs):
     torch.cuda.synchronize()
     assert ctx.read_device_errors() == 0
     assert np.array_equal(out.cpu().float().numpy(), base)
+
+
+@pytest.mark.parametrize("D,bs", [(128, 16), (64, 1), (256, 32)])
+def test_token_permutation_within_tolerance(D, bs):
+    """Moving every token's K and V rows together to another position of the
+    same sequence changes only the order of the softmax sums: the fp32 results
+    agree to the kernel's own rounding, and both meet the oracle bar."""
+    import torch
+    from gpu_util import assert_close_to_oracle
+    w = _w(seed=30 + D + bs, D=D, bs=bs, lens=(1000, 3, 0, 257, 64 * 5 + 7))
+    ctx = context_for(w)
+    t = upload(w)
+    base = ctx.decode(t["q"], t["k_pool"], t["v_pool"], t["block_table"], t["seq_lens"],
+                      out_dtype=torch.float32).cpu().numpy().astype(np.float64)
+    rng = np.random.default_rng(31)
+    k2, v2 = w.k_pool.copy(), w.v_pool.copy()
+    for b in range(w.B):
+        n = int(w.seq_lens[b])
+        tok = np.arange(n)
+        src = (w.block_table[b, tok // w.block_size], tok % w.block_size)
+        pt = rng.permutation(n)
+        dst = (w.block_table[b, pt // w.block_size], pt % w.block_size)
+        k2[dst] = w.k_pool[src]
+        v2[dst] = w.v_pool[src]
+    w.k_pool, w.v_pool = k2, v2
+    t = upload(w)
+    perm = ctx.decode(t["q"], t["k_pool"], t["v_pool"], t["block_table"], t["seq_lens"],
+                      out_dtype=torch.float32).cpu().numpy().astype(np.float64)
+    torch.cuda.synchronize()
+    assert ctx.read_device_errors() == 0
+    assert np.abs(perm - base).max() <= 2e-4  # twice the fp32 error budget of one decode
+    ref = oracle.load().decode(w.q, w.k_pool, w.v_pool, w.block_table, w.seq_lens, Hq=w.Hq,
+                               Hkv=w.Hkv, D=w.D, block_size=w.block_size)
+    assert_close_to_oracle(perm, ref, "token permutation", rounded=False)
+
+
+def test_split_units_merge_identically_call_after_call():
+    """The pieces of a unit split across CTAs find the piece that merges them
+    through per-unit counters that every launch leaves at zero: repeated calls,
+    and calls alternating between batches whose units split differently, give
+    the same bits each time."""
+    import torch
+    a = _w(seed=40, lens=(4096, 5000, 17, 2049, 3333, 1, 0, 1024), G=4, Hkv=2)
+    b = _w(seed=41, lens=(64 * 300 + 5, 3, 700), G=8, Hkv=1)
+    ctx_a = context_for(a, max_seqs=8)
+    ta = upload(a)
+    first = ctx_a.decode(ta["q"], ta["k_pool"], ta["v_pool"], ta["block_table"], ta["seq_lens"]).clone()
+    ctx_b = context_for(b)
+    tb = upload(b)
+    first_b = ctx_b.decode(tb["q"], tb["k_pool"], tb["v_pool"], tb["block_table"], tb["seq_lens"]).clone()
+    for _ in range(4):
+        again = ctx_a.decode(ta["q"], ta["k_pool"], ta["v_pool"], ta["block_table"], ta["seq_lens"])
+        again_b = ctx_b.decode(tb["q"], tb["k_pool"], tb["v_pool"], tb["block_table"], tb["seq_lens"])
+        torch.cuda.synchronize()
+        assert torch.equal(again, first) and torch.equal(again_b, first_b)
+    # the same context on a batch with another split, then the first batch again
+    c = _w(seed=42, lens=(100, 9000, 64, 65), G=4, Hkv=2)
+    tc = upload(c)
+    ctx_a.decode(tc["q"], tc["k_pool"], tc["v_pool"], tc["block_table"], tc["seq_lens"])
+    again = ctx_a.decode(ta["q"], ta["k_pool"], ta["v_pool"], ta["block_table"], ta["seq_lens"])
+    torch.cuda.synchronize()
+    assert torch.equal(again, first)
+    assert ctx_a.read_device_errors() == 0 and ctx_b.read_device_errors() == 0
+    ref = oracle.load().decode(a.q, a.k_pool, a.v_pool, a.block_table, a.seq_lens, Hq=a.Hq,
+                               Hkv=a.Hkv, D=a.D, block_size=a.block_size)
+    from gpu_util import assert_close_to_oracle
+    assert_close_to_oracle(host_f64(first), ref, "split-unit merge")
