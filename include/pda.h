@@ -81,7 +81,9 @@ enum {
  *   head_dim       D; [TA] validate caps it at 256; this build has kernels for
  *                  64, 128 and 256.
  *   block_size     tokens per KV block: 1, 2, 4, 8, 16, 32 or 64 in this build
- *                  (from 8 up, one TMA copy per block and pool; below 8 the
+ *                  (one TMA copy per block and pool when a block's rows fill
+ *                  whole 1024-byte swizzle spans: block sizes from 8, 4 with
+ *                  head_dim 128 or 256, 2 with head_dim 256; otherwise the
  *                  rows are gathered, four per TMA gather4 copy when the pool
  *                  strides are multiples of head_dim, else with 16-byte
  *                  copies).  block_size 1 is the token-granular page of [CK]
@@ -368,21 +370,25 @@ pda_status pda_get_launch_info(const pda_ctx* ctx, pda_launch_info* info);
  * blocks_given != 0), spans nv_b = nb_b + unit_cost positions (0 when
  * nb_b = 0), its blocks first.  The unit cost stands for the fixed work of a
  * segment, so that CTAs covering many short units get fewer blocks; a
- * context's value is in pda_launch_info.unit_cost (one stage of blocks).
- * CTA c takes positions [floor(c*W/P), floor((c+1)*W/P)).  For unit
- * u = b*Hkv + g this reports the first and last CTA holding one of its
- * blocks (-1, -1 when it has none); a CTA's partial state for unit u goes to
- * slot u + c.
- *   lens        [batch] host int32 (tokens, or block counts).
- *   unit_cost   >= 0.
+ * context's value is in pda_launch_info.unit_cost.  CTA c takes positions
+ * [floor(c*W/P), floor((c+1)*W/P)).  Small batches are planned by unit
+ * instead: when batch*Hkv <= P and no unit holds more than 4 stages of rows
+ * (4 * stage_tokens tokens; pda_launch_info.stage_tokens), CTA u processes
+ * unit u whole.  For unit u = b*Hkv + g this reports the first and last CTA
+ * holding one of its blocks (-1, -1 when it has none); a CTA's partial state
+ * for unit u goes to slot u + c.
+ *   lens         [batch] host int32 (tokens, or block counts).
+ *   unit_cost    >= 0.
+ *   stage_tokens rows per pipeline stage; 0 plans every batch by the even
+ *                split.
  *   first_cta,
- *   last_cta    [batch*Hkv] outputs.
+ *   last_cta     [batch*Hkv] outputs.
  *   total_blocks receives W.
  */
 pda_status pda_plan_units(const int32_t* lens, int32_t batch, int32_t blocks_given,
                           int32_t block_size, int32_t num_kv_heads, int32_t split_ctas,
-                          int32_t unit_cost, int32_t* first_cta, int32_t* last_cta,
-                          int64_t* total_blocks);
+                          int32_t unit_cost, int32_t stage_tokens, int32_t* first_cta,
+                          int32_t* last_cta, int64_t* total_blocks);
 
 /*
  * One-shot decode that allocates nothing -- no counterpart on the pages; it

@@ -102,7 +102,7 @@ def lib() -> ctypes.CDLL:
         "pda_set_timing_events": (I32, [P, P, P, P]),
         "pda_check_wait_timeout": (I32, [P, I64, P]),
         "pda_get_launch_info": (I32, [P, ctypes.POINTER(LaunchInfo)]),
-        "pda_plan_units": (I32, [P, I32, I32, I32, I32, I32, I32, P, P, ctypes.POINTER(I64)]),
+        "pda_plan_units": (I32, [P, I32, I32, I32, I32, I32, I32, I32, P, P, ctypes.POINTER(I64)]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(L, name)
@@ -152,9 +152,10 @@ def slot_strides(**kw) -> Tuple[int, int, int]:
 
 
 def plan_units(lens: Sequence[int], *, block_size: int, num_kv_heads: int, split_ctas: int,
-               blocks_given: bool = False, unit_cost: int = 0):
+               blocks_given: bool = False, unit_cost: int = 0, stage_tokens: int = 0):
     """(first_cta, last_cta, total_blocks) of the split plan (host only); a
-    context's unit_cost is in its launch_info()."""
+    context's unit_cost and stage_tokens are in its launch_info() (stage_tokens
+    0: the even split for every batch, without the small-batch unit plan)."""
     import numpy as np
     lens = np.ascontiguousarray(lens, dtype=np.int32)
     n = lens.shape[0] * num_kv_heads
@@ -162,8 +163,8 @@ def plan_units(lens: Sequence[int], *, block_size: int, num_kv_heads: int, split
     last = np.zeros(max(n, 1), dtype=np.int32)
     total = ctypes.c_int64()
     _check(lib().pda_plan_units(lens.ctypes.data, lens.shape[0], int(blocks_given), block_size,
-                                num_kv_heads, split_ctas, unit_cost, first.ctypes.data, last.ctypes.data,
-                                ctypes.byref(total)))
+                                num_kv_heads, split_ctas, unit_cost, stage_tokens, first.ctypes.data,
+                                last.ctypes.data, ctypes.byref(total)))
     return first[:n], last[:n], int(total.value)
 
 

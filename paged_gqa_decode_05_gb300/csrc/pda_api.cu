@@ -159,14 +159,14 @@ pda_status check_pool(const PoolArgs& a) {
 }
 
 // The split kernel's KV loader for a pool, with its two tensor maps: one 5-D
-// box per block and pool for block sizes from 8 (row mode 0); below 8 the
-// rows are gathered, with TMA gather4 when the three strides are multiples of
-// D (row mode 1), else with 16-byte cp.async (row mode 2, maps unused).  The
-// consumers' shared-memory layout depends on this choice, so every launch
-// path takes it from here.
+// box per block and pool where a block fills whole 1024-byte swizzle spans
+// (row mode 0, see block_boxes); otherwise the rows are gathered, with TMA
+// gather4 when the three strides are multiples of D (row mode 1), else with
+// 16-byte cp.async (row mode 2, maps unused).  The consumers' shared-memory
+// layout depends on this choice, so every launch path takes it from here.
 pda_status encode_loader(const pda_dims& d, const PoolArgs& a, CUtensorMap* tk, CUtensorMap* tv,
                          int32_t* row_mode) {
-    if (d.block_size >= 8) {
+    if (pda::block_boxes(d.head_dim, d.block_size)) {
         pda_status st = encode_pool(d, a.k, a, tk);
         if (st == PDA_OK) st = encode_pool(d, a.v, a, tv);
         *row_mode = 0;
@@ -281,7 +281,7 @@ pda_status run(pda_ctx* ctx, const RunArgs& r) {
     if (r.table_stride < 1)
         return fail(PDA_ERR_INVALID_ARG, "block table width must be >= 1 (got %d)", r.table_stride);
     st = check_plan_size((int64_t)r.batch * r.q_len, r.table_stride,
-                         pda::unit_cost_blocks(ctx->stage_rows, d.block_size, r.mode == pda::kMulti));
+                         pda::unit_cost_blocks(ctx->stage_rows, d.head_dim, d.block_size, r.mode == pda::kMulti));
     if (st != PDA_OK) return st;
     float scale_log2 = 0.f;
     st = check_scale(r.scale, d.head_dim, &scale_log2);
@@ -342,7 +342,7 @@ pda_status run(pda_ctx* ctx, const RunArgs& r) {
         p.Hkv = Hkv;
         p.G = ctx->G;
         p.bs = d.block_size;
-        p.unit_cost = pda::unit_cost_blocks(ctx->stage_rows, d.block_size, r.mode == pda::kMulti);
+        p.unit_cost = pda::unit_cost_blocks(ctx->stage_rows, d.head_dim, d.block_size, r.mode == pda::kMulti);
         p.dbg_row_tokens = (int32_t)dbg_row_tokens;
         p.scale_log2 = scale_log2;
         const size_t smem = pda::smem_layout(D, ctx->stage_rows, ctx->stages, ctx->G, cb).total;
@@ -701,24 +701,30 @@ PDA_EXPORT pda_status pda_get_launch_info(const pda_ctx* ctx, pda_launch_info* i
     info->smem_bytes = ctx->smem_max;
     info->stage_tokens = ctx->stage_rows;
     info->partial_slots = ctx->slots;
-    info->unit_cost = pda::unit_cost_blocks(ctx->stage_rows, ctx->dims.block_size, false);
+    info->unit_cost = pda::unit_cost_blocks(ctx->stage_rows, ctx->dims.head_dim, ctx->dims.block_size, false);
     return PDA_OK;
 }
 
 PDA_EXPORT pda_status pda_plan_units(const int32_t* lens, int32_t batch, int32_t blocks_given,
                                      int32_t block_size, int32_t num_kv_heads, int32_t split_ctas,
-                                     int32_t unit_cost, int32_t* first_cta, int32_t* last_cta,
-                                     int64_t* total_blocks) {
+                                     int32_t unit_cost, int32_t stage_tokens, int32_t* first_cta,
+                                     int32_t* last_cta, int64_t* total_blocks) {
     if (batch < 0 || block_size < 1 || num_kv_heads < 1 || split_ctas < 1 || unit_cost < 0 ||
-        (batch > 0 && (!lens || !first_cta || !last_cta)) || !total_blocks)
+        stage_tokens < 0 || (batch > 0 && (!lens || !first_cta || !last_cta)) || !total_blocks)
         return fail(PDA_ERR_INVALID_ARG, "bad plan arguments");
     auto blocks = [&](int32_t b) {
         return blocks_given ? std::max(lens[b], 0) : pda::blocks_for_tokens(lens[b], block_size);
     };
     int64_t sum = 0;
-    for (int32_t b = 0; b < batch; ++b) sum += pda::plan_blocks(blocks(b), unit_cost);
+    int32_t nb_max = 0;
+    for (int32_t b = 0; b < batch; ++b) {
+        sum += pda::plan_blocks(blocks(b), unit_cost);
+        nb_max = std::max(nb_max, blocks(b));
+    }
     const int64_t W = sum * num_kv_heads, P = split_ctas;
     *total_blocks = W;
+    const bool by_unit = stage_tokens > 0 &&
+                         pda::unit_mode((int64_t)batch * num_kv_heads, P, nb_max, stage_tokens, block_size);
     int64_t pfx = 0;
     for (int32_t b = 0; b < batch; ++b) {
         const int32_t nb = blocks(b), nv = pda::plan_blocks(nb, unit_cost);
@@ -726,6 +732,10 @@ PDA_EXPORT pda_status pda_plan_units(const int32_t* lens, int32_t batch, int32_t
             const int64_t u = (int64_t)b * num_kv_heads + g;
             if (nb == 0) {
                 first_cta[u] = last_cta[u] = -1;
+                continue;
+            }
+            if (by_unit) {
+                first_cta[u] = last_cta[u] = (int32_t)u;
                 continue;
             }
             const int64_t su = pfx * num_kv_heads + (int64_t)g * nv;
@@ -889,7 +899,7 @@ PDA_EXPORT pda_status pda_decode_noalloc(const pda_bf16* q, const pda_bf16* k_po
     if (!block_table || !seq_lens || !aligned(block_table, 4) || !aligned(seq_lens, 4))
         return fail(PDA_ERR_INVALID_ARG, "block_table / seq_lens must be non-NULL and 4-byte aligned");
     if (max_blocks < 1) return fail(PDA_ERR_INVALID_ARG, "max_blocks must be >= 1");
-    const int32_t unit_cost = pda::unit_cost_blocks(rows, block_size, false);
+    const int32_t unit_cost = pda::unit_cost_blocks(rows, D, block_size, false);
     if ((st = check_plan_size(batch, max_blocks, unit_cost)) != PDA_OK) return st;
     PoolArgs pool = {k_pool, v_pool, num_blocks, (int64_t)block_size * num_kv_heads * head_dim,
                      (int64_t)num_kv_heads * head_dim, (int64_t)head_dim};

@@ -12,18 +12,18 @@ namespace pda {
 
 // Split-kernel shape: a pipeline stage holds ST KV rows, read by ST / 16
 // consumer warps of 16 rows; one more warp is the TMA producer.  ST = 64,
-// except for head_dim 256 with block sizes below 8: there the producer copies
-// rows (4 per gather4 copy, or 16-byte cp.async) and is bound by its
-// instruction rate, and with 64-row stages only one CTA (one producer) fits
-// on an SM; ST = 32 fits two.  (For head_dim 128, already two CTAs per SM,
-// 32-row stages were measured slower.)
+// except for head_dim 256 with rows gathered one by one (block size 1): there
+// the producer copies rows (4 per gather4 copy, or 16-byte cp.async) and is
+// bound by its instruction rate, and with 64-row stages only one CTA (one
+// producer) fits on an SM; ST = 32 fits two.  (For head_dim 128, already two
+// CTAs per SM, 32-row stages were measured slower.)
 constexpr int kMaxConsumerWarps = 4;
 constexpr int kMaxLaunchBatch = 1024;                    // sequences per kernel launch
 constexpr int kMaxGroup = 8;                             // q heads per kv head (n8 MMA)
 
 PDA_HD int split_threads(int st) { return (st / 16 + 1) * 32; }
 // Stage rows for a head size and block size.
-PDA_HD int stage_tokens(int D, int block_size) { return D == 256 && block_size < 8 ? 32 : 64; }
+PDA_HD int stage_tokens(int D, int block_size) { return D == 256 && !block_boxes(D, block_size) ? 32 : 64; }
 
 // kOneShot: decode, output written; kTiled: fold a tile into the running
 // state; kGather: copy the staged rows out (loader check); kMulti: causal
@@ -58,7 +58,7 @@ struct SplitParams {
     float* out_f32;              // [B, Hq, D] fp32 instead of out when non-null
     float* part_o;               // [slots, G, D]
     float* part_ml;              // [slots, G, 2] (m in base-2 units, l)
-    int32_t* unit_sync;          // [B*Hkv][2] per split unit: pieces that took a ticket, pieces
+    int32_t* unit_sync;          // [B*Hkv][2] per split unit: pieces that drew a ticket, pieces
                                  // whose partial state is stored (0 between launches)
     float* m_state;              // tiled: running state [B*Hq], [B*Hq], [B*Hq*D]
     float* l_state;
@@ -103,7 +103,7 @@ PDA_HD SmemLayout smem_layout(int D, int st, int stages, int G, int B) {
     L.bars = off;  off += 2u * stages * 8u;
     L.cbar = off;  off += 8u;
     L.meta = off;  off += (uint32_t)stages * (uint32_t)sizeof(StageMeta);
-    L.scan = off;  off += 32u;  // one int per warp (block-prefix scan)
+    L.scan = off;  off += 64u;  // per warp: block-prefix sum [8], largest unit [8]
     L.st_m = off;  off += kMaxConsumerWarps * kMaxGroup * 4u;
     L.st_l = off;  off += kMaxConsumerWarps * kMaxGroup * 4u;
     L.st_x = off;  off += 2u * kMaxGroup * 4u + 16u;  // old running (m, l) of a unit's rows; role word

@@ -105,10 +105,32 @@ PDA_HD int64_t piece_cta(const UnitPieces& u, int64_t i, const GroupRange& gr) {
 constexpr int32_t kUnitCostX4 = 8;
 constexpr int32_t kUnitCostGatherX4 = 2;
 constexpr int32_t kUnitCostMultiX4 = 16;
-PDA_HD int32_t unit_cost_blocks(int32_t stage_rows, int32_t block_size, bool multi_query) {
+
+// Whether a block's rows are loaded with one TMA box per block and pool: a
+// block of bs rows of D bf16 lands as [D/64 slabs][bs rows][128 bytes] and
+// must fill whole 1024-byte spans of the 128-byte swizzle, so that every box
+// starts on a span (block sizes from 8; 4 for head sizes from 128; 2 for head
+// size 256).  Otherwise the rows are gathered one by one.
+PDA_HD bool block_boxes(int32_t head_dim, int32_t block_size) {
+    return block_size >= 8 || (block_size * head_dim * 2) % 1024 == 0;
+}
+
+PDA_HD int32_t unit_cost_blocks(int32_t stage_rows, int32_t head_dim, int32_t block_size, bool multi_query) {
     const int32_t nb = stage_rows / block_size;
-    const int32_t x4 = multi_query ? kUnitCostMultiX4 : block_size < 8 ? kUnitCostGatherX4 : kUnitCostX4;
+    const int32_t x4 = multi_query ? kUnitCostMultiX4
+                     : block_boxes(head_dim, block_size) ? kUnitCostX4 : kUnitCostGatherX4;
     return (nb < 1 ? 1 : nb) * x4 / 4;
+}
+
+// Small batches ("unit mode").  When there are no more units than CTAs and no
+// unit holds more than kUnitModeStages stages of rows, CTA c processes unit c
+// whole: no unit is split and nothing merges (splitting units of a few stages
+// over many CTAs would buy no bandwidth and cost a merge each).  Otherwise the
+// flattened range is split evenly over all CTAs.
+constexpr int32_t kUnitModeStages = 4;
+PDA_HD bool unit_mode(int64_t units, int64_t ctas, int32_t max_unit_blocks, int32_t stage_rows,
+                      int32_t block_size) {
+    return units <= ctas && (int64_t)max_unit_blocks * block_size <= (int64_t)kUnitModeStages * stage_rows;
 }
 
 // Plan blocks of a unit with nb blocks.

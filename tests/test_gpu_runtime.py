@@ -78,10 +78,12 @@ def test_two_contexts_on_two_streams():
 
 
 @pytest.mark.parametrize("D,bs,rows,per_sm", [(128, 16, 64, 2), (64, 16, 64, 2), (256, 16, 64, 1),
-                                              (256, 64, 64, 1), (256, 4, 32, 2), (256, 1, 32, 2)])
+                                              (256, 64, 64, 1), (256, 4, 64, 1), (256, 2, 64, 1),
+                                              (256, 1, 32, 2), (128, 4, 64, 2), (128, 1, 64, 2)])
 def test_split_kernel_shape(D, bs, rows, per_sm):
     """Stage rows and CTAs per SM as designed: two CTAs per SM at head size
-    <= 128; at 256 one, or two with 32-row stages for block sizes below 8."""
+    <= 128; at 256 one, or two with 32-row stages where rows are gathered one
+    by one (block size 1: blocks of 2 and 4 rows load as one box each)."""
     import paged_gqa_decode_05_gb300 as pda
     ctx = pda.Context(max_seqs=32, num_q_heads=32, num_kv_heads=8, head_dim=D, block_size=bs)
     info = ctx.launch_info()

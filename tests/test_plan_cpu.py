@@ -92,3 +92,28 @@ def test_block_counts_mode():
                                     blocks_given=True)
     assert W == 16
     assert list(first[2:4]) == [-1, -1]
+
+
+def test_small_batches_are_planned_by_unit():
+    """No more units than CTAs and every unit at most 4 stages of rows: CTA u
+    processes unit u whole (no unit is split, so nothing merges); a unit one
+    block longer than that, or more units than CTAs, takes the even split."""
+    st, bs, Hkv = 64, 16, 2
+    lens = [37, 0, 4 * st, 1]
+    first, last, _ = pda.plan_units(lens, block_size=bs, num_kv_heads=Hkv, split_ctas=304,
+                                    unit_cost=8, stage_tokens=st)
+    for u in range(len(lens) * Hkv):
+        if lens[u // Hkv] == 0:
+            assert first[u] == last[u] == -1
+        else:
+            assert first[u] == last[u] == u
+    # one block longer than four stages: the even split, units spread over CTAs
+    first, last, _ = pda.plan_units([37, 4 * st + bs], block_size=bs, num_kv_heads=Hkv,
+                                    split_ctas=304, unit_cost=8, stage_tokens=st)
+    assert last[2] > first[2]
+    # more units than CTAs: the even split
+    first, last, W = pda.plan_units([5] * 4, block_size=bs, num_kv_heads=Hkv, split_ctas=7,
+                                    unit_cost=8, stage_tokens=st)
+    ref, ref_last, ref_W = pda.plan_units([5] * 4, block_size=bs, num_kv_heads=Hkv, split_ctas=7,
+                                          unit_cost=8)
+    assert W == ref_W and list(first) == list(ref) and list(last) == list(ref_last)
