@@ -621,19 +621,14 @@ __device__ __forceinline__ void merge_state(float& M, float& Ls, float4& Os, flo
     M = Mn;
 }
 
-// Segment-end roles (see the epilogue in run_consumer).  kRoleMerge: the
-// other pieces were already stored when the last stage began; kRoleMergeWait:
-// they still have to be waited for.
-enum SegRole : int32_t {
-    kRoleWhole = 0, kRoleStore = 1, kRoleMerge = 2, kRoleMergeWait = 3, kRoleAbort = -1
-};
-constexpr int kMergeBatch = 8;  // partial states loaded per memory round trip
+// Segment-end roles (see the epilogue in run_consumer).
+enum SegRole : int32_t { kRoleWhole = 0, kRoleStore = 1, kRoleMerge = 2, kRoleAbort = -1 };
 
 template <int D, int ST, int MODE>
 __device__ __forceinline__ void run_consumer(const SplitParams& p, uint32_t base_s, uint8_t* base,
                                              const SmemLayout& L, const StageMeta* meta,
-                                             const int32_t* pfx, volatile int* abort_flag, int warp,
-                                             int lane) {
+                                             const int32_t* pfx, const GroupRange& gr,
+                                             volatile int* abort_flag, int warp, int lane) {
     using C = Cfg<D, ST>;
     constexpr int S = C::kStages;
     constexpr int KS = C::kKSteps;
@@ -653,10 +648,11 @@ __device__ __forceinline__ void run_consumer(const SplitParams& p, uint32_t base
     const int pv_row = r0 + (lane & 7) + ((lane >> 4) << 3);
     const int pv_cpar = (lane >> 3) & 1;
     const int lbs = p.row_gather ? C::kLogST : 31 - __clz(p.bs);  // gathered rows: one ST-row block
-    // swizzle of this lane's ldmatrix rows (both patterns have row & 7 == lane & 7):
-    // swz(row, h) = sw ^ (h * hx & 7)
-    const int sw = lbs >= 3 ? (lane & 7) : (lane & ((1 << lbs) - 1));
-    const int hx = lbs >= 3 ? 0 : (1 << lbs);
+    // swizzle of this lane's ldmatrix rows in slab h, swz(row, h) (both patterns
+    // have row & 7 == lane & 7), fixed for the launch
+    int swh[C::kHalves];
+#pragma unroll
+    for (int h = 0; h < C::kHalves; ++h) swh[h] = swz(lane, h, lbs);
     const uint32_t hs = (uint32_t)(128 << lbs);  // bytes between 64-column slabs of a block
     const uint32_t qk_off = row_off<D>(qk_row, lbs);
     const uint32_t pv_off = row_off<D>(pv_row, lbs);
@@ -674,8 +670,7 @@ __device__ __forceinline__ void run_consumer(const SplitParams& p, uint32_t base
     uint32_t cphase = 0;
     int stage = 0;
     uint32_t phase = 0;
-    int32_t ticket = 0;  // consumer thread 0: this piece's ticket for its split unit,
-    int32_t stored = 0;  // and the unit's stored count when its last stage began
+    int32_t ticket = 0;  // consumer thread 0: this piece's ticket for its split unit
 
     if constexpr (writes_output(MODE)) {
         // A unit with no tokens has no segment: its output rows are zero.  Such
@@ -706,15 +701,11 @@ __device__ __forceinline__ void run_consumer(const SplitParams& p, uint32_t base
         }
         const StageMeta m = meta[stage];
         if (m.flags & kDone) break;
-        // The last stage of a piece of a split unit: take the piece's ticket and
-        // read the unit's stored count now, so that both round trips overlap this
-        // stage's math (see the epilogue).  Both are relaxed: nothing here waits
-        // for them; the epilogue completes the acquire with a fence.
-        if (MODE != kGather && warp == 0 && lane == 0 && (m.flags & kSegEnd) && !(m.flags & kWholeUnit)) {
-            int32_t* cnt = p.unit_sync + 2 * (m.b * p.Hkv + m.kvh);
-            ticket = atomicAdd(cnt, 1);
-            stored = ld_relaxed_gpu(cnt + 1);
-        }
+        // The last stage of a piece of a split unit: take the piece's ticket now, so
+        // that the atomic's round trip overlaps this stage's math.  Tickets only
+        // assign roles: the piece that draws the last one merges all pieces.
+        if (MODE != kGather && warp == 0 && lane == 0 && (m.flags & kSegEnd) && !(m.flags & kWholeUnit))
+            ticket = atomicAdd(p.unit_sync + 2 * (m.b * p.Hkv + m.kvh), 1);
         const uint32_t sK = base_s + (uint32_t)stage * C::kStageBytes;
         const uint32_t sV = sK + C::kTileBytes;
 
@@ -752,7 +743,7 @@ __device__ __forceinline__ void run_consumer(const SplitParams& p, uint32_t base
 #pragma unroll
                 for (int kk = 0; kk < KS; ++kk) {
                     uint32_t a[4];
-                    const int cc = (((kk & 3) << 1) + qk_cpar) ^ sw ^ (((kk >> 2) * hx) & 7);
+                    const int cc = (((kk & 3) << 1) + qk_cpar) ^ swh[kk >> 2];
                     ldsm_x4(sK + qk_off + (uint32_t)(kk >> 2) * hs + (cc << 4), a);
                     mma_16816(acc[kk & 1], a, qf[kk][0], qf[kk][1]);
                 }
@@ -813,7 +804,7 @@ __device__ __forceinline__ void run_consumer(const SplitParams& p, uint32_t base
 #pragma unroll
                 for (int mt = 0; mt < KS; ++mt) {
                     uint32_t a[4];
-                    const int cc = (((mt & 3) << 1) + pv_cpar) ^ sw ^ (((mt >> 2) * hx) & 7);
+                    const int cc = (((mt & 3) << 1) + pv_cpar) ^ swh[mt >> 2];
                     ldsm_x4_trans(sV + pv_off + (uint32_t)(mt >> 2) * hs + (cc << 4), a);
                     mma_16816(o[mt], a, pb0, pb1);
                     mma_16816(o[mt], a, pc0, pc1);
@@ -830,15 +821,13 @@ __device__ __forceinline__ void run_consumer(const SplitParams& p, uint32_t base
             //   piece of a split unit that did not draw the last ticket: store
             //     the partial (m, l, o) in slot u + blockIdx.x and signal it with
             //     a release increment of the unit's stored count;
-            //   piece that drew the last ticket: once the other pieces' partials
-            //     are stored (usually already when its last stage began; else a
-            //     bounded wait), merge every piece in piece order, write o / l
-            //     (or fold), and zero the unit's counters for the next launch.
+            //   piece that drew the last ticket: wait (bounded) until the other
+            //     pieces' partials are stored, merge them with its own state,
+            //     write o / l (or fold), and zero the unit's counters for the
+            //     next launch.
             // The last-ticket piece only waits for pieces that have already
             // drawn their tickets, i.e. are running towards their own store, so
-            // the wait cannot deadlock whichever CTAs are resident.  Tickets are
-            // drawn when the last stage begins, so the last-ticket piece is
-            // nearly always the last to finish and rarely waits.
+            // the wait cannot deadlock whichever CTAs are resident.
             float* st_m = reinterpret_cast<float*>(base + L.st_m);
             float* st_l = reinterpret_cast<float*>(base + L.st_l);
             float* st_x = reinterpret_cast<float*>(base + L.st_x);  // old running m [8], l [8]
@@ -849,32 +838,9 @@ __device__ __forceinline__ void run_consumer(const SplitParams& p, uint32_t base
                 l0 += __shfl_xor_sync(0xffffffffu, l0, off);
                 l1 += __shfl_xor_sync(0xffffffffu, l1, off);
             }
-            const bool whole = (m.flags & kWholeUnit) != 0;
-            const int u = m.b * p.Hkv + m.kvh;
-            UnitPieces pc;
-            pc.cf = 0; pc.su = 0; pc.n = 1; pc.every = true;
-            GroupRange gr;  // of this CTA: a split unit lies in it
-            gr.F0 = 0; gr.W = 0; gr.Pg = 1; gr.g = 0;
-            if (!whole) {
-                gr = group_of_cta(blockIdx.x, pfx, p.B, rows_per_seq<MQ>(p), p.Hkv, gridDim.x);
-                pc = unit_pieces(pfx, m.b, m.kvh, p.Hkv, p.unit_cost, gr);
-            }
-            const int ct = warp * 32 + lane;
-            const int NR = MQ ? m.nr : G;  // q rows of the unit
-            const int SR = MQ ? p.rows_per_slot : G;  // rows per partial slot
-            if (ct == 0) {
-                const int32_t role = whole ? kRoleWhole : ticket != pc.n - 1 ? kRoleStore
-                                   : stored == pc.n - 1 ? kRoleMerge : kRoleMergeWait;
-                if (role == kRoleMerge) {  // every piece has drawn and stored: reset for the next launch
-                    fence_acquire_gpu();  // with the relaxed read of the count: the pieces' stores are visible
-                    p.unit_sync[2 * u] = 0;
-                    p.unit_sync[2 * u + 1] = 0;
-                }
-                *st_role = role;
-            }
             if (!consumer_sync(cbar, cphase, p.err, abort_flag)) break;  // all reads of the stage done
-            int role = *st_role;
             const int h0 = 2 * t, h1 = 2 * t + 1;
+            const int NR = MQ ? m.nr : G;  // q rows of the unit
             if (g == 0) {
                 if (h0 < NR) { st_m[warp * kMaxGroup + h0] = m0; st_l[warp * kMaxGroup + h0] = l0; }
                 if (h1 < NR) { st_m[warp * kMaxGroup + h1] = m1; st_l[warp * kMaxGroup + h1] = l1; }
@@ -893,6 +859,12 @@ __device__ __forceinline__ void run_consumer(const SplitParams& p, uint32_t base
                     r[d + 8] = o[mt][3];
                 }
             }
+            const bool whole = (m.flags & kWholeUnit) != 0;
+            const int u = m.b * p.Hkv + m.kvh;
+            UnitPieces pc;
+            pc.cf = 0; pc.su = 0; pc.n = 1; pc.every = true;
+            if (!whole) pc = unit_pieces(pfx, m.b, m.kvh, p.Hkv, p.unit_cost, gr);
+            const int ct = warp * 32 + lane;
             if constexpr (MODE == kTiled) {
                 // the running state's (m, l) of the unit's rows, read before any is rewritten
                 if (ct < NR) {
@@ -901,30 +873,94 @@ __device__ __forceinline__ void run_consumer(const SplitParams& p, uint32_t base
                     st_x[kMaxGroup + ct] = p.l_state[row];
                 }
             }
-            if (role == kRoleMergeWait && ct == 0) {
-                int32_t* cnt = p.unit_sync + 2 * u;
-                bool ready = false;
-                const uint64_t t0 = global_ns();
-                while (!(ready = ld_acquire_gpu(cnt + 1) == pc.n - 1) && global_ns() - t0 <= kWaitLimitNs) {
+            if (ct == 0) {
+                int32_t role = whole ? kRoleWhole : ticket == pc.n - 1 ? kRoleMerge : kRoleStore;
+                if (role == kRoleMerge) {
+                    int32_t* cnt = p.unit_sync + 2 * u;
+                    bool ready = ld_acquire_gpu(cnt + 1) == pc.n - 1;
+                    if (!ready) {
+                        const uint64_t t0 = global_ns();
+                        while (!(ready = ld_acquire_gpu(cnt + 1) == pc.n - 1) && global_ns() - t0 <= kWaitLimitNs) {
+                        }
+                    }
+                    if (ready) {
+                        cnt[0] = 0;  // every piece has drawn and stored: reset for the next launch
+                        cnt[1] = 0;
+                    } else {
+                        atomicOr(p.err, PDA_DEVERR_TIMEOUT_);
+                        *abort_flag = 1;
+                        role = kRoleAbort;
+                    }
                 }
-                if (ready) {
-                    cnt[0] = 0;
-                    cnt[1] = 0;
-                } else {
-                    atomicOr(p.err, PDA_DEVERR_TIMEOUT_);
-                    *abort_flag = 1;
-                    *st_role = kRoleAbort;
-                }
+                *st_role = role;
             }
             if (!consumer_sync(cbar, cphase, p.err, abort_flag)) break;
-            role = *st_role;
+            const int role = *st_role;
             if (role == kRoleAbort) break;
             const RowInfo ri = row_info<MQ>(p, m.b);
-            // Writes the merged state of q row h, columns d4..d4+3: o / l, or folded
-            // into the running state.
-            auto emit = [&](int h, int d4, float M, float Ls, float4 Os) {
+            const int SR = MQ ? p.rows_per_slot : G;  // rows per partial slot
+            for (int i4 = ct; i4 < NR * D / 4; i4 += C::kConsumerWarps * 32) {
+                const int h = (4 * i4) / D, d4 = 4 * i4 - h * D;  // h: q row of the unit
+                float M = kNegInf;
+#pragma unroll
+                for (int w = 0; w < C::kConsumerWarps; ++w) M = fmaxf(M, st_m[w * kMaxGroup + h]);
+                float Ls = 0.f;
+                float4 Os = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (M != kNegInf) {
+#pragma unroll
+                    for (int w = 0; w < C::kConsumerWarps; ++w) {
+                        const float f = ex2(st_m[w * kMaxGroup + h] - M);
+                        const float4 v = *reinterpret_cast<const float4*>(st_o + (size_t)(w * NR + h) * (D + 4) + d4);
+                        Ls += st_l[w * kMaxGroup + h] * f;
+                        Os.x += v.x * f; Os.y += v.y * f; Os.z += v.z * f; Os.w += v.w * f;
+                    }
+                }
+                if (role == kRoleStore) {
+                    const int64_t r = (int64_t)(u + (int)blockIdx.x) * SR + h;
+                    *reinterpret_cast<float4*>(p.part_o + r * D + d4) = Os;
+                    if (d4 == 0) {
+                        p.part_ml[r * 2] = M;
+                        p.part_ml[r * 2 + 1] = Ls;
+                    }
+                    continue;
+                }
+                if (role == kRoleMerge) {
+                    // every piece in piece order (this piece's own state in its
+                    // place), so the result does not depend on which piece
+                    // finished last; the others' partials are loaded up to eight
+                    // per memory round trip
+                    float Mr = kNegInf, Lr = 0.f;
+                    float4 Or = make_float4(0.f, 0.f, 0.f, 0.f);
+                    for (int i0 = 0; i0 < pc.n; i0 += 8) {
+                        float mi[8], li[8];
+                        float4 oi[8];
+                        bool own[8];
+#pragma unroll
+                        for (int k = 0; k < 8; ++k) {
+                            mi[k] = kNegInf;
+                            li[k] = 0.f;
+                            oi[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+                            const int64_t c = piece_cta(pc, i0 + k, gr);
+                            own[k] = i0 + k < pc.n && c == (int64_t)blockIdx.x;
+                            if (i0 + k >= pc.n || own[k]) continue;
+                            const int64_t r = (u + c) * SR + h;
+                            mi[k] = ld_cg(p.part_ml + r * 2);
+                            li[k] = ld_cg(p.part_ml + r * 2 + 1);
+                            oi[k] = __ldcg(reinterpret_cast<const float4*>(p.part_o + r * D + d4));
+                        }
+#pragma unroll
+                        for (int k = 0; k < 8; ++k) {
+                            if (own[k]) merge_state(Mr, Lr, Or, M, Ls, Os);
+                            else merge_state(Mr, Lr, Or, mi[k], li[k], oi[k]);
+                        }
+                    }
+                    M = Mr;
+                    Ls = Lr;
+                    Os = Or;
+                }
                 if constexpr (MODE == kTiled) {
-                    const int64_t row = (int64_t)m.b * p.Hq + (int64_t)m.kvh * G + h;  // plain decode rows
+                    // fold into the running state (plain decode rows: b*Hq + kvh*G + h)
+                    const int64_t row = (int64_t)m.b * p.Hq + (int64_t)m.kvh * G + h;
                     float Mo = st_x[h], Lo = st_x[kMaxGroup + h];
                     float4* so = reinterpret_cast<float4*>(p.o_state + row * D + d4);
                     float4 Oo = *so;
@@ -938,7 +974,7 @@ __device__ __forceinline__ void run_consumer(const SplitParams& p, uint32_t base
                     const float4 v = Ls > 0.f ? make_float4(Os.x / Ls, Os.y / Ls, Os.z / Ls, Os.w / Ls)
                                               : make_float4(0.f, 0.f, 0.f, 0.f);
                     const int64_t o = MQ ? qo_offset<MQ>(p, ri.b, ri.first + h / G, m.kvh * G + h % G, D) + d4
-                                         : qo_offset<MQ>(p, m.b, 0, m.kvh * G, D) + h * D + d4;
+                                         : qo_offset<MQ>(p, m.b, 0, m.kvh * G, D) + 4 * i4;
                     if (p.out_f32) {
                         *reinterpret_cast<float4*>(p.out_f32 + o) = v;
                     } else {
@@ -948,71 +984,6 @@ __device__ __forceinline__ void run_consumer(const SplitParams& p, uint32_t base
                         *reinterpret_cast<uint2*>(p.out + o) = w2;
                     }
                 }
-            };
-            // This CTA's own merged state of q row h, columns d4..d4+3, from the
-            // consumer warps' states staged in shared memory.
-            auto own_state = [&](int h, int d4, float& M, float& Ls, float4& Os) {
-                M = kNegInf;
-#pragma unroll
-                for (int w = 0; w < C::kConsumerWarps; ++w) M = fmaxf(M, st_m[w * kMaxGroup + h]);
-                Ls = 0.f;
-                Os = make_float4(0.f, 0.f, 0.f, 0.f);
-                if (M == kNegInf) return;
-#pragma unroll
-                for (int w = 0; w < C::kConsumerWarps; ++w) {
-                    const float f = ex2(st_m[w * kMaxGroup + h] - M);
-                    const float4 v = *reinterpret_cast<const float4*>(st_o + (size_t)(w * NR + h) * (D + 4) + d4);
-                    Ls += st_l[w * kMaxGroup + h] * f;
-                    Os.x += v.x * f; Os.y += v.y * f; Os.z += v.z * f; Os.w += v.w * f;
-                }
-            };
-            // In a merge, the partials of a batch of pieces are loaded together
-            // before any is folded.  Every piece is folded in piece order (this
-            // CTA's own piece from its own state), so the result does not depend
-            // on which piece merges.  A batch slot past the last piece, or this
-            // CTA's own, reads this CTA's slot and is not folded (the loads stay
-            // unconditional, so they issue back to back).
-            const int64_t self_row = (int64_t)(u + (int)blockIdx.x) * SR;
-            for (int i4 = ct; i4 < NR * D / 4; i4 += C::kConsumerWarps * 32) {
-                const int h = (4 * i4) / D, d4 = 4 * i4 - h * D;  // h: q row of the unit
-                float M, Ls;
-                float4 Os;
-                own_state(h, d4, M, Ls, Os);
-                if (role == kRoleStore) {
-                    *reinterpret_cast<float4*>(p.part_o + (self_row + h) * D + d4) = Os;
-                    if (d4 == 0) {
-                        p.part_ml[(self_row + h) * 2] = M;
-                        p.part_ml[(self_row + h) * 2 + 1] = Ls;
-                    }
-                    continue;
-                }
-                if (role != kRoleWhole) {
-                    float Mr = kNegInf, Lr = 0.f;
-                    float4 Or = make_float4(0.f, 0.f, 0.f, 0.f);
-                    for (int i0 = 0; i0 < pc.n; i0 += kMergeBatch) {
-                        float mi[kMergeBatch], li[kMergeBatch];
-                        float4 oi[kMergeBatch];
-                        int kind[kMergeBatch];  // 0: past the last piece, 1: own, 2: stored partial
-#pragma unroll
-                        for (int k = 0; k < kMergeBatch; ++k) {
-                            const int64_t c = piece_cta(pc, i0 + k, gr);
-                            kind[k] = i0 + k >= pc.n ? 0 : c == (int64_t)blockIdx.x ? 1 : 2;
-                            const int64_t row = (kind[k] == 2 ? (u + c) * SR : self_row) + h;
-                            mi[k] = ld_cg(p.part_ml + row * 2);
-                            li[k] = ld_cg(p.part_ml + row * 2 + 1);
-                            oi[k] = __ldcg(reinterpret_cast<const float4*>(p.part_o + row * D + d4));
-                        }
-#pragma unroll
-                        for (int k = 0; k < kMergeBatch; ++k) {
-                            if (kind[k] == 1) merge_state(Mr, Lr, Or, M, Ls, Os);
-                            else if (kind[k] == 2) merge_state(Mr, Lr, Or, mi[k], li[k], oi[k]);
-                        }
-                    }
-                    M = Mr;
-                    Ls = Lr;
-                    Os = Or;
-                }
-                emit(h, d4, M, Ls, Os);
             }
             if (!consumer_sync(cbar, cphase, p.err, abort_flag)) break;
             // a stored piece signals after every consumer thread's stores (ordered
@@ -1072,10 +1043,12 @@ __global__ void __maxnreg__(split_max_regs(D)) split_kernel(const __grid_constan
     pdl_wait_primary();
     // ends with __syncthreads (which also publishes the barriers)
     const int32_t nv_max = build_prefix<MODE == kMulti, C::kThreads>(p, pfx, scan);
-    const int64_t units = (int64_t)p.B * p.Hkv;
     int64_t begin, end;
+    const GroupRange gr = group_of_cta(blockIdx.x, pfx, p.B, rows_per_seq<MODE == kMulti>(p), p.Hkv,
+                                       gridDim.x);
+    const int64_t units = (int64_t)p.B * p.Hkv;
     if (unit_mode(units, gridDim.x, real_blocks(nv_max, p.unit_cost), C::kST, p.bs)) {
-        // CTA c: unit c whole (every segment is a whole unit)
+        // CTA c: unit c whole (every segment is a whole unit; gr is not used)
         begin = end = 0;
         if ((int64_t)blockIdx.x < units) {
             const int b = blockIdx.x / p.Hkv, kvh = blockIdx.x - b * p.Hkv;
@@ -1084,8 +1057,6 @@ __global__ void __maxnreg__(split_max_regs(D)) split_kernel(const __grid_constan
             end = begin + nv;
         }
     } else {
-        const GroupRange gr = group_of_cta(blockIdx.x, pfx, p.B, rows_per_seq<MODE == kMulti>(p), p.Hkv,
-                                           gridDim.x);
         group_cta_range(gr, blockIdx.x, &begin, &end);
     }
 
@@ -1093,7 +1064,7 @@ __global__ void __maxnreg__(split_max_regs(D)) split_kernel(const __grid_constan
         run_producer<D, ST, MODE>(p, base_s, L, pfx, meta, &abort_flag, begin, end, lane);
         return;
     }
-    run_consumer<D, ST, MODE>(p, base_s, base, L, meta, pfx, &abort_flag, warp, lane);
+    run_consumer<D, ST, MODE>(p, base_s, base, L, meta, pfx, gr, &abort_flag, warp, lane);
 }
 
 // Host side of one split-kernel shape: its entry points by mode and its

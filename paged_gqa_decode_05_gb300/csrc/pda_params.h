@@ -71,8 +71,8 @@ struct SplitParams {
     int64_t blk_s, tok_s, kvh_s;
     int64_t num_blocks;
     int32_t table_stride;
-    int32_t row_gather;          // 0: one 5-D TMA box per block; 1: TMA gather4 of rows
-                                 // (block sizes below 8); 2: 16-byte cp.async rows
+    int32_t row_gather;          // 0: one 5-D TMA box per block; rows one by one: 1: TMA
+                                 // gather4; 2: 16-byte cp.async
     int64_t row_blk, row_tok, row_kvh;  // strides in rows of D elements (gather4)
     int32_t lens_are_blocks;
     int32_t q_len;               // causal queries per sequence (0 or 1: plain decode)

@@ -194,18 +194,6 @@ __device__ __forceinline__ int32_t ld_acquire_gpu(const int32_t* p) {
     return v;
 }
 
-// A relaxed device-scope load (does not hold back later memory operations the
-// way an acquire load does); fence_acquire_gpu after it completes an acquire.
-__device__ __forceinline__ int32_t ld_relaxed_gpu(const int32_t* p) {
-    int32_t v;
-    asm volatile("ld.relaxed.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-    return v;
-}
-
-__device__ __forceinline__ void fence_acquire_gpu() {
-    asm volatile("fence.acq_rel.gpu;" ::: "memory");
-}
-
 // A float written by another CTA of this grid, read from L2 (never a stale
 // line of this SM's L1).
 __device__ __forceinline__ float ld_cg(const float* p) { return __ldcg(p); }
