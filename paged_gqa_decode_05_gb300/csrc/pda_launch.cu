@@ -5,6 +5,24 @@
 
 namespace pda {
 
+namespace {
+// Launch with programmatic stream serialization (see pda_aux.cuh).
+template <typename... Args>
+cudaError_t launch_pdl(void (*kernel)(Args...), int grid, int block, cudaStream_t stream, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid, 1, 1);
+    cfg.blockDim = dim3((unsigned)block, 1, 1);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+}  // namespace
+
 #define PDA_DECLARE_D(D)                                                                     \
     const void* split_kernel_fn_d##D(int st, int mode);                                     \
     int split_stages_d##D(int st);                                                           \
@@ -47,8 +65,7 @@ cudaError_t launch_reset_state(float* m, float* l, float* o, int64_t n_q, int32_
     if (n_q <= 0) return cudaSuccess;
     const int64_t n = n_q * D;
     const int grid = (int)((n + 255) / 256 < 4096 ? (n + 255) / 256 : 4096);
-    reset_state_kernel<<<grid, 256, 0, stream>>>(m, l, o, n_q, D);
-    return cudaGetLastError();
+    return launch_pdl(reset_state_kernel, grid, 256, stream, m, l, o, n_q, D);
 }
 
 cudaError_t launch_finalize(const float* l, const float* o, uint16_t* out, float* out_f32,
@@ -56,8 +73,7 @@ cudaError_t launch_finalize(const float* l, const float* o, uint16_t* out, float
     if (n_q <= 0) return cudaSuccess;
     const int64_t n = n_q * D;
     const int grid = (int)((n + 255) / 256 < 4096 ? (n + 255) / 256 : 4096);
-    finalize_kernel<<<grid, 256, 0, stream>>>(l, o, out, out_f32, n_q, D);
-    return cudaGetLastError();
+    return launch_pdl(finalize_kernel, grid, 256, stream, l, o, out, out_f32, n_q, D);
 }
 
 }  // namespace pda
@@ -86,8 +102,7 @@ cudaError_t launch_export_state(const float* m2, const float* l, const float* o,
     if (n_q <= 0) return cudaSuccess;
     const int64_t n = n_q * D;
     const int grid = (int)((n + 255) / 256 < 4096 ? (n + 255) / 256 : 4096);
-    export_state_kernel<<<grid, 256, 0, stream>>>(m2, l, o, m_out, l_out, o_out, n_q, D);
-    return cudaGetLastError();
+    return launch_pdl(export_state_kernel, grid, 256, stream, m2, l, o, m_out, l_out, o_out, n_q, D);
 }
 
 cudaError_t launch_merge_states(const float* m_parts, const float* l_parts, const float* o_parts,
@@ -96,8 +111,8 @@ cudaError_t launch_merge_states(const float* m_parts, const float* l_parts, cons
     if (n_q <= 0) return cudaSuccess;
     const int64_t n4 = n_q * D / 4;
     const int grid = (int)((n4 + 255) / 256 < 4096 ? (n4 + 255) / 256 : 4096);
-    merge_states_kernel<<<grid, 256, 0, stream>>>(m_parts, l_parts, o_parts, n_parts, n_q, D, out, out_f32);
-    return cudaGetLastError();
+    return launch_pdl(merge_states_kernel, grid, 256, stream, m_parts, l_parts, o_parts, n_parts, n_q, D,
+                      out, out_f32);
 }
 
 }  // namespace pda
