@@ -47,7 +47,7 @@
 extern "C" {
 #endif
 
-#define PDA_ABI_VERSION 3
+#define PDA_ABI_VERSION 4
 
 typedef struct pda_ctx pda_ctx;
 typedef void* pda_stream;      /* cudaStream_t */
@@ -203,9 +203,14 @@ pda_status pda_decode_contiguous(pda_ctx* ctx, const pda_bf16* q, const pda_bf16
  *   q, out   [batch, q_len, Hq, D] bf16, dense.
  *   seq_lens [batch] total tokens per sequence (device).
  *   batch * q_len <= max_seqs; other arguments as pda_decode.
- * Each query row is split like a sequence of its own; rows of one sequence
- * read the same blocks at nearly the same time, so the repeated reads come
- * mostly from L2.
+ * The queries of a sequence are packed G q heads each into launch rows, each
+ * row split over the GPU like a sequence of its own with one walk over the
+ * sequence's KV: up to 8 q rows per walk with the q rows as the MMA's N
+ * ("n8 form"); with more than 8 q rows per sequence (q_len * G > 8) and head
+ * sizes up to 128, up to 32 per walk with the q rows as the MMA's M ("row
+ * form", [CK] Overview: split-Q MMA).  Rows of one sequence read the same
+ * blocks at nearly the same time, so repeated walks read mostly from L2.
+ * pda_get_multi_info tells the shape a q_len takes.
  */
 pda_status pda_decode_multi(pda_ctx* ctx, const pda_bf16* q, const pda_bf16* k_pool,
                             const pda_bf16* v_pool, int64_t num_blocks,
@@ -361,6 +366,23 @@ typedef struct pda_launch_info {
     int32_t unit_cost;
 } pda_launch_info;
 pda_status pda_get_launch_info(const pda_ctx* ctx, pda_launch_info* info);
+
+/*
+ * The launch pda_decode_multi makes for q_len queries per sequence (host
+ * only): the form (0: n8, q rows as the MMA's N; 1: row form, q rows as its
+ * M), queries per launch row and their q rows (queries x G), launch rows
+ * (KV walks) per sequence, the grid and the pipeline depth.  q_len outside
+ * [1, split_ctas] is PDA_ERR_INVALID_ARG; q_len 1 describes plain decode.
+ */
+typedef struct pda_multi_info {
+    int32_t form;
+    int32_t queries_per_walk;
+    int32_t rows_per_walk;
+    int32_t walks_per_seq;
+    int32_t split_ctas;
+    int32_t stages;
+} pda_multi_info;
+pda_status pda_get_multi_info(const pda_ctx* ctx, int32_t q_len, pda_multi_info* info);
 
 /*
  * The split plan on its own (host only; no GPU needed).  The decode kernel

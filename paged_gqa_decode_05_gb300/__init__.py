@@ -58,8 +58,14 @@ class LaunchInfo(ctypes.Structure):
                 ("partial_slots", ctypes.c_int64), ("unit_cost", ctypes.c_int32)]
 
 
+class MultiInfo(ctypes.Structure):
+    _fields_ = [("form", ctypes.c_int32), ("queries_per_walk", ctypes.c_int32),
+                ("rows_per_walk", ctypes.c_int32), ("walks_per_seq", ctypes.c_int32),
+                ("split_ctas", ctypes.c_int32), ("stages", ctypes.c_int32)]
+
+
 _LIB: Optional[ctypes.CDLL] = None
-ABI_VERSION = 3  # PDA_ABI_VERSION of include/pda.h that these signatures follow
+ABI_VERSION = 4  # PDA_ABI_VERSION of include/pda.h that these signatures follow
 
 
 def library_path() -> str:
@@ -102,6 +108,7 @@ def lib() -> ctypes.CDLL:
         "pda_set_timing_events": (I32, [P, P, P, P]),
         "pda_check_wait_timeout": (I32, [P, I64, P]),
         "pda_get_launch_info": (I32, [P, ctypes.POINTER(LaunchInfo)]),
+        "pda_get_multi_info": (I32, [P, I32, ctypes.POINTER(MultiInfo)]),
         "pda_plan_units": (I32, [P, I32, I32, I32, I32, I32, I32, I32, P, P, ctypes.POINTER(I64)]),
     }
     for name, (res, args) in sig.items():
@@ -231,6 +238,12 @@ class Context:
         info = LaunchInfo()
         _check(lib().pda_get_launch_info(self._ctx, ctypes.byref(info)))
         return {f: getattr(info, f) for f, _ in LaunchInfo._fields_}
+
+    def multi_info(self, q_len: int) -> dict:
+        """The launch decode_multi makes for q_len queries per sequence (pda_get_multi_info)."""
+        info = MultiInfo()
+        _check(lib().pda_get_multi_info(self._ctx, int(q_len), ctypes.byref(info)))
+        return {f: getattr(info, f) for f, _ in MultiInfo._fields_}
 
     # -- argument checks (marshalling only)
     def _bf16(self, t, name, shape=None):

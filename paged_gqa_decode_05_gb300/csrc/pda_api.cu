@@ -75,6 +75,11 @@ struct pda_ctx {
     int split_ctas = 0;
     int smem_max = 0;
     int64_t slots = 0;
+    int64_t part_rows = 0;  // q rows the partial-state buffers hold (all slots)
+    // Row form of multi-query (one / two 16-row q tiles): grid and pipeline
+    // depth; a grid of 0 when the shape does not exist (head size 256).
+    int rows_ctas[2] = {0, 0};
+    int rows_stages[2] = {0, 0};
     float* part_o = nullptr;
     float* part_ml = nullptr;
     int32_t* unit_sync = nullptr;  // [chunk_b*Hkv][2] split-unit tickets and stored counts
@@ -190,22 +195,24 @@ void set_pool_params(pda::SplitParams& p, const pda_dims& d, const PoolArgs& a, 
     p.row_kvh = a.kvh / d.head_dim;
 }
 
-// Dynamic shared memory allowed for a split-kernel shape: what a launch of a
-// full batch (kMaxLaunchBatch sequences) uses, so every caller sets the same
-// value and none lowers it below what another launches with.
-int split_smem_limit(int D, int st) {
-    return (int)pda::smem_layout(D, st, pda::split_stages(D, st), pda::kMaxGroup, pda::kMaxLaunchBatch).total;
+// Dynamic shared memory allowed for a split-kernel shape and mode: what a
+// launch of a full batch (max_launch_rows(mode) sequences) uses, so every
+// caller sets the same value and none lowers it below what another launches
+// with.
+int split_smem_limit(int D, int st, int mode) {
+    return (int)pda::smem_layout(D, st, mode, pda::split_stages(D, st, mode), pda::max_launch_rows(mode)).total;
 }
 
 // Sets the shared-memory attributes of every mode of a split-kernel shape on
-// the current device.
+// the current device (modes the shape does not have are skipped).
 pda_status set_split_attributes(int D, int st, int optin) {
-    const int limit = split_smem_limit(D, st);
-    if (limit > optin)
-        return fail(PDA_ERR_UNSUPPORTED, "needs %d bytes of shared memory per CTA (device allows %d)",
-                    limit, optin);
     for (int mode = 0; mode < pda::kNumModes; ++mode) {
         const void* fn = pda::split_kernel_fn(D, st, mode);
+        if (!fn) continue;
+        const int limit = split_smem_limit(D, st, mode);
+        if (limit > optin)
+            return fail(PDA_ERR_UNSUPPORTED, "needs %d bytes of shared memory per CTA (device allows %d)",
+                        limit, optin);
         cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, limit);
         if (e == cudaSuccess)
             e = cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout,
@@ -254,6 +261,28 @@ pda_status check_plan_size(int64_t rows, int32_t table_width, int32_t unit_cost)
     return PDA_OK;
 }
 
+// The launch shape of a call: the mode, queries per launch row (qp), grid
+// and pipeline depth.  Multi-query calls with more than 8 q rows per
+// sequence (q_len * G) take the row form when the context's shape has it.
+struct MultiShape {
+    int mode, qp, grid, stages;
+};
+MultiShape multi_shape(const pda_ctx* ctx, int mode, int32_t q_len) {
+    MultiShape s = {mode, 1, ctx->split_ctas, ctx->stages};
+    if (mode != pda::kMulti) return s;
+    const int G = ctx->G;
+    if (q_len * G > pda::kMaxGroup && ctx->rows_ctas[1] > 0) {
+        s.qp = std::min(q_len, pda::kMaxRowsPerWalk / G);
+        const int k = s.qp * G <= 16 && ctx->rows_ctas[0] > 0 ? 0 : 1;
+        s.mode = k ? pda::kMultiRows32 : pda::kMultiRows16;
+        s.grid = ctx->rows_ctas[k];
+        s.stages = ctx->rows_stages[k];
+    } else {
+        s.qp = std::max(1, std::min(q_len, pda::kMaxGroup / G));
+    }
+    return s;
+}
+
 pda_status run(pda_ctx* ctx, const RunArgs& r) {
     if (!ctx) return fail(PDA_ERR_INVALID_ARG, "ctx is NULL");
     const pda_dims& d = ctx->dims;
@@ -281,7 +310,7 @@ pda_status run(pda_ctx* ctx, const RunArgs& r) {
     if (r.table_stride < 1)
         return fail(PDA_ERR_INVALID_ARG, "block table width must be >= 1 (got %d)", r.table_stride);
     st = check_plan_size((int64_t)r.batch * r.q_len, r.table_stride,
-                         pda::unit_cost_blocks(ctx->stage_rows, d.head_dim, d.block_size, r.mode == pda::kMulti));
+                         pda::unit_cost_blocks(ctx->stage_rows, d.head_dim, d.block_size, pda::is_multi(r.mode)));
     if (st != PDA_OK) return st;
     float scale_log2 = 0.f;
     st = check_scale(r.scale, d.head_dim, &scale_log2);
@@ -306,13 +335,23 @@ pda_status run(pda_ctx* ctx, const RunArgs& r) {
     const int32_t Hq = d.num_q_heads, Hkv = d.num_kv_heads, D = d.head_dim;
     const bool timing = ctx->ev_begin && ctx->ev_split && ctx->ev_end && pda::writes_output(r.mode);
     const int64_t dbg_row_tokens = (int64_t)r.table_stride * d.block_size;
-    // Causal multi-query: qp queries of a sequence share one launch row (the
-    // MMA's N = qp*G <= 8); a sequence has Qr rows.  The launch is over
-    // batch * Qr rows, chunked on whole sequences.
-    const int32_t qp = r.q_len > 1 ? std::max(1, std::min(r.q_len, pda::kMaxGroup / ctx->G)) : 1;
+    // Causal multi-query: qp queries of a sequence share one launch row of
+    // qp*G q rows; a sequence has Qr launch rows.  Up to 8 q rows take the n8
+    // form; more take the row form where the shape has it (head sizes up to
+    // 128): one KV walk for up to 32 q rows, one or two 16-row q tiles.
+    const MultiShape ms = multi_shape(ctx, r.mode, r.q_len);
+    const int mode = ms.mode, qp = ms.qp, grid = ms.grid, stages = ms.stages;
     const int32_t Qr = (r.q_len + qp - 1) / qp;
+    const int32_t SR = r.q_len > 1 ? qp * ctx->G : ctx->G;  // q rows per partial-state slot
     const int32_t rows_total = r.batch * Qr;
-    const int32_t chunk_rows = (pda::kMaxLaunchBatch / Qr) * Qr;
+    // Launch rows per chunk (whole sequences): at most max_launch_rows(mode),
+    // and the partial states of (rows x Hkv + grid) slots of SR rows must fit
+    // the context's buffers.
+    const int64_t fit = (ctx->part_rows / SR - grid) / Hkv;
+    const int32_t chunk_rows = (int32_t)(std::min<int64_t>(pda::max_launch_rows(mode), fit) / Qr) * Qr;
+    if (chunk_rows < 1)
+        return fail(PDA_ERR_UNSUPPORTED, "q_len %d: a sequence's %d launch rows exceed the partial-state buffers",
+                    r.q_len, Qr);
     for (int32_t c0 = 0; c0 < rows_total; c0 += chunk_rows) {
         const int32_t cb = std::min(chunk_rows, rows_total - c0);
         const int32_t s0 = c0 / Qr;  // first sequence of the chunk
@@ -321,7 +360,7 @@ pda_status run(pda_ctx* ctx, const RunArgs& r) {
         p.lens = r.lens + s0;
         p.q_len = r.q_len;
         p.qp = qp;
-        p.rows_per_slot = qp * ctx->G;
+        p.rows_per_slot = SR;
         p.last_valid = r.last_valid ? r.last_valid + s0 : nullptr;
         p.out = r.out ? r.out + (int64_t)s0 * r.q_len * Hq * D : nullptr;
         p.out_f32 = r.out_f32 ? r.out_f32 + (int64_t)s0 * r.q_len * Hq * D : nullptr;
@@ -342,17 +381,17 @@ pda_status run(pda_ctx* ctx, const RunArgs& r) {
         p.Hkv = Hkv;
         p.G = ctx->G;
         p.bs = d.block_size;
-        p.unit_cost = pda::unit_cost_blocks(ctx->stage_rows, d.head_dim, d.block_size, r.mode == pda::kMulti);
+        p.unit_cost = pda::unit_cost_blocks(ctx->stage_rows, d.head_dim, d.block_size, mode == pda::kMulti);
         p.dbg_row_tokens = (int32_t)dbg_row_tokens;
         p.scale_log2 = scale_log2;
-        const size_t smem = pda::smem_layout(D, ctx->stage_rows, ctx->stages, ctx->G, cb).total;
+        const size_t smem = pda::smem_layout(D, ctx->stage_rows, mode, stages, cb).total;
 
         cudaError_t e;
         if (timing && c0 == 0 && (e = cudaEventRecord(ctx->ev_begin, r.stream)) != cudaSuccess)
             return cuda_fail(e, "cudaEventRecord");
-        e = pda::launch_split(D, ctx->stage_rows, r.mode, p, ctx->split_ctas, smem, r.stream);
+        e = pda::launch_split(D, ctx->stage_rows, mode, p, grid, smem, r.stream);
         if (e != cudaSuccess) return cuda_fail(e, "split kernel launch");
-        if (r.mode == pda::kGather) continue;
+        if (mode == pda::kGather) continue;
         if (timing && ((e = cudaEventRecord(ctx->ev_split, r.stream)) != cudaSuccess ||
                        (e = cudaEventRecord(ctx->ev_end, r.stream)) != cudaSuccess))
             return cuda_fail(e, "cudaEventRecord");
@@ -458,9 +497,9 @@ PDA_EXPORT pda_status pda_create(const pda_dims* dims, pda_ctx** out_ctx) {
     ctx->num_sms = prop.multiProcessorCount;
     const int D = dims->head_dim;
     ctx->stage_rows = pda::stage_tokens(D, dims->block_size);
-    ctx->stages = pda::split_stages(D, ctx->stage_rows);
+    ctx->stages = pda::split_stages(D, ctx->stage_rows, pda::kOneShot);
     const int chunk_b = std::min(dims->max_seqs, pda::kMaxLaunchBatch);
-    ctx->smem_max = (int)pda::smem_layout(D, ctx->stage_rows, ctx->stages, ctx->G, chunk_b).total;
+    ctx->smem_max = (int)pda::smem_layout(D, ctx->stage_rows, pda::kOneShot, ctx->stages, chunk_b).total;
     if (ctx->smem_max > (int)prop.sharedMemPerBlockOptin) {
         delete ctx;
         return fail(PDA_ERR_UNSUPPORTED, "needs %d bytes of shared memory per CTA (device allows %d)",
@@ -473,18 +512,42 @@ PDA_EXPORT pda_status pda_create(const pda_dims* dims, pda_ctx** out_ctx) {
     int per_sm = 0;
     e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm,
                                                       pda::split_kernel_fn(D, ctx->stage_rows, pda::kOneShot),
-                                                      pda::split_threads(ctx->stage_rows), ctx->smem_max);
+                                                      pda::split_threads(ctx->stage_rows, pda::kOneShot),
+                                                      ctx->smem_max);
     if (e != cudaSuccess) { delete ctx; return cuda_fail(e, "occupancy query"); }
     if (per_sm < 1) { delete ctx; return fail(PDA_ERR_UNSUPPORTED, "split kernel does not fit on an SM"); }
     ctx->ctas_per_sm = per_sm;
     ctx->split_ctas = per_sm * ctx->num_sms;
     ctx->slots = (int64_t)chunk_b * dims->num_kv_heads + ctx->split_ctas;
+    // The row form of multi-query, where the shape has it: its own occupancy.
+    for (int k = 0; k < 2; ++k) {
+        const int mode = k ? pda::kMultiRows32 : pda::kMultiRows16;
+        const void* fn = pda::split_kernel_fn(D, ctx->stage_rows, mode);
+        if (!fn) continue;
+        int n = 0;
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, pda::split_threads(ctx->stage_rows, mode),
+                                                          split_smem_limit(D, ctx->stage_rows, mode));
+        if (e != cudaSuccess) { delete ctx; return cuda_fail(e, "occupancy query"); }
+        ctx->rows_ctas[k] = n * ctx->num_sms;
+        ctx->rows_stages[k] = pda::split_stages(D, ctx->stage_rows, mode);
+    }
+    // Partial states: slots of G <= 8 rows for plain decode and the n8 form
+    // (chunk_b x Hkv units plus one slot per CTA).  The row form's launch
+    // rows hold up to 32 q rows, but a full batch of max_seqs <= 1024
+    // sequences has launch rows x Hkv x rows per slot below 2 x max_seqs x
+    // Hq <= 16 x chunk_b x Hkv, plus 32 rows per CTA of its grid: with that
+    // room every call runs in one launch.
+    ctx->part_rows = ctx->slots * pda::kMaxGroup;
+    if (ctx->rows_ctas[1] > 0)
+        ctx->part_rows = std::max<int64_t>(ctx->part_rows,
+                                           (int64_t)chunk_b * dims->num_kv_heads * 2 * pda::kMaxGroup +
+                                               (int64_t)std::max(ctx->rows_ctas[0], ctx->rows_ctas[1]) *
+                                                   pda::kMaxRowsPerWalk);
 
     const int64_t nq = (int64_t)dims->max_seqs * dims->num_q_heads;
     struct { void** ptr; size_t bytes; } allocs[] = {
-        // partial states: up to kMaxGroup q rows per slot (packed multi-query rows)
-        {(void**)&ctx->part_o, (size_t)ctx->slots * pda::kMaxGroup * D * sizeof(float)},
-        {(void**)&ctx->part_ml, (size_t)ctx->slots * pda::kMaxGroup * 2 * sizeof(float)},
+        {(void**)&ctx->part_o, (size_t)ctx->part_rows * D * sizeof(float)},
+        {(void**)&ctx->part_ml, (size_t)ctx->part_rows * 2 * sizeof(float)},
         {(void**)&ctx->unit_sync, (size_t)chunk_b * dims->num_kv_heads * 2 * sizeof(int32_t)},
         {(void**)&ctx->err, sizeof(uint32_t)},
         {(void**)&ctx->m_state, (size_t)nq * sizeof(float)},
@@ -705,6 +768,21 @@ PDA_EXPORT pda_status pda_get_launch_info(const pda_ctx* ctx, pda_launch_info* i
     return PDA_OK;
 }
 
+PDA_EXPORT pda_status pda_get_multi_info(const pda_ctx* ctx, int32_t q_len, pda_multi_info* info) {
+    if (!ctx || !info) return fail(PDA_ERR_INVALID_ARG, "NULL argument");
+    if (q_len < 1 || q_len > std::min(pda::kMaxLaunchBatch, ctx->split_ctas))
+        return fail(PDA_ERR_INVALID_ARG, "q_len %d outside [1, %d]", q_len,
+                    std::min(pda::kMaxLaunchBatch, ctx->split_ctas));
+    const MultiShape ms = multi_shape(ctx, q_len > 1 ? pda::kMulti : pda::kOneShot, q_len);
+    info->form = pda::q_tiles(ms.mode) > 0 ? 1 : 0;
+    info->queries_per_walk = ms.qp;
+    info->rows_per_walk = ms.qp * ctx->G;
+    info->walks_per_seq = (q_len + ms.qp - 1) / ms.qp;
+    info->split_ctas = ms.grid;
+    info->stages = ms.stages;
+    return PDA_OK;
+}
+
 PDA_EXPORT pda_status pda_plan_units(const int32_t* lens, int32_t batch, int32_t blocks_given,
                                      int32_t block_size, int32_t num_kv_heads, int32_t split_ctas,
                                      int32_t unit_cost, int32_t stage_tokens, int32_t* first_cta,
@@ -871,11 +949,12 @@ PDA_EXPORT pda_status pda_decode_noalloc(const pda_bf16* q, const pda_bf16* k_po
     }
 
     const int rows = pda::stage_tokens(D, block_size);  // split-kernel shape, as pda_create picks it
-    const int stages = pda::split_stages(D, rows);
-    const size_t smem = pda::smem_layout(D, rows, stages, G, batch).total;
+    const int stages = pda::split_stages(D, rows, pda::kOneShot);
+    const size_t smem = pda::smem_layout(D, rows, pda::kOneShot, stages, batch).total;
     const void* split_fn = pda::split_kernel_fn(D, rows, pda::kOneShot);
     int per_sm = 0;
-    if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, split_fn, pda::split_threads(rows), smem)) !=
+    if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, split_fn,
+                                                           pda::split_threads(rows, pda::kOneShot), smem)) !=
         cudaSuccess)
         return cuda_fail(e, "occupancy query");
     if (per_sm < 1) return fail(PDA_ERR_UNSUPPORTED, "split kernel does not fit on an SM");

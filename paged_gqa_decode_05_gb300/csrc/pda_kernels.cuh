@@ -34,6 +34,9 @@
 namespace pda {
 
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // each mbarrier wait gives up after 2 s
+// Row form of multi-query: how far (base-2 units) a row's softmax reference may
+// lag its running max before o is rescaled (weights stay below 2^8).
+constexpr float kLazyLog2 = 8.f;
 #define kNegInf (-__int_as_float(0x7f800000))
 
 #define PDA_DEVERR_BAD_BLOCK_ID_ 0x1u
@@ -55,24 +58,49 @@ constexpr uint64_t kWaitLimitNs = 2000000000ull;  // each mbarrier wait gives up
 #define PDA_STAGES_D256_ST32 3
 #endif
 
-// Register cap of the split kernel (see split_kernel).
-constexpr int split_max_regs(int D) { return D == 256 ? 255 : 168; }
+// Register cap of the split kernel (see split_kernel).  An SM's registers
+// are four 16K quarters, one per scheduler, and a warp takes its registers
+// from its scheduler's quarter: with 9 or 10 warps per SM (one CTA of 9 warps,
+// or two of 5) a quarter holds 3 warps, at most 168 registers per thread.
+constexpr int split_max_regs(int D, int mode) { return D == 256 && q_tiles(mode) == 0 ? 255 : 168; }
 
-template <int D, int ST>
+// Row form of multi-query (q rows as the MMA's M): one q tile runs two CTAs
+// per SM like plain decode; two q tiles (8 consumer warps) run one CTA per
+// SM with a deeper ring.
+#ifndef PDA_STAGES_ROWS16_D64
+#define PDA_STAGES_ROWS16_D64 5
+#endif
+#ifndef PDA_STAGES_ROWS16_D128
+#define PDA_STAGES_ROWS16_D128 3
+#endif
+#ifndef PDA_STAGES_ROWS32_D64
+#define PDA_STAGES_ROWS32_D64 10
+#endif
+#ifndef PDA_STAGES_ROWS32_D128
+#define PDA_STAGES_ROWS32_D128 5
+#endif
+
+// Split-kernel shape: head size D, ST KV rows per stage, MODE (the row form
+// of multi-query has its own warp count and q area).
+template <int D, int ST, int MODE>
 struct Cfg {
     static constexpr int kST = ST;                       // KV rows per stage (64 or 32)
     static constexpr int kLogST = ST == 64 ? 6 : 5;
-    static constexpr int kConsumerWarps = ST / 16;       // 16 rows each
+    static constexpr int kQTiles = q_tiles(MODE);        // 16-row q tiles (0: n8 form)
+    static constexpr int kConsumerWarps = consumer_warps(ST, MODE);  // 16 KV rows each (per q tile)
     static constexpr int kThreads = (kConsumerWarps + 1) * 32;  // + the producer warp
     static constexpr int kHalves = D / 64;               // 64-column swizzled slabs per row
     static constexpr int kHalfBytes = ST * 128;          // ST rows of one slab
     static constexpr int kTileBytes = kHalves * kHalfBytes;
-    static constexpr int kStageBytes = 2 * kTileBytes + 16 * D;
-    static constexpr int kStages = D == 64 ? PDA_STAGES_D64
+    static constexpr int kStageBytes = 2 * kTileBytes + stage_q_rows(MODE) * D * 2;
+    static constexpr int kStages = kQTiles == 1 ? (D == 64 ? PDA_STAGES_ROWS16_D64 : PDA_STAGES_ROWS16_D128)
+                                 : kQTiles == 2 ? (D == 64 ? PDA_STAGES_ROWS32_D64 : PDA_STAGES_ROWS32_D128)
+                                 : D == 64 ? PDA_STAGES_D64
                                  : D == 128 ? PDA_STAGES_D128
                                  : ST == 32 ? PDA_STAGES_D256_ST32 : PDA_STAGES_D256;
     static constexpr int kKSteps = D / 16;
     static_assert(ST == 64 || ST == 32, "stage rows");
+    static_assert(kQTiles == 0 || (ST == 64 && D <= 128), "row form: 64-row stages, head size <= 128");
 };
 
 // Causal multi-query decode packs qp queries of a sequence into one launch
@@ -209,12 +237,12 @@ __device__ __forceinline__ int32_t build_prefix(const SplitParams& p, int32_t* p
     }
     if (lane == 31) {
         scan[warp] = x;
-        scan[8 + warp] = big;
+        scan[16 + warp] = big;
     }
     __syncthreads();
     int32_t run = x - sum;
     for (int w = 0; w < warp; ++w) run += scan[w];
-    for (int w = 0; w < kThreads / 32; ++w) big = max(big, scan[8 + w]);
+    for (int w = 0; w < kThreads / 32; ++w) big = max(big, scan[16 + w]);
     if (tid == kThreads - 1) pfx[p.B] = run + sum;
 #pragma unroll
     for (int k = 0; k < kPer; ++k)
@@ -242,9 +270,9 @@ __device__ __forceinline__ void run_producer(const SplitParams& p, uint32_t base
     // 128 entries of the current sequence's row (the next kv head starts
     // there) and nx[] those of the next non-empty sequence, loaded one unit
     // ahead together with the entry its last block's valid slots come from.
-    using C = Cfg<D, ST>;
+    using C = Cfg<D, ST, MODE>;
     constexpr int S = C::kStages;
-    constexpr bool MQ = MODE == kMulti;
+    constexpr bool MQ = is_multi(MODE);
     const uint32_t full0 = base_s + L.bars, empty0 = full0 + 8 * S;
     const bool leader = lane == 0;
     // K/V are read once: evict them first.  With several query rows per
@@ -629,13 +657,14 @@ __device__ __forceinline__ void run_consumer(const SplitParams& p, uint32_t base
                                              const SmemLayout& L, const StageMeta* meta,
                                              const int32_t* pfx, const GroupRange& gr,
                                              volatile int* abort_flag, int warp, int lane) {
-    using C = Cfg<D, ST>;
+    using C = Cfg<D, ST, MODE>;
     constexpr int S = C::kStages;
     constexpr int KS = C::kKSteps;
     const uint32_t full0 = base_s + L.bars, empty0 = full0 + 8 * S;
     const int g = lane >> 2, t = lane & 3;
     const int r0 = warp * 16;
     constexpr bool MQ = MODE == kMulti;
+    static_assert(C::kQTiles == 0, "n8 form");
     const int G = p.G;
     const float sl2 = p.scale_log2;
     // multi-query: the queries of this lane's two score columns (column n is
@@ -997,6 +1026,381 @@ __device__ __forceinline__ void run_consumer(const SplitParams& p, uint32_t base
     }
 }
 
+// ------------------------------------------------------- row-form consumer
+//
+// Causal multi-query with more than 8 q rows per KV walk (head sizes up to
+// 128).  The launch row's packed q rows (row r: query r / G, head r % G) are
+// the MMA's M, so one walk over the KV serves up to 32 of them.  Consumer
+// warp w takes token slice ts = w % (ST/16), the stage rows 16 ts .. 16 ts +
+// 15, and q tile qt = w / (ST/16), the q rows 16 qt .. 16 qt + 15:
+//   S (16 q rows x 16 tokens) = Q K^T as two n8 tiles of tokens, K read as the
+//     B operand (ldmatrix, rows = tokens);
+//   the online-softmax update runs per q row on the accumulator fragments
+//     (max over the tokens: the four lanes of a quad);
+//   O (16 q rows x D) += P V, the score fragments serving as P's A fragments
+//     where they stand (bf16 hi + lo parts), V read transposed as the B operand.
+// Each warp keeps (m, l, o) of its q rows over its token slice.  At a segment
+// end the slices of each q tile merge in shared memory, one q tile at a time,
+// and the unit roles follow as in the n8 form (run_consumer).
+
+// Zero output rows of the units with no tokens (they have no segment), shared
+// round-robin over the grid: the stores overlap the wait for the first stage.
+template <int D, int kThreadsC>
+__device__ __forceinline__ void zero_empty_rows(const SplitParams& p, const int32_t* pfx, int ct) {
+    for (int u = blockIdx.x; u < p.B * p.Hkv; u += gridDim.x) {
+        const int sq = u / p.Hkv, kvh = u - sq * p.Hkv;
+        if (pfx[sq + 1] != pfx[sq]) continue;
+        const RowInfo ri = row_info<true>(p, sq);
+        const int NR = ri.cnt * p.G;
+        for (int i4 = ct; i4 < NR * D / 4; i4 += kThreadsC) {
+            const int h = (4 * i4) / D, d4 = 4 * i4 - h * D;
+            const int64_t o = qo_offset<true>(p, ri.b, ri.first + h / p.G, kvh * p.G + h % p.G, D) + d4;
+            if (p.out_f32) *reinterpret_cast<float4*>(p.out_f32 + o) = make_float4(0.f, 0.f, 0.f, 0.f);
+            else *reinterpret_cast<uint2*>(p.out + o) = make_uint2(0u, 0u);
+        }
+    }
+}
+
+template <int D, int ST, int MODE>
+__device__ __forceinline__ void run_consumer_rows(const SplitParams& p, uint32_t base_s, uint8_t* base,
+                                                  const SmemLayout& L, const StageMeta* meta,
+                                                  const int32_t* pfx, const GroupRange& gr,
+                                                  volatile int* abort_flag, int warp, int lane) {
+    using C = Cfg<D, ST, MODE>;
+    constexpr int S = C::kStages;
+    constexpr int KS = C::kKSteps;       // 16-column steps of D
+    constexpr int NT = D / 8;            // n8 tiles of O over D
+    constexpr int kSlices = ST / 16;     // token slices of a stage
+    constexpr int kThreadsC = C::kConsumerWarps * 32;
+    constexpr int kOStride = D + 8;      // staged o row (floats): quads of rows fall in distinct banks
+    static_assert(C::kQTiles > 0, "row form");
+    static_assert(kSlices * 16 * kOStride * 4 <= C::kStageBytes, "one q tile's staged states fit a stage");
+    static_assert(kSlices <= 4 && C::kQTiles * 16 <= kMaxRowsPerWalk, "st_m / st_l capacity");
+    const uint32_t full0 = base_s + L.bars, empty0 = full0 + 8 * S;
+    const int g = lane >> 2, t = lane & 3;
+    const int ts = warp % kSlices, qt = warp / kSlices;
+    const int r0 = ts * 16;                          // the warp's first row of a stage
+    const int G = p.G;
+    const float sl2 = p.scale_log2;
+    const int row0 = qt * 16 + g, row1 = row0 + 8;   // this lane's q rows
+    const int qc0 = row0 / G, qc1 = row1 / G;        // their queries within the launch row
+    // ldmatrix row addresses: QK reads K as the B operand (matrices: tokens
+    // 0-7 / 8-15 by columns lo / hi), PV reads V transposed as the B operand
+    // (matrices: tokens 0-7 / 8-15 of columns lo, then of columns hi).
+    const int k_row = r0 + (lane & 7) + ((lane >> 4) << 3);
+    const int k_cpar = (lane >> 3) & 1;
+    const int v_row = r0 + (lane & 7) + (((lane >> 3) & 1) << 3);
+    const int v_cpar = lane >> 4;
+    const int lbs = p.row_gather ? C::kLogST : 31 - __clz(p.bs);
+    int swh[C::kHalves];  // swizzle of this lane's ldmatrix rows in slab h (row & 7 == lane & 7)
+#pragma unroll
+    for (int h = 0; h < C::kHalves; ++h) swh[h] = swz(lane, h, lbs);
+    const uint32_t hs = (uint32_t)(128 << lbs);
+    const uint32_t k_off = row_off<D>(k_row, lbs);
+    const uint32_t v_off = row_off<D>(v_row, lbs);
+
+    float o[NT][4];      // rows row0 ([0], [1]) and row1 ([2], [3]), columns 8i + 2t, + 1
+    uint32_t qa[KS][4];  // Q's A fragments
+    float m0 = kNegInf, m1 = kNegInf, l0 = 0.f, l1 = 0.f;
+#pragma unroll
+    for (int i = 0; i < NT; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+#pragma unroll
+    for (int kk = 0; kk < KS; ++kk) qa[kk][0] = qa[kk][1] = qa[kk][2] = qa[kk][3] = 0u;
+
+    const uint32_t cbar = base_s + L.cbar;
+    uint32_t cphase = 0;
+    int stage = 0;
+    uint32_t phase = 0;
+    int32_t ticket = 0;  // consumer thread 0: this piece's ticket for its split unit
+    const int ct = warp * 32 + lane;
+    zero_empty_rows<D, kThreadsC>(p, pfx, ct);
+
+    while (true) {
+        if (*abort_flag) break;
+        if (!mbar_wait_bounded(full0 + 8 * stage, phase, kWaitLimitNs)) {
+            atomicOr(p.err, PDA_DEVERR_TIMEOUT_);
+            *abort_flag = 1;
+            break;
+        }
+        const StageMeta m = meta[stage];
+        if (m.flags & kDone) break;
+        if (warp == 0 && lane == 0 && (m.flags & kSegEnd) && !(m.flags & kWholeUnit))
+            ticket = atomicAdd(p.unit_sync + 2 * (m.b * p.Hkv + m.kvh), 1);
+        const uint32_t sK = base_s + (uint32_t)stage * C::kStageBytes;
+        const uint32_t sV = sK + C::kTileBytes;
+
+        if (m.flags & kSegBegin) {  // (m, l, o) are reset: at the start and after each segment end
+            const uint8_t* sq = base + (sV - base_s) + C::kTileBytes;  // [nr][D] bf16
+            const bool v0 = row0 < m.nr, v1 = row1 < m.nr;
+#pragma unroll
+            for (int kk = 0; kk < KS; ++kk) {
+                const uint8_t* ra = sq + (size_t)(row0 * D + 16 * kk + 2 * t) * 2;
+                const uint8_t* rb = sq + (size_t)(row1 * D + 16 * kk + 2 * t) * 2;
+                qa[kk][0] = v0 ? *reinterpret_cast<const uint32_t*>(ra) : 0u;
+                qa[kk][1] = v1 ? *reinterpret_cast<const uint32_t*>(rb) : 0u;
+                qa[kk][2] = v0 ? *reinterpret_cast<const uint32_t*>(ra + 16) : 0u;
+                qa[kk][3] = v1 ? *reinterpret_cast<const uint32_t*>(rb + 16) : 0u;
+            }
+        }
+        // a q tile past the launch row's rows has nothing to compute
+        if (r0 < m.n_valid && qt * 16 < m.nr) {
+            const bool partial = r0 + 16 > m.n_valid;
+            if (partial) {  // V rows past the valid ones may hold anything: P V must see zeros
+                zero_rows<D>(sV, m.n_valid, r0 + 16, lbs, lane);
+                __syncwarp();
+            }
+            // S = Q K^T: s[j] holds tokens r0 + 8j .. r0 + 8j + 7 (two independent chains)
+            float s[2][4];
+#pragma unroll
+            for (int j = 0; j < 2; ++j) s[j][0] = s[j][1] = s[j][2] = s[j][3] = 0.f;
+#pragma unroll
+            for (int kk = 0; kk < KS; ++kk) {
+                uint32_t b[4];
+                const int cc = (((kk & 3) << 1) + k_cpar) ^ swh[kk >> 2];
+                ldsm_x4(sK + k_off + (uint32_t)(kk >> 2) * hs + (cc << 4), b);
+                mma_16816(s[0], qa[kk], b[0], b[1]);
+                mma_16816(s[1], qa[kk], b[2], b[3]);
+            }
+            // element [j][e]: q row e < 2 ? row0 : row1, stage row r0 + 8j + 2t + (e & 1)
+#pragma unroll
+            for (int j = 0; j < 2; ++j)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) s[j][e] *= sl2;
+            // Masks: the rows past the stage's valid ones and, causally, the tokens
+            // past a row's query (query qi of the launch row sees tokens up to
+            // m.lim + qi).  Element [j][e] stays iff 8j + (e & 1) <= th(e); the
+            // thresholds are taken once, and stages that need no mask skip it.
+            const int pos0 = m.j0 * p.bs + r0;  // the warp's first token
+            if (partial || pos0 + 15 > m.lim) {
+                const int tv = m.n_valid - 1 - r0 - 2 * t;
+                const int th0 = min(tv, m.lim + qc0 - pos0 - 2 * t);
+                const int th1 = min(tv, m.lim + qc1 - pos0 - 2 * t);
+#pragma unroll
+                for (int j = 0; j < 2; ++j)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        if (8 * j + (e & 1) > (e < 2 ? th0 : th1)) s[j][e] = kNegInf;
+            }
+            // row max over the 16 tokens (the quad's lanes)
+            float x0 = fmaxf(fmaxf(s[0][0], s[0][1]), fmaxf(s[1][0], s[1][1]));
+            float x1 = fmaxf(fmaxf(s[0][2], s[0][3]), fmaxf(s[1][2], s[1][3]));
+            x0 = fmaxf(x0, __shfl_xor_sync(0xffffffffu, x0, 1));
+            x1 = fmaxf(x1, __shfl_xor_sync(0xffffffffu, x1, 1));
+            x0 = fmaxf(x0, __shfl_xor_sync(0xffffffffu, x0, 2));
+            x1 = fmaxf(x1, __shfl_xor_sync(0xffffffffu, x1, 2));
+            // Lazy rescale: a row's reference m moves only when the stage's max
+            // exceeds it by more than kLazyLog2, so the weights p = 2^(s - m) stay
+            // below 2^kLazyLog2; (m, l, o) means the same for any reference, and
+            // o is rescaled only a few times per segment, not whenever a max grows.
+            const bool up0 = x0 > m0 + kLazyLog2, up1 = x1 > m1 + kLazyLog2;
+            if (__any_sync(0xffffffffu, up0 || up1)) {
+                const float a0 = up0 ? ex2(m0 - x0) : 1.f;  // an empty row (m = -inf): 0
+                const float a1 = up1 ? ex2(m1 - x1) : 1.f;
+                if (up0) m0 = x0;
+                if (up1) m1 = x1;
+                l0 *= a0;
+                l1 *= a1;
+#pragma unroll
+                for (int i = 0; i < NT; ++i) {
+                    o[i][0] *= a0; o[i][1] *= a0; o[i][2] *= a1; o[i][3] *= a1;
+                }
+            }
+            const float u0 = m0 == kNegInf ? 0.f : m0;  // a row with no token yet: every p is 0
+            const float u1 = m1 == kNegInf ? 0.f : m1;
+            float pr[2][4];
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                pr[j][0] = ex2(s[j][0] - u0);
+                pr[j][1] = ex2(s[j][1] - u0);
+                pr[j][2] = ex2(s[j][2] - u1);
+                pr[j][3] = ex2(s[j][3] - u1);
+            }
+            // P's A fragments (rows row0 / row1, tokens 2t.. / 8 + 2t..) as bf16
+            // hi + lo parts (p = hi + lo to about 2^-17 relative)
+            uint32_t ah[4], al[4];
+            ah[0] = pack_bf16x2(pr[0][0], pr[0][1]);
+            ah[1] = pack_bf16x2(pr[0][2], pr[0][3]);
+            ah[2] = pack_bf16x2(pr[1][0], pr[1][1]);
+            ah[3] = pack_bf16x2(pr[1][2], pr[1][3]);
+            al[0] = pack_bf16x2(pr[0][0] - bf16_lo(ah[0]), pr[0][1] - bf16_hi(ah[0]));
+            al[1] = pack_bf16x2(pr[0][2] - bf16_lo(ah[1]), pr[0][3] - bf16_hi(ah[1]));
+            al[2] = pack_bf16x2(pr[1][0] - bf16_lo(ah[2]), pr[1][1] - bf16_hi(ah[2]));
+            al[3] = pack_bf16x2(pr[1][2] - bf16_lo(ah[3]), pr[1][3] - bf16_hi(ah[3]));
+            // l sums the fp32 weights (this lane's four tokens; the quad is summed at the end)
+            l0 += (pr[0][0] + pr[0][1]) + (pr[1][0] + pr[1][1]);
+            l1 += (pr[0][2] + pr[0][3]) + (pr[1][2] + pr[1][3]);
+            // O += P V over 16 columns of D per ldmatrix
+#pragma unroll
+            for (int mt = 0; mt < D / 16; ++mt) {
+                uint32_t b[4];
+                const int cc = (((mt & 3) << 1) + v_cpar) ^ swh[mt >> 2];
+                ldsm_x4_trans(sV + v_off + (uint32_t)(mt >> 2) * hs + (cc << 4), b);
+                mma_16816(o[2 * mt], ah, b[0], b[1]);
+                mma_16816(o[2 * mt + 1], ah, b[2], b[3]);
+                mma_16816(o[2 * mt], al, b[0], b[1]);
+                mma_16816(o[2 * mt + 1], al, b[2], b[3]);
+            }
+            if (partial) fence_proxy_async_smem();  // generic writes before the next TMA
+        }
+        if (m.flags & kSegEnd) {
+            // ---- segment end: per q tile, the token slices' states merge
+            // through this stage's memory (released only afterwards); roles as
+            // in run_consumer.
+            float* st_m = reinterpret_cast<float*>(base + L.st_m);  // [slice][32 q rows]
+            float* st_l = reinterpret_cast<float*>(base + L.st_l);
+            int32_t* st_role = reinterpret_cast<int32_t*>(base + L.st_x) + 2 * kMaxGroup;
+            float* st_o = reinterpret_cast<float*>(base + (sK - base_s));  // [slice][16][kOStride]
+            // the next segment loads its own q fragments (no live values across the epilogue)
+#pragma unroll
+            for (int kk = 0; kk < KS; ++kk) qa[kk][0] = qa[kk][1] = qa[kk][2] = qa[kk][3] = 0u;
+            l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
+            l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
+            l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
+            l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
+            if (!consumer_sync(cbar, cphase, p.err, abort_flag)) break;  // all reads of the stage done
+            const int NR = m.nr;
+            const bool whole = (m.flags & kWholeUnit) != 0;
+            const int u = m.b * p.Hkv + m.kvh;
+            UnitPieces pc;
+            pc.cf = 0; pc.su = 0; pc.n = 1; pc.every = true;
+            if (!whole) pc = unit_pieces(pfx, m.b, m.kvh, p.Hkv, p.unit_cost, gr);
+            const RowInfo ri = row_info<true>(p, m.b);
+            const int SR = p.rows_per_slot;
+            int role = kRoleAbort;
+            bool stop = false;
+            for (int tile = 0; tile < C::kQTiles && !stop; ++tile) {
+                // the previous tile's staged states are read: overwrite them
+                if (tile > 0 && !consumer_sync(cbar, cphase, p.err, abort_flag)) { stop = true; break; }
+                if (qt == tile) {
+                    if (t == 0) {
+                        st_m[ts * kMaxRowsPerWalk + row0] = m0;
+                        st_m[ts * kMaxRowsPerWalk + row1] = m1;
+                        st_l[ts * kMaxRowsPerWalk + row0] = l0;
+                        st_l[ts * kMaxRowsPerWalk + row1] = l1;
+                    }
+                    float* ra = st_o + (size_t)(ts * 16 + g) * kOStride + 2 * t;
+                    float* rb = ra + 8 * kOStride;
+#pragma unroll
+                    for (int i = 0; i < NT; ++i) {
+                        *reinterpret_cast<float2*>(ra + 8 * i) = make_float2(o[i][0], o[i][1]);
+                        *reinterpret_cast<float2*>(rb + 8 * i) = make_float2(o[i][2], o[i][3]);
+                        o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;  // the next segment's start
+                    }
+                    m0 = m1 = kNegInf;
+                    l0 = l1 = 0.f;
+                }
+                if (tile == 0 && ct == 0) {
+                    int32_t r = whole ? kRoleWhole : ticket == pc.n - 1 ? kRoleMerge : kRoleStore;
+                    if (r == kRoleMerge) {
+                        int32_t* cnt = p.unit_sync + 2 * u;
+                        bool ready = ld_acquire_gpu(cnt + 1) == pc.n - 1;
+                        if (!ready) {
+                            const uint64_t t0 = global_ns();
+                            while (!(ready = ld_acquire_gpu(cnt + 1) == pc.n - 1) &&
+                                   global_ns() - t0 <= kWaitLimitNs) {
+                            }
+                        }
+                        if (ready) {
+                            cnt[0] = 0;  // every piece has drawn and stored: reset for the next launch
+                            cnt[1] = 0;
+                        } else {
+                            atomicOr(p.err, PDA_DEVERR_TIMEOUT_);
+                            *abort_flag = 1;
+                            r = kRoleAbort;
+                        }
+                    }
+                    *st_role = r;
+                }
+                if (!consumer_sync(cbar, cphase, p.err, abort_flag)) { stop = true; break; }
+                role = *st_role;
+                if (role == kRoleAbort) { stop = true; break; }
+                const int h0 = tile * 16, nrt = min(16, NR - h0);
+                for (int i4 = ct; i4 < nrt * D / 4; i4 += kThreadsC) {
+                    const int hr = (4 * i4) / D, d4 = 4 * i4 - hr * D;
+                    const int h = h0 + hr;  // q row of the unit
+                    float M = kNegInf;
+#pragma unroll
+                    for (int w = 0; w < kSlices; ++w) M = fmaxf(M, st_m[w * kMaxRowsPerWalk + h]);
+                    float Ls = 0.f;
+                    float4 Os = make_float4(0.f, 0.f, 0.f, 0.f);
+                    if (M != kNegInf) {
+#pragma unroll
+                        for (int w = 0; w < kSlices; ++w) {
+                            const float f = ex2(st_m[w * kMaxRowsPerWalk + h] - M);
+                            const float4 v =
+                                *reinterpret_cast<const float4*>(st_o + (size_t)(w * 16 + hr) * kOStride + d4);
+                            Ls += st_l[w * kMaxRowsPerWalk + h] * f;
+                            Os.x += v.x * f; Os.y += v.y * f; Os.z += v.z * f; Os.w += v.w * f;
+                        }
+                    }
+                    if (role == kRoleStore) {
+                        const int64_t r = (int64_t)(u + (int)blockIdx.x) * SR + h;
+                        *reinterpret_cast<float4*>(p.part_o + r * D + d4) = Os;
+                        if (d4 == 0) {
+                            p.part_ml[r * 2] = M;
+                            p.part_ml[r * 2 + 1] = Ls;
+                        }
+                        continue;
+                    }
+                    if (role == kRoleMerge) {
+                        // every piece in piece order, this piece's own state in its
+                        // place, up to four partials per memory round trip (the
+                        // row form's registers allow four)
+                        float Mr = kNegInf, Lr = 0.f;
+                        float4 Or = make_float4(0.f, 0.f, 0.f, 0.f);
+                        for (int i0 = 0; i0 < pc.n; i0 += 4) {
+                            float mi[4], li[4];
+                            float4 oi[4];
+                            bool own[4];
+#pragma unroll
+                            for (int k = 0; k < 4; ++k) {
+                                mi[k] = kNegInf;
+                                li[k] = 0.f;
+                                oi[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+                                const int64_t c = piece_cta(pc, i0 + k, gr);
+                                own[k] = i0 + k < pc.n && c == (int64_t)blockIdx.x;
+                                if (i0 + k >= pc.n || own[k]) continue;
+                                const int64_t r = (u + c) * SR + h;
+                                mi[k] = ld_cg(p.part_ml + r * 2);
+                                li[k] = ld_cg(p.part_ml + r * 2 + 1);
+                                oi[k] = __ldcg(reinterpret_cast<const float4*>(p.part_o + r * D + d4));
+                            }
+#pragma unroll
+                            for (int k = 0; k < 4; ++k) {
+                                if (own[k]) merge_state(Mr, Lr, Or, M, Ls, Os);
+                                else merge_state(Mr, Lr, Or, mi[k], li[k], oi[k]);
+                            }
+                        }
+                        M = Mr;
+                        Ls = Lr;
+                        Os = Or;
+                    }
+                    const float4 v = Ls > 0.f ? make_float4(Os.x / Ls, Os.y / Ls, Os.z / Ls, Os.w / Ls)
+                                              : make_float4(0.f, 0.f, 0.f, 0.f);
+                    const int64_t oo = qo_offset<true>(p, ri.b, ri.first + h / G, m.kvh * G + h % G, D) + d4;
+                    if (p.out_f32) {
+                        *reinterpret_cast<float4*>(p.out_f32 + oo) = v;
+                    } else {
+                        uint2 w2;
+                        w2.x = pack_bf16x2(v.x, v.y);
+                        w2.y = pack_bf16x2(v.z, v.w);
+                        *reinterpret_cast<uint2*>(p.out + oo) = w2;
+                    }
+                }
+            }
+            if (stop) break;
+            if (!consumer_sync(cbar, cphase, p.err, abort_flag)) break;
+            // a stored piece signals after every consumer thread's stores (ordered
+            // before this thread's release by the consumer barrier)
+            if (role == kRoleStore && ct == 0) red_release_gpu_add(p.unit_sync + 2 * u + 1, 1);
+            fence_proxy_async_smem();  // staging writes before the next TMA into this stage
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(empty0 + 8 * stage);
+        if (++stage == S) { stage = 0; phase ^= 1u; }
+    }
+}
+
 // ------------------------------------------------------------------ kernels
 
 // Register cap: for D <= 128 two CTAs share an SM (two 3-stage rings keep as
@@ -1007,14 +1411,14 @@ __device__ __forceinline__ void run_consumer(const SplitParams& p, uint32_t base
 // runs one CTA per SM; with 32-row stages (block sizes below 8) a CTA has two
 // consumer warps and one producer warp, and two CTAs share an SM.
 template <int D, int ST, int MODE>
-__global__ void __maxnreg__(split_max_regs(D)) split_kernel(const __grid_constant__ SplitParams p) {
-    using C = Cfg<D, ST>;
+__global__ void __maxnreg__(split_max_regs(D, MODE)) split_kernel(const __grid_constant__ SplitParams p) {
+    using C = Cfg<D, ST, MODE>;
     extern __shared__ uint8_t smem_raw[];
     __shared__ int abort_flag;
     const uint32_t raw_s = smem_u32(smem_raw);
     const uint32_t base_s = (raw_s + 1023u) & ~1023u;
     uint8_t* base = smem_raw + (base_s - raw_s);
-    const SmemLayout L = smem_layout(D, ST, C::kStages, p.G, p.B);
+    const SmemLayout L = smem_layout(D, ST, MODE, C::kStages, p.B);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     int32_t* pfx = reinterpret_cast<int32_t*>(base + L.pfx);
     int32_t* scan = reinterpret_cast<int32_t*>(base + L.scan);
@@ -1042,9 +1446,9 @@ __global__ void __maxnreg__(split_max_regs(D)) split_kernel(const __grid_constan
     }
     pdl_wait_primary();
     // ends with __syncthreads (which also publishes the barriers)
-    const int32_t nv_max = build_prefix<MODE == kMulti, C::kThreads>(p, pfx, scan);
+    const int32_t nv_max = build_prefix<is_multi(MODE), C::kThreads>(p, pfx, scan);
     int64_t begin, end;
-    const GroupRange gr = group_of_cta(blockIdx.x, pfx, p.B, rows_per_seq<MODE == kMulti>(p), p.Hkv,
+    const GroupRange gr = group_of_cta(blockIdx.x, pfx, p.B, rows_per_seq<is_multi(MODE)>(p), p.Hkv,
                                        gridDim.x);
     const int64_t units = (int64_t)p.B * p.Hkv;
     if (unit_mode(units, gridDim.x, real_blocks(nv_max, p.unit_cost), C::kST, p.bs)) {
@@ -1064,13 +1468,20 @@ __global__ void __maxnreg__(split_max_regs(D)) split_kernel(const __grid_constan
         run_producer<D, ST, MODE>(p, base_s, L, pfx, meta, &abort_flag, begin, end, lane);
         return;
     }
-    run_consumer<D, ST, MODE>(p, base_s, base, L, meta, pfx, gr, &abort_flag, warp, lane);
+    if constexpr (q_tiles(MODE) > 0)
+        run_consumer_rows<D, ST, MODE>(p, base_s, base, L, meta, pfx, gr, &abort_flag, warp, lane);
+    else
+        run_consumer<D, ST, MODE>(p, base_s, base, L, meta, pfx, gr, &abort_flag, warp, lane);
 }
 
-// Host side of one split-kernel shape: its entry points by mode and its
-// launch (programmatic stream serialization: the prologue may overlap the
-// previous kernel; the kernel waits with griddepcontrol.wait before reading
-// global memory).
+// Host side of one split-kernel shape: its entry points by mode, their
+// pipeline depth and their launch (programmatic stream serialization: the
+// prologue may overlap the previous kernel; the kernel waits with
+// griddepcontrol.wait before reading global memory).  The row form of
+// multi-query exists for 64-row stages at head sizes up to 128.
+template <int D, int ST>
+constexpr bool has_rows_form() { return ST == 64 && D <= 128; }
+
 template <int D, int ST>
 const void* split_fn_of(int mode) {
     switch (mode) {
@@ -1078,15 +1489,33 @@ const void* split_fn_of(int mode) {
         case kTiled: return reinterpret_cast<const void*>(&split_kernel<D, ST, kTiled>);
         case kGather: return reinterpret_cast<const void*>(&split_kernel<D, ST, kGather>);
         case kMulti: return reinterpret_cast<const void*>(&split_kernel<D, ST, kMulti>);
+        case kMultiRows16:
+            if constexpr (has_rows_form<D, ST>())
+                return reinterpret_cast<const void*>(&split_kernel<D, ST, kMultiRows16>);
+            return nullptr;
+        case kMultiRows32:
+            if constexpr (has_rows_form<D, ST>())
+                return reinterpret_cast<const void*>(&split_kernel<D, ST, kMultiRows32>);
+            return nullptr;
         default: return nullptr;
     }
 }
 
 template <int D, int ST>
-cudaError_t launch_split_of(int mode, const SplitParams& p, int grid, size_t smem, cudaStream_t stream) {
+int split_stages_of(int mode) {
+    if (q_tiles(mode) > 0 && !has_rows_form<D, ST>()) return 0;
+    switch (mode) {
+        case kMultiRows16: return Cfg<D, ST, has_rows_form<D, ST>() ? kMultiRows16 : kOneShot>::kStages;
+        case kMultiRows32: return Cfg<D, ST, has_rows_form<D, ST>() ? kMultiRows32 : kOneShot>::kStages;
+        default: return Cfg<D, ST, kOneShot>::kStages;
+    }
+}
+
+template <int D, int ST, int MODE>
+cudaError_t launch_split_mode(const SplitParams& p, int grid, size_t smem, cudaStream_t stream) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)grid, 1, 1);
-    cfg.blockDim = dim3(Cfg<D, ST>::kThreads, 1, 1);
+    cfg.blockDim = dim3(Cfg<D, ST, MODE>::kThreads, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
@@ -1094,11 +1523,22 @@ cudaError_t launch_split_of(int mode, const SplitParams& p, int grid, size_t sme
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, split_kernel<D, ST, MODE>, p);
+}
+
+template <int D, int ST>
+cudaError_t launch_split_of(int mode, const SplitParams& p, int grid, size_t smem, cudaStream_t stream) {
     switch (mode) {
-        case kOneShot: return cudaLaunchKernelEx(&cfg, split_kernel<D, ST, kOneShot>, p);
-        case kTiled: return cudaLaunchKernelEx(&cfg, split_kernel<D, ST, kTiled>, p);
-        case kGather: return cudaLaunchKernelEx(&cfg, split_kernel<D, ST, kGather>, p);
-        case kMulti: return cudaLaunchKernelEx(&cfg, split_kernel<D, ST, kMulti>, p);
+        case kOneShot: return launch_split_mode<D, ST, kOneShot>(p, grid, smem, stream);
+        case kTiled: return launch_split_mode<D, ST, kTiled>(p, grid, smem, stream);
+        case kGather: return launch_split_mode<D, ST, kGather>(p, grid, smem, stream);
+        case kMulti: return launch_split_mode<D, ST, kMulti>(p, grid, smem, stream);
+        case kMultiRows16:
+            if constexpr (has_rows_form<D, ST>()) return launch_split_mode<D, ST, kMultiRows16>(p, grid, smem, stream);
+            return cudaErrorInvalidValue;
+        case kMultiRows32:
+            if constexpr (has_rows_form<D, ST>()) return launch_split_mode<D, ST, kMultiRows32>(p, grid, smem, stream);
+            return cudaErrorInvalidValue;
         default: return cudaErrorInvalidValue;
     }
 }

@@ -9,8 +9,8 @@ const void* split_kernel_fn_d256(int st, int mode) {
     return st == 32 ? split_fn_of<256, 32>(mode) : st == 64 ? split_fn_of<256, 64>(mode) : nullptr;
 }
 
-int split_stages_d256(int st) {
-    return st == 32 ? Cfg<256, 32>::kStages : st == 64 ? Cfg<256, 64>::kStages : 0;
+int split_stages_d256(int st, int mode) {
+    return st == 32 ? split_stages_of<256, 32>(mode) : st == 64 ? split_stages_of<256, 64>(mode) : 0;
 }
 
 cudaError_t launch_split_d256(int st, int mode, const SplitParams& p, int grid, size_t smem,

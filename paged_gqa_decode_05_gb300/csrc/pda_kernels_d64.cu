@@ -1,5 +1,6 @@
 // Split-kernel instantiations for head_dim 64 (one translation unit per head
-// size so the build compiles them in parallel): 64-row stages.
+// size so the build compiles them in parallel): 64-row stages, every mode
+// including the row form of multi-query.
 #include "pda_kernels.cuh"
 
 namespace pda {
@@ -8,7 +9,7 @@ const void* split_kernel_fn_d64(int st, int mode) {
     return st == 64 ? split_fn_of<64, 64>(mode) : nullptr;
 }
 
-int split_stages_d64(int st) { return st == 64 ? Cfg<64, 64>::kStages : 0; }
+int split_stages_d64(int st, int mode) { return st == 64 ? split_stages_of<64, 64>(mode) : 0; }
 
 cudaError_t launch_split_d64(int st, int mode, const SplitParams& p, int grid, size_t smem,
                              cudaStream_t stream) {

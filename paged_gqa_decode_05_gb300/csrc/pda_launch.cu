@@ -25,18 +25,18 @@ cudaError_t launch_pdl(void (*kernel)(Args...), int grid, int block, cudaStream_
 
 #define PDA_DECLARE_D(D)                                                                     \
     const void* split_kernel_fn_d##D(int st, int mode);                                     \
-    int split_stages_d##D(int st);                                                           \
+    int split_stages_d##D(int st, int mode);                                                 \
     cudaError_t launch_split_d##D(int st, int mode, const SplitParams& p, int grid,          \
                                   size_t smem, cudaStream_t stream);
 PDA_DECLARE_D(64)
 PDA_DECLARE_D(128)
 PDA_DECLARE_D(256)
 
-int split_stages(int D, int st) {
+int split_stages(int D, int st, int mode) {
     switch (D) {
-        case 64: return split_stages_d64(st);
-        case 128: return split_stages_d128(st);
-        case 256: return split_stages_d256(st);
+        case 64: return split_stages_d64(st, mode);
+        case 128: return split_stages_d128(st, mode);
+        case 256: return split_stages_d256(st, mode);
         default: return 0;
     }
 }

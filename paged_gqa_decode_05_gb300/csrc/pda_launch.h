@@ -7,8 +7,9 @@
 namespace pda {
 
 // Entry points defined per head_dim (pda_kernels_d*.cu).
-// st: stage rows of the split kernel's shape (stage_tokens(D, block_size)).
-int split_stages(int D, int st);
+// st: stage rows of the split kernel's shape (stage_tokens(D, block_size));
+// a mode whose shape does not exist has 0 stages and a null entry point.
+int split_stages(int D, int st, int mode);
 const void* split_kernel_fn(int D, int st, int mode);
 cudaError_t launch_split(int D, int st, int mode, const SplitParams& p, int grid, size_t smem,
                          cudaStream_t stream);

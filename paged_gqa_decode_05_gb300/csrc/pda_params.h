@@ -17,21 +17,42 @@ namespace pda {
 // bound by its instruction rate, and with 64-row stages only one CTA (one
 // producer) fits on an SM; ST = 32 fits two.  (For head_dim 128, already two
 // CTAs per SM, 32-row stages were measured slower.)
-constexpr int kMaxConsumerWarps = 4;
 constexpr int kMaxLaunchBatch = 1024;                    // sequences per kernel launch
 constexpr int kMaxGroup = 8;                             // q heads per kv head (n8 MMA)
-
-PDA_HD int split_threads(int st) { return (st / 16 + 1) * 32; }
-// Stage rows for a head size and block size.
-PDA_HD int stage_tokens(int D, int block_size) { return D == 256 && !block_boxes(D, block_size) ? 32 : 64; }
+constexpr int kMaxRowsPerWalk = 32;                      // q rows one KV walk serves (row form)
 
 // kOneShot: decode, output written; kTiled: fold a tile into the running
 // state; kGather: copy the staged rows out (loader check); kMulti: causal
 // multi-query decode, output written (the other modes see one query per
-// sequence, known at compile time).
-enum Mode : int { kOneShot = 0, kTiled = 1, kGather = 2, kMulti = 3 };
-constexpr int kNumModes = 4;
-__host__ __device__ constexpr bool writes_output(int mode) { return mode == kOneShot || mode == kMulti; }
+// sequence, known at compile time).  kMulti packs at most 8 q rows (queries
+// x G heads) into the MMA's N (the n8 form).  kMultiRows16 / kMultiRows32
+// are the row form for head sizes up to 128: the packed q rows are the MMA's
+// M, in one or two tiles of 16 rows, so that one walk over the KV serves up
+// to 32 q rows.
+enum Mode : int { kOneShot = 0, kTiled = 1, kGather = 2, kMulti = 3, kMultiRows16 = 4, kMultiRows32 = 5 };
+constexpr int kNumModes = 6;
+__host__ __device__ constexpr bool is_multi(int mode) {
+    return mode == kMulti || mode == kMultiRows16 || mode == kMultiRows32;
+}
+__host__ __device__ constexpr bool writes_output(int mode) { return mode == kOneShot || is_multi(mode); }
+// 16-row q tiles of the row form (0: the n8 form).
+__host__ __device__ constexpr int q_tiles(int mode) {
+    return mode == kMultiRows16 ? 1 : mode == kMultiRows32 ? 2 : 0;
+}
+// q rows a stage's q area holds.
+__host__ __device__ constexpr int stage_q_rows(int mode) { return q_tiles(mode) ? 16 * q_tiles(mode) : kMaxGroup; }
+// Consumer warps: one per 16 KV rows of a stage, times the q tiles in the row form.
+__host__ __device__ constexpr int consumer_warps(int st, int mode) {
+    return (st / 16) * (q_tiles(mode) ? q_tiles(mode) : 1);
+}
+constexpr int kMaxConsumerWarps = 8;
+PDA_HD int split_threads(int st, int mode) { return (consumer_warps(st, mode) + 1) * 32; }
+// Stage rows for a head size and block size.
+PDA_HD int stage_tokens(int D, int block_size) { return D == 256 && !block_boxes(D, block_size) ? 32 : 64; }
+// Sequences (launch rows) per launch of a mode: the row form with one q tile
+// runs two CTAs per SM with three 36 KB stages at head size 128, which
+// leaves room for a 512-entry block prefix.
+PDA_HD int max_launch_rows(int mode) { return mode == kMultiRows16 ? 512 : kMaxLaunchBatch; }
 
 // Per-stage record the producer writes before arming the stage's barrier.
 struct StageMeta {
@@ -56,8 +77,8 @@ struct SplitParams {
     const int32_t* last_valid;   // [B] valid slots of the last listed block (tiled) or null
     uint16_t* out;               // [B, Hq, D] bf16 (one-shot)
     float* out_f32;              // [B, Hq, D] fp32 instead of out when non-null
-    float* part_o;               // [slots, G, D]
-    float* part_ml;              // [slots, G, 2] (m in base-2 units, l)
+    float* part_o;               // [slots, rows_per_slot, D]
+    float* part_ml;              // [slots, rows_per_slot, 2] (m in base-2 units, l)
     int32_t* unit_sync;          // [B*Hkv][2] per split unit: pieces that drew a ticket, pieces
                                  // whose partial state is stored (0 between launches)
     float* m_state;              // tiled: running state [B*Hq], [B*Hq], [B*Hq*D]
@@ -76,7 +97,8 @@ struct SplitParams {
     int64_t row_blk, row_tok, row_kvh;  // strides in rows of D elements (gather4)
     int32_t lens_are_blocks;
     int32_t q_len;               // causal queries per sequence (0 or 1: plain decode)
-    int32_t qp;                  // queries packed into one launch row (MMA N = qp*G <= 8)
+    int32_t qp;                  // queries packed into one launch row (qp*G q rows: <= 8 in
+                                 // the n8 form, <= 32 in the row form)
     int32_t rows_per_slot;       // rows of a partial-state slot (0: G)
     int32_t B, Hq, Hkv, G, bs;
     int32_t unit_cost;           // plan blocks added to every non-empty unit
@@ -88,24 +110,26 @@ struct SmemLayout {
     uint32_t bars, cbar, meta, scan, st_m, st_l, st_x, pfx, total;
 };
 
-// K and V tiles of ST rows plus the group's q rows (up to 8 x D bf16).
-PDA_HD uint32_t stage_bytes(int D, int st) {
-    return 2u * (uint32_t)(D / 64) * (uint32_t)st * 128u + 16u * D;
+// K and V tiles of ST rows plus the stage's q rows (stage_q_rows x D bf16).
+PDA_HD uint32_t stage_bytes(int D, int st, int mode) {
+    return 2u * (uint32_t)(D / 64) * (uint32_t)st * 128u + (uint32_t)stage_q_rows(mode) * D * 2u;
 }
 
 // Dynamic shared memory of the split kernel (the +1024 pays for aligning the
 // base to the 128-byte-swizzle atom).  The segment epilogue stages its o tiles
-// (ST/16 warps x 8 rows x (D+4) floats <= 2 * ST * D * 2 bytes) in the
-// finished stage.
-PDA_HD SmemLayout smem_layout(int D, int st, int stages, int G, int B) {
+// in the finished stage: n8 form, ST/16 warps x 8 rows x (D+4) floats <=
+// 2 * ST * D * 2 bytes; row form, one q tile at a time, ST/16 warps x 16 rows
+// x (D+4) floats <= the stage with its q area.  st_m / st_l hold one (m, l)
+// per consumer warp and q row: [ST/16 token slices][32 rows] in the row form.
+PDA_HD SmemLayout smem_layout(int D, int st, int mode, int stages, int B) {
     SmemLayout L;
-    uint32_t off = (uint32_t)stages * stage_bytes(D, st);
+    uint32_t off = (uint32_t)stages * stage_bytes(D, st, mode);
     L.bars = off;  off += 2u * stages * 8u;
     L.cbar = off;  off += 8u;
     L.meta = off;  off += (uint32_t)stages * (uint32_t)sizeof(StageMeta);
-    L.scan = off;  off += 64u;  // per warp: block-prefix sum [8], largest unit [8]
-    L.st_m = off;  off += kMaxConsumerWarps * kMaxGroup * 4u;
-    L.st_l = off;  off += kMaxConsumerWarps * kMaxGroup * 4u;
+    L.scan = off;  off += 128u;  // per warp: block-prefix sum [16], largest unit [16]
+    L.st_m = off;  off += 4u * kMaxRowsPerWalk * 4u;
+    L.st_l = off;  off += 4u * kMaxRowsPerWalk * 4u;
     L.st_x = off;  off += 2u * kMaxGroup * 4u + 16u;  // old running (m, l) of a unit's rows; role word
     L.pfx = off;   off += (uint32_t)(B + 1) * 4u;
     L.total = off + 1024u;
