@@ -310,7 +310,8 @@ pda_status run(pda_ctx* ctx, const RunArgs& r) {
     if (r.table_stride < 1)
         return fail(PDA_ERR_INVALID_ARG, "block table width must be >= 1 (got %d)", r.table_stride);
     st = check_plan_size((int64_t)r.batch * r.q_len, r.table_stride,
-                         pda::unit_cost_blocks(ctx->stage_rows, d.head_dim, d.block_size, pda::is_multi(r.mode)));
+                         pda::unit_cost_blocks(ctx->stage_rows, d.head_dim, d.block_size,
+                                               pda::cost_class(multi_shape(ctx, r.mode, r.q_len).mode)));
     if (st != PDA_OK) return st;
     float scale_log2 = 0.f;
     st = check_scale(r.scale, d.head_dim, &scale_log2);
@@ -381,7 +382,7 @@ pda_status run(pda_ctx* ctx, const RunArgs& r) {
         p.Hkv = Hkv;
         p.G = ctx->G;
         p.bs = d.block_size;
-        p.unit_cost = pda::unit_cost_blocks(ctx->stage_rows, d.head_dim, d.block_size, mode == pda::kMulti);
+        p.unit_cost = pda::unit_cost_blocks(ctx->stage_rows, d.head_dim, d.block_size, pda::cost_class(mode));
         p.dbg_row_tokens = (int32_t)dbg_row_tokens;
         p.scale_log2 = scale_log2;
         const size_t smem = pda::smem_layout(D, ctx->stage_rows, mode, stages, cb).total;
@@ -764,7 +765,7 @@ PDA_EXPORT pda_status pda_get_launch_info(const pda_ctx* ctx, pda_launch_info* i
     info->smem_bytes = ctx->smem_max;
     info->stage_tokens = ctx->stage_rows;
     info->partial_slots = ctx->slots;
-    info->unit_cost = pda::unit_cost_blocks(ctx->stage_rows, ctx->dims.head_dim, ctx->dims.block_size, false);
+    info->unit_cost = pda::unit_cost_blocks(ctx->stage_rows, ctx->dims.head_dim, ctx->dims.block_size, pda::kCostDecode);
     return PDA_OK;
 }
 
@@ -978,7 +979,7 @@ PDA_EXPORT pda_status pda_decode_noalloc(const pda_bf16* q, const pda_bf16* k_po
     if (!block_table || !seq_lens || !aligned(block_table, 4) || !aligned(seq_lens, 4))
         return fail(PDA_ERR_INVALID_ARG, "block_table / seq_lens must be non-NULL and 4-byte aligned");
     if (max_blocks < 1) return fail(PDA_ERR_INVALID_ARG, "max_blocks must be >= 1");
-    const int32_t unit_cost = pda::unit_cost_blocks(rows, D, block_size, false);
+    const int32_t unit_cost = pda::unit_cost_blocks(rows, D, block_size, pda::kCostDecode);
     if ((st = check_plan_size(batch, max_blocks, unit_cost)) != PDA_OK) return st;
     PoolArgs pool = {k_pool, v_pool, num_blocks, (int64_t)block_size * num_kv_heads * head_dim,
                      (int64_t)num_kv_heads * head_dim, (int64_t)head_dim};

@@ -1064,8 +1064,8 @@ __device__ __forceinline__ void zero_empty_rows(const SplitParams& p, const int3
 template <int D, int ST, int MODE>
 __device__ __forceinline__ void run_consumer_rows(const SplitParams& p, uint32_t base_s, uint8_t* base,
                                                   const SmemLayout& L, const StageMeta* meta,
-                                                  const int32_t* pfx, const GroupRange& gr,
-                                                  volatile int* abort_flag, int warp, int lane) {
+                                                  const int32_t* pfx, volatile int* abort_flag, int warp,
+                                                  int lane) {
     using C = Cfg<D, ST, MODE>;
     constexpr int S = C::kStages;
     constexpr int KS = C::kKSteps;       // 16-column steps of D
@@ -1263,7 +1263,9 @@ __device__ __forceinline__ void run_consumer_rows(const SplitParams& p, uint32_t
             const int u = m.b * p.Hkv + m.kvh;
             UnitPieces pc;
             pc.cf = 0; pc.su = 0; pc.n = 1; pc.every = true;
-            if (!whole) pc = unit_pieces(pfx, m.b, m.kvh, p.Hkv, p.unit_cost, gr);
+            // the CTA's group, recomputed here rather than kept in registers over the loop
+            const GroupRange grs = group_of_cta(blockIdx.x, pfx, p.B, rows_per_seq<true>(p), p.Hkv, gridDim.x);
+            if (!whole) pc = unit_pieces(pfx, m.b, m.kvh, p.Hkv, p.unit_cost, grs);
             const RowInfo ri = row_info<true>(p, m.b);
             const int SR = p.rows_per_slot;
             int role = kRoleAbort;
@@ -1357,7 +1359,7 @@ __device__ __forceinline__ void run_consumer_rows(const SplitParams& p, uint32_t
                                 mi[k] = kNegInf;
                                 li[k] = 0.f;
                                 oi[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-                                const int64_t c = piece_cta(pc, i0 + k, gr);
+                                const int64_t c = piece_cta(pc, i0 + k, grs);
                                 own[k] = i0 + k < pc.n && c == (int64_t)blockIdx.x;
                                 if (i0 + k >= pc.n || own[k]) continue;
                                 const int64_t r = (u + c) * SR + h;
@@ -1469,7 +1471,7 @@ __global__ void __maxnreg__(split_max_regs(D, MODE)) split_kernel(const __grid_c
         return;
     }
     if constexpr (q_tiles(MODE) > 0)
-        run_consumer_rows<D, ST, MODE>(p, base_s, base, L, meta, pfx, gr, &abort_flag, warp, lane);
+        run_consumer_rows<D, ST, MODE>(p, base_s, base, L, meta, pfx, &abort_flag, warp, lane);
     else
         run_consumer<D, ST, MODE>(p, base_s, base, L, meta, pfx, gr, &abort_flag, warp, lane);
 }

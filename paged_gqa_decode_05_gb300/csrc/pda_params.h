@@ -53,6 +53,11 @@ PDA_HD int stage_tokens(int D, int block_size) { return D == 256 && !block_boxes
 // runs two CTAs per SM with three 36 KB stages at head size 128, which
 // leaves room for a 512-entry block prefix.
 PDA_HD int max_launch_rows(int mode) { return mode == kMultiRows16 ? 512 : kMaxLaunchBatch; }
+// The unit-cost class of a mode (pda_plan.h).
+PDA_HD int32_t cost_class(int mode) {
+    return mode == kMulti ? kCostMultiN8 : mode == kMultiRows16 ? kCostRows16
+         : mode == kMultiRows32 ? kCostRows32 : kCostDecode;
+}
 
 // Per-stage record the producer writes before arming the stage's barrier.
 struct StageMeta {
