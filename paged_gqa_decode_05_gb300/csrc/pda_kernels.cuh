@@ -15,6 +15,10 @@
 //     online-softmax update runs on the accumulator fragments (warp-shuffle
 //     max over tokens), P is transposed in registers (movmatrix) and
 //     O^T += V^T P^T accumulates over D in 16-row slabs.
+//   * causal multi-query with more than 8 q rows per sequence (head sizes up
+//     to 128) takes the row form instead (run_consumer_rows): the packed q
+//     rows are the MMA's M (S = Q K^T, O += P V), one KV walk serving up to
+//     32 of them.
 //   * at the end of a segment the consumer warps' states are merged in shared
 //     memory; a segment that covers its whole unit writes bf16 o / l
 //     directly (or folds its state into the running state, in tiled steps).
