@@ -268,9 +268,12 @@ pda_status pda_finalize_f32(pda_ctx* ctx, float* out, int32_t num_seqs, pda_stre
  * pda_export_state copies the running state of sequences [0, num_seqs) into
  * caller-owned DEVICE buffers m, l [num_seqs*Hq] and o [num_seqs*Hq*D] (fp32,
  * 4-byte aligned), in natural-log units of the scaled scores:
- *   m = max_t s_t,  l = sum_t exp(s_t - m),  o = sum_t exp(s_t - m) v_t,
+ *   l = sum_t exp(s_t - m),  o = sum_t exp(s_t - m) v_t,
  * s_t = scale * q . K_t over the tokens folded so far ((-inf, 0, 0) when
- * none).  num_seqs must be <= max_seqs.
+ * none), where m is the reference the kernels keep: the running max of s_t,
+ * or at most 8 ln 2 below it (the reference moves only when the max runs
+ * past it by more than that).  o / l and the merge below do not depend on
+ * which reference a state was taken against.  num_seqs must be <= max_seqs.
  *
  * pda_merge_states combines n_parts (>= 1) such states per (sequence, q head)
  * row, laid out part-major: m_parts, l_parts [n_parts][num_seqs*Hq] and

@@ -38,8 +38,12 @@
 namespace pda {
 
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // each mbarrier wait gives up after 2 s
-// Row form of multi-query: how far (base-2 units) a row's softmax reference may
-// lag its running max before o is rescaled (weights stay below 2^8).
+// How far (base-2 units) a q row's softmax reference may lag its running max
+// before o is rescaled: the reference m of a row moves only when a stage's max
+// exceeds it by more than this, so the weights p = 2^(s - m) stay below 2^8
+// (well inside fp32 and the bf16 hi + lo split of P), and (m, l, o), which
+// means the same for any reference, is rescaled a few times per segment
+// instead of whenever a max grows.
 constexpr float kLazyLog2 = 8.f;
 #define kNegInf (-__int_as_float(0x7f800000))
 
@@ -806,11 +810,23 @@ __device__ __forceinline__ void run_consumer(const SplitParams& p, uint32_t base
                     x0 = fmaxf(x0, __shfl_xor_sync(0xffffffffu, x0, off));
                     x1 = fmaxf(x1, __shfl_xor_sync(0xffffffffu, x1, off));
                 }
-                const float n0 = fmaxf(m0, x0), n1 = fmaxf(m1, x1);
-                const float u0 = n0 == kNegInf ? 0.f : n0;
-                const float u1 = n1 == kNegInf ? 0.f : n1;
-                const float a0 = m0 == n0 ? 1.f : ex2(m0 - u0);
-                const float a1 = m1 == n1 ? 1.f : ex2(m1 - u1);
+                // lazy reference (kLazyLog2): o is rescaled only when a column's max
+                // runs more than 2^8 past its reference
+                const bool up0 = x0 > m0 + kLazyLog2, up1 = x1 > m1 + kLazyLog2;
+                if (__any_sync(0xffffffffu, up0 || up1)) {
+                    const float a0 = up0 ? ex2(m0 - x0) : 1.f;  // an empty column (m = -inf): 0
+                    const float a1 = up1 ? ex2(m1 - x1) : 1.f;
+                    if (up0) m0 = x0;
+                    if (up1) m1 = x1;
+                    l0 *= a0;
+                    l1 *= a1;
+#pragma unroll
+                    for (int i = 0; i < KS; ++i) {
+                        o[i][0] *= a0; o[i][1] *= a1; o[i][2] *= a0; o[i][3] *= a1;
+                    }
+                }
+                const float u0 = m0 == kNegInf ? 0.f : m0;
+                const float u1 = m1 == kNegInf ? 0.f : m1;
                 // P enters the tensor core as bf16 hi + lo parts (p = hi + lo to
                 // about 2^-17 relative), so P.V keeps fp32-level accuracy whatever
                 // running maximum the weights were taken against.
@@ -821,16 +837,8 @@ __device__ __forceinline__ void run_consumer(const SplitParams& p, uint32_t base
                 const uint32_t qy = pack_bf16x2(p2 - bf16_lo(py), p3 - bf16_hi(py));
                 // l sums the fp32 weights; the ones that multiply V (hi + lo)
                 // equal them to about 2^-17 relative
-                l0 = l0 * a0 + (p0 + p2);
-                l1 = l1 * a1 + (p1 + p3);
-                m0 = n0;
-                m1 = n1;
-                if (!__all_sync(0xffffffffu, a0 == 1.f && a1 == 1.f)) {
-#pragma unroll
-                    for (int i = 0; i < KS; ++i) {
-                        o[i][0] *= a0; o[i][1] *= a1; o[i][2] *= a0; o[i][3] *= a1;
-                    }
-                }
+                l0 += p0 + p2;
+                l1 += p1 + p3;
                 const uint32_t pb0 = movmatrix_trans(px), pb1 = movmatrix_trans(py);
                 const uint32_t pc0 = movmatrix_trans(qx), pc1 = movmatrix_trans(qy);
                 // O^T (D x 8 heads) += V^T P^T, 16 rows of D per mma
@@ -1192,10 +1200,8 @@ __device__ __forceinline__ void run_consumer_rows(const SplitParams& p, uint32_t
             x1 = fmaxf(x1, __shfl_xor_sync(0xffffffffu, x1, 1));
             x0 = fmaxf(x0, __shfl_xor_sync(0xffffffffu, x0, 2));
             x1 = fmaxf(x1, __shfl_xor_sync(0xffffffffu, x1, 2));
-            // Lazy rescale: a row's reference m moves only when the stage's max
-            // exceeds it by more than kLazyLog2, so the weights p = 2^(s - m) stay
-            // below 2^kLazyLog2; (m, l, o) means the same for any reference, and
-            // o is rescaled only a few times per segment, not whenever a max grows.
+            // lazy reference (kLazyLog2): o is rescaled only when a row's max
+            // runs more than 2^8 past its reference
             const bool up0 = x0 > m0 + kLazyLog2, up1 = x1 > m1 + kLazyLog2;
             if (__any_sync(0xffffffffu, up0 || up1)) {
                 const float a0 = up0 ? ex2(m0 - x0) : 1.f;  // an empty row (m = -inf): 0
