@@ -242,6 +242,18 @@ pda_status pda_begin_step(pda_ctx* ctx, int32_t num_seqs, pda_stream stream);
  *   scale              NaN selects 1/sqrt(D).  [TA] passes no scale.
  * Tiles of one step may be given in any order of blocks; the state after all
  * tiles equals the one-shot result up to fp32 rounding.
+ *
+ * Overlap: a tile step issued right behind another tile step of the same
+ * step (same context, same stream) starts reading its inputs -- q, the pools,
+ * tile_blocks, tile_block_counts, tile_last_valid -- while the previous one
+ * is still finishing, and waits for it only before it touches the running
+ * state.  So a kernel that the caller launches between two tile steps of a
+ * step on that stream must not write the second step's inputs while
+ * triggering its dependents early (programmatic dependent launch); kernels
+ * launched without such a trigger, copies and host-side changes between the
+ * calls are always waited for.  The first tile step of a step waits for
+ * whatever precedes it.  pda_set_tile_overlap(ctx, 0) makes every tile step
+ * wait.
  */
 pda_status pda_step_tile(pda_ctx* ctx, const pda_bf16* q, const pda_bf16* k_pool,
                          const pda_bf16* v_pool, int64_t num_blocks,
@@ -249,6 +261,8 @@ pda_status pda_step_tile(pda_ctx* ctx, const pda_bf16* q, const pda_bf16* k_pool
                          const int32_t* tile_last_valid, int32_t num_seqs,
                          int64_t blk_stride, int64_t tok_stride, int64_t kvh_stride,
                          float scale, pda_stream stream);
+/* Tile-step overlap on (enable != 0, the default) or off.  Host only. */
+pda_status pda_set_tile_overlap(pda_ctx* ctx, int32_t enable);
 
 /*
  * Tiled lifecycle, step 3 -- [TA] finalize: out[s, h, :] = bf16(o / l) for

@@ -109,6 +109,7 @@ def lib() -> ctypes.CDLL:
         "pda_check_wait_timeout": (I32, [P, I64, P]),
         "pda_get_launch_info": (I32, [P, ctypes.POINTER(LaunchInfo)]),
         "pda_get_multi_info": (I32, [P, I32, ctypes.POINTER(MultiInfo)]),
+        "pda_set_tile_overlap": (I32, [P, I32]),
         "pda_plan_units": (I32, [P, I32, I32, I32, I32, I32, I32, I32, P, P, ctypes.POINTER(I64)]),
     }
     for name, (res, args) in sig.items():
@@ -381,6 +382,10 @@ class Context:
         return out
 
     # -- tiled lifecycle
+    def set_tile_overlap(self, enable: bool) -> None:
+        """Tile steps of one step on one stream overlap (default) or each waits (pda_set_tile_overlap)."""
+        _check(lib().pda_set_tile_overlap(self._ctx, int(bool(enable))))
+
     def begin_step(self, num_seqs: int, stream=None) -> None:
         _check(lib().pda_begin_step(self._ctx, int(num_seqs), _stream(stream)))
 
@@ -417,8 +422,9 @@ class Context:
     # -- partial states across contexts (context-parallel decode)
     def export_state(self, num_seqs: int, stream=None):
         """The running (m, l, o) of sequences [0, num_seqs) as fp32 tensors
-        [num_seqs, Hq], [num_seqs, Hq], [num_seqs, Hq, D]; m in natural-log units
-        of the scaled scores, l = sum exp(s - m), o = sum exp(s - m) v."""
+        [num_seqs, Hq], [num_seqs, Hq], [num_seqs, Hq, D]: m the reference (natural-log
+        units of the scaled scores; the running max or up to 8 ln 2 below it),
+        l = sum exp(s - m), o = sum exp(s - m) v."""
         torch = _torch()
         d = self.dims
         m = torch.empty((num_seqs, d.num_q_heads), device=self.device, dtype=torch.float32)

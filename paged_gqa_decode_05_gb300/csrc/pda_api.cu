@@ -89,6 +89,12 @@ struct pda_ctx {
     float* l_state = nullptr;
     float* o_state = nullptr;
     cudaEvent_t ev_begin = nullptr, ev_split = nullptr, ev_end = nullptr;
+    // Tiled lifecycle: tile steps since the last begin_step and the stream of
+    // the last one; a tile step right behind another on the same stream reads
+    // its inputs early (pda_set_tile_overlap turns that off).
+    int64_t tile_steps = 0;
+    cudaStream_t tile_stream = nullptr;
+    bool tile_overlap = true;
     // The last pool's tensor maps: a decode loop over one cache encodes them
     // once (encoding costs host time on every call otherwise).
     bool maps_valid = false;
@@ -247,6 +253,7 @@ struct RunArgs {
     cudaStream_t stream;
     bool contiguous = false;  // no table: block b*table_stride + j (contiguous cache)
     int32_t q_len = 1;        // causal queries per sequence (q, out: [batch, q_len, Hq, D])
+    bool early_inputs = false;  // tiled: a tile step right behind another of the same step
 };
 
 // The kernels keep a launch's plan-block prefix in int32: up to
@@ -384,6 +391,8 @@ pda_status run(pda_ctx* ctx, const RunArgs& r) {
         p.bs = d.block_size;
         p.unit_cost = pda::unit_cost_blocks(ctx->stage_rows, d.head_dim, d.block_size, pda::cost_class(mode));
         p.dbg_row_tokens = (int32_t)dbg_row_tokens;
+        // a later chunk is right behind this call's previous chunk
+        p.early_inputs = mode == pda::kTiled && (r.early_inputs || c0 > 0) ? 1 : 0;
         p.scale_log2 = scale_log2;
         const size_t smem = pda::smem_layout(D, ctx->stage_rows, mode, stages, cb).total;
 
@@ -618,6 +627,7 @@ PDA_EXPORT pda_status pda_begin_step(pda_ctx* ctx, int32_t num_seqs, pda_stream 
     cudaError_t e = pda::launch_reset_state(ctx->m_state, ctx->l_state, ctx->o_state,
                                             (int64_t)num_seqs * ctx->dims.num_q_heads,
                                             ctx->dims.head_dim, (cudaStream_t)stream);
+    ctx->tile_steps = 0;
     return e == cudaSuccess ? PDA_OK : cuda_fail(e, "state reset launch");
 }
 
@@ -631,7 +641,19 @@ PDA_EXPORT pda_status pda_step_tile(pda_ctx* ctx, const pda_bf16* q, const pda_b
     RunArgs r = {pda::kTiled, q, {k_pool, v_pool, num_blocks, blk_stride, tok_stride, kvh_stride},
                  tile_blocks, ctx->dims.tile_capacity, tile_block_counts, 1, tile_last_valid,
                  num_seqs, scale, nullptr, nullptr, nullptr, nullptr, (cudaStream_t)stream};
-    return run(ctx, r);
+    r.early_inputs = ctx->tile_overlap && ctx->tile_steps > 0 && ctx->tile_stream == (cudaStream_t)stream;
+    const pda_status st = run(ctx, r);
+    if (st == PDA_OK) {
+        ++ctx->tile_steps;
+        ctx->tile_stream = (cudaStream_t)stream;
+    }
+    return st;
+}
+
+PDA_EXPORT pda_status pda_set_tile_overlap(pda_ctx* ctx, int32_t enable) {
+    if (!ctx) return fail(PDA_ERR_INVALID_ARG, "ctx is NULL");
+    ctx->tile_overlap = enable != 0;
+    return PDA_OK;
 }
 
 static pda_status finalize_impl(pda_ctx* ctx, pda_bf16* out, float* out_f32, int32_t num_seqs,

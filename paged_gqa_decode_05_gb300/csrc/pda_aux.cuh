@@ -2,9 +2,10 @@
 // state's reset and finalize, and the export and merge of partial states
 // across contexts.  Included by one translation unit (pda_launch.cu).
 //
-// Each is launched with programmatic dependent launch: it lets the next kernel
-// in the stream start its set-up at once and touches global memory only after
-// the previous kernel has completed (griddepcontrol.wait).
+// Each is launched with programmatic dependent launch: it touches global
+// memory only after the previous kernel has completed (griddepcontrol.wait),
+// and only then lets the next kernel in the stream launch, so that a kernel
+// launched early behind it knows every kernel before this one complete.
 #pragma once
 
 #include "pda_kernels.cuh"
@@ -13,8 +14,8 @@ namespace pda {
 
 // (m, l, o) = (-inf, 0, 0) for n_q query slots.
 __global__ void reset_state_kernel(float* m, float* l, float* o, int64_t n_q, int32_t D) {
-    pdl_launch_dependents();
     pdl_wait_primary();
+    pdl_launch_dependents();
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n_q * D; i += stride) {
         o[i] = 0.f;
@@ -29,8 +30,8 @@ __global__ void reset_state_kernel(float* m, float* l, float* o, int64_t n_q, in
 // scale * log2 e) to natural-log units of the scaled scores.
 __global__ void export_state_kernel(const float* m2, const float* l, const float* o, float* m_out,
                                     float* l_out, float* o_out, int64_t n_q, int32_t D) {
-    pdl_launch_dependents();
     pdl_wait_primary();
+    pdl_launch_dependents();
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n_q * D; i += stride) {
         o_out[i] = o[i];
@@ -47,8 +48,8 @@ __global__ void export_state_kernel(const float* m2, const float* l, const float
 __global__ void merge_states_kernel(const float* m_parts, const float* l_parts, const float* o_parts,
                                     int32_t n_parts, int64_t n_q, int32_t D, uint16_t* out,
                                     float* out_f32) {
-    pdl_launch_dependents();
     pdl_wait_primary();
+    pdl_launch_dependents();
     const int64_t n4 = n_q * D / 4;
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
     for (int64_t i4 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i4 < n4; i4 += stride) {
@@ -84,8 +85,8 @@ __global__ void merge_states_kernel(const float* m_parts, const float* l_parts, 
 // out = o / l (bf16 round-to-nearest-even, or fp32); l == 0 gives 0.
 __global__ void finalize_kernel(const float* l, const float* o, uint16_t* out, float* out_f32,
                                 int64_t n_q, int32_t D) {
-    pdl_launch_dependents();
     pdl_wait_primary();
+    pdl_launch_dependents();
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n_q * D; i += stride) {
         const float li = l[i / D];

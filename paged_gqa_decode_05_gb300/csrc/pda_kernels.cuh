@@ -708,6 +708,8 @@ __device__ __forceinline__ void run_consumer(const SplitParams& p, uint32_t base
     int stage = 0;
     uint32_t phase = 0;
     int32_t ticket = 0;  // consumer thread 0: this piece's ticket for its split unit
+    // an early tile step waits for the previous kernel before its first segment end
+    bool waited = !(MODE == kTiled && p.early_inputs != 0);
 
     if constexpr (writes_output(MODE)) {
         // A unit with no tokens has no segment: its output rows are zero.  Such
@@ -738,6 +740,10 @@ __device__ __forceinline__ void run_consumer(const SplitParams& p, uint32_t base
         }
         const StageMeta m = meta[stage];
         if (m.flags & kDone) break;
+        if (!waited && (m.flags & kSegEnd)) {  // the tickets, slots and running state come next
+            pdl_wait_primary();
+            waited = true;
+        }
         // The last stage of a piece of a split unit: take the piece's ticket now, so
         // that the atomic's round trip overlaps this stage's math.  Tickets only
         // assign roles: the piece that draws the last one merges all pieces.
@@ -1436,11 +1442,22 @@ __global__ void __maxnreg__(split_max_regs(D, MODE)) split_kernel(const __grid_c
     int32_t* scan = reinterpret_cast<int32_t*>(base + L.scan);
     StageMeta* meta = reinterpret_cast<StageMeta*>(base + L.meta);
 
-    // Programmatic dependent launch: let the next kernel in the stream be
-    // scheduled as CTAs of this one exit, set up barriers and descriptors
-    // while the previous kernel finishes, and read no global memory before it
-    // has completed.
-    if (MODE != kGather) pdl_launch_dependents();
+    // Programmatic dependent launch: barriers and descriptors are set up while
+    // the previous kernel finishes; global memory is read only after
+    // griddepcontrol.wait (the previous kernel complete, its writes visible),
+    // and only then may the next kernel launch (its CTAs are scheduled as
+    // this kernel's exit), so a kernel launched early behind this one knows
+    // every kernel before this one complete.
+    // A tile step right behind another tile step of the same step on the same
+    // stream (p.early_inputs) instead lets the next kernel launch at once and
+    // reads its inputs (lengths, tile lists, q, K/V) without waiting: the
+    // first tile step of a chain waited for everything before it, so the
+    // kernels that may still run beside this one are tile steps of the same
+    // step, and no tile step writes another's inputs.  Its consumers wait
+    // before their first access to what a tile step writes (the unit
+    // counters, the partial slots, the running state).
+    const bool early = MODE == kTiled && p.early_inputs != 0;
+    if (early) pdl_launch_dependents();
     if (tid == 0) {
         for (int s = 0; s < C::kStages; ++s) {
             // full: the producer's arrive (+ one cp.async arrival per lane when
@@ -1456,7 +1473,10 @@ __global__ void __maxnreg__(split_max_regs(D, MODE)) split_kernel(const __grid_c
         prefetch_tensormap(&p.tm_k);
         prefetch_tensormap(&p.tm_v);
     }
-    pdl_wait_primary();
+    if (!early) {
+        pdl_wait_primary();
+        if (MODE != kGather) pdl_launch_dependents();
+    }
     // ends with __syncthreads (which also publishes the barriers)
     const int32_t nv_max = build_prefix<is_multi(MODE), C::kThreads>(p, pfx, scan);
     int64_t begin, end;

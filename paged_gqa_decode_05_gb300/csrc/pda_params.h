@@ -108,6 +108,8 @@ struct SplitParams {
     int32_t B, Hq, Hkv, G, bs;
     int32_t unit_cost;           // plan blocks added to every non-empty unit
     int32_t dbg_row_tokens;      // tokens per (b, kvh) row of the gather output
+    int32_t early_inputs;        // tiled: read the inputs before the previous kernel completes
+                                 // (a tile step right behind another of the same step)
     float scale_log2;            // softmax scale * log2(e)
 };
 

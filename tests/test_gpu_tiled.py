@@ -111,3 +111,96 @@ def test_eight_b_tiled_full_size():
     one = host_f64(ctx.decode(t["q"], t["k_pool"], t["v_pool"], t["block_table"], t["seq_lens"],
                               out_dtype=torch.float32))
     assert np.max(np.abs(f32 - one)) <= TILED_VS_ONESHOT
+
+
+def _steps(ctx, w, dev_tiles, t):
+    """One step on the current stream: reset, the device-resident tiles, fp32 finalize."""
+    import torch
+    ctx.begin_step(w.B)
+    for blocks, counts, last in dev_tiles:
+        ctx.step_tile(t["q"], t["k_pool"], t["v_pool"], blocks, counts, last)
+    return ctx.finalize(w.B, out_dtype=torch.float32)
+
+
+@pytest.mark.parametrize("tiles_per_seq", [4, 16])
+def test_overlapped_tile_steps_match_waiting_ones(tiles_per_seq):
+    """Tile steps issued back to back (device-resident tile lists, so each
+    starts streaming while the previous finishes) give the same state, bit for
+    bit, as tile steps that each wait for the previous one."""
+    import torch
+    w = workloads.eight_b()
+    cap = 256 // tiles_per_seq
+    ctx = context_for(w, tile_capacity=cap)
+    t = upload(w)
+    tiles = [(dev(b), dev(c), dev(l)) for b, c, l in make_tiles(w, cap, np.random.default_rng(5))]
+    torch.cuda.synchronize()
+    over = _steps(ctx, w, tiles, t).clone()
+    ctx.set_tile_overlap(False)
+    wait = _steps(ctx, w, tiles, t).clone()
+    ctx.set_tile_overlap(True)
+    again = _steps(ctx, w, tiles, t)
+    torch.cuda.synchronize()
+    assert ctx.read_device_errors() == 0
+    assert torch.equal(over, wait) and torch.equal(over, again)
+    one = host_f64(ctx.decode(t["q"], t["k_pool"], t["v_pool"], t["block_table"], t["seq_lens"],
+                              out_dtype=torch.float32))
+    assert np.max(np.abs(host_f64(over) - one)) <= TILED_VS_ONESHOT
+
+
+def test_overlapped_tile_steps_replayed_from_a_graph():
+    """A whole step (reset, overlapped tiles, finalize) captured once and
+    replayed matches the eager step, and follows new q contents."""
+    import torch
+    w = workloads.make_workload("graph_tiles", B=6, Hq=16, Hkv=4, D=128, block_size=16,
+                                seq_lens=[1000, 5, 0, 333, 4096, 77], seed=23)
+    ctx = context_for(w, tile_capacity=12)
+    t = upload(w)
+    tiles = [(dev(b), dev(c), dev(l)) for b, c, l in make_tiles(w, 12, np.random.default_rng(6))]
+    eager = _steps(ctx, w, tiles, t).clone()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        _steps(ctx, w, tiles, t)  # warm-up on the capture stream
+    torch.cuda.current_stream().wait_stream(s)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        out = _steps(ctx, w, tiles, t)
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(out, eager)
+    t["q"].mul_(-1)
+    g.replay()
+    flipped = _steps(ctx, w, tiles, t)
+    torch.cuda.synchronize()
+    assert torch.equal(out, flipped) and not torch.equal(out, eager)
+    assert ctx.read_device_errors() == 0
+
+
+def test_tile_steps_on_alternating_streams():
+    """Tile steps of one step on two streams (each ordered after the previous
+    one by an event) wait for their predecessor and match one stream."""
+    import torch
+    w = workloads.make_workload("streams_tiles", B=4, Hq=8, Hkv=2, D=64, block_size=16,
+                                seq_lens=[2000, 17, 640, 1], seed=24)
+    ctx = context_for(w, tile_capacity=9)
+    t = upload(w)
+    tiles = [(dev(b), dev(c), dev(l)) for b, c, l in make_tiles(w, 9, np.random.default_rng(7))]
+    ref = _steps(ctx, w, tiles, t).clone()
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    main = torch.cuda.current_stream()
+    for st in streams:
+        st.wait_stream(main)
+    ctx.begin_step(w.B, stream=streams[0])
+    prev = streams[0]
+    for i, (blocks, counts, last) in enumerate(tiles):
+        st = streams[i % 2]
+        st.wait_stream(prev)
+        with torch.cuda.stream(st):
+            ctx.step_tile(t["q"], t["k_pool"], t["v_pool"], blocks, counts, last, stream=st)
+        prev = st
+    main.wait_stream(prev)
+    got = ctx.finalize(w.B, out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    assert torch.equal(got, ref)
+    assert ctx.read_device_errors() == 0
