@@ -290,6 +290,8 @@ MultiShape multi_shape(const pda_ctx* ctx, int mode, int32_t q_len) {
     return s;
 }
 
+constexpr int64_t kPrefetchMinTokens = 2048;
+
 pda_status run(pda_ctx* ctx, const RunArgs& r) {
     if (!ctx) return fail(PDA_ERR_INVALID_ARG, "ctx is NULL");
     const pda_dims& d = ctx->dims;
@@ -393,6 +395,13 @@ pda_status run(pda_ctx* ctx, const RunArgs& r) {
         p.dbg_row_tokens = (int32_t)dbg_row_tokens;
         // a later chunk is right behind this call's previous chunk
         p.early_inputs = mode == pda::kTiled && (r.early_inputs || c0 > 0) ? 1 : 0;
+        // Speculative prefetch of the first stages before the grid-dependency
+        // wait: for single-query launches of block boxes of 8+ rows with at
+        // least kPrefetchMinTokens (token, kv head) rows per CTA by the table's
+        // width (small launches pay more for the extra round trips than the
+        // overlap returns; small blocks spend the TMA issue slots).
+        p.prefetch = !pda::is_multi(mode) && mode != pda::kGather && d.block_size >= 8 && row_mode == 0 &&
+                     (int64_t)cb * r.table_stride * d.block_size * Hkv >= kPrefetchMinTokens * (int64_t)grid;
         p.scale_log2 = scale_log2;
         const size_t smem = pda::smem_layout(D, ctx->stage_rows, mode, stages, cb).total;
 

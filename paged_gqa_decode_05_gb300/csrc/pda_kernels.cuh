@@ -96,7 +96,8 @@ struct Cfg {
     static constexpr int kLogST = ST == 64 ? 6 : 5;
     static constexpr int kQTiles = q_tiles(MODE);        // 16-row q tiles (0: n8 form)
     static constexpr int kConsumerWarps = consumer_warps(ST, MODE);  // 16 KV rows each (per q tile)
-    static constexpr int kThreads = (kConsumerWarps + 1) * 32;  // + the producer warp
+    static constexpr int kMainThreads = (kConsumerWarps + 1) * 32;  // + the producer warp
+    static constexpr int kThreads = kMainThreads + 32;              // + the prefetch warp
     static constexpr int kHalves = D / 64;               // 64-column swizzled slabs per row
     static constexpr int kHalfBytes = ST * 128;          // ST rows of one slab
     static constexpr int kTileBytes = kHalves * kHalfBytes;
@@ -166,24 +167,24 @@ __device__ __forceinline__ int32_t tokens_of(const SplitParams& p, int s, int32_
 }
 
 // Blocks of sequence b with length entry L, validated and clamped (flags
-// bad lengths).
-template <bool MQ>
+// bad lengths, unless FLAG is false: a speculative read).
+template <bool MQ, bool FLAG = true>
 __device__ __forceinline__ int32_t blocks_of(const SplitParams& p, int b, int32_t L) {
     int32_t len = p.lens_are_blocks ? L : tokens_of<MQ>(p, b, L);
     if (p.lens_are_blocks) {
         if (len < 0 || len > p.table_stride) {
-            atomicOr(p.err, PDA_DEVERR_BAD_LENGTH_);
+            if (FLAG) atomicOr(p.err, PDA_DEVERR_BAD_LENGTH_);
             len = len < 0 ? 0 : p.table_stride;
         }
         return len;
     }
     if (len < 0) {
-        atomicOr(p.err, PDA_DEVERR_BAD_LENGTH_);
+        if (FLAG) atomicOr(p.err, PDA_DEVERR_BAD_LENGTH_);
         len = 0;
     }
     int32_t nb = blocks_for_tokens(len, p.bs);
     if (nb > p.table_stride) {
-        atomicOr(p.err, PDA_DEVERR_BAD_LENGTH_);
+        if (FLAG) atomicOr(p.err, PDA_DEVERR_BAD_LENGTH_);
         nb = p.table_stride;
     }
     return nb;
@@ -218,6 +219,9 @@ __device__ __forceinline__ int32_t last_block_slots(const SplitParams& p, int b,
 // Thread t owns sequences [t*per, t*per + per): it loads all their length
 // entries at once (one memory round trip), stores their plan blocks in pfx,
 // and the per-thread sums are scanned with warp shuffles and the warp totals.
+// Run by the kThreads threads of the consumer and producer warps (threads
+// 0 .. kThreads-1), synchronised by named barrier 1; ends with that barrier
+// (which also publishes the stage barriers).
 template <bool MQ, int kThreads>
 __device__ __forceinline__ int32_t build_prefix(const SplitParams& p, int32_t* pfx, int32_t* scan) {
     constexpr int kPer = (kMaxLaunchBatch + kThreads - 1) / kThreads;
@@ -247,7 +251,7 @@ __device__ __forceinline__ int32_t build_prefix(const SplitParams& p, int32_t* p
         scan[warp] = x;
         scan[16 + warp] = big;
     }
-    __syncthreads();
+    asm volatile("bar.sync 1, %0;" ::"n"(kThreads) : "memory");
     int32_t run = x - sum;
     for (int w = 0; w < warp; ++w) run += scan[w];
     for (int w = 0; w < kThreads / 32; ++w) big = max(big, scan[16 + w]);
@@ -259,7 +263,7 @@ __device__ __forceinline__ int32_t build_prefix(const SplitParams& p, int32_t* p
             pfx[lo + k] = run;
             run += v;
         }
-    __syncthreads();
+    asm volatile("bar.sync 1, %0;" ::"n"(kThreads) : "memory");
     return big;
 }
 
@@ -1421,6 +1425,139 @@ __device__ __forceinline__ void run_consumer_rows(const SplitParams& p, uint32_t
 
 // ------------------------------------------------------------------ kernels
 
+// The flattened range [begin, end) of this CTA (pda_plan.h): in unit mode CTA
+// c takes unit c whole, otherwise its share of its row group's range.  Returns
+// the CTA's group (not used in unit mode).
+template <int MODE>
+__device__ __forceinline__ GroupRange cta_range(const SplitParams& p, const int32_t* pfx, int32_t nv_max,
+                                                int stage_rows, int64_t* begin, int64_t* end) {
+    const GroupRange gr = group_of_cta(blockIdx.x, pfx, p.B, rows_per_seq<is_multi(MODE)>(p), p.Hkv,
+                                       gridDim.x);
+    const int64_t units = (int64_t)p.B * p.Hkv;
+    if (unit_mode(units, gridDim.x, real_blocks(nv_max, p.unit_cost), stage_rows, p.bs)) {
+        *begin = *end = 0;
+        if ((int64_t)blockIdx.x < units) {
+            const int b = blockIdx.x / p.Hkv, kvh = blockIdx.x - b * p.Hkv;
+            const int32_t nv = pfx[b + 1] - pfx[b];
+            *begin = (int64_t)pfx[b] * p.Hkv + (int64_t)kvh * nv;
+            *end = *begin + nv;
+        }
+    } else {
+        group_cta_range(gr, blockIdx.x, begin, end);
+    }
+    return gr;
+}
+
+#ifndef PDA_PREFETCH_STAGES
+#define PDA_PREFETCH_STAGES 8
+#endif
+constexpr int kPrefetchStages = PDA_PREFETCH_STAGES;  // stages of blocks prefetched
+
+// The prefetch warp: a speculative L2 prefetch of the blocks of the CTA's
+// first stages, before the grid-dependency wait, so that while the previous
+// kernel finishes, those blocks' K/V rows move towards L2.  It builds its own
+// plan in registers (lengths read from L2, so no L1 line of them outlives the
+// wait; no flags raised), reads the first block ids from L2 and prefetches
+// their boxes, then exits: it shares no barrier with the other warps, which
+// wait and run the decode as without it.  What it reads may be stale (the
+// previous kernel may still be writing it): it only chooses which boxes to
+// prefetch, every index is kept inside the CTA's table row and the pool, and
+// the decode itself reads everything after the wait.  Single-query launches
+// of block boxes.
+template <int D, int ST, int MODE, int KPER>
+__device__ __noinline__ void prefetch_first_stages_k(const SplitParams& p, int lane) {
+    using C = Cfg<D, ST, MODE>;
+    const int per = (p.B + 31) / 32;  // <= KPER
+    const int lo = min(p.B, lane * per), hi = min(p.B, lo + per);
+    const int lbs = 31 - __clz(p.bs);  // block sizes are powers of two
+    int32_t v[KPER];  // plan blocks of this lane's sequences
+#pragma unroll
+    for (int k = 0; k < KPER; ++k) v[k] = lo + k < hi ? __ldcg(p.lens + lo + k) : 0;
+    int32_t sum = 0, big = 0;
+#pragma unroll
+    for (int k = 0; k < KPER; ++k) {
+        int32_t nb = v[k];  // blocks (tile steps) or tokens -> blocks, clamped to the table
+        if (!p.lens_are_blocks) nb = nb > 0 ? (int32_t)(((int64_t)nb + p.bs - 1) >> lbs) : 0;
+        nb = nb < 0 ? 0 : nb > p.table_stride ? p.table_stride : nb;
+        v[k] = lo + k < hi ? plan_blocks(nb, p.unit_cost) : 0;
+        sum += v[k];
+        big = max(big, v[k]);
+    }
+    int32_t x = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int32_t y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+        big = max(big, __shfl_xor_sync(0xffffffffu, big, o));
+    }
+    const int32_t base = x - sum;  // plan blocks before this lane's sequences
+    const int64_t Hkv = p.Hkv, W = (int64_t)__shfl_sync(0xffffffffu, x, 31) * Hkv;
+    const int64_t units = (int64_t)p.B * Hkv, c = blockIdx.x;
+    int64_t begin, end;
+    int32_t b = 0, nvb = 0, pfb = 0;
+    if (unit_mode(units, gridDim.x, real_blocks(big, p.unit_cost), C::kST, p.bs)) {
+        if (c >= units) return;
+        b = (int32_t)(c / Hkv);
+        int32_t pf = base;
+#pragma unroll
+        for (int k = 0; k < KPER; ++k) {
+            if (lo + k == b) { pfb = pf; nvb = v[k]; }
+            pf += v[k];
+        }
+        const int owner = b / per;  // per >= 1: b < B
+        pfb = __shfl_sync(0xffffffffu, pfb, owner);
+        nvb = __shfl_sync(0xffffffffu, nvb, owner);
+        begin = (int64_t)pfb * Hkv + (c - (int64_t)b * Hkv) * nvb;
+        end = begin + nvb;
+    } else {
+        begin = cta_begin(c, W, gridDim.x);
+        end = cta_begin(c + 1, W, gridDim.x);
+        const bool mine = sum > 0 && (int64_t)base * Hkv <= begin && begin < (int64_t)(base + sum) * Hkv;
+        const unsigned who = __ballot_sync(0xffffffffu, mine);
+        if (begin >= end || who == 0u) return;
+        const int sel = __ffs(who) - 1;
+        int32_t pf = base;
+        bool found = false;
+#pragma unroll
+        for (int k = 0; k < KPER; ++k) {
+            if (!found && v[k] > 0 && begin < (int64_t)(pf + v[k]) * Hkv) {
+                b = lo + k; nvb = v[k]; pfb = pf; found = true;
+            }
+            pf += v[k];
+        }
+        b = __shfl_sync(0xffffffffu, b, sel);
+        nvb = __shfl_sync(0xffffffffu, nvb, sel);
+        pfb = __shfl_sync(0xffffffffu, pfb, sel);
+    }
+    const int64_t rem = begin - (int64_t)pfb * Hkv;
+    if (nvb <= 0 || rem < 0 || b < 0 || b >= p.B) return;
+    const int64_t kvh = rem / nvb, j = rem % nvb;
+    if (kvh >= p.Hkv || j >= p.table_stride) return;
+    const int64_t n = min(min(min((int64_t)real_blocks(nvb, p.unit_cost) - j, end - begin),
+                              (int64_t)(kPrefetchStages * (C::kST / p.bs))),
+                          (int64_t)p.table_stride - j);
+    const int64_t row = (int64_t)b * p.table_stride + j;
+    for (int64_t i = lane; i < n; i += 32) {  // the unit's next n blocks (one unit at most)
+        const int64_t id = p.table ? (int64_t)__ldcg(p.table + row + i) : row + i;
+        if (id >= 0 && id < p.num_blocks) {
+            tma_prefetch_5d(&p.tm_k, 0, 0, 0, (int32_t)kvh, (int32_t)id);
+            tma_prefetch_5d(&p.tm_v, 0, 0, 0, (int32_t)kvh, (int32_t)id);
+        }
+    }
+}
+
+// The plan in registers is sized to the batch (up to 1, 4 or 32 sequences a
+// lane).  Not inlined: kept out of the split kernel's own code, whose start
+// every launch fetches (inlined, it cost small batches 0.4 us a call).
+template <int D, int ST, int MODE>
+__device__ __noinline__ void prefetch_first_stages(const SplitParams& p, int lane) {
+    if constexpr (!is_multi(MODE)) {
+        if (p.B <= 32) prefetch_first_stages_k<D, ST, MODE, 1>(p, lane);
+        else if (p.B <= 128) prefetch_first_stages_k<D, ST, MODE, 4>(p, lane);
+        else prefetch_first_stages_k<D, ST, MODE, kMaxLaunchBatch / 32>(p, lane);
+    }
+}
+
 // Register cap: for D <= 128 two CTAs share an SM (two 3-stage rings keep as
 // many bytes in flight as one 6-stage ring, and a second set of consumer warps
 // hides the MMA/shuffle latency; measured 4 % faster than one CTA with six
@@ -1473,28 +1610,18 @@ __global__ void __maxnreg__(split_max_regs(D, MODE)) split_kernel(const __grid_c
         prefetch_tensormap(&p.tm_k);
         prefetch_tensormap(&p.tm_v);
     }
+    if (warp == C::kConsumerWarps + 1) {  // the prefetch warp: joins nothing below
+        if (!early && MODE != kGather && p.prefetch) prefetch_first_stages<D, ST, MODE>(p, lane);
+        return;
+    }
     if (!early) {
         pdl_wait_primary();
         if (MODE != kGather) pdl_launch_dependents();
     }
-    // ends with __syncthreads (which also publishes the barriers)
-    const int32_t nv_max = build_prefix<is_multi(MODE), C::kThreads>(p, pfx, scan);
+    // ends with the main warps' barrier (which also publishes the stage barriers)
+    const int32_t nv_max = build_prefix<is_multi(MODE), C::kMainThreads>(p, pfx, scan);
     int64_t begin, end;
-    const GroupRange gr = group_of_cta(blockIdx.x, pfx, p.B, rows_per_seq<is_multi(MODE)>(p), p.Hkv,
-                                       gridDim.x);
-    const int64_t units = (int64_t)p.B * p.Hkv;
-    if (unit_mode(units, gridDim.x, real_blocks(nv_max, p.unit_cost), C::kST, p.bs)) {
-        // CTA c: unit c whole (every segment is a whole unit; gr is not used)
-        begin = end = 0;
-        if ((int64_t)blockIdx.x < units) {
-            const int b = blockIdx.x / p.Hkv, kvh = blockIdx.x - b * p.Hkv;
-            const int32_t nv = pfx[b + 1] - pfx[b];
-            begin = (int64_t)pfx[b] * p.Hkv + (int64_t)kvh * nv;
-            end = begin + nv;
-        }
-    } else {
-        group_cta_range(gr, blockIdx.x, &begin, &end);
-    }
+    const GroupRange gr = cta_range<MODE>(p, pfx, nv_max, C::kST, &begin, &end);
 
     if (warp == C::kConsumerWarps) {
         run_producer<D, ST, MODE>(p, base_s, L, pfx, meta, &abort_flag, begin, end, lane);
@@ -1547,7 +1674,8 @@ template <int D, int ST, int MODE>
 cudaError_t launch_split_mode(const SplitParams& p, int grid, size_t smem, cudaStream_t stream) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)grid, 1, 1);
-    cfg.blockDim = dim3(Cfg<D, ST, MODE>::kThreads, 1, 1);
+    // the prefetch warp is launched only when the call prefetches
+    cfg.blockDim = dim3(p.prefetch ? Cfg<D, ST, MODE>::kThreads : Cfg<D, ST, MODE>::kMainThreads, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];

@@ -46,7 +46,9 @@ __host__ __device__ constexpr int consumer_warps(int st, int mode) {
     return (st / 16) * (q_tiles(mode) ? q_tiles(mode) : 1);
 }
 constexpr int kMaxConsumerWarps = 8;
-PDA_HD int split_threads(int st, int mode) { return (consumer_warps(st, mode) + 1) * 32; }
+// Threads of a split CTA: the consumer warps, the producer warp and the
+// prefetch warp.
+PDA_HD int split_threads(int st, int mode) { return (consumer_warps(st, mode) + 2) * 32; }
 // Stage rows for a head size and block size.
 PDA_HD int stage_tokens(int D, int block_size) { return D == 256 && !block_boxes(D, block_size) ? 32 : 64; }
 // Sequences (launch rows) per launch of a mode: the row form with one q tile
@@ -108,6 +110,7 @@ struct SplitParams {
     int32_t B, Hq, Hkv, G, bs;
     int32_t unit_cost;           // plan blocks added to every non-empty unit
     int32_t dbg_row_tokens;      // tokens per (b, kvh) row of the gather output
+    int32_t prefetch;            // speculative L2 prefetch of the first stages before the wait
     int32_t early_inputs;        // tiled: read the inputs before the previous kernel completes
                                  // (a tile step right behind another of the same step)
     float scale_log2;            // softmax scale * log2(e)

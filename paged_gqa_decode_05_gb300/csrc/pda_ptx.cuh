@@ -86,6 +86,14 @@ __device__ __forceinline__ void tma_load_5d(uint32_t dst, const void* tm, int32_
         : "memory");
 }
 
+// Prefetch of one 5-D tiled box into L2 (no shared memory, no completion).
+__device__ __forceinline__ void tma_prefetch_5d(const void* tm, int32_t c0, int32_t c1, int32_t c2,
+                                                int32_t c3, int32_t c4) {
+    asm volatile("cp.async.bulk.prefetch.tensor.5d.L2.global.tile [%0, {%1, %2, %3, %4, %5}];" ::"l"(tm),
+                 "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4)
+                 : "memory");
+}
+
 // Four rows (r0..r3) of a 2-D tiled tensor, one box {64 columns, 1 row} each,
 // starting at column c0: 4 x 128 bytes land consecutively (swizzled).
 __device__ __forceinline__ void tma_gather4(uint32_t dst, const void* tm, int32_t c0, int32_t r0,
