@@ -396,11 +396,12 @@ pda_status run(pda_ctx* ctx, const RunArgs& r) {
         // a later chunk is right behind this call's previous chunk
         p.early_inputs = mode == pda::kTiled && (r.early_inputs || c0 > 0) ? 1 : 0;
         // Speculative prefetch of the first stages before the grid-dependency
-        // wait: for single-query launches of block boxes of 8+ rows with at
-        // least kPrefetchMinTokens (token, kv head) rows per CTA by the table's
-        // width (small launches pay more for the extra round trips than the
-        // overlap returns; small blocks spend the TMA issue slots).
-        p.prefetch = !pda::is_multi(mode) && mode != pda::kGather && d.block_size >= 8 && row_mode == 0 &&
+        // wait (the prefetch warp): for launches of block boxes of 8+ rows, one
+        // launch row per sequence, with at least kPrefetchMinTokens (token, kv
+        // head) rows per CTA by the table's width (small launches gain nothing;
+        // small blocks spend the TMA issue slots).
+        p.prefetch = mode != pda::kGather && mode != pda::kMultiRows32 && Qr == 1 && d.block_size >= 8 &&
+                     row_mode == 0 &&
                      (int64_t)cb * r.table_stride * d.block_size * Hkv >= kPrefetchMinTokens * (int64_t)grid;
         p.scale_log2 = scale_log2;
         const size_t smem = pda::smem_layout(D, ctx->stage_rows, mode, stages, cb).total;

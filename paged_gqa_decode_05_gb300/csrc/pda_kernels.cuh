@@ -1463,7 +1463,7 @@ constexpr int kPrefetchStages = PDA_PREFETCH_STAGES;  // stages of blocks prefet
 // previous kernel may still be writing it): it only chooses which boxes to
 // prefetch, every index is kept inside the CTA's table row and the pool, and
 // the decode itself reads everything after the wait.  Single-query launches
-// of block boxes.
+// of block boxes (multi-query with one launch row per sequence).
 template <int D, int ST, int MODE, int KPER>
 __device__ __noinline__ void prefetch_first_stages_k(const SplitParams& p, int lane) {
     using C = Cfg<D, ST, MODE>;
@@ -1551,11 +1551,12 @@ __device__ __noinline__ void prefetch_first_stages_k(const SplitParams& p, int l
 // every launch fetches (inlined, it cost small batches 0.4 us a call).
 template <int D, int ST, int MODE>
 __device__ __noinline__ void prefetch_first_stages(const SplitParams& p, int lane) {
-    if constexpr (!is_multi(MODE)) {
-        if (p.B <= 32) prefetch_first_stages_k<D, ST, MODE, 1>(p, lane);
-        else if (p.B <= 128) prefetch_first_stages_k<D, ST, MODE, 4>(p, lane);
-        else prefetch_first_stages_k<D, ST, MODE, kMaxLaunchBatch / 32>(p, lane);
-    }
+    // multi-query: one launch row per sequence only (then row s is sequence s
+    // and reads its whole length, like plain decode)
+    if (is_multi(MODE) && rows_per_seq<is_multi(MODE)>(p) != 1) return;
+    if (p.B <= 32) prefetch_first_stages_k<D, ST, MODE, 1>(p, lane);
+    else if (p.B <= 128) prefetch_first_stages_k<D, ST, MODE, 4>(p, lane);
+    else prefetch_first_stages_k<D, ST, MODE, kMaxLaunchBatch / 32>(p, lane);
 }
 
 // Register cap: for D <= 128 two CTAs share an SM (two 3-stage rings keep as
@@ -1611,7 +1612,10 @@ __global__ void __maxnreg__(split_max_regs(D, MODE)) split_kernel(const __grid_c
         prefetch_tensormap(&p.tm_v);
     }
     if (warp == C::kConsumerWarps + 1) {  // the prefetch warp: joins nothing below
-        if (!early && MODE != kGather && p.prefetch) prefetch_first_stages<D, ST, MODE>(p, lane);
+        // (not in the two-q-tile row form: the call alone costs its main loop
+        // registers, and its consumers set its time)
+        if constexpr (MODE != kGather && MODE != kMultiRows32)
+            if (!early && p.prefetch) prefetch_first_stages<D, ST, MODE>(p, lane);
         return;
     }
     if (!early) {
