@@ -290,8 +290,6 @@ MultiShape multi_shape(const pda_ctx* ctx, int mode, int32_t q_len) {
     return s;
 }
 
-constexpr int64_t kPrefetchMinTokens = 2048;
-
 pda_status run(pda_ctx* ctx, const RunArgs& r) {
     if (!ctx) return fail(PDA_ERR_INVALID_ARG, "ctx is NULL");
     const pda_dims& d = ctx->dims;
@@ -396,13 +394,11 @@ pda_status run(pda_ctx* ctx, const RunArgs& r) {
         // a later chunk is right behind this call's previous chunk
         p.early_inputs = mode == pda::kTiled && (r.early_inputs || c0 > 0) ? 1 : 0;
         // Speculative prefetch of the first stages before the grid-dependency
-        // wait (the prefetch warp): for launches of block boxes of 8+ rows, one
-        // launch row per sequence, with at least kPrefetchMinTokens (token, kv
-        // head) rows per CTA by the table's width (small launches gain nothing;
-        // small blocks spend the TMA issue slots).
-        p.prefetch = mode != pda::kGather && mode != pda::kMultiRows32 && Qr == 1 && d.block_size >= 8 &&
-                     row_mode == 0 &&
-                     (int64_t)cb * r.table_stride * d.block_size * Hkv >= kPrefetchMinTokens * (int64_t)grid;
+        // wait (the prefetch warp): for launches that wait for their
+        // predecessor, of block boxes of 8+ rows (smaller blocks spend the TMA
+        // issue slots) and one launch row per sequence.
+        p.prefetch = mode != pda::kGather && mode != pda::kMultiRows32 && !p.early_inputs && Qr == 1 &&
+                     d.block_size >= 8 && row_mode == 0;
         p.scale_log2 = scale_log2;
         const size_t smem = pda::smem_layout(D, ctx->stage_rows, mode, stages, cb).total;
 
