@@ -115,3 +115,43 @@ def test_bound_decode_matches_decode_and_tracks_contents():
     ctx.close()
     with pytest.raises(pda.PdaError):
         run()
+
+
+def test_back_to_back_decodes_with_changing_tables_in_a_graph():
+    """Consecutive decodes replayed from one graph overlap their starts (the
+    next call's prefetch warp reads lengths and block ids before the previous
+    call ends); with a different table, lengths and q in every call, each
+    output still equals its own decode run alone."""
+    import torch
+    ws = [workloads.make_workload("b2b", B=8, Hq=32, Hkv=8, D=128, block_size=16,
+                                  seq_lens=lens, seed=40 + k, pool_blocks=1100)
+          for k, lens in enumerate([[4096, 17, 2000, 1, 3000, 512, 0, 4096],
+                                    [1, 4096, 33, 2500, 64, 4096, 1500, 7],
+                                    [2048] * 8])]
+    ctx = context_for(ws[0])
+    ts = [upload(w) for w in ws]
+    alone = []
+    for t in ts:
+        alone.append(ctx.decode(t["q"], t["k_pool"], t["v_pool"], t["block_table"],
+                                t["seq_lens"]).clone())
+        torch.cuda.synchronize()
+    outs = [torch.empty_like(a) for a in alone]
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        for t, o in zip(ts, outs):
+            ctx.decode(t["q"], t["k_pool"], t["v_pool"], t["block_table"], t["seq_lens"], out=o)
+    torch.cuda.current_stream().wait_stream(s)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for _ in range(3):
+            for t, o in zip(ts, outs):
+                ctx.decode(t["q"], t["k_pool"], t["v_pool"], t["block_table"], t["seq_lens"], out=o)
+    for o in outs:
+        o.zero_()
+    for _ in range(4):
+        g.replay()
+    torch.cuda.synchronize()
+    assert ctx.read_device_errors() == 0
+    for o, a in zip(outs, alone):
+        assert torch.equal(o, a)
