@@ -677,7 +677,9 @@ def run_ours(args):
                      "timing": ("achieved = algorithmic bytes / the split kernel's average "
                                 "launch duration over the timed region (CUDA events around the "
                                 "K graph-replayed launches on their stream; one launch per "
-                                "call, so consecutive launches overlap only their set-up)"),
+                                "call; consecutive launches overlap their set-up, and the next "
+                                "launch's prefetch warp moves its first stages into L2 while "
+                                "the previous one finishes)"),
                      "isolated_us": None if math.isnan(split_avg) else split_avg * 1e3,
                      "isolated_timing": ("the kernel with CUDA events before and after every "
                                          "launch, which also stops the next launch's early "
