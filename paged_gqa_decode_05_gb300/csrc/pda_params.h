@@ -58,7 +58,7 @@ PDA_HD int max_launch_rows(int mode) { return mode == kMultiRows16 ? 512 : kMaxL
 // The unit-cost class of a mode (pda_plan.h).
 PDA_HD int32_t cost_class(int mode) {
     return mode == kMulti ? kCostMultiN8 : mode == kMultiRows16 ? kCostRows16
-         : mode == kMultiRows32 ? kCostRows32 : kCostDecode;
+         : mode == kMultiRows32 ? kCostRows32 : mode == kTiled ? kCostTiled : kCostDecode;
 }
 
 // Per-stage record the producer writes before arming the stage's barrier.

@@ -103,14 +103,16 @@ PDA_HD int64_t piece_cta(const UnitPieces& u, int64_t i, const GroupRange& gr) {
 // Causal multi-query, n8 form, whose CTAs cover about q_len times more
 // segments and read most stages from L2: four stages.  Row form (q rows as
 // the MMA's M), whose segments end in a merge of 16 or 32 q rows: four
-// stages with one q tile, six with two.
+// stages with one q tile, six with two.  Tile steps of block boxes, whose
+// segments end in a fold into the running state: six stages.
 constexpr int32_t kUnitCostX4 = 8;
 constexpr int32_t kUnitCostGatherX4 = 2;
 constexpr int32_t kUnitCostMultiX4 = 16;
 constexpr int32_t kUnitCostRows16X4 = 16;
 constexpr int32_t kUnitCostRows32X4 = 24;
+constexpr int32_t kUnitCostTiledX4 = 24;
 // Cost classes of unit_cost_blocks.
-enum UnitCostClass : int32_t { kCostDecode = 0, kCostMultiN8 = 1, kCostRows16 = 2, kCostRows32 = 3 };
+enum UnitCostClass : int32_t { kCostDecode = 0, kCostMultiN8 = 1, kCostRows16 = 2, kCostRows32 = 3, kCostTiled = 4 };
 
 // Whether a block's rows are loaded with one TMA box per block and pool: a
 // block of bs rows of D bf16 lands as [D/64 slabs][bs rows][128 bytes] and
@@ -123,10 +125,12 @@ PDA_HD bool block_boxes(int32_t head_dim, int32_t block_size) {
 
 PDA_HD int32_t unit_cost_blocks(int32_t stage_rows, int32_t head_dim, int32_t block_size, int32_t cost_class) {
     const int32_t nb = stage_rows / block_size;
+    const bool boxes = block_boxes(head_dim, block_size);
     const int32_t x4 = cost_class == kCostMultiN8 ? kUnitCostMultiX4
                      : cost_class == kCostRows16 ? kUnitCostRows16X4
                      : cost_class == kCostRows32 ? kUnitCostRows32X4
-                     : block_boxes(head_dim, block_size) ? kUnitCostX4 : kUnitCostGatherX4;
+                     : cost_class == kCostTiled && boxes ? kUnitCostTiledX4
+                     : boxes ? kUnitCostX4 : kUnitCostGatherX4;
     return (nb < 1 ? 1 : nb) * x4 / 4;
 }
 
