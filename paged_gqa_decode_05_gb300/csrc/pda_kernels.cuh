@@ -1,7 +1,7 @@
 // pda_kernels.cuh -- split-KV paged GQA decode kernels for sm_103a.
 //
 // Split kernel (one persistent CTA per resident slot; grid = SMs x CTAs/SM):
-//   * the last warp is the producer: it walks the CTA's share of the
+//   * the warp after the consumers is the producer: it walks the CTA's share of the
 //     flattened (sequence, kv head, block) space (pda_plan.h), looks every
 //     block up in the block table and copies whole K/V block rows of one kv
 //     head into a ring of shared-memory stages with one 5-D TMA tensor copy
@@ -19,6 +19,9 @@
 //     to 128) takes the row form instead (run_consumer_rows): the packed q
 //     rows are the MMA's M (S = Q K^T, O += P V), one KV walk serving up to
 //     32 of them.
+//   * a last, optional warp prefetches the CTA's first stages into L2 before
+//     the kernel's dependency wait, while the previous kernel finishes
+//     (prefetch_first_stages), and exits.
 //   * at the end of a segment the consumer warps' states are merged in shared
 //     memory; a segment that covers its whole unit writes bf16 o / l
 //     directly (or folds its state into the running state, in tiled steps).
