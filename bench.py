@@ -10,8 +10,8 @@ Default workload: the 8B-style batch (B=32, Hq=32, Hkv=8, D=128, block 16,
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                   [--workload 8b|1b|wide|ragged|tiny] [--block-size BS]
-                  [--q-len Q] [--layout paged|contiguous] [--tiles T]
-                  [--no-graph] [--no-e2e] [--no-cpu-baseline] [--no-others] [--quick]
+                  [--q-len Q] [--multi-form mma|tc] [--layout paged|contiguous]
+                  [--tiles T] [--no-graph] [--no-e2e] [--no-cpu-baseline] [--no-others] [--quick]
 
 Prints ONE JSON line (rank 0).  ``--impl reference`` times the CPU oracle
 (the fp64 definition) on this host's cores instead of the GPU path.
@@ -64,6 +64,9 @@ def parse_args():
                     help="redraw the workload with this block size (e.g. 1 for token pages)")
     ap.add_argument("--q-len", type=int, default=1,
                     help="causal queries per sequence (pda_decode_multi) instead of one")
+    ap.add_argument("--multi-form", choices=["mma", "tc"], default="mma",
+                    help="with --q-len: launch rows of 17-32 q rows on the mma.sync row form "
+                         "(the default) or the tcgen05 one")
     ap.add_argument("--tiles", type=int, default=0,
                     help="decode with the tiled lifecycle instead: begin_step, this many "
                          "step_tile calls (each 1/T of every sequence's blocks), finalize")
@@ -432,6 +435,7 @@ def run_ours(args):
             tiles.append((to_dev(blocks), to_dev(counts), to_dev(last)))
     ctx = pda.Context(max_seqs=w.B * args.q_len, num_q_heads=w.Hq, num_kv_heads=w.Hkv,
                       head_dim=w.D, block_size=w.block_size, tile_capacity=tile_cap)
+    ctx.set_multi_tc(args.multi_form == "tc")
     stream = torch.cuda.current_stream()
 
     def call(s, out):
@@ -656,6 +660,8 @@ def run_ours(args):
         "data": "synthetic: seeded N(0,1) q/K/V rounded to bf16, shuffled block table",
         "config": {**w.describe(), "workload": w.name, "kv_layout": args.layout,
                    "q_len": args.q_len, "tiles": args.tiles,
+                   **({"multi_form": ["n8", "row form (mma.sync)", "row form (tcgen05)"][
+                       ctx.multi_info(args.q_len)["form"]]} if args.q_len > 1 else {}),
                    "l2": f"inputs larger than L2 ({input_bytes / 1e6:.0f} MB per set, "
                          f"{n_sets} sets rotated, L2 {l2 / 2 ** 20:.0f} MiB)",
                    "parallelism": "replicas" if world > 1 else "single GPU",

@@ -65,7 +65,7 @@ class MultiInfo(ctypes.Structure):
 
 
 _LIB: Optional[ctypes.CDLL] = None
-ABI_VERSION = 4  # PDA_ABI_VERSION of include/pda.h that these signatures follow
+ABI_VERSION = 5  # PDA_ABI_VERSION of include/pda.h that these signatures follow
 
 
 def library_path() -> str:
@@ -110,6 +110,7 @@ def lib() -> ctypes.CDLL:
         "pda_get_launch_info": (I32, [P, ctypes.POINTER(LaunchInfo)]),
         "pda_get_multi_info": (I32, [P, I32, ctypes.POINTER(MultiInfo)]),
         "pda_set_tile_overlap": (I32, [P, I32]),
+        "pda_set_multi_tc": (I32, [P, I32]),
         "pda_plan_units": (I32, [P, I32, I32, I32, I32, I32, I32, I32, P, P, ctypes.POINTER(I64)]),
     }
     for name, (res, args) in sig.items():
@@ -241,10 +242,16 @@ class Context:
         return {f: getattr(info, f) for f, _ in LaunchInfo._fields_}
 
     def multi_info(self, q_len: int) -> dict:
-        """The launch decode_multi makes for q_len queries per sequence (pda_get_multi_info)."""
+        """The launch decode_multi makes for q_len queries per sequence (pda_get_multi_info);
+        form 0: n8, 1: row form on mma.sync, 2: row form on tcgen05."""
         info = MultiInfo()
         _check(lib().pda_get_multi_info(self._ctx, int(q_len), ctypes.byref(info)))
         return {f: getattr(info, f) for f, _ in MultiInfo._fields_}
+
+    def set_multi_tc(self, enable: bool) -> None:
+        """decode_multi takes the tcgen05 row form where it applies, or the mma.sync row form
+        (the default) (pda_set_multi_tc)."""
+        _check(lib().pda_set_multi_tc(self._ctx, int(bool(enable))))
 
     # -- argument checks (marshalling only)
     def _bf16(self, t, name, shape=None):

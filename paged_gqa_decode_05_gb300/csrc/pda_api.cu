@@ -8,6 +8,7 @@
 // finalize.  Errors are returned as status codes, never thrown.
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -80,6 +81,12 @@ struct pda_ctx {
     // depth; a grid of 0 when the shape does not exist (head size 256).
     int rows_ctas[2] = {0, 0};
     int rows_stages[2] = {0, 0};
+    // The tcgen05 row form (launch rows of 17 to 32 q rows): grid and depth
+    // (0: not on this shape), and whether calls take it (pda_set_multi_tc; off
+    // by default: measured slower than the mma.sync row form).
+    int tc_ctas = 0;
+    int tc_stages = 0;
+    bool multi_tc = false;
     float* part_o = nullptr;
     float* part_ml = nullptr;
     int32_t* unit_sync = nullptr;  // [chunk_b*Hkv][2] split-unit tickets and stored counts
@@ -101,6 +108,7 @@ struct pda_ctx {
     pda_pool_key maps_key;
     int32_t maps_row_mode = 0;
     CUtensorMap map_k, map_v;
+    CUtensorMap map_k1, map_v1;  // one-slab boxes (head size 128, block boxes): the tcgen05 form
 };
 
 namespace {
@@ -117,14 +125,16 @@ struct PoolArgs {
 // head's rows of one block: a single TMA copy per block and pool, landing in
 // shared memory as [slab][slot][128 bytes] with the 128-byte swizzle.  The
 // stride triple (block, token, kv head) places any row layout in this view.
-pda_status encode_pool(const pda_dims& d, const void* base, const PoolArgs& a, CUtensorMap* tm) {
+pda_status encode_pool(const pda_dims& d, const void* base, const PoolArgs& a, CUtensorMap* tm,
+                       bool one_slab = false) {
     auto enc = tensor_map_encoder();
     if (!enc) return fail(PDA_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
     const cuuint64_t dims[5] = {64, (cuuint64_t)d.block_size, (cuuint64_t)(d.head_dim / 64),
                                 (cuuint64_t)d.num_kv_heads, (cuuint64_t)a.num_blocks};
     const cuuint64_t strides[4] = {(cuuint64_t)a.tok * 2, 128, (cuuint64_t)a.kvh * 2,
                                    (cuuint64_t)a.blk * 2};
-    const cuuint32_t box[5] = {64, (cuuint32_t)d.block_size, (cuuint32_t)(d.head_dim / 64), 1, 1};
+    const cuuint32_t box[5] = {64, (cuuint32_t)d.block_size, one_slab ? 1u : (cuuint32_t)(d.head_dim / 64), 1,
+                               1};
     const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
     CUresult r = enc(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(base), dims, strides,
                      box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -274,6 +284,14 @@ pda_status check_plan_size(int64_t rows, int32_t table_width, int32_t unit_cost)
 struct MultiShape {
     int mode, qp, grid, stages;
 };
+// The tcgen05 form lands every stage tile as [slab][64 rows][128 B]: with one
+// box per block and slab, each box must fill whole 1024-byte swizzle atoms
+// (blocks of 8+ rows); smaller blocks qualify when their rows are gathered one
+// by one (blocks that are not whole 1024-byte boxes).
+bool tc_layout_ok(const pda_dims& d) {
+    return d.block_size >= 8 || !pda::block_boxes(d.head_dim, d.block_size);
+}
+
 MultiShape multi_shape(const pda_ctx* ctx, int mode, int32_t q_len) {
     MultiShape s = {mode, 1, ctx->split_ctas, ctx->stages};
     if (mode != pda::kMulti) return s;
@@ -284,6 +302,11 @@ MultiShape multi_shape(const pda_ctx* ctx, int mode, int32_t q_len) {
         s.mode = k ? pda::kMultiRows32 : pda::kMultiRows16;
         s.grid = ctx->rows_ctas[k];
         s.stages = ctx->rows_stages[k];
+        if (k == 1 && ctx->multi_tc && ctx->tc_ctas > 0 && tc_layout_ok(ctx->dims)) {
+            s.mode = pda::kMultiTc;
+            s.grid = ctx->tc_ctas;
+            s.stages = ctx->tc_stages;
+        }
     } else {
         s.qp = std::max(1, std::min(q_len, pda::kMaxGroup / G));
     }
@@ -332,12 +355,18 @@ pda_status run(pda_ctx* ctx, const RunArgs& r) {
           mk.blk == key.blk && mk.tok == key.tok && mk.kvh == key.kvh)) {
         ctx->maps_valid = false;
         st = encode_loader(d, r.pool, &ctx->map_k, &ctx->map_v, &ctx->maps_row_mode);
+        if (st == PDA_OK && ctx->maps_row_mode == 0 && d.head_dim == 128 && ctx->tc_ctas > 0) {
+            st = encode_pool(d, r.pool.k, r.pool, &ctx->map_k1, true);
+            if (st == PDA_OK) st = encode_pool(d, r.pool.v, r.pool, &ctx->map_v1, true);
+        }
         if (st != PDA_OK) return st;
         ctx->maps_key = key;
         ctx->maps_valid = true;
     }
     p.tm_k = ctx->map_k;
     p.tm_v = ctx->map_v;
+    p.tm_k1 = ctx->map_k1;
+    p.tm_v1 = ctx->map_v1;
     const int32_t row_mode = ctx->maps_row_mode;
 
     const int32_t Hq = d.num_q_heads, Hkv = d.num_kv_heads, D = d.head_dim;
@@ -397,7 +426,8 @@ pda_status run(pda_ctx* ctx, const RunArgs& r) {
         // wait (the prefetch warp): for launches that wait for their
         // predecessor, of block boxes of 8+ rows (smaller blocks spend the TMA
         // issue slots) and one launch row per sequence.
-        p.prefetch = mode != pda::kGather && mode != pda::kMultiRows32 && !p.early_inputs && Qr == 1 &&
+        p.prefetch = mode != pda::kGather && mode != pda::kMultiRows32 && mode != pda::kMultiTc &&
+                     !p.early_inputs && Qr == 1 &&
                      d.block_size >= 8 && row_mode == 0;
         p.scale_log2 = scale_log2;
         const size_t smem = pda::smem_layout(D, ctx->stage_rows, mode, stages, cb).total;
@@ -547,6 +577,14 @@ PDA_EXPORT pda_status pda_create(const pda_dims* dims, pda_ctx** out_ctx) {
         ctx->rows_ctas[k] = n * ctx->num_sms;
         ctx->rows_stages[k] = pda::split_stages(D, ctx->stage_rows, mode);
     }
+    if (const void* fn = pda::split_kernel_fn(D, ctx->stage_rows, pda::kMultiTc)) {
+        int n = 0;
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, pda::split_threads(ctx->stage_rows, pda::kMultiTc),
+                                                          split_smem_limit(D, ctx->stage_rows, pda::kMultiTc));
+        if (e != cudaSuccess) { delete ctx; return cuda_fail(e, "occupancy query"); }
+        ctx->tc_ctas = n * ctx->num_sms;
+        ctx->tc_stages = pda::split_stages(D, ctx->stage_rows, pda::kMultiTc);
+    }
     // Partial states: slots of G <= 8 rows for plain decode and the n8 form
     // (chunk_b x Hkv units plus one slot per CTA).  The row form's launch
     // rows hold up to 32 q rows, but a full batch of max_seqs <= 1024
@@ -557,7 +595,8 @@ PDA_EXPORT pda_status pda_create(const pda_dims* dims, pda_ctx** out_ctx) {
     if (ctx->rows_ctas[1] > 0)
         ctx->part_rows = std::max<int64_t>(ctx->part_rows,
                                            (int64_t)chunk_b * dims->num_kv_heads * 2 * pda::kMaxGroup +
-                                               (int64_t)std::max(ctx->rows_ctas[0], ctx->rows_ctas[1]) *
+                                               (int64_t)std::max({ctx->rows_ctas[0], ctx->rows_ctas[1],
+                                                                  ctx->tc_ctas}) *
                                                    pda::kMaxRowsPerWalk);
 
     const int64_t nq = (int64_t)dims->max_seqs * dims->num_q_heads;
@@ -659,6 +698,12 @@ PDA_EXPORT pda_status pda_step_tile(pda_ctx* ctx, const pda_bf16* q, const pda_b
 PDA_EXPORT pda_status pda_set_tile_overlap(pda_ctx* ctx, int32_t enable) {
     if (!ctx) return fail(PDA_ERR_INVALID_ARG, "ctx is NULL");
     ctx->tile_overlap = enable != 0;
+    return PDA_OK;
+}
+
+PDA_EXPORT pda_status pda_set_multi_tc(pda_ctx* ctx, int32_t enable) {
+    if (!ctx) return fail(PDA_ERR_INVALID_ARG, "ctx is NULL");
+    ctx->multi_tc = enable != 0;
     return PDA_OK;
 }
 
@@ -803,7 +848,7 @@ PDA_EXPORT pda_status pda_get_multi_info(const pda_ctx* ctx, int32_t q_len, pda_
         return fail(PDA_ERR_INVALID_ARG, "q_len %d outside [1, %d]", q_len,
                     std::min(pda::kMaxLaunchBatch, ctx->split_ctas));
     const MultiShape ms = multi_shape(ctx, q_len > 1 ? pda::kMulti : pda::kOneShot, q_len);
-    info->form = pda::q_tiles(ms.mode) > 0 ? 1 : 0;
+    info->form = pda::is_tc(ms.mode) ? 2 : pda::q_tiles(ms.mode) > 0 ? 1 : 0;
     info->queries_per_walk = ms.qp;
     info->rows_per_walk = ms.qp * ctx->G;
     info->walks_per_seq = (q_len + ms.qp - 1) / ms.qp;

@@ -18,7 +18,9 @@
 //   * causal multi-query with more than 8 q rows per sequence (head sizes up
 //     to 128) takes the row form instead (run_consumer_rows): the packed q
 //     rows are the MMA's M (S = Q K^T, O += P V), one KV walk serving up to
-//     32 of them.
+//     32 of them.  A tcgen05 version of it (run_mma_tc / run_consumer_tc:
+//     tensor-memory accumulators, one MMA-issuing thread) is switched on per
+//     context.
 //   * a last, optional warp prefetches the CTA's first stages into L2 before
 //     the kernel's dependency wait, while the previous kernel finishes
 //     (prefetch_first_stages), and exits.
@@ -73,7 +75,10 @@ constexpr float kLazyLog2 = 8.f;
 // are four 16K quarters, one per scheduler, and a warp takes its registers
 // from its scheduler's quarter: with 9 or 10 warps per SM (one CTA of 9 warps,
 // or two of 5) a quarter holds 3 warps, at most 168 registers per thread.
-constexpr int split_max_regs(int D, int mode) { return D == 256 && q_tiles(mode) == 0 ? 255 : 168; }
+// The tcgen05 form runs one CTA of 7 warps per SM: no cap below the ISA's.
+constexpr int split_max_regs(int D, int mode) {
+    return is_tc(mode) || (D == 256 && q_tiles(mode) == 0) ? 255 : 168;
+}
 
 // Row form of multi-query (q rows as the MMA's M): one q tile runs two CTAs
 // per SM like plain decode; two q tiles (8 consumer warps) run one CTA per
@@ -90,6 +95,13 @@ constexpr int split_max_regs(int D, int mode) { return D == 256 && q_tiles(mode)
 #ifndef PDA_STAGES_ROWS32_D128
 #define PDA_STAGES_ROWS32_D128 5
 #endif
+// tcgen05 form: one CTA per SM (it holds all 512 tensor-memory columns).
+#ifndef PDA_STAGES_TC_D64
+#define PDA_STAGES_TC_D64 10
+#endif
+#ifndef PDA_STAGES_TC_D128
+#define PDA_STAGES_TC_D128 5
+#endif
 
 // Split-kernel shape: head size D, ST KV rows per stage, MODE (the row form
 // of multi-query has its own warp count and q area).
@@ -99,13 +111,16 @@ struct Cfg {
     static constexpr int kLogST = ST == 64 ? 6 : 5;
     static constexpr int kQTiles = q_tiles(MODE);        // 16-row q tiles (0: n8 form)
     static constexpr int kConsumerWarps = consumer_warps(ST, MODE);  // 16 KV rows each (per q tile)
-    static constexpr int kMainThreads = (kConsumerWarps + 1) * 32;  // + the producer warp
+    static constexpr bool kTc = is_tc(MODE);
+    // + the producer warp (warp kConsumerWarps) and the tcgen05 form's MMA warp
+    static constexpr int kMainThreads = (kConsumerWarps + 1 + (kTc ? 1 : 0)) * 32;
     static constexpr int kThreads = kMainThreads + 32;              // + the prefetch warp
     static constexpr int kHalves = D / 64;               // 64-column swizzled slabs per row
     static constexpr int kHalfBytes = ST * 128;          // ST rows of one slab
     static constexpr int kTileBytes = kHalves * kHalfBytes;
     static constexpr int kStageBytes = 2 * kTileBytes + stage_q_rows(MODE) * D * 2;
-    static constexpr int kStages = kQTiles == 1 ? (D == 64 ? PDA_STAGES_ROWS16_D64 : PDA_STAGES_ROWS16_D128)
+    static constexpr int kStages = kTc ? (D == 64 ? PDA_STAGES_TC_D64 : PDA_STAGES_TC_D128)
+                                 : kQTiles == 1 ? (D == 64 ? PDA_STAGES_ROWS16_D64 : PDA_STAGES_ROWS16_D128)
                                  : kQTiles == 2 ? (D == 64 ? PDA_STAGES_ROWS32_D64 : PDA_STAGES_ROWS32_D128)
                                  : D == 64 ? PDA_STAGES_D64
                                  : D == 128 ? PDA_STAGES_D128
@@ -113,6 +128,8 @@ struct Cfg {
     static constexpr int kKSteps = D / 16;
     static_assert(ST == 64 || ST == 32, "stage rows");
     static_assert(kQTiles == 0 || (ST == 64 && D <= 128), "row form: 64-row stages, head size <= 128");
+    // tcgen05 form: tensor-memory columns (two S buffers, O, Q, two P buffers)
+    static constexpr uint32_t kTmemCols = 512u;
 };
 
 // Causal multi-query decode packs qp queries of a sequence into one launch
@@ -530,9 +547,19 @@ __device__ __forceinline__ void run_producer(const SplitParams& p, uint32_t base
                     atomicOr(p.err, PDA_DEVERR_BAD_BLOCK_ID_);
                     id = 0;  // stays in bounds; the flag marks the result invalid
                 }
-                const uint32_t off = (uint32_t)(lane * bs) * (uint32_t)(D * 2);
-                tma_load_5d(sK + off, &p.tm_k, 0, 0, 0, kvh, id, full, pol);
-                tma_load_5d(sV + off, &p.tm_v, 0, 0, 0, kvh, id, full, pol);
+                if constexpr (is_tc(MODE) && D == 128) {
+                    // one box per slab: the stage tile is [slab][64 rows][128 B]
+                    const uint32_t off = (uint32_t)(lane * bs) * 128u;
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        tma_load_5d(sK + off + (uint32_t)h * C::kHalfBytes, &p.tm_k1, 0, 0, h, kvh, id, full, pol);
+                        tma_load_5d(sV + off + (uint32_t)h * C::kHalfBytes, &p.tm_v1, 0, 0, h, kvh, id, full, pol);
+                    }
+                } else {
+                    const uint32_t off = (uint32_t)(lane * bs) * (uint32_t)(D * 2);
+                    tma_load_5d(sK + off, &p.tm_k, 0, 0, 0, kvh, id, full, pol);
+                    tma_load_5d(sV + off, &p.tm_v, 0, 0, 0, kvh, id, full, pol);
+                }
             }
         }
         issued |= 1u << stage;
@@ -1086,6 +1113,124 @@ __device__ __forceinline__ void zero_empty_rows(const SplitParams& p, const int3
     }
 }
 
+// One 16-row q tile of a row-form segment end, once the consumers have
+// staged their token slices' states: st_m / st_l [slice][32 q rows], st_o
+// [slice][16 rows of the tile][D + 8].  The first tile decides the piece's
+// role (whole unit, stored partial, or the last piece, which merges every
+// stored partial with its own); each (row, 4 columns) of the tile is then
+// combined over the slices and written (bf16 o / l, or the fp32 partial).
+// Returns false when the CTA aborts.
+template <int D, int kSlices, int kThreadsC>
+__device__ __forceinline__ bool rows_tile_merge(const SplitParams& p, const StageMeta& m, int tile, int ct,
+                                                int32_t ticket, const UnitPieces& pc, const GroupRange& grs,
+                                                const RowInfo& ri, const float* st_m, const float* st_l,
+                                                const float* st_o, int32_t* st_role, uint32_t cbar,
+                                                uint32_t& cphase, volatile int* abort_flag, int& role) {
+    constexpr int kOStride = D + 8;
+    const bool whole = (m.flags & kWholeUnit) != 0;
+    const int u = m.b * p.Hkv + m.kvh;
+    const int NR = m.nr, SR = p.rows_per_slot, G = p.G;
+        if (tile == 0 && ct == 0) {
+            int32_t r = whole ? kRoleWhole : ticket == pc.n - 1 ? kRoleMerge : kRoleStore;
+            if (r == kRoleMerge) {
+                int32_t* cnt = p.unit_sync + 2 * u;
+                bool ready = ld_acquire_gpu(cnt + 1) == pc.n - 1;
+                if (!ready) {
+                    const uint64_t t0 = global_ns();
+                    while (!(ready = ld_acquire_gpu(cnt + 1) == pc.n - 1) &&
+                           global_ns() - t0 <= kWaitLimitNs) {
+                    }
+                }
+                if (ready) {
+                    cnt[0] = 0;  // every piece has drawn and stored: reset for the next launch
+                    cnt[1] = 0;
+                } else {
+                    atomicOr(p.err, PDA_DEVERR_TIMEOUT_);
+                    *abort_flag = 1;
+                    r = kRoleAbort;
+                }
+            }
+            *st_role = r;
+        }
+        if (!consumer_sync(cbar, cphase, p.err, abort_flag)) return false;
+        role = *st_role;
+        if (role == kRoleAbort) return false;
+        const int h0 = tile * 16, nrt = min(16, NR - h0);
+        for (int i4 = ct; i4 < nrt * D / 4; i4 += kThreadsC) {
+            const int hr = (4 * i4) / D, d4 = 4 * i4 - hr * D;
+            const int h = h0 + hr;  // q row of the unit
+            float M = kNegInf;
+#pragma unroll
+            for (int w = 0; w < kSlices; ++w) M = fmaxf(M, st_m[w * kMaxRowsPerWalk + h]);
+            float Ls = 0.f;
+            float4 Os = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (M != kNegInf) {
+#pragma unroll
+                for (int w = 0; w < kSlices; ++w) {
+                    const float f = ex2(st_m[w * kMaxRowsPerWalk + h] - M);
+                    const float4 v =
+                        *reinterpret_cast<const float4*>(st_o + (size_t)(w * 16 + hr) * kOStride + d4);
+                    Ls += st_l[w * kMaxRowsPerWalk + h] * f;
+                    Os.x += v.x * f; Os.y += v.y * f; Os.z += v.z * f; Os.w += v.w * f;
+                }
+            }
+            if (role == kRoleStore) {
+                const int64_t r = (int64_t)(u + (int)blockIdx.x) * SR + h;
+                *reinterpret_cast<float4*>(p.part_o + r * D + d4) = Os;
+                if (d4 == 0) {
+                    p.part_ml[r * 2] = M;
+                    p.part_ml[r * 2 + 1] = Ls;
+                }
+                continue;
+            }
+            if (role == kRoleMerge) {
+                // every piece in piece order, this piece's own state in its
+                // place, up to four partials per memory round trip (the
+                // row form's registers allow four)
+                float Mr = kNegInf, Lr = 0.f;
+                float4 Or = make_float4(0.f, 0.f, 0.f, 0.f);
+                for (int i0 = 0; i0 < pc.n; i0 += 4) {
+                    float mi[4], li[4];
+                    float4 oi[4];
+                    bool own[4];
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        mi[k] = kNegInf;
+                        li[k] = 0.f;
+                        oi[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+                        const int64_t c = piece_cta(pc, i0 + k, grs);
+                        own[k] = i0 + k < pc.n && c == (int64_t)blockIdx.x;
+                        if (i0 + k >= pc.n || own[k]) continue;
+                        const int64_t r = (u + c) * SR + h;
+                        mi[k] = ld_cg(p.part_ml + r * 2);
+                        li[k] = ld_cg(p.part_ml + r * 2 + 1);
+                        oi[k] = __ldcg(reinterpret_cast<const float4*>(p.part_o + r * D + d4));
+                    }
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        if (own[k]) merge_state(Mr, Lr, Or, M, Ls, Os);
+                        else merge_state(Mr, Lr, Or, mi[k], li[k], oi[k]);
+                    }
+                }
+                M = Mr;
+                Ls = Lr;
+                Os = Or;
+            }
+            const float4 v = Ls > 0.f ? make_float4(Os.x / Ls, Os.y / Ls, Os.z / Ls, Os.w / Ls)
+                                      : make_float4(0.f, 0.f, 0.f, 0.f);
+            const int64_t oo = qo_offset<true>(p, ri.b, ri.first + h / G, m.kvh * G + h % G, D) + d4;
+            if (p.out_f32) {
+                *reinterpret_cast<float4*>(p.out_f32 + oo) = v;
+            } else {
+                uint2 w2;
+                w2.x = pack_bf16x2(v.x, v.y);
+                w2.y = pack_bf16x2(v.z, v.w);
+                *reinterpret_cast<uint2*>(p.out + oo) = w2;
+            }
+        }
+    return true;
+}
+
 template <int D, int ST, int MODE>
 __device__ __forceinline__ void run_consumer_rows(const SplitParams& p, uint32_t base_s, uint8_t* base,
                                                   const SmemLayout& L, const StageMeta* meta,
@@ -1281,7 +1426,6 @@ __device__ __forceinline__ void run_consumer_rows(const SplitParams& p, uint32_t
             l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
             l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
             if (!consumer_sync(cbar, cphase, p.err, abort_flag)) break;  // all reads of the stage done
-            const int NR = m.nr;
             const bool whole = (m.flags & kWholeUnit) != 0;
             const int u = m.b * p.Hkv + m.kvh;
             UnitPieces pc;
@@ -1290,7 +1434,6 @@ __device__ __forceinline__ void run_consumer_rows(const SplitParams& p, uint32_t
             const GroupRange grs = group_of_cta(blockIdx.x, pfx, p.B, rows_per_seq<true>(p), p.Hkv, gridDim.x);
             if (!whole) pc = unit_pieces(pfx, m.b, m.kvh, p.Hkv, p.unit_cost, grs);
             const RowInfo ri = row_info<true>(p, m.b);
-            const int SR = p.rows_per_slot;
             int role = kRoleAbort;
             bool stop = false;
             for (int tile = 0; tile < C::kQTiles && !stop; ++tile) {
@@ -1314,103 +1457,10 @@ __device__ __forceinline__ void run_consumer_rows(const SplitParams& p, uint32_t
                     m0 = m1 = kNegInf;
                     l0 = l1 = 0.f;
                 }
-                if (tile == 0 && ct == 0) {
-                    int32_t r = whole ? kRoleWhole : ticket == pc.n - 1 ? kRoleMerge : kRoleStore;
-                    if (r == kRoleMerge) {
-                        int32_t* cnt = p.unit_sync + 2 * u;
-                        bool ready = ld_acquire_gpu(cnt + 1) == pc.n - 1;
-                        if (!ready) {
-                            const uint64_t t0 = global_ns();
-                            while (!(ready = ld_acquire_gpu(cnt + 1) == pc.n - 1) &&
-                                   global_ns() - t0 <= kWaitLimitNs) {
-                            }
-                        }
-                        if (ready) {
-                            cnt[0] = 0;  // every piece has drawn and stored: reset for the next launch
-                            cnt[1] = 0;
-                        } else {
-                            atomicOr(p.err, PDA_DEVERR_TIMEOUT_);
-                            *abort_flag = 1;
-                            r = kRoleAbort;
-                        }
-                    }
-                    *st_role = r;
-                }
-                if (!consumer_sync(cbar, cphase, p.err, abort_flag)) { stop = true; break; }
-                role = *st_role;
-                if (role == kRoleAbort) { stop = true; break; }
-                const int h0 = tile * 16, nrt = min(16, NR - h0);
-                for (int i4 = ct; i4 < nrt * D / 4; i4 += kThreadsC) {
-                    const int hr = (4 * i4) / D, d4 = 4 * i4 - hr * D;
-                    const int h = h0 + hr;  // q row of the unit
-                    float M = kNegInf;
-#pragma unroll
-                    for (int w = 0; w < kSlices; ++w) M = fmaxf(M, st_m[w * kMaxRowsPerWalk + h]);
-                    float Ls = 0.f;
-                    float4 Os = make_float4(0.f, 0.f, 0.f, 0.f);
-                    if (M != kNegInf) {
-#pragma unroll
-                        for (int w = 0; w < kSlices; ++w) {
-                            const float f = ex2(st_m[w * kMaxRowsPerWalk + h] - M);
-                            const float4 v =
-                                *reinterpret_cast<const float4*>(st_o + (size_t)(w * 16 + hr) * kOStride + d4);
-                            Ls += st_l[w * kMaxRowsPerWalk + h] * f;
-                            Os.x += v.x * f; Os.y += v.y * f; Os.z += v.z * f; Os.w += v.w * f;
-                        }
-                    }
-                    if (role == kRoleStore) {
-                        const int64_t r = (int64_t)(u + (int)blockIdx.x) * SR + h;
-                        *reinterpret_cast<float4*>(p.part_o + r * D + d4) = Os;
-                        if (d4 == 0) {
-                            p.part_ml[r * 2] = M;
-                            p.part_ml[r * 2 + 1] = Ls;
-                        }
-                        continue;
-                    }
-                    if (role == kRoleMerge) {
-                        // every piece in piece order, this piece's own state in its
-                        // place, up to four partials per memory round trip (the
-                        // row form's registers allow four)
-                        float Mr = kNegInf, Lr = 0.f;
-                        float4 Or = make_float4(0.f, 0.f, 0.f, 0.f);
-                        for (int i0 = 0; i0 < pc.n; i0 += 4) {
-                            float mi[4], li[4];
-                            float4 oi[4];
-                            bool own[4];
-#pragma unroll
-                            for (int k = 0; k < 4; ++k) {
-                                mi[k] = kNegInf;
-                                li[k] = 0.f;
-                                oi[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-                                const int64_t c = piece_cta(pc, i0 + k, grs);
-                                own[k] = i0 + k < pc.n && c == (int64_t)blockIdx.x;
-                                if (i0 + k >= pc.n || own[k]) continue;
-                                const int64_t r = (u + c) * SR + h;
-                                mi[k] = ld_cg(p.part_ml + r * 2);
-                                li[k] = ld_cg(p.part_ml + r * 2 + 1);
-                                oi[k] = __ldcg(reinterpret_cast<const float4*>(p.part_o + r * D + d4));
-                            }
-#pragma unroll
-                            for (int k = 0; k < 4; ++k) {
-                                if (own[k]) merge_state(Mr, Lr, Or, M, Ls, Os);
-                                else merge_state(Mr, Lr, Or, mi[k], li[k], oi[k]);
-                            }
-                        }
-                        M = Mr;
-                        Ls = Lr;
-                        Os = Or;
-                    }
-                    const float4 v = Ls > 0.f ? make_float4(Os.x / Ls, Os.y / Ls, Os.z / Ls, Os.w / Ls)
-                                              : make_float4(0.f, 0.f, 0.f, 0.f);
-                    const int64_t oo = qo_offset<true>(p, ri.b, ri.first + h / G, m.kvh * G + h % G, D) + d4;
-                    if (p.out_f32) {
-                        *reinterpret_cast<float4*>(p.out_f32 + oo) = v;
-                    } else {
-                        uint2 w2;
-                        w2.x = pack_bf16x2(v.x, v.y);
-                        w2.y = pack_bf16x2(v.z, v.w);
-                        *reinterpret_cast<uint2*>(p.out + oo) = w2;
-                    }
+                if (!rows_tile_merge<D, kSlices, kThreadsC>(p, m, tile, ct, ticket, pc, grs, ri, st_m, st_l, st_o,
+                                                            st_role, cbar, cphase, abort_flag, role)) {
+                    stop = true;
+                    break;
                 }
             }
             if (stop) break;
@@ -1424,6 +1474,371 @@ __device__ __forceinline__ void run_consumer_rows(const SplitParams& p, uint32_t
         if (lane == 0) mbar_arrive(empty0 + 8 * stage);
         if (++stage == S) { stage = 0; phase ^= 1u; }
     }
+}
+
+// ------------------------------------------------------------ tcgen05 form
+//
+// Row form of causal multi-query on the tcgen05 tensor cores, for up to 32 q
+// rows per launch row and head sizes up to 128 (switched on per context).
+// Per stage of 64 KV rows:
+//   S = Q K^T   (M = 128: Q in four copies of the launch row's 32 q rows, one
+//                per tensor-memory lane quarter, as the A operand in tensor
+//                memory; N = the stage's 64 tokens, K from shared memory; fp32
+//                in one of two tensor-memory S buffers)
+//   softmax     (warp w, lane r: q row r over the 16 tokens of slice w, read
+//                from lanes 32w + r, columns 16w..16w+15 of the buffer)
+//   O += P V    (P as bf16 hi and lo parts in tensor memory, zero outside
+//                each copy's own slice: lane quarter w of O accumulates slice
+//                w alone; V as the MN-major B operand; O in D columns)
+// so the four slices keep their own (m, l, o) like the mma.sync row form and
+// merge at the segment end the same way.  One thread of the MMA warp issues
+// every MMA, S up to one stage ahead of P V; tcgen05.commit arrivals tell the
+// softmax warps that S (and every MMA issued before it) is done or that a P V
+// is, and the producer that a stage is free.  The stage tiles are
+// [slab][64 rows][128 B] for every loader (one TMA box per block and slab at
+// head size 128).
+
+// Tensor-memory columns (512 allocated): S buffers, O, Q, P buffers (hi, lo).
+constexpr uint32_t kTmS = 0, kTmO = 128, kTmQ = 256, kTmP = 320;
+
+// The tcgen05 form's stage tiles are [slab][64 rows][128 B], 128-byte
+// swizzled, for every loader: one box per block and slab (head size 128),
+// one box per block (head size 64), or rows gathered one by one.  So the
+// 64 rows of a slab are one K-major operand of N = 64 (8-row groups 1024
+// bytes apart), and token chunk c of V starts at c * 2048 (slabs
+// kHalfBytes apart).
+#ifndef PDA_TC_P_LO
+#define PDA_TC_P_LO 1  // P V also over the bf16 low parts of P (p = hi + lo)
+#endif
+
+// Barriers of the tcgen05 form (base + L.tcb), each at most one phase ahead of
+// its waiter: Q ready (the softmax warps, once per segment), S done of buffer
+// b (commit), P ready of buffer b (the softmax warps), P V done for even / odd
+// stages (commit), finish (commit); then the tensor-memory base address.
+enum TcBar : uint32_t { kTcQ = 0, kTcS = 8, kTcP = 24, kTcPV = 40, kTcFin = 56, kTcSlot = 64 };
+
+// A bounded barrier wait whose outcome the whole warp shares (the warp then
+// reaches the warp-wide tensor-memory loads together, or leaves together).
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity) {
+    return __all_sync(0xffffffffu, mbar_wait_bounded(bar, parity, kWaitLimitNs) ? 1 : 0) != 0;
+}
+
+template <int D, int ST, int MODE>
+__device__ __forceinline__ void run_mma_tc(const SplitParams& p, uint32_t base_s, const SmemLayout& L,
+                                           const StageMeta* meta, volatile int* abort_flag, uint32_t tmem) {
+    using C = Cfg<D, ST, MODE>;
+    constexpr int S = C::kStages;
+    constexpr int KS = C::kKSteps;
+    constexpr uint32_t idS = umma_idesc_bf16(128, 64, false);
+    constexpr uint32_t idO = umma_idesc_bf16(128, D, true);
+    const uint32_t full0 = base_s + L.bars, empty0 = full0 + 8 * S, tcb = base_s + L.tcb;
+    // S cursor (next stage whose S to issue) and P V cursor, as counts and ring slots
+    uint32_t sit = 0, pit = 0, segs = 0;
+    int ss = 0, ps = 0;
+    uint32_t sph = 0;
+    bool ok = true, done = false;
+    auto issue_s = [&](const StageMeta& m) {
+        tc_fence_after();
+        const uint32_t sK = base_s + (uint32_t)ss * C::kStageBytes;
+        const uint32_t tS = tmem + kTmS + 64u * (sit & 1u);
+        (void)m;
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks) {
+            const uint64_t b = umma_sdesc(sK + (uint32_t)(ks >> 2) * C::kHalfBytes + (uint32_t)(ks & 3) * 32u, 16u,
+                                          1024u);
+            umma_bf16_ts(tS, tmem + kTmQ + 8u * ks, b, idS, ks > 0);
+        }
+        umma_commit(tcb + kTcS + 8u * (sit & 1u));
+        if (m.flags & kSegBegin) ++segs;
+        ++sit;
+        if (++ss == S) { ss = 0; sph ^= 1u; }
+    };
+    // Polls for whichever is ready: the next stage's S (its rows landed, its Q
+    // written at a segment start, and its S buffer read: at most one S ahead of
+    // the P V cursor), then the pending P V (its P written).  S goes first: the
+    // softmax warps wait for it.
+    uint64_t idle_since = 0;
+    bool idle = false;
+    while (true) {
+        if (*abort_flag) break;
+        bool progressed = false;
+        if (!done && sit <= pit + 1 && mbar_test_wait(full0 + 8 * ss, sph)) {
+            const StageMeta m = meta[ss];
+            if (m.flags & kDone) {
+                done = true;
+            } else if (!(m.flags & kSegBegin) || mbar_test_wait(tcb + kTcQ, segs & 1u)) {
+                issue_s(m);
+                progressed = true;
+            }
+        }
+        if (pit < sit && mbar_test_wait(tcb + kTcP + 8u * (pit & 1u), (pit >> 1) & 1u)) {
+            tc_fence_after();
+            const StageMeta m = meta[ps];
+            const uint32_t sV = base_s + (uint32_t)ps * C::kStageBytes + C::kTileBytes;
+            const uint32_t tP = tmem + kTmP + 64u * (pit & 1u);
+            const int nch = (m.n_valid + 15) >> 4;
+            bool acc = (m.flags & kSegBegin) == 0;
+            for (int c = 0; c < nch; ++c) {
+                const uint64_t b = umma_sdesc(sV + 2048u * c, C::kHalfBytes, 1024u);
+                umma_bf16_ts(tmem + kTmO, tP + 8u * c, b, idO, acc);
+                if (PDA_TC_P_LO) umma_bf16_ts(tmem + kTmO, tP + 32u + 8u * c, b, idO, true);
+                acc = true;
+            }
+            umma_commit(tcb + kTcPV + 8u * (pit & 1u));
+            umma_commit(empty0 + 8 * ps);
+            ++pit;
+            if (++ps == S) ps = 0;
+            progressed = true;
+        }
+        if (done && pit == sit) break;
+        if (progressed) {
+            idle = false;
+        } else if (!idle) {
+            idle = true;
+            idle_since = global_ns();
+        } else if (global_ns() - idle_since > kWaitLimitNs) {
+            ok = false;
+            break;
+        }
+    }
+    if (!ok) {
+        atomicOr(p.err, PDA_DEVERR_TIMEOUT_);
+        *abort_flag = 1;
+    }
+    // every MMA issued has completed before the tensor memory is freed
+    umma_commit(tcb + kTcFin);
+    if (!mbar_wait_bounded(tcb + kTcFin, 0, kWaitLimitNs)) {
+        atomicOr(p.err, PDA_DEVERR_TIMEOUT_);
+        *abort_flag = 1;
+    }
+}
+
+template <int D, int ST, int MODE>
+__device__ __forceinline__ void run_consumer_tc(const SplitParams& p, uint32_t base_s, uint8_t* base,
+                                                const SmemLayout& L, const StageMeta* meta,
+                                                const int32_t* pfx, volatile int* abort_flag, int warp,
+                                                int lane, uint32_t tmem) {
+    using C = Cfg<D, ST, MODE>;
+    constexpr int S = C::kStages;
+    constexpr int kSlices = 4;
+    constexpr int kThreadsC = C::kConsumerWarps * 32;
+    constexpr int kOStride = D + 8;
+    static_assert(C::kConsumerWarps == 4 && ST == 64, "tcgen05 form: four warps of 16-row slices");
+    static_assert(kSlices * 16 * kOStride * 4 <= C::kStageBytes, "one q tile's staged states fit a stage");
+    const uint32_t full0 = base_s + L.bars, empty0 = full0 + 8 * S, tcb = base_s + L.tcb;
+    const int w = warp;                                   // token slice and lane quarter
+    const uint32_t tl = tmem + ((uint32_t)(32 * w) << 16);  // this warp's tensor-memory lanes
+    const uint32_t tO = tl + kTmO;
+    const int r = lane;                                   // this thread's q row
+    const int qi = r / p.G;                               // its query within the launch row
+    const float sl2 = p.scale_log2;
+    const int lbs = C::kLogST;  // one 64-row block per stage tile
+    float mref = kNegInf, l = 0.f;
+
+    {   // P is zero outside each copy's own slice: this warp's lanes, every P buffer
+        uint32_t z[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) z[i] = 0u;
+#pragma unroll
+        for (int c = 0; c < 128; c += 16) tmem_st16u(tl + kTmP + (uint32_t)c, z);
+        tmem_wait_st();
+    }
+    const uint32_t cbar = base_s + L.cbar;
+    uint32_t cphase = 0, it = 0;
+    int stage = 0;
+    uint32_t phase = 0;
+    int32_t ticket = 0;
+    const int ct = warp * 32 + lane;
+    zero_empty_rows<D, kThreadsC>(p, pfx, ct);
+
+    auto give_up = [&]() {
+        atomicOr(p.err, PDA_DEVERR_TIMEOUT_);
+        *abort_flag = 1;
+    };
+    // This warp's copy of a segment's q rows (the q area of stage st, nr rows)
+    // into tensor memory (lane r: q row r, zero past the launch row's rows),
+    // once every S of the previous segment is done; then Q ready.  Rows are
+    // D * 2 bytes apart: lane r reads the 16-byte chunks of each 128-byte half
+    // in the order c ^ (r & 7), so that 8 lanes in a row hit 8 different
+    // banks, and swaps them back into place.
+    auto write_q = [&](int st, int nr) {
+        const uint8_t* sq = base + (uint32_t)st * C::kStageBytes + 2 * C::kTileBytes + (size_t)r * D * 2;
+        const int x = r & 7;
+#pragma unroll
+        for (int h = 0; h < D / 64; ++h) {
+            uint4 t[8];
+#pragma unroll
+            for (int c = 0; c < 8; ++c)
+                t[c] = r < nr ? *reinterpret_cast<const uint4*>(sq + 128 * h + 16 * (c ^ x))
+                              : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+            for (int bit = 1; bit < 8; bit <<= 1) {
+                const bool sw = (x & bit) != 0;
+#pragma unroll
+                for (int c = 0; c < 8; ++c)
+                    if (!(c & bit)) {
+                        const uint4 a = t[c], d = t[c | bit];
+                        t[c] = sw ? d : a;
+                        t[c | bit] = sw ? a : d;
+                    }
+            }
+#pragma unroll
+            for (int k = 0; k < 2; ++k) {
+                uint32_t v[16];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const uint4 y = t[4 * k + j];
+                    v[4 * j] = y.x; v[4 * j + 1] = y.y; v[4 * j + 2] = y.z; v[4 * j + 3] = y.w;
+                }
+                tmem_st16u(tl + kTmQ + 32u * h + 16u * k, v);
+            }
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(tcb + kTcQ);
+    };
+    bool q_written = false;  // the next segment's Q went in before this segment's end
+    while (true) {
+        if (*abort_flag) break;
+        if (!warp_wait(full0 + 8 * stage, phase)) { give_up(); break; }
+        const StageMeta m = meta[stage];
+        if (m.flags & kDone) break;
+        if (w == 0 && lane == 0 && (m.flags & kSegEnd) && !(m.flags & kWholeUnit))
+            ticket = atomicAdd(p.unit_sync + 2 * (m.b * p.Hkv + m.kvh), 1);
+        const uint32_t sK = base_s + (uint32_t)stage * C::kStageBytes;
+        const uint32_t sV = sK + C::kTileBytes;
+        if (m.flags & kSegBegin) {
+            if (!q_written) write_q(stage, m.nr);
+            q_written = false;
+            mref = kNegInf;
+            l = 0.f;
+        }
+        if (!warp_wait(tcb + kTcS + 8u * (it & 1u), (it >> 1) & 1u)) { give_up(); break; }
+        tc_fence_after();
+        float s[16];
+        tmem_ld16(tl + kTmS + 64u * (it & 1u) + 16u * w, s);
+        // Masks: the slice's rows past the stage's valid ones, the launch row's
+        // rows past its own, and causally the tokens past the row's query
+        // (query qi of the launch row sees tokens up to m.lim + qi).
+        const int pos0 = m.j0 * p.bs + 16 * w;  // the slice's first token
+        const int th = r < m.nr ? min(m.n_valid - 1 - 16 * w, m.lim + qi - pos0) : -1;
+        float x = kNegInf;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            s[i] = i <= th ? s[i] * sl2 : kNegInf;
+            x = fmaxf(x, s[i]);
+        }
+        // lazy reference: o is rescaled only when the max runs more than 2^8
+        // past the reference (a row with no weight yet has o = 0: nothing to
+        // scale), after the previous stage's P V is done
+        const bool up = x > mref + kLazyLog2;
+        const bool scale_o = up && mref != kNegInf;
+        if (__any_sync(0xffffffffu, scale_o)) {
+            if (!warp_wait(tcb + kTcPV + 8u * ((it - 1) & 1u), ((it - 1) >> 1) & 1u)) { give_up(); break; }
+            tc_fence_after();
+            const float a = scale_o ? ex2(mref - x) : 1.f;
+            l *= a;
+#pragma unroll 1
+            for (int k = 0; k < D / 16; ++k) {
+                float o[16];
+                tmem_ld16(tO + 16u * k, o);
+#pragma unroll
+                for (int i = 0; i < 16; ++i) o[i] *= a;
+                tmem_st16(tO + 16u * k, o);
+            }
+        }
+        if (up) mref = x;
+        const float u = mref == kNegInf ? 0.f : mref;
+        uint32_t hi[8], lo[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const float p0 = ex2(s[2 * i] - u), p1 = ex2(s[2 * i + 1] - u);
+            l += p0 + p1;
+            hi[i] = pack_bf16x2(p0, p1);
+            lo[i] = PDA_TC_P_LO ? pack_bf16x2(p0 - bf16_lo(hi[i]), p1 - bf16_hi(hi[i])) : 0u;
+        }
+        // this slice's 8 columns of the stage's P buffer (a P V two stages back,
+        // the last reader, is done: it was issued before this stage's S)
+        const uint32_t tP = tl + kTmP + 64u * (it & 1u) + 8u * w;
+        tmem_st8u(tP, hi);
+        if (PDA_TC_P_LO) tmem_st8u(tP + 32u, lo);
+        // V rows past the valid ones may hold anything: P V must see zeros
+        if (16 * w < m.n_valid && m.n_valid < 16 * w + 16) {
+            zero_rows<D>(sV, m.n_valid, 16 * w + 16, lbs, lane);
+            fence_proxy_async_smem();
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(tcb + kTcP + 8u * (it & 1u));
+        if (m.flags & kSegEnd) {
+            // ---- segment end: first the next segment's Q (its stage is the next
+            // one), so that its S runs during this epilogue; then the slices'
+            // states merge per 16-row q tile through this stage's memory, as in
+            // the mma.sync row form
+            {
+                const int ns = stage + 1 == S ? 0 : stage + 1;
+                if (!warp_wait(full0 + 8 * ns, ns == 0 ? phase ^ 1u : phase)) { give_up(); break; }
+                const StageMeta mn = meta[ns];
+                if ((mn.flags & (kDone | kSegBegin)) == kSegBegin) {
+                    write_q(ns, mn.nr);
+                    q_written = true;
+                }
+            }
+            if (!warp_wait(tcb + kTcPV + 8u * (it & 1u), (it >> 1) & 1u)) { give_up(); break; }
+            tc_fence_after();
+            float* st_m = reinterpret_cast<float*>(base + L.st_m);  // [slice][32 q rows]
+            float* st_l = reinterpret_cast<float*>(base + L.st_l);
+            int32_t* st_role = reinterpret_cast<int32_t*>(base + L.st_x) + 2 * kMaxGroup;
+            float* st_o = reinterpret_cast<float*>(base + (sK - base_s));  // [slice][16][kOStride]
+            const bool read = consumer_sync(cbar, cphase, p.err, abort_flag);  // all reads of the stage done
+            if (!__all_sync(0xffffffffu, read ? 1 : 0)) break;
+            const bool whole = (m.flags & kWholeUnit) != 0;
+            const int u = m.b * p.Hkv + m.kvh;
+            UnitPieces pc;
+            pc.cf = 0; pc.su = 0; pc.n = 1; pc.every = true;
+            const GroupRange grs = group_of_cta(blockIdx.x, pfx, p.B, rows_per_seq<true>(p), p.Hkv, gridDim.x);
+            if (!whole) pc = unit_pieces(pfx, m.b, m.kvh, p.Hkv, p.unit_cost, grs);
+            const RowInfo ri = row_info<true>(p, m.b);
+            st_m[w * kMaxRowsPerWalk + r] = mref;
+            st_l[w * kMaxRowsPerWalk + r] = l;
+            int role = kRoleAbort;
+            bool stop = false;
+            for (int tile = 0; tile < 2; ++tile) {
+                // (outcomes shared by the warp: its lanes reach the tensor-memory loads together)
+                const bool ok = tile == 0 || consumer_sync(cbar, cphase, p.err, abort_flag);
+                if (!__all_sync(0xffffffffu, ok ? 1 : 0)) { stop = true; break; }
+                const bool mine = (r >> 4) == tile;  // this lane's row is in the tile
+                float* ro = st_o + (size_t)(w * 16 + (r & 15)) * kOStride;
+#pragma unroll 1
+                for (int k = 0; k < D / 16; ++k) {
+                    float o[16];
+                    tmem_ld16(tO + 16u * k, o);
+                    if (mine) {
+#pragma unroll
+                        for (int i = 0; i < 16; i += 4)
+                            *reinterpret_cast<float4*>(ro + 16 * k + i) = make_float4(o[i], o[i + 1], o[i + 2], o[i + 3]);
+                    }
+                }
+                const bool merged = rows_tile_merge<D, kSlices, kThreadsC>(
+                    p, m, tile, ct, ticket, pc, grs, ri, st_m, st_l, st_o, st_role, cbar, cphase, abort_flag, role);
+                if (!__all_sync(0xffffffffu, merged ? 1 : 0)) { stop = true; break; }
+            }
+            if (stop) break;
+            const bool synced = consumer_sync(cbar, cphase, p.err, abort_flag);
+            if (!__all_sync(0xffffffffu, synced ? 1 : 0)) break;
+            if (role == kRoleStore && ct == 0) red_release_gpu_add(p.unit_sync + 2 * u + 1, 1);
+            fence_proxy_async_smem();  // staging writes before the next TMA into this stage
+            mref = kNegInf;
+            l = 0.f;
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(empty0 + 8 * stage);
+        ++it;
+        if (++stage == S) { stage = 0; phase ^= 1u; }
+    }
+    tc_fence_before();
 }
 
 // ------------------------------------------------------------------ kernels
@@ -1603,10 +2018,20 @@ __global__ void __maxnreg__(split_max_regs(D, MODE)) split_kernel(const __grid_c
         for (int s = 0; s < C::kStages; ++s) {
             // full: the producer's arrive (+ one cp.async arrival per lane when
             // rows are copied with cp.async); empty: one arrival per consumer warp
+            // (+ the MMA warp's commit in the tcgen05 form)
             mbar_init(base_s + L.bars + 8 * s, p.row_gather == 2 ? 33 : 1);
-            mbar_init(base_s + L.bars + 8 * (C::kStages + s), C::kConsumerWarps);
+            mbar_init(base_s + L.bars + 8 * (C::kStages + s), C::kConsumerWarps + (C::kTc ? 1 : 0));
         }
         mbar_init(base_s + L.cbar, C::kConsumerWarps * 32);
+        if constexpr (C::kTc) {
+            mbar_init(base_s + L.tcb + kTcQ, C::kConsumerWarps);
+            for (int b = 0; b < 2; ++b) {
+                mbar_init(base_s + L.tcb + kTcS + 8 * b, 1);
+                mbar_init(base_s + L.tcb + kTcP + 8 * b, C::kConsumerWarps);
+                mbar_init(base_s + L.tcb + kTcPV + 8 * b, 1);
+            }
+            mbar_init(base_s + L.tcb + kTcFin, 1);
+        }
         fence_mbar_init();
         abort_flag = 0;
     }
@@ -1614,12 +2039,19 @@ __global__ void __maxnreg__(split_max_regs(D, MODE)) split_kernel(const __grid_c
         prefetch_tensormap(&p.tm_k);
         prefetch_tensormap(&p.tm_v);
     }
-    if (warp == C::kConsumerWarps + 1) {  // the prefetch warp: joins nothing below
-        // (not in the two-q-tile row form: the call alone costs its main loop
+    if (warp == C::kMainThreads / 32) {  // the prefetch warp: joins nothing below
+        // (not in the two-q-tile row forms: the call alone costs its main loop
         // registers, and its consumers set its time)
-        if constexpr (MODE != kGather && MODE != kMultiRows32)
+        if constexpr (MODE != kGather && MODE != kMultiRows32 && !C::kTc)
             if (!early && p.prefetch) prefetch_first_stages<D, ST, MODE>(p, lane);
         return;
+    }
+    if constexpr (C::kTc) {
+        if (warp == C::kConsumerWarps + 1) {  // the MMA warp holds the tensor memory
+            tmem_alloc(base_s + L.tcb + kTcSlot, C::kTmemCols);
+            tmem_relinquish();
+            tc_fence_before();
+        }
     }
     if (!early) {
         pdl_wait_primary();
@@ -1634,17 +2066,34 @@ __global__ void __maxnreg__(split_max_regs(D, MODE)) split_kernel(const __grid_c
         run_producer<D, ST, MODE>(p, base_s, L, pfx, meta, &abort_flag, begin, end, lane);
         return;
     }
-    if constexpr (q_tiles(MODE) > 0)
+    if constexpr (C::kTc) {
+        // the softmax warps and the MMA warp meet once more before the tensor
+        // memory is freed (named barrier 2: 4 + 1 warps)
+        tc_fence_after();
+        const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(base + L.tcb + kTcSlot);
+        if (warp == C::kConsumerWarps + 1) {
+            if (lane == 0) run_mma_tc<D, ST, MODE>(p, base_s, L, meta, &abort_flag, tmem);
+            __syncwarp();
+            asm volatile("bar.sync 2, %0;" ::"n"((C::kConsumerWarps + 1) * 32) : "memory");
+            tc_fence_after();
+            tmem_dealloc(tmem, C::kTmemCols);
+        } else {
+            run_consumer_tc<D, ST, MODE>(p, base_s, base, L, meta, pfx, &abort_flag, warp, lane, tmem);
+            asm volatile("bar.sync 2, %0;" ::"n"((C::kConsumerWarps + 1) * 32) : "memory");
+        }
+    } else if constexpr (q_tiles(MODE) > 0) {
         run_consumer_rows<D, ST, MODE>(p, base_s, base, L, meta, pfx, &abort_flag, warp, lane);
-    else
+    } else {
         run_consumer<D, ST, MODE>(p, base_s, base, L, meta, pfx, gr, &abort_flag, warp, lane);
+    }
 }
 
 // Host side of one split-kernel shape: its entry points by mode, their
 // pipeline depth and their launch (programmatic stream serialization: the
 // prologue may overlap the previous kernel; the kernel waits with
-// griddepcontrol.wait before reading global memory).  The row form of
-// multi-query exists for 64-row stages at head sizes up to 128.
+// griddepcontrol.wait before reading global memory).  The row forms of
+// multi-query (mma.sync and tcgen05) exist for 64-row stages at head sizes up
+// to 128.
 template <int D, int ST>
 constexpr bool has_rows_form() { return ST == 64 && D <= 128; }
 
@@ -1663,6 +2112,10 @@ const void* split_fn_of(int mode) {
             if constexpr (has_rows_form<D, ST>())
                 return reinterpret_cast<const void*>(&split_kernel<D, ST, kMultiRows32>);
             return nullptr;
+        case kMultiTc:
+            if constexpr (has_rows_form<D, ST>())
+                return reinterpret_cast<const void*>(&split_kernel<D, ST, kMultiTc>);
+            return nullptr;
         default: return nullptr;
     }
 }
@@ -1673,6 +2126,7 @@ int split_stages_of(int mode) {
     switch (mode) {
         case kMultiRows16: return Cfg<D, ST, has_rows_form<D, ST>() ? kMultiRows16 : kOneShot>::kStages;
         case kMultiRows32: return Cfg<D, ST, has_rows_form<D, ST>() ? kMultiRows32 : kOneShot>::kStages;
+        case kMultiTc: return Cfg<D, ST, has_rows_form<D, ST>() ? kMultiTc : kOneShot>::kStages;
         default: return Cfg<D, ST, kOneShot>::kStages;
     }
 }
@@ -1705,6 +2159,9 @@ cudaError_t launch_split_of(int mode, const SplitParams& p, int grid, size_t sme
             return cudaErrorInvalidValue;
         case kMultiRows32:
             if constexpr (has_rows_form<D, ST>()) return launch_split_mode<D, ST, kMultiRows32>(p, grid, smem, stream);
+            return cudaErrorInvalidValue;
+        case kMultiTc:
+            if constexpr (has_rows_form<D, ST>()) return launch_split_mode<D, ST, kMultiTc>(p, grid, smem, stream);
             return cudaErrorInvalidValue;
         default: return cudaErrorInvalidValue;
     }

@@ -28,27 +28,34 @@ constexpr int kMaxRowsPerWalk = 32;                      // q rows one KV walk s
 // x G heads) into the MMA's N (the n8 form).  kMultiRows16 / kMultiRows32
 // are the row form for head sizes up to 128: the packed q rows are the MMA's
 // M, in one or two tiles of 16 rows, so that one walk over the KV serves up
-// to 32 q rows.
-enum Mode : int { kOneShot = 0, kTiled = 1, kGather = 2, kMulti = 3, kMultiRows16 = 4, kMultiRows32 = 5 };
-constexpr int kNumModes = 6;
+// to 32 q rows.  kMultiTc is the row form of 32 q rows on the tcgen05
+// tensor cores: accumulators in tensor memory, one thread issues the MMAs.
+enum Mode : int {
+    kOneShot = 0, kTiled = 1, kGather = 2, kMulti = 3, kMultiRows16 = 4, kMultiRows32 = 5, kMultiTc = 6
+};
+constexpr int kNumModes = 7;
 __host__ __device__ constexpr bool is_multi(int mode) {
-    return mode == kMulti || mode == kMultiRows16 || mode == kMultiRows32;
+    return mode == kMulti || mode == kMultiRows16 || mode == kMultiRows32 || mode == kMultiTc;
 }
+__host__ __device__ constexpr bool is_tc(int mode) { return mode == kMultiTc; }
 __host__ __device__ constexpr bool writes_output(int mode) { return mode == kOneShot || is_multi(mode); }
-// 16-row q tiles of the row form (0: the n8 form).
+// 16-row q tiles of the row form (0: the n8 form); the tcgen05 form's segment
+// end merges its 32 rows in two such tiles.
 __host__ __device__ constexpr int q_tiles(int mode) {
-    return mode == kMultiRows16 ? 1 : mode == kMultiRows32 ? 2 : 0;
+    return mode == kMultiRows16 ? 1 : (mode == kMultiRows32 || mode == kMultiTc) ? 2 : 0;
 }
 // q rows a stage's q area holds.
 __host__ __device__ constexpr int stage_q_rows(int mode) { return q_tiles(mode) ? 16 * q_tiles(mode) : kMaxGroup; }
-// Consumer warps: one per 16 KV rows of a stage, times the q tiles in the row form.
+// Consumer warps: one per 16 KV rows of a stage, times the q tiles in the
+// mma.sync row form; the tcgen05 form's four softmax warps, one per 16-row
+// token slice and tensor-memory lane quarter.
 __host__ __device__ constexpr int consumer_warps(int st, int mode) {
-    return (st / 16) * (q_tiles(mode) ? q_tiles(mode) : 1);
+    return is_tc(mode) ? 4 : (st / 16) * (q_tiles(mode) ? q_tiles(mode) : 1);
 }
 constexpr int kMaxConsumerWarps = 8;
-// Threads of a split CTA: the consumer warps, the producer warp and the
-// prefetch warp.
-PDA_HD int split_threads(int st, int mode) { return (consumer_warps(st, mode) + 2) * 32; }
+// Threads of a split CTA: the consumer warps, the producer warp, the MMA warp
+// of the tcgen05 form and the prefetch warp.
+PDA_HD int split_threads(int st, int mode) { return (consumer_warps(st, mode) + 2 + (is_tc(mode) ? 1 : 0)) * 32; }
 // Stage rows for a head size and block size.
 PDA_HD int stage_tokens(int D, int block_size) { return D == 256 && !block_boxes(D, block_size) ? 32 : 64; }
 // Sequences (launch rows) per launch of a mode: the row form with one q tile
@@ -58,7 +65,7 @@ PDA_HD int max_launch_rows(int mode) { return mode == kMultiRows16 ? 512 : kMaxL
 // The unit-cost class of a mode (pda_plan.h).
 PDA_HD int32_t cost_class(int mode) {
     return mode == kMulti ? kCostMultiN8 : mode == kMultiRows16 ? kCostRows16
-         : mode == kMultiRows32 ? kCostRows32 : mode == kTiled ? kCostTiled : kCostDecode;
+         : (mode == kMultiRows32 || mode == kMultiTc) ? kCostRows32 : mode == kTiled ? kCostTiled : kCostDecode;
 }
 
 // Per-stage record the producer writes before arming the stage's barrier.
@@ -78,6 +85,8 @@ struct SplitParams {
     CUtensorMap tm_k;            // K pool, 5-D {64, bs, D/64, Hkv, num_blocks}, box {64, bs, D/64, 1, 1};
                                  // for gather4 2-D {D, rows}, box {64, 1}
     CUtensorMap tm_v;            // V pool, same shape
+    CUtensorMap tm_k1;           // head size 128, tcgen05 form: box {64, bs, 1, 1, 1} (one slab), so
+    CUtensorMap tm_v1;           // that a stage tile is [slab][64 rows][128 B]
     const uint16_t* q;           // [B, Hq, D] bf16
     const int32_t* table;        // [B, table_stride] block ids; null = contiguous cache
     const int32_t* lens;         // [B] tokens (one-shot) or block counts (tiled)
@@ -117,7 +126,7 @@ struct SplitParams {
 };
 
 struct SmemLayout {
-    uint32_t bars, cbar, meta, scan, st_m, st_l, st_x, pfx, total;
+    uint32_t bars, cbar, tcb, meta, scan, st_m, st_l, st_x, pfx, total;
 };
 
 // K and V tiles of ST rows plus the stage's q rows (stage_q_rows x D bf16).
@@ -136,6 +145,7 @@ PDA_HD SmemLayout smem_layout(int D, int st, int mode, int stages, int B) {
     uint32_t off = (uint32_t)stages * stage_bytes(D, st, mode);
     L.bars = off;  off += 2u * stages * 8u;
     L.cbar = off;  off += 8u;
+    L.tcb = off;   off += is_tc(mode) ? 72u : 0u;  // tcgen05 form: 8 barriers, the tensor-memory base
     L.meta = off;  off += (uint32_t)stages * (uint32_t)sizeof(StageMeta);
     L.scan = off;  off += 128u;  // per warp: block-prefix sum [16], largest unit [16]
     L.st_m = off;  off += 4u * kMaxRowsPerWalk * 4u;

@@ -32,9 +32,9 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_version_and_status_strings(lib):
-    assert lib.pda_abi_version() == 4
+    assert lib.pda_abi_version() == 5
     hdr = open(HEADER).read()
-    assert int(re.search(r"#define PDA_ABI_VERSION (\d+)", hdr).group(1)) == pda.ABI_VERSION == 4
+    assert int(re.search(r"#define PDA_ABI_VERSION (\d+)", hdr).group(1)) == pda.ABI_VERSION == 5
     assert lib.pda_status_string(0) == b"ok"
     assert b"invalid" in lib.pda_status_string(1)
 

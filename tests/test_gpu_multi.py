@@ -15,21 +15,29 @@ def _ctx(w, q_len):
                        block_size=w.block_size)
 
 
-@pytest.mark.parametrize("D,bs,G,q_len", [
+TWO_TILE_CASES = [(64, 16, 2, 9), (128, 32, 8, 5), (128, 16, 4, 8), (64, 16, 8, 4), (128, 4, 4, 8),
+                  (64, 2, 2, 9), (128, 8, 3, 7), (128, 16, 8, 8), (128, 2, 1, 33), (64, 8, 4, 6),
+                  (128, 64, 2, 11), (128, 1, 8, 4)]
+
+
+@pytest.mark.parametrize("D,bs,G,q_len,tc", [
     # n8 form (q_len * G <= 8, or head size 256)
-    (128, 16, 4, 2), (64, 16, 2, 3), (256, 8, 2, 7), (256, 4, 2, 5), (256, 2, 8, 3),
+    (128, 16, 4, 2, True), (64, 16, 2, 3, True), (256, 8, 2, 7, True), (256, 4, 2, 5, True),
+    (256, 2, 8, 3, True),
     # row form, one q tile (9..16 q rows per walk)
-    (128, 16, 4, 4), (64, 32, 8, 2), (128, 1, 4, 3), (128, 16, 1, 16), (64, 1, 4, 4),
-    # row form, two q tiles (17..32 q rows per walk), several walks per sequence
-    (64, 16, 2, 9), (128, 32, 8, 5), (128, 16, 4, 8), (64, 16, 8, 4), (128, 4, 4, 8),
-    (64, 2, 2, 9), (128, 8, 3, 7), (128, 16, 8, 8), (128, 2, 1, 33)])
-def test_multi_matches_oracle(D, bs, G, q_len):
+    (128, 16, 4, 4, True), (64, 32, 8, 2, True), (128, 1, 4, 3, True), (128, 16, 1, 16, True),
+    (64, 1, 4, 4, True)] +
+    # 17..32 q rows per walk, several walks per sequence: the tcgen05 row form
+    # (where the block layout allows it) and the mma.sync row form with two q tiles
+    [c + (tc,) for c in TWO_TILE_CASES for tc in (True, False)])
+def test_multi_matches_oracle(D, bs, G, q_len, tc):
     import torch
     lens = [q_len, 1, q_len + bs, 900, 2 * 64 + 5, 3000]
     w = workloads.make_workload("multi", B=len(lens), Hq=G * 2, Hkv=2, D=D, block_size=bs,
                                 seq_lens=lens, seed=D + bs + G + q_len)
     q = workloads.multi_queries(w, q_len)
     ctx = _ctx(w, q_len)
+    ctx.set_multi_tc(tc)
     t = upload(w)
     out = ctx.decode_multi(dev(q), t["k_pool"], t["v_pool"], t["block_table"], t["seq_lens"])
     torch.cuda.synchronize()
@@ -38,18 +46,27 @@ def test_multi_matches_oracle(D, bs, G, q_len):
                                      q_len=q_len, Hq=w.Hq, Hkv=w.Hkv, D=D, block_size=bs,
                                      n_threads=oracle.host_threads())
     assert_close_to_oracle(host_f64(out), ref, f"q_len={q_len}")
+    info = ctx.multi_info(q_len)
+    rows = info["rows_per_walk"]
+    tc_layout = bs >= 8 or (bs * D * 2) % 1024 != 0  # whole 1024-byte boxes, or gathered rows
+    assert info["form"] == (2 if tc and rows > 16 and tc_layout else 1 if rows > 8 and D <= 128 else 0)
 
 
-@pytest.mark.parametrize("D,G,q_len,form,qp,walks", [
-    (128, 4, 2, 0, 2, 1), (128, 4, 3, 1, 3, 1), (128, 4, 4, 1, 4, 1), (128, 4, 8, 1, 8, 1),
-    (128, 4, 9, 1, 8, 2), (128, 8, 2, 1, 2, 1), (128, 8, 5, 1, 4, 2), (64, 1, 8, 0, 8, 1),
-    (64, 1, 9, 1, 9, 1), (64, 2, 16, 1, 16, 1), (256, 4, 4, 0, 2, 2), (256, 8, 3, 0, 1, 3)])
-def test_multi_launch_shape(D, G, q_len, form, qp, walks):
+@pytest.mark.parametrize("D,G,q_len,form,qp,walks,tc", [
+    (128, 4, 2, 0, 2, 1, True), (128, 4, 3, 1, 3, 1, True), (128, 4, 4, 1, 4, 1, True),
+    (128, 4, 8, 2, 8, 1, True), (128, 4, 8, 1, 8, 1, False), (128, 4, 9, 2, 8, 2, True),
+    (128, 8, 2, 1, 2, 1, True), (128, 8, 5, 2, 4, 2, True), (128, 8, 5, 1, 4, 2, False),
+    (64, 1, 8, 0, 8, 1, True), (64, 1, 9, 1, 9, 1, True), (64, 2, 16, 2, 16, 1, True),
+    (64, 2, 16, 1, 16, 1, False), (256, 4, 4, 0, 2, 2, True), (256, 8, 3, 0, 1, 3, True)])
+def test_multi_launch_shape(D, G, q_len, form, qp, walks, tc):
     """The form a q_len takes: up to 8 q rows per sequence (and every head size
-    256 call) the n8 form; more, the row form with up to 32 q rows per walk,
-    one q tile (two CTAs per SM) up to 16 rows and two (one CTA per SM) above."""
+    256 call) the n8 form; more, the row form with up to 32 q rows per walk:
+    one q tile on mma.sync (two CTAs per SM) up to 16 rows, and above that two
+    q tiles on mma.sync, or the tcgen05 form where it is switched on (one CTA
+    per SM either way)."""
     import paged_gqa_decode_05_gb300 as pda
     ctx = pda.Context(max_seqs=64, num_q_heads=2 * G, num_kv_heads=2, head_dim=D, block_size=16)
+    ctx.set_multi_tc(tc)
     info = ctx.multi_info(q_len)
     launch = ctx.launch_info()
     assert (info["form"], info["queries_per_walk"], info["walks_per_seq"]) == (form, qp, walks)
@@ -62,8 +79,8 @@ def test_multi_launch_shape(D, G, q_len, form, qp, walks):
     ctx.close()
 
 
-@pytest.mark.parametrize("q_len", [2, 4, 8])
-def test_multi_garbage_outside_valid_rows_ignored(q_len):
+@pytest.mark.parametrize("q_len,tc", [(2, True), (4, True), (8, True), (8, False)])
+def test_multi_garbage_outside_valid_rows_ignored(q_len, tc):
     """NaN bits in unused blocks, unused table entries and the slots past each
     sequence's length leave every form's output unchanged, bit for bit."""
     import torch
@@ -72,6 +89,7 @@ def test_multi_garbage_outside_valid_rows_ignored(q_len):
                                 seq_lens=lens, seed=61, pool_blocks=200, max_blocks=140)
     q = workloads.multi_queries(w, q_len)
     ctx = _ctx(w, q_len)
+    ctx.set_multi_tc(tc)
 
     def run():
         t = upload(w)
@@ -99,8 +117,8 @@ def test_multi_garbage_outside_valid_rows_ignored(q_len):
     assert ctx.read_device_errors() == 0
 
 
-@pytest.mark.parametrize("q_len", [4, 8])
-def test_multi_later_tokens_do_not_reach_earlier_queries(q_len):
+@pytest.mark.parametrize("q_len,tc", [(4, True), (8, True), (8, False)])
+def test_multi_later_tokens_do_not_reach_earlier_queries(q_len, tc):
     """Causality: new K/V values at a sequence's last token change only its
     last query's output; the earlier queries' outputs stay bit-identical."""
     import torch
@@ -109,6 +127,7 @@ def test_multi_later_tokens_do_not_reach_earlier_queries(q_len):
                                 seq_lens=lens, seed=62)
     q = workloads.multi_queries(w, q_len)
     ctx = _ctx(w, q_len)
+    ctx.set_multi_tc(tc)
 
     def run():
         t = upload(w)
@@ -145,7 +164,8 @@ def test_single_query_is_decode_bit_for_bit():
 @pytest.mark.parametrize("q_len", [4, 8])
 def test_eight_b_speculative_verify(q_len):
     """The 8B-style cache with 4 or 8 verified tokens per sequence (16 or 32 q
-    rows per kv head: the row form with one or two q tiles)."""
+    rows per kv head: the mma.sync row form with one or two q tiles; at 32 rows
+    also the tcgen05 form, which agrees with it to fp32 rounding)."""
     import torch
     w = workloads.eight_b()
     q = workloads.multi_queries(w, q_len)
@@ -158,3 +178,12 @@ def test_eight_b_speculative_verify(q_len):
                                      Hq=w.Hq, Hkv=w.Hkv, D=w.D, block_size=w.block_size,
                                      n_threads=oracle.host_threads())
     assert_close_to_oracle(host_f64(out), ref, f"8b q_len={q_len}")
+    ctx.set_multi_tc(True)
+    if ctx.multi_info(q_len)["form"] == 2:
+        out2 = ctx.decode_multi(dev(q), t["k_pool"], t["v_pool"], t["block_table"], t["seq_lens"])
+        torch.cuda.synchronize()
+        assert ctx.read_device_errors() == 0
+        assert_close_to_oracle(host_f64(out2), ref, f"8b q_len={q_len} tcgen05")
+        # the two forms differ only in fp32 summation order (and then the bf16 rounding of o)
+        a, b = out.float(), out2.float()
+        assert float((a - b).abs().max()) <= 2 ** -6 * max(1.0, float(b.abs().max()))
