@@ -187,3 +187,53 @@ def test_eight_b_speculative_verify(q_len):
         # the two forms differ only in fp32 summation order (and then the bf16 rounding of o)
         a, b = out.float(), out2.float()
         assert float((a - b).abs().max()) <= 2 ** -6 * max(1.0, float(b.abs().max()))
+
+
+def test_tc_form_back_to_back_with_plain_decodes_in_a_graph():
+    """The tcgen05 form holds all 512 tensor-memory columns of an SM per CTA.
+    Replayed from one graph, tcgen05 multi-query calls interleaved with plain
+    decodes (each launch overlapping the previous one's tail) give, every
+    call, the output of the same call run alone, bit for bit."""
+    import torch
+    q_len = 8
+    ws = [workloads.make_workload("tc_b2b", B=8, Hq=32, Hkv=8, D=128, block_size=16,
+                                  seq_lens=lens, seed=70 + k, pool_blocks=1100)
+          for k, lens in enumerate([[4096, 17, 2000, 9, 3000, 512, 8, 4096],
+                                    [2048] * 8])]
+    qs = [dev(workloads.multi_queries(w, q_len)) for w in ws]
+    ctx = _ctx(ws[0], q_len)
+    ctx.set_multi_tc(True)
+    assert ctx.multi_info(q_len)["form"] == 2
+    ts = [upload(w) for w in ws]
+
+    def calls(outs_m, outs_d):
+        for t, q, om, od in zip(ts, qs, outs_m, outs_d):
+            ctx.decode_multi(q, t["k_pool"], t["v_pool"], t["block_table"], t["seq_lens"], out=om)
+            ctx.decode(t["q"], t["k_pool"], t["v_pool"], t["block_table"], t["seq_lens"], out=od)
+    alone_m, alone_d = [], []
+    for t, q in zip(ts, qs):
+        alone_m.append(ctx.decode_multi(q, t["k_pool"], t["v_pool"], t["block_table"],
+                                        t["seq_lens"]).clone())
+        torch.cuda.synchronize()
+        alone_d.append(ctx.decode(t["q"], t["k_pool"], t["v_pool"], t["block_table"],
+                                  t["seq_lens"]).clone())
+        torch.cuda.synchronize()
+    outs_m = [torch.empty_like(a) for a in alone_m]
+    outs_d = [torch.empty_like(a) for a in alone_d]
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        calls(outs_m, outs_d)
+    torch.cuda.current_stream().wait_stream(s)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for _ in range(3):
+            calls(outs_m, outs_d)
+    for o in outs_m + outs_d:
+        o.zero_()
+    for _ in range(4):
+        g.replay()
+    torch.cuda.synchronize()
+    assert ctx.read_device_errors() == 0
+    for o, a in zip(outs_m + outs_d, alone_m + alone_d):
+        assert torch.equal(o, a)
