@@ -387,8 +387,9 @@ pda_status pda_get_launch_info(const pda_ctx* ctx, pda_launch_info* info);
 /*
  * The launch pda_decode_multi makes for q_len queries per sequence (host
  * only): the form (0: n8, q rows as the MMA's N; 1: row form, q rows as its
- * M, on mma.sync; 2: the row form on the tcgen05 tensor cores, for launch
- * rows of 17 to 32 q rows, accumulators in tensor memory), queries per launch
+ * M, on mma.sync; 2: the row form on the tcgen05 tensor cores at head size
+ * 128, for launch rows of 17 to 32 q rows, accumulators in tensor memory,
+ * when switched on with pda_set_multi_tc), queries per launch
  * row and their q rows (queries x G), launch rows (KV walks) per sequence,
  * the grid and the pipeline depth.  q_len outside [1, split_ctas] is
  * PDA_ERR_INVALID_ARG; q_len 1 describes plain decode.
@@ -405,7 +406,7 @@ pda_status pda_get_multi_info(const pda_ctx* ctx, int32_t q_len, pda_multi_info*
 /*
  * Whether pda_decode_multi takes the tcgen05 row form where it applies
  * (enable != 0) or the mma.sync row form (0, the default).  The form exists
- * for head sizes up to 128 with blocks of 8+ rows or rows gathered one by one
+ * for head size 128 with blocks of 8+ rows or rows gathered one by one
  * (block sizes below 8 whose blocks are not whole 1024-byte boxes).  Both
  * forms compute the same function (up to fp32 summation order).  The tcgen05
  * form measures 15-20 % slower on the multi-query workloads tried, hence off

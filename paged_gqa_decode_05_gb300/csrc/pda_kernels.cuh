@@ -18,9 +18,9 @@
 //   * causal multi-query with more than 8 q rows per sequence (head sizes up
 //     to 128) takes the row form instead (run_consumer_rows): the packed q
 //     rows are the MMA's M (S = Q K^T, O += P V), one KV walk serving up to
-//     32 of them.  A tcgen05 version of it (run_mma_tc / run_consumer_tc:
-//     tensor-memory accumulators, one MMA-issuing thread) is switched on per
-//     context.
+//     32 of them.  A tcgen05 version of it at head size 128 (run_mma_tc /
+//     run_consumer_tc: tensor-memory accumulators, one MMA-issuing thread) is
+//     switched on per context.
 //   * a last, optional warp prefetches the CTA's first stages into L2 before
 //     the kernel's dependency wait, while the previous kernel finishes
 //     (prefetch_first_stages), and exits.
@@ -75,10 +75,7 @@ constexpr float kLazyLog2 = 8.f;
 // are four 16K quarters, one per scheduler, and a warp takes its registers
 // from its scheduler's quarter: with 9 or 10 warps per SM (one CTA of 9 warps,
 // or two of 5) a quarter holds 3 warps, at most 168 registers per thread.
-// The tcgen05 form runs one CTA of 7 warps per SM: no cap below the ISA's.
-constexpr int split_max_regs(int D, int mode) {
-    return is_tc(mode) || (D == 256 && q_tiles(mode) == 0) ? 255 : 168;
-}
+constexpr int split_max_regs(int D, int mode) { return D == 256 && q_tiles(mode) == 0 ? 255 : 168; }
 
 // Row form of multi-query (q rows as the MMA's M): one q tile runs two CTAs
 // per SM like plain decode; two q tiles (8 consumer warps) run one CTA per
@@ -95,10 +92,8 @@ constexpr int split_max_regs(int D, int mode) {
 #ifndef PDA_STAGES_ROWS32_D128
 #define PDA_STAGES_ROWS32_D128 5
 #endif
-// tcgen05 form: one CTA per SM (it holds all 512 tensor-memory columns).
-#ifndef PDA_STAGES_TC_D64
-#define PDA_STAGES_TC_D64 10
-#endif
+// tcgen05 form (head size 128): one CTA per SM (a kernel with tcgen05
+// instructions gets one CTA per SM), five 40 KB stages.
 #ifndef PDA_STAGES_TC_D128
 #define PDA_STAGES_TC_D128 5
 #endif
@@ -119,7 +114,7 @@ struct Cfg {
     static constexpr int kHalfBytes = ST * 128;          // ST rows of one slab
     static constexpr int kTileBytes = kHalves * kHalfBytes;
     static constexpr int kStageBytes = 2 * kTileBytes + stage_q_rows(MODE) * D * 2;
-    static constexpr int kStages = kTc ? (D == 64 ? PDA_STAGES_TC_D64 : PDA_STAGES_TC_D128)
+    static constexpr int kStages = kTc ? PDA_STAGES_TC_D128
                                  : kQTiles == 1 ? (D == 64 ? PDA_STAGES_ROWS16_D64 : PDA_STAGES_ROWS16_D128)
                                  : kQTiles == 2 ? (D == 64 ? PDA_STAGES_ROWS32_D64 : PDA_STAGES_ROWS32_D128)
                                  : D == 64 ? PDA_STAGES_D64
@@ -128,8 +123,9 @@ struct Cfg {
     static constexpr int kKSteps = D / 16;
     static_assert(ST == 64 || ST == 32, "stage rows");
     static_assert(kQTiles == 0 || (ST == 64 && D <= 128), "row form: 64-row stages, head size <= 128");
-    // tcgen05 form: tensor-memory columns (two S buffers, O, Q, two P buffers)
-    static constexpr uint32_t kTmemCols = 512u;
+    // tcgen05 form: tensor-memory columns (two S buffers, O^T, Q)
+    static constexpr uint32_t kTmemCols = 256u;
+    static_assert(!kTc || D == 128, "tcgen05 form: head size 128");
 };
 
 // Causal multi-query decode packs qp queries of a sequence into one launch
@@ -1479,43 +1475,50 @@ __device__ __forceinline__ void run_consumer_rows(const SplitParams& p, uint32_t
 // ------------------------------------------------------------ tcgen05 form
 //
 // Row form of causal multi-query on the tcgen05 tensor cores, for up to 32 q
-// rows per launch row and head sizes up to 128 (switched on per context).
-// Per stage of 64 KV rows:
-//   S = Q K^T   (M = 128: Q in four copies of the launch row's 32 q rows, one
-//                per tensor-memory lane quarter, as the A operand in tensor
-//                memory; N = the stage's 64 tokens, K from shared memory; fp32
-//                in one of two tensor-memory S buffers)
-//   softmax     (warp w, lane r: q row r over the 16 tokens of slice w, read
-//                from lanes 32w + r, columns 16w..16w+15 of the buffer)
-//   O += P V    (P as bf16 hi and lo parts in tensor memory, zero outside
-//                each copy's own slice: lane quarter w of O accumulates slice
-//                w alone; V as the MN-major B operand; O in D columns)
-// so the four slices keep their own (m, l, o) like the mma.sync row form and
-// merge at the segment end the same way.  One thread of the MMA warp issues
-// every MMA, S up to one stage ahead of P V; tcgen05.commit arrivals tell the
-// softmax warps that S (and every MMA issued before it) is done or that a P V
-// is, and the producer that a stage is free.  The stage tiles are
+// rows per launch row at head size 128 (switched on per context).  Two groups
+// of four softmax warps take the even and the odd stages.  Per stage of 64 KV
+// rows:
+//   S = Q K^T     (M = 128: Q in four copies of the launch row's 32 q rows, one
+//                  per tensor-memory lane quarter, as the A operand in tensor
+//                  memory; N = the stage's 64 tokens, K from shared memory;
+//                  fp32 in the group's tensor-memory S buffer)
+//   softmax       (warp w of the group, lane r: q row r over the 16 tokens of
+//                  slice w, read from lanes 32w + r, columns 16w..16w+15; the
+//                  four slices' row maxima meet in shared memory, so a row
+//                  keeps one reference per group)
+//   O^T += V^T P^T (M = D = 128: V as an MN-major A operand; N = the 32 q rows:
+//                  P as bf16 hi and lo parts, [q row][token], written into the
+//                  stage's q area once the stage's q rows are in tensor memory;
+//                  the group's O^T in 32 tensor-memory columns: lane =
+//                  head-dim element)
+// At a segment end the two groups' states merge as two slices.  One thread of
+// the MMA warp issues every MMA, S up to one stage ahead of P V; the
+// tcgen05.commit arrivals tell the softmax warps that S (and every MMA issued
+// before it) is done or that a P V is, and the producer that a stage is free.
+// A kernel with tcgen05 instructions runs one CTA per SM.  The stage tiles are
 // [slab][64 rows][128 B] for every loader (one TMA box per block and slab at
 // head size 128).
 
-// Tensor-memory columns (512 allocated): S buffers, O, Q, P buffers (hi, lo).
-constexpr uint32_t kTmS = 0, kTmO = 128, kTmQ = 256, kTmP = 320;
+// Tensor-memory columns (256 allocated): an S buffer and an O^T per group of
+// softmax warps, Q.
+constexpr uint32_t kTmS = 0, kTmO = 128, kTmQ = 192;
 
-// The tcgen05 form's stage tiles are [slab][64 rows][128 B], 128-byte
-// swizzled, for every loader: one box per block and slab (head size 128),
-// one box per block (head size 64), or rows gathered one by one.  So the
+// The stage tiles are [slab][64 rows][128 B], 128-byte swizzled, for every
+// loader: one box per block and slab, or rows gathered one by one.  So the
 // 64 rows of a slab are one K-major operand of N = 64 (8-row groups 1024
-// bytes apart), and token chunk c of V starts at c * 2048 (slabs
-// kHalfBytes apart).
+// bytes apart), and token chunk c of V, as the MN-major A operand of O^T,
+// starts at c * 2048 (its 64-element slabs kHalfBytes apart).
 #ifndef PDA_TC_P_LO
 #define PDA_TC_P_LO 1  // P V also over the bf16 low parts of P (p = hi + lo)
 #endif
+constexpr uint32_t kTcPLo = 4096;  // the lo part of P after the hi part ([32][64] bf16 each)
 
 // Barriers of the tcgen05 form (base + L.tcb), each at most one phase ahead of
-// its waiter: Q ready (the softmax warps, once per segment), S done of buffer
-// b (commit), P ready of buffer b (the softmax warps), P V done for even / odd
-// stages (commit), finish (commit); then the tensor-memory base address.
-enum TcBar : uint32_t { kTcQ = 0, kTcS = 8, kTcP = 24, kTcPV = 40, kTcFin = 56, kTcSlot = 64 };
+// its waiter: Q ready (a group of softmax warps, once per segment); for the
+// even / odd stages (the two groups) S done (commit), P ready (the group) and
+// P V done (commit); finish (commit); each group's own barrier (its four
+// warps); then the tensor-memory base address.
+enum TcBar : uint32_t { kTcQ = 0, kTcS = 8, kTcP = 24, kTcPV = 40, kTcFin = 56, kTcG = 64, kTcSlot = 80 };
 
 // A bounded barrier wait whose outcome the whole warp shares (the warp then
 // reaches the warp-wide tensor-memory loads together, or leaves together).
@@ -1530,10 +1533,12 @@ __device__ __forceinline__ void run_mma_tc(const SplitParams& p, uint32_t base_s
     constexpr int S = C::kStages;
     constexpr int KS = C::kKSteps;
     constexpr uint32_t idS = umma_idesc_bf16(128, 64, false);
-    constexpr uint32_t idO = umma_idesc_bf16(128, D, true);
+    constexpr uint32_t idO = umma_idesc_bf16(D, kMaxRowsPerWalk, false, true);
+    static_assert(D == 128, "O^T takes the head dimension as the MMA's M = 128");
     const uint32_t full0 = base_s + L.bars, empty0 = full0 + 8 * S, tcb = base_s + L.tcb;
     // S cursor (next stage whose S to issue) and P V cursor, as counts and ring slots
     uint32_t sit = 0, pit = 0, segs = 0;
+    uint32_t fresh = 3u;  // bit g: group g's O^T holds nothing of the current segment yet
     int ss = 0, ps = 0;
     uint32_t sph = 0;
     bool ok = true, done = false;
@@ -1541,7 +1546,6 @@ __device__ __forceinline__ void run_mma_tc(const SplitParams& p, uint32_t base_s
         tc_fence_after();
         const uint32_t sK = base_s + (uint32_t)ss * C::kStageBytes;
         const uint32_t tS = tmem + kTmS + 64u * (sit & 1u);
-        (void)m;
 #pragma unroll
         for (int ks = 0; ks < KS; ++ks) {
             const uint64_t b = umma_sdesc(sK + (uint32_t)(ks >> 2) * C::kHalfBytes + (uint32_t)(ks & 3) * 32u, 16u,
@@ -1575,13 +1579,16 @@ __device__ __forceinline__ void run_mma_tc(const SplitParams& p, uint32_t base_s
             tc_fence_after();
             const StageMeta m = meta[ps];
             const uint32_t sV = base_s + (uint32_t)ps * C::kStageBytes + C::kTileBytes;
-            const uint32_t tP = tmem + kTmP + 64u * (pit & 1u);
+            const uint32_t sP = sV + C::kTileBytes;  // the stage's q area holds P
             const int nch = (m.n_valid + 15) >> 4;
-            bool acc = (m.flags & kSegBegin) == 0;
+            if (m.flags & kSegBegin) fresh = 3u;
+            const uint32_t tO = tmem + kTmO + 32u * (pit & 1u);  // the stage's group's O^T
+            bool acc = ((fresh >> (pit & 1u)) & 1u) == 0u;
+            fresh &= ~(1u << (pit & 1u));
             for (int c = 0; c < nch; ++c) {
-                const uint64_t b = umma_sdesc(sV + 2048u * c, C::kHalfBytes, 1024u);
-                umma_bf16_ts(tmem + kTmO, tP + 8u * c, b, idO, acc);
-                if (PDA_TC_P_LO) umma_bf16_ts(tmem + kTmO, tP + 32u + 8u * c, b, idO, true);
+                const uint64_t a = umma_sdesc(sV + 2048u * c, C::kHalfBytes, 1024u);
+                umma_bf16_ss(tO, a, umma_sdesc(sP + 32u * c, 16u, 1024u), idO, acc);
+                if (PDA_TC_P_LO) umma_bf16_ss(tO, a, umma_sdesc(sP + kTcPLo + 32u * c, 16u, 1024u), idO, true);
                 acc = true;
             }
             umma_commit(tcb + kTcPV + 8u * (pit & 1u));
@@ -1620,31 +1627,29 @@ __device__ __forceinline__ void run_consumer_tc(const SplitParams& p, uint32_t b
                                                 int lane, uint32_t tmem) {
     using C = Cfg<D, ST, MODE>;
     constexpr int S = C::kStages;
-    constexpr int kSlices = 4;
     constexpr int kThreadsC = C::kConsumerWarps * 32;
     constexpr int kOStride = D + 8;
-    static_assert(C::kConsumerWarps == 4 && ST == 64, "tcgen05 form: four warps of 16-row slices");
-    static_assert(kSlices * 16 * kOStride * 4 <= C::kStageBytes, "one q tile's staged states fit a stage");
+    static_assert(C::kConsumerWarps == 8 && ST == 64 && D == 128, "tcgen05 form: two groups of four slice warps");
+    static_assert(2 * 2 * 16 * kOStride * 4 <= C::kStageBytes, "both groups' staged o rows fit a stage");
     const uint32_t full0 = base_s + L.bars, empty0 = full0 + 8 * S, tcb = base_s + L.tcb;
-    const int w = warp;                                   // token slice and lane quarter
+    const int g = warp >> 2;                              // group: the stages whose index has parity g
+    const int w = warp & 3;                               // token slice and lane quarter
     const uint32_t tl = tmem + ((uint32_t)(32 * w) << 16);  // this warp's tensor-memory lanes
-    const uint32_t tO = tl + kTmO;
-    const int r = lane;                                   // this thread's q row
+    const uint32_t tS = tl + kTmS + 64u * g + 16u * w;    // this group's S buffer, this slice's columns
+    const uint32_t tO = tl + kTmO + 32u * g;              // this group's O^T (lane: head-dim element)
+    const int r = lane;                                   // this thread's q row (S, P)
     const int qi = r / p.G;                               // its query within the launch row
     const float sl2 = p.scale_log2;
     const int lbs = C::kLogST;  // one 64-row block per stage tile
-    float mref = kNegInf, l = 0.f;
+    float* xmax = reinterpret_cast<float*>(base + L.tcx);  // [group][2][4 slices][32 rows]
+    float* lpart = xmax + 2 * 2 * 4 * kMaxRowsPerWalk;    // [8 warps][32 rows]
+    float mref = kNegInf;  // the row's reference in this group (the same in its four warps)
+    float lw = 0.f;        // the row's weight sum over this warp's slice of this group's stages
+    bool active = false;   // this group has a stage in the current segment
 
-    {   // P is zero outside each copy's own slice: this warp's lanes, every P buffer
-        uint32_t z[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) z[i] = 0u;
-#pragma unroll
-        for (int c = 0; c < 128; c += 16) tmem_st16u(tl + kTmP + (uint32_t)c, z);
-        tmem_wait_st();
-    }
-    const uint32_t cbar = base_s + L.cbar;
-    uint32_t cphase = 0, it = 0;
+    const uint32_t cbar = base_s + L.cbar;           // the eight softmax warps
+    const uint32_t gbar = tcb + kTcG + 8u * g;       // this group's four warps
+    uint32_t cphase = 0, gphase = 0, it = 0;
     int stage = 0;
     uint32_t phase = 0;
     int32_t ticket = 0;
@@ -1654,6 +1659,16 @@ __device__ __forceinline__ void run_consumer_tc(const SplitParams& p, uint32_t b
     auto give_up = [&]() {
         atomicOr(p.err, PDA_DEVERR_TIMEOUT_);
         *abort_flag = 1;
+    };
+    // Barriers among the softmax warps (all eight; this group's four) whose
+    // outcome each warp shares.
+    auto sync_all = [&]() -> bool {
+        const bool ok = consumer_sync(cbar, cphase, p.err, abort_flag);
+        return __all_sync(0xffffffffu, ok ? 1 : 0) != 0;
+    };
+    auto sync_group = [&]() -> bool {
+        const bool ok = consumer_sync(gbar, gphase, p.err, abort_flag);
+        return __all_sync(0xffffffffu, ok ? 1 : 0) != 0;
     };
     // This warp's copy of a segment's q rows (the q area of stage st, nr rows)
     // into tensor memory (lane r: q row r, zero past the launch row's rows),
@@ -1698,86 +1713,104 @@ __device__ __forceinline__ void run_consumer_tc(const SplitParams& p, uint32_t b
         __syncwarp();
         if (lane == 0) mbar_arrive(tcb + kTcQ);
     };
-    bool q_written = false;  // the next segment's Q went in before this segment's end
+    bool q_written = false;  // this group wrote the next segment's Q before the segment's end
+    // Every warp of both groups walks every stage: its own group's stages in
+    // full, the other group's for their flags (a segment end gathers both).
     while (true) {
         if (*abort_flag) break;
         if (!warp_wait(full0 + 8 * stage, phase)) { give_up(); break; }
         const StageMeta m = meta[stage];
         if (m.flags & kDone) break;
-        if (w == 0 && lane == 0 && (m.flags & kSegEnd) && !(m.flags & kWholeUnit))
-            ticket = atomicAdd(p.unit_sync + 2 * (m.b * p.Hkv + m.kvh), 1);
         const uint32_t sK = base_s + (uint32_t)stage * C::kStageBytes;
         const uint32_t sV = sK + C::kTileBytes;
-        if (m.flags & kSegBegin) {
-            if (!q_written) write_q(stage, m.nr);
-            q_written = false;
-            mref = kNegInf;
-            l = 0.f;
-        }
-        if (!warp_wait(tcb + kTcS + 8u * (it & 1u), (it >> 1) & 1u)) { give_up(); break; }
-        tc_fence_after();
-        float s[16];
-        tmem_ld16(tl + kTmS + 64u * (it & 1u) + 16u * w, s);
-        // Masks: the slice's rows past the stage's valid ones, the launch row's
-        // rows past its own, and causally the tokens past the row's query
-        // (query qi of the launch row sees tokens up to m.lim + qi).
-        const int pos0 = m.j0 * p.bs + 16 * w;  // the slice's first token
-        const int th = r < m.nr ? min(m.n_valid - 1 - 16 * w, m.lim + qi - pos0) : -1;
-        float x = kNegInf;
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            s[i] = i <= th ? s[i] * sl2 : kNegInf;
-            x = fmaxf(x, s[i]);
-        }
-        // lazy reference: o is rescaled only when the max runs more than 2^8
-        // past the reference (a row with no weight yet has o = 0: nothing to
-        // scale), after the previous stage's P V is done
-        const bool up = x > mref + kLazyLog2;
-        const bool scale_o = up && mref != kNegInf;
-        if (__any_sync(0xffffffffu, scale_o)) {
-            if (!warp_wait(tcb + kTcPV + 8u * ((it - 1) & 1u), ((it - 1) >> 1) & 1u)) { give_up(); break; }
-            tc_fence_after();
-            const float a = scale_o ? ex2(mref - x) : 1.f;
-            l *= a;
-#pragma unroll 1
-            for (int k = 0; k < D / 16; ++k) {
-                float o[16];
-                tmem_ld16(tO + 16u * k, o);
-#pragma unroll
-                for (int i = 0; i < 16; ++i) o[i] *= a;
-                tmem_st16(tO + 16u * k, o);
+        const uint32_t sP = sV + C::kTileBytes;  // the q area; P once Q is in tensor memory
+        if ((it & 1u) == (uint32_t)g) {
+            if (m.flags & kSegBegin) {
+                if (!q_written) write_q(stage, m.nr);
+                q_written = false;
             }
-        }
-        if (up) mref = x;
-        const float u = mref == kNegInf ? 0.f : mref;
-        uint32_t hi[8], lo[8];
+            active = true;
+            if (!warp_wait(tcb + kTcS + 8u * g, (it >> 1) & 1u)) { give_up(); break; }
+            tc_fence_after();
+            float s[16];
+            tmem_ld16(tS, s);
+            // Masks: the slice's rows past the stage's valid ones, the launch row's
+            // rows past its own, and causally the tokens past the row's query
+            // (query qi of the launch row sees tokens up to m.lim + qi).
+            const int pos0 = m.j0 * p.bs + 16 * w;  // the slice's first token
+            const int th = r < m.nr ? min(m.n_valid - 1 - 16 * w, m.lim + qi - pos0) : -1;
+            float xw = kNegInf;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const float p0 = ex2(s[2 * i] - u), p1 = ex2(s[2 * i + 1] - u);
-            l += p0 + p1;
-            hi[i] = pack_bf16x2(p0, p1);
-            lo[i] = PDA_TC_P_LO ? pack_bf16x2(p0 - bf16_lo(hi[i]), p1 - bf16_hi(hi[i])) : 0u;
+            for (int i = 0; i < 16; ++i) {
+                s[i] = i <= th ? s[i] * sl2 : kNegInf;
+                xw = fmaxf(xw, s[i]);
+            }
+            // the row's max over the stage: the group's four slice maxima meet in
+            // shared memory (the barrier also ends every read of the stage's q
+            // rows, so P may overwrite them)
+            float* xm = xmax + (size_t)((2 * g + ((it >> 1) & 1u)) * 4) * kMaxRowsPerWalk;
+            xm[32 * w + r] = xw;
+            if (!sync_group()) break;
+            const float x = fmaxf(fmaxf(xm[r], xm[32 + r]), fmaxf(xm[64 + r], xm[96 + r]));
+            // lazy reference: o is rescaled only when the max runs more than 2^8
+            // past the reference (a row with no weight yet has o = 0: nothing to
+            // scale); this group's previous P V is done (it was issued before this
+            // stage's S); every warp scales its lanes of the group's O^T for all 32
+            // rows
+            const bool up = x > mref + kLazyLog2;
+            const bool scale_o = up && mref != kNegInf;
+            if (__any_sync(0xffffffffu, scale_o)) {
+                const float a = scale_o ? ex2(mref - x) : 1.f;
+                lw *= a;
+#pragma unroll
+                for (int k = 0; k < 2; ++k) {
+                    float o[16];
+                    tmem_ld16(tO + 16u * k, o);
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) o[i] *= __shfl_sync(0xffffffffu, a, 16 * k + i);
+                    tmem_st16(tO + 16u * k, o);
+                }
+            }
+            if (up) mref = x;
+            const float u = mref == kNegInf ? 0.f : mref;
+            uint32_t hi[8], lo[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const float p0 = ex2(s[2 * i] - u), p1 = ex2(s[2 * i + 1] - u);
+                lw += p0 + p1;
+                hi[i] = pack_bf16x2(p0, p1);
+                lo[i] = PDA_TC_P_LO ? pack_bf16x2(p0 - bf16_lo(hi[i]), p1 - bf16_hi(hi[i])) : 0u;
+            }
+            // P row r, this slice's 16 tokens: [32 rows][64 tokens] bf16, K-major, swizzled
+#pragma unroll
+            for (int k = 0; k < 2; ++k) {
+                const uint32_t off = (uint32_t)r * 128u + (uint32_t)(((2 * w + k) ^ (r & 7)) << 4);
+                asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(sP + off), "r"(hi[4 * k]),
+                             "r"(hi[4 * k + 1]), "r"(hi[4 * k + 2]), "r"(hi[4 * k + 3])
+                             : "memory");
+                if (PDA_TC_P_LO)
+                    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(sP + kTcPLo + off),
+                                 "r"(lo[4 * k]), "r"(lo[4 * k + 1]), "r"(lo[4 * k + 2]), "r"(lo[4 * k + 3])
+                                 : "memory");
+            }
+            // V rows past the valid ones may hold anything: P V must see zeros
+            if (16 * w < m.n_valid && m.n_valid < 16 * w + 16) zero_rows<D>(sV, m.n_valid, 16 * w + 16, lbs, lane);
+            fence_proxy_async_smem();  // P and the zeroed rows, before the MMA reads them
+            tmem_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(tcb + kTcP + 8u * g);
         }
-        // this slice's 8 columns of the stage's P buffer (a P V two stages back,
-        // the last reader, is done: it was issued before this stage's S)
-        const uint32_t tP = tl + kTmP + 64u * (it & 1u) + 8u * w;
-        tmem_st8u(tP, hi);
-        if (PDA_TC_P_LO) tmem_st8u(tP + 32u, lo);
-        // V rows past the valid ones may hold anything: P V must see zeros
-        if (16 * w < m.n_valid && m.n_valid < 16 * w + 16) {
-            zero_rows<D>(sV, m.n_valid, 16 * w + 16, lbs, lane);
-            fence_proxy_async_smem();
-        }
-        tmem_wait_st();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(tcb + kTcP + 8u * (it & 1u));
         if (m.flags & kSegEnd) {
-            // ---- segment end: first the next segment's Q (its stage is the next
-            // one), so that its S runs during this epilogue; then the slices'
-            // states merge per 16-row q tile through this stage's memory, as in
-            // the mma.sync row form
-            {
+            // ---- segment end, both groups: once this stage's P V is done (and so
+            // every MMA of the segment, issued before it: no S still reads the
+            // segment's Q), first the next segment's Q (by the group whose stage it
+            // is), so that its S runs during this epilogue; then each group's
+            // o / l as one slice through this stage's memory, and the unit roles of
+            // the row forms
+            if (!warp_wait(tcb + kTcPV + 8u * (it & 1u), (it >> 1) & 1u)) { give_up(); break; }
+            tc_fence_after();
+            if (((it + 1u) & 1u) == (uint32_t)g) {
                 const int ns = stage + 1 == S ? 0 : stage + 1;
                 if (!warp_wait(full0 + 8 * ns, ns == 0 ? phase ^ 1u : phase)) { give_up(); break; }
                 const StageMeta mn = meta[ns];
@@ -1786,52 +1819,50 @@ __device__ __forceinline__ void run_consumer_tc(const SplitParams& p, uint32_t b
                     q_written = true;
                 }
             }
-            if (!warp_wait(tcb + kTcPV + 8u * (it & 1u), (it >> 1) & 1u)) { give_up(); break; }
-            tc_fence_after();
-            float* st_m = reinterpret_cast<float*>(base + L.st_m);  // [slice][32 q rows]
-            float* st_l = reinterpret_cast<float*>(base + L.st_l);
-            int32_t* st_role = reinterpret_cast<int32_t*>(base + L.st_x) + 2 * kMaxGroup;
-            float* st_o = reinterpret_cast<float*>(base + (sK - base_s));  // [slice][16][kOStride]
-            const bool read = consumer_sync(cbar, cphase, p.err, abort_flag);  // all reads of the stage done
-            if (!__all_sync(0xffffffffu, read ? 1 : 0)) break;
             const bool whole = (m.flags & kWholeUnit) != 0;
             const int u = m.b * p.Hkv + m.kvh;
+            if (ct == 0 && !whole) ticket = atomicAdd(p.unit_sync + 2 * u, 1);
+            float* st_m = reinterpret_cast<float*>(base + L.st_m);  // [group][32 q rows]
+            float* st_l = reinterpret_cast<float*>(base + L.st_l);
+            int32_t* st_role = reinterpret_cast<int32_t*>(base + L.st_x) + 2 * kMaxGroup;
+            float* st_o = reinterpret_cast<float*>(base + (sK - base_s));  // [tile][group][16][kOStride]
+            if (!sync_all()) break;  // every read of the stage's tiles done
+            lpart[32 * warp + r] = lw;
+#pragma unroll
+            for (int k = 0; k < 2; ++k) {  // q rows 16k..16k+15: tile k
+                float o[16];
+                tmem_ld16(tO + 16u * k, o);
+#pragma unroll
+                for (int i = 0; i < 16; ++i)
+                    st_o[(size_t)((2 * k + g) * 16 + i) * kOStride + 32 * w + lane] = active ? o[i] : 0.f;
+            }
+            if (!sync_all()) break;
+            if (w == 0) {
+                st_m[32 * g + r] = mref;
+                st_l[32 * g + r] = (lpart[32 * (4 * g) + r] + lpart[32 * (4 * g + 1) + r]) +
+                                   (lpart[32 * (4 * g + 2) + r] + lpart[32 * (4 * g + 3) + r]);
+            }
+            if (!sync_all()) break;
             UnitPieces pc;
             pc.cf = 0; pc.su = 0; pc.n = 1; pc.every = true;
             const GroupRange grs = group_of_cta(blockIdx.x, pfx, p.B, rows_per_seq<true>(p), p.Hkv, gridDim.x);
             if (!whole) pc = unit_pieces(pfx, m.b, m.kvh, p.Hkv, p.unit_cost, grs);
             const RowInfo ri = row_info<true>(p, m.b);
-            st_m[w * kMaxRowsPerWalk + r] = mref;
-            st_l[w * kMaxRowsPerWalk + r] = l;
             int role = kRoleAbort;
             bool stop = false;
             for (int tile = 0; tile < 2; ++tile) {
-                // (outcomes shared by the warp: its lanes reach the tensor-memory loads together)
-                const bool ok = tile == 0 || consumer_sync(cbar, cphase, p.err, abort_flag);
-                if (!__all_sync(0xffffffffu, ok ? 1 : 0)) { stop = true; break; }
-                const bool mine = (r >> 4) == tile;  // this lane's row is in the tile
-                float* ro = st_o + (size_t)(w * 16 + (r & 15)) * kOStride;
-#pragma unroll 1
-                for (int k = 0; k < D / 16; ++k) {
-                    float o[16];
-                    tmem_ld16(tO + 16u * k, o);
-                    if (mine) {
-#pragma unroll
-                        for (int i = 0; i < 16; i += 4)
-                            *reinterpret_cast<float4*>(ro + 16 * k + i) = make_float4(o[i], o[i + 1], o[i + 2], o[i + 3]);
-                    }
-                }
-                const bool merged = rows_tile_merge<D, kSlices, kThreadsC>(
-                    p, m, tile, ct, ticket, pc, grs, ri, st_m, st_l, st_o, st_role, cbar, cphase, abort_flag, role);
+                const bool merged = rows_tile_merge<D, 2, kThreadsC>(p, m, tile, ct, ticket, pc, grs, ri, st_m, st_l,
+                                                                     st_o + (size_t)tile * 2 * 16 * kOStride, st_role,
+                                                                     cbar, cphase, abort_flag, role);
                 if (!__all_sync(0xffffffffu, merged ? 1 : 0)) { stop = true; break; }
             }
             if (stop) break;
-            const bool synced = consumer_sync(cbar, cphase, p.err, abort_flag);
-            if (!__all_sync(0xffffffffu, synced ? 1 : 0)) break;
+            if (!sync_all()) break;
             if (role == kRoleStore && ct == 0) red_release_gpu_add(p.unit_sync + 2 * u + 1, 1);
             fence_proxy_async_smem();  // staging writes before the next TMA into this stage
             mref = kNegInf;
-            l = 0.f;
+            lw = 0.f;
+            active = false;
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(empty0 + 8 * stage);
@@ -2024,11 +2055,12 @@ __global__ void __maxnreg__(split_max_regs(D, MODE)) split_kernel(const __grid_c
         }
         mbar_init(base_s + L.cbar, C::kConsumerWarps * 32);
         if constexpr (C::kTc) {
-            mbar_init(base_s + L.tcb + kTcQ, C::kConsumerWarps);
+            mbar_init(base_s + L.tcb + kTcQ, C::kConsumerWarps / 2);
             for (int b = 0; b < 2; ++b) {
                 mbar_init(base_s + L.tcb + kTcS + 8 * b, 1);
-                mbar_init(base_s + L.tcb + kTcP + 8 * b, C::kConsumerWarps);
+                mbar_init(base_s + L.tcb + kTcP + 8 * b, C::kConsumerWarps / 2);
                 mbar_init(base_s + L.tcb + kTcPV + 8 * b, 1);
+                mbar_init(base_s + L.tcb + kTcG + 8 * b, C::kConsumerWarps / 2 * 32);
             }
             mbar_init(base_s + L.tcb + kTcFin, 1);
         }
@@ -2096,6 +2128,8 @@ __global__ void __maxnreg__(split_max_regs(D, MODE)) split_kernel(const __grid_c
 // to 128.
 template <int D, int ST>
 constexpr bool has_rows_form() { return ST == 64 && D <= 128; }
+template <int D, int ST>
+constexpr bool has_tc_form() { return ST == 64 && D == 128; }
 
 template <int D, int ST>
 const void* split_fn_of(int mode) {
@@ -2113,7 +2147,7 @@ const void* split_fn_of(int mode) {
                 return reinterpret_cast<const void*>(&split_kernel<D, ST, kMultiRows32>);
             return nullptr;
         case kMultiTc:
-            if constexpr (has_rows_form<D, ST>())
+            if constexpr (has_tc_form<D, ST>())
                 return reinterpret_cast<const void*>(&split_kernel<D, ST, kMultiTc>);
             return nullptr;
         default: return nullptr;
@@ -2126,7 +2160,7 @@ int split_stages_of(int mode) {
     switch (mode) {
         case kMultiRows16: return Cfg<D, ST, has_rows_form<D, ST>() ? kMultiRows16 : kOneShot>::kStages;
         case kMultiRows32: return Cfg<D, ST, has_rows_form<D, ST>() ? kMultiRows32 : kOneShot>::kStages;
-        case kMultiTc: return Cfg<D, ST, has_rows_form<D, ST>() ? kMultiTc : kOneShot>::kStages;
+        case kMultiTc: return has_tc_form<D, ST>() ? Cfg<D, ST, has_tc_form<D, ST>() ? kMultiTc : kOneShot>::kStages : 0;
         default: return Cfg<D, ST, kOneShot>::kStages;
     }
 }
@@ -2161,7 +2195,7 @@ cudaError_t launch_split_of(int mode, const SplitParams& p, int grid, size_t sme
             if constexpr (has_rows_form<D, ST>()) return launch_split_mode<D, ST, kMultiRows32>(p, grid, smem, stream);
             return cudaErrorInvalidValue;
         case kMultiTc:
-            if constexpr (has_rows_form<D, ST>()) return launch_split_mode<D, ST, kMultiTc>(p, grid, smem, stream);
+            if constexpr (has_tc_form<D, ST>()) return launch_split_mode<D, ST, kMultiTc>(p, grid, smem, stream);
             return cudaErrorInvalidValue;
         default: return cudaErrorInvalidValue;
     }

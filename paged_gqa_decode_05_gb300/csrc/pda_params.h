@@ -47,21 +47,24 @@ __host__ __device__ constexpr int q_tiles(int mode) {
 // q rows a stage's q area holds.
 __host__ __device__ constexpr int stage_q_rows(int mode) { return q_tiles(mode) ? 16 * q_tiles(mode) : kMaxGroup; }
 // Consumer warps: one per 16 KV rows of a stage, times the q tiles in the
-// mma.sync row form; the tcgen05 form's four softmax warps, one per 16-row
-// token slice and tensor-memory lane quarter.
+// mma.sync row form; the tcgen05 form's eight softmax warps, two groups (even
+// and odd stages) of one per 16-row token slice and tensor-memory lane
+// quarter.
 __host__ __device__ constexpr int consumer_warps(int st, int mode) {
-    return is_tc(mode) ? 4 : (st / 16) * (q_tiles(mode) ? q_tiles(mode) : 1);
+    return is_tc(mode) ? 8 : (st / 16) * (q_tiles(mode) ? q_tiles(mode) : 1);
 }
 constexpr int kMaxConsumerWarps = 8;
-// Threads of a split CTA: the consumer warps, the producer warp, the MMA warp
-// of the tcgen05 form and the prefetch warp.
-PDA_HD int split_threads(int st, int mode) { return (consumer_warps(st, mode) + 2 + (is_tc(mode) ? 1 : 0)) * 32; }
+// Threads of a split CTA as launched at most: the consumer warps, the
+// producer warp and the prefetch warp (the tcgen05 form: the MMA warp
+// instead; it launches no prefetch warp).
+PDA_HD int split_threads(int st, int mode) { return (consumer_warps(st, mode) + 2) * 32; }
 // Stage rows for a head size and block size.
 PDA_HD int stage_tokens(int D, int block_size) { return D == 256 && !block_boxes(D, block_size) ? 32 : 64; }
 // Sequences (launch rows) per launch of a mode: the row form with one q tile
-// runs two CTAs per SM with three 36 KB stages at head size 128, which
-// leaves room for a 512-entry block prefix.
-PDA_HD int max_launch_rows(int mode) { return mode == kMultiRows16 ? 512 : kMaxLaunchBatch; }
+// runs two CTAs per SM with three 36 KB stages at head size 128, the tcgen05
+// form one CTA with five 40 KB stages, which leaves room for a 512-entry
+// block prefix.
+PDA_HD int max_launch_rows(int mode) { return (mode == kMultiRows16 || mode == kMultiTc) ? 512 : kMaxLaunchBatch; }
 // The unit-cost class of a mode (pda_plan.h).
 PDA_HD int32_t cost_class(int mode) {
     return mode == kMulti ? kCostMultiN8 : mode == kMultiRows16 ? kCostRows16
@@ -126,7 +129,7 @@ struct SplitParams {
 };
 
 struct SmemLayout {
-    uint32_t bars, cbar, tcb, meta, scan, st_m, st_l, st_x, pfx, total;
+    uint32_t bars, cbar, tcb, tcx, meta, scan, st_m, st_l, st_x, pfx, total;
 };
 
 // K and V tiles of ST rows plus the stage's q rows (stage_q_rows x D bf16).
@@ -145,7 +148,9 @@ PDA_HD SmemLayout smem_layout(int D, int st, int mode, int stages, int B) {
     uint32_t off = (uint32_t)stages * stage_bytes(D, st, mode);
     L.bars = off;  off += 2u * stages * 8u;
     L.cbar = off;  off += 8u;
-    L.tcb = off;   off += is_tc(mode) ? 72u : 0u;  // tcgen05 form: 8 barriers, the tensor-memory base
+    L.tcb = off;   off += is_tc(mode) ? 96u : 0u;  // tcgen05 form: 10 barriers, the tensor-memory base
+    // tcgen05 form: row maxima of the slices [group][2][4][32], weight sums [8 warps][32]
+    L.tcx = off;   off += is_tc(mode) ? (2u * 2u * 4u + 8u) * kMaxRowsPerWalk * 4u : 0u;
     L.meta = off;  off += (uint32_t)stages * (uint32_t)sizeof(StageMeta);
     L.scan = off;  off += 128u;  // per warp: block-prefix sum [16], largest unit [16]
     L.st_m = off;  off += 4u * kMaxRowsPerWalk * 4u;

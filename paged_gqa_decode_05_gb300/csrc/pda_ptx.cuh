@@ -201,11 +201,22 @@ __device__ __forceinline__ uint64_t umma_sdesc(uint32_t addr, uint32_t lbo, uint
 }
 
 // Instruction descriptor of kind::f16 with bf16 A and B, fp32 accumulator:
-// D format (bits 4-5) = 1, A / B format (7-9 / 10-12) = 1, A K-major, B
-// MN-major when b_mn (bit 16), N >> 3 (17-22), M >> 4 (24-28).
-__host__ __device__ constexpr uint32_t umma_idesc_bf16(int M, int N, bool b_mn) {
-    return (1u << 4) | (1u << 7) | (1u << 10) | (b_mn ? (1u << 16) : 0u) | ((uint32_t)(N >> 3) << 17) |
-           ((uint32_t)(M >> 4) << 24);
+// D format (bits 4-5) = 1, A / B format (7-9 / 10-12) = 1, A MN-major when
+// a_mn (bit 15), B MN-major when b_mn (bit 16), N >> 3 (17-22), M >> 4
+// (24-28).
+__host__ __device__ constexpr uint32_t umma_idesc_bf16(int M, int N, bool b_mn, bool a_mn = false) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | (a_mn ? (1u << 15) : 0u) | (b_mn ? (1u << 16) : 0u) |
+           ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+// D[tmem] (+)= A[smem] * B[smem], issued by one thread; accumulate when acc.
+__device__ __forceinline__ void umma_bf16_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                             bool acc) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(acc ? 1u : 0u)
+        : "memory");
 }
 
 // D[tmem] (+)= A[tmem] * B[smem], issued by one thread; accumulate when acc.

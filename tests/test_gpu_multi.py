@@ -49,21 +49,22 @@ def test_multi_matches_oracle(D, bs, G, q_len, tc):
     info = ctx.multi_info(q_len)
     rows = info["rows_per_walk"]
     tc_layout = bs >= 8 or (bs * D * 2) % 1024 != 0  # whole 1024-byte boxes, or gathered rows
-    assert info["form"] == (2 if tc and rows > 16 and tc_layout else 1 if rows > 8 and D <= 128 else 0)
+    tc_form = tc and rows > 16 and D == 128 and tc_layout
+    assert info["form"] == (2 if tc_form else 1 if rows > 8 and D <= 128 else 0)
 
 
 @pytest.mark.parametrize("D,G,q_len,form,qp,walks,tc", [
     (128, 4, 2, 0, 2, 1, True), (128, 4, 3, 1, 3, 1, True), (128, 4, 4, 1, 4, 1, True),
     (128, 4, 8, 2, 8, 1, True), (128, 4, 8, 1, 8, 1, False), (128, 4, 9, 2, 8, 2, True),
     (128, 8, 2, 1, 2, 1, True), (128, 8, 5, 2, 4, 2, True), (128, 8, 5, 1, 4, 2, False),
-    (64, 1, 8, 0, 8, 1, True), (64, 1, 9, 1, 9, 1, True), (64, 2, 16, 2, 16, 1, True),
+    (64, 1, 8, 0, 8, 1, True), (64, 1, 9, 1, 9, 1, True), (64, 2, 16, 1, 16, 1, True),
     (64, 2, 16, 1, 16, 1, False), (256, 4, 4, 0, 2, 2, True), (256, 8, 3, 0, 1, 3, True)])
 def test_multi_launch_shape(D, G, q_len, form, qp, walks, tc):
     """The form a q_len takes: up to 8 q rows per sequence (and every head size
     256 call) the n8 form; more, the row form with up to 32 q rows per walk:
     one q tile on mma.sync (two CTAs per SM) up to 16 rows, and above that two
-    q tiles on mma.sync, or the tcgen05 form where it is switched on (one CTA
-    per SM either way)."""
+    q tiles on mma.sync, or at head size 128 the tcgen05 form where it is
+    switched on (one CTA per SM either way)."""
     import paged_gqa_decode_05_gb300 as pda
     ctx = pda.Context(max_seqs=64, num_q_heads=2 * G, num_kv_heads=2, head_dim=D, block_size=16)
     ctx.set_multi_tc(tc)
