@@ -1802,12 +1802,20 @@ __device__ __forceinline__ void run_consumer_tc(const SplitParams& p, uint32_t b
             if (lane == 0) mbar_arrive(tcb + kTcP + 8u * g);
         }
         if (m.flags & kSegEnd) {
-            // ---- segment end, both groups: once this stage's P V is done (and so
-            // every MMA of the segment, issued before it: no S still reads the
-            // segment's Q), first the next segment's Q (by the group whose stage it
-            // is), so that its S runs during this epilogue; then each group's
-            // o / l as one slice through this stage's memory, and the unit roles of
-            // the row forms
+            // ---- segment end, both groups.  First all eight warps meet: the
+            // stage's own group arrives only after its S wait, which makes its
+            // previous P V complete, so the P V barrier of the stage's parity is at
+            // this stage's phase for either group to wait on (a parity wait on a
+            // barrier one phase behind would pass at once).  Once this stage's P V
+            // is done (and so every MMA of the segment, issued before it: no S still
+            // reads the segment's Q and no MMA reads the stage), the group whose
+            // stage is next writes the next segment's Q, so that its S runs during
+            // this epilogue; then each group's o / l as one slice through this
+            // stage's memory, and the unit roles of the row forms
+            const bool whole = (m.flags & kWholeUnit) != 0;
+            const int u = m.b * p.Hkv + m.kvh;
+            if (ct == 0 && !whole) ticket = atomicAdd(p.unit_sync + 2 * u, 1);
+            if (!sync_all()) break;
             if (!warp_wait(tcb + kTcPV + 8u * (it & 1u), (it >> 1) & 1u)) { give_up(); break; }
             tc_fence_after();
             if (((it + 1u) & 1u) == (uint32_t)g) {
@@ -1819,14 +1827,10 @@ __device__ __forceinline__ void run_consumer_tc(const SplitParams& p, uint32_t b
                     q_written = true;
                 }
             }
-            const bool whole = (m.flags & kWholeUnit) != 0;
-            const int u = m.b * p.Hkv + m.kvh;
-            if (ct == 0 && !whole) ticket = atomicAdd(p.unit_sync + 2 * u, 1);
             float* st_m = reinterpret_cast<float*>(base + L.st_m);  // [group][32 q rows]
             float* st_l = reinterpret_cast<float*>(base + L.st_l);
             int32_t* st_role = reinterpret_cast<int32_t*>(base + L.st_x) + 2 * kMaxGroup;
             float* st_o = reinterpret_cast<float*>(base + (sK - base_s));  // [tile][group][16][kOStride]
-            if (!sync_all()) break;  // every read of the stage's tiles done
             lpart[32 * warp + r] = lw;
 #pragma unroll
             for (int k = 0; k < 2; ++k) {  // q rows 16k..16k+15: tile k
