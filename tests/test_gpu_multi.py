@@ -238,3 +238,28 @@ def test_tc_form_back_to_back_with_plain_decodes_in_a_graph():
     assert ctx.read_device_errors() == 0
     for o, a in zip(outs_m + outs_d, alone_m + alone_d):
         assert torch.equal(o, a)
+
+
+@pytest.mark.parametrize("tc", [True, False])
+def test_multi_more_launch_rows_than_one_launch(tc):
+    """640 sequences of 8 queries: the tcgen05 form launches at most 512 launch
+    rows (two chunks here), the mma.sync form 1024 (one); both against the
+    oracle."""
+    import torch
+    rng = np.random.default_rng(71)
+    lens = [int(x) for x in rng.integers(8, 200, size=640)]
+    q_len = 8
+    w = workloads.make_workload("multi_chunks", B=len(lens), Hq=8, Hkv=2, D=128, block_size=16,
+                                seq_lens=lens, seed=72)
+    q = workloads.multi_queries(w, q_len)
+    ctx = _ctx(w, q_len)
+    ctx.set_multi_tc(tc)
+    assert ctx.multi_info(q_len)["form"] == (2 if tc else 1)
+    t = upload(w)
+    out = ctx.decode_multi(dev(q), t["k_pool"], t["v_pool"], t["block_table"], t["seq_lens"])
+    torch.cuda.synchronize()
+    assert ctx.read_device_errors() == 0
+    ref = oracle.load().decode_multi(q, w.k_pool, w.v_pool, w.block_table, w.seq_lens, q_len=q_len,
+                                     Hq=w.Hq, Hkv=w.Hkv, D=w.D, block_size=w.block_size,
+                                     n_threads=oracle.host_threads())
+    assert_close_to_oracle(host_f64(out), ref, "multi chunks")
